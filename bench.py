@@ -1,0 +1,382 @@
+#!/usr/bin/env python3
+"""Decode benchmark: tokens/s and HBM-roofline fraction of the batch-1 decode
+step on one GB300 (default workload: the Llama-2-7B shape in fp32).
+
+A step is one forward(token, pos) -> logits over the whole model.  Warm-up
+steps decode positions 0..W-1, the timed steps positions W..W+K-1 of one
+teacher-forced stream of seeded uniform tokens (positions wrap to 0, with the
+cache rewound, after seq_len).  The weights (26.4 GB at the 7B shape) are far
+larger than L2, so every step streams them from HBM.
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle on
+the host cores on the same workload instead (a bounded sample of steps).
+Multi-GPU (torchrun): each rank runs an independent replica, no collective on
+the data path; value = all ranks' tokens / the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+from synth import WORKLOADS  # noqa: E402
+
+METRIC = "decode tokens/s at batch 1 and % of HBM roofline (GB/s vs ~8 TB/s), 1 GB300"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of
+# the dominant kernel, from the ncu capture summarised in
+# profiles/gemv_w13_llama2_7b.md, valid only for the kernel source whose
+# sha256 prefix is recorded beside it.
+W13_NCU_TRAFFIC = None  # (bytes per launch, gemv.cu sha256 prefix)
+
+
+def weight_bytes(wl) -> int:
+    """Weight bytes one step streams: every matrix, the RMSNorm gains, the
+    classifier, one embedding row."""
+    d, h, L, kv, V = wl.dim, wl.hidden_dim, wl.n_layers, wl.kv_dim, wl.vocab_size
+    return 4 * (L * (2 * d * d + 2 * kv * d + 3 * d * h + 2 * d) + V * d + 2 * d)
+
+
+def kv_bytes(wl, pos: int) -> int:
+    """K and V cache bytes one step at ``pos`` reads."""
+    return 4 * wl.n_layers * 2 * wl.kv_dim * (pos + 1)
+
+
+def w13_bytes(wl) -> int:
+    """Algorithmic bytes of one rmsnorm+W1/W3+SwiGLU launch: both matrices,
+    the gain vector, x in and hb out."""
+    return 4 * (2 * wl.hidden_dim * wl.dim + 2 * wl.dim + wl.hidden_dim)
+
+
+def measured_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return json.load(f)
+    except OSError:
+        return {}
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")),
+            int(os.environ.get("WORLD_SIZE", "1")))
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str | None):
+        self.uuid = uuid
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            if self.thread:
+                self.thread.join(timeout=2)
+
+    def summary(self) -> dict:
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) != 9:
+                continue
+            if self.uuid and self.uuid not in parts[0]:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def config_of(wl, batch: int = 1) -> dict:
+    return {"workload": wl.name, "dim": wl.dim, "hidden_dim": wl.hidden_dim, "n_layers": wl.n_layers,
+            "n_heads": wl.n_heads, "n_kv_heads": wl.n_kv_heads, "vocab_size": wl.vocab_size,
+            "seq_len": wl.seq_len, "batch": batch, "parallelism": "replicas",
+            "weights": "seeded random (synth)", "tokens": "seeded uniform, teacher-forced",
+            "l2": "inputs larger than L2" if weight_bytes(wl) > 129e6 else "weights fit in L2 (effective bandwidth)"}
+
+
+def load_weights_device(wl, keep_host: bool):
+    """Device tensors of the workload's weights; host arrays too if asked."""
+    import torch
+    if keep_host:
+        host = synth.make_weights(wl)
+        import llama_transformer_decode_gb300 as pkg
+        return pkg.to_device(host), host
+    dev = {}
+    chunk = 1 << 26
+    buf = torch.empty(chunk, dtype=torch.float32, pin_memory=True)
+    bnp = buf.numpy()
+    for name in wl.tensor_names():
+        if name == "wcls" and wl.shared_wcls:
+            dev["wcls"] = dev["emb"]
+            continue
+        t = torch.empty(wl.shape(name), dtype=torch.float32, device="cuda")
+        flat = t.view(-1)
+        for st in range(0, flat.numel(), chunk):
+            n = min(chunk, flat.numel() - st)
+            synth.fill_range(wl, name, st, bnp[:n])
+            flat[st:st + n].copy_(buf[:n], non_blocking=False)
+        dev[name] = t
+    return dev, None
+
+
+def oracle_rate(wl, host_w, tokens, budget_s: float, min_steps: int = 2):
+    """Teacher-forced oracle steps from position 0 until the time budget is
+    spent; returns (steps, seconds, threads)."""
+    import oracle
+    m = oracle.Model(wl.config_tuple(), host_w)
+    t0 = time.perf_counter()
+    n = 0
+    while n < len(tokens) and (n < min_steps or time.perf_counter() - t0 < budget_s):
+        m.forward(int(tokens[n]), n)
+        n += 1
+    el = time.perf_counter() - t0
+    threads = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    return n, el, threads
+
+
+def run_reference(args, wl):
+    rank, _, world = dist_env()
+    if rank != 0:
+        return 0
+    host_w = synth.make_weights(wl)
+    toks = synth.token_stream(wl, 0, wl.seq_len)
+    import oracle
+    m = oracle.Model(wl.config_tuple(), host_w)
+    for p in range(args.warmup):
+        m.forward(int(toks[p % wl.seq_len]), p % wl.seq_len)
+    # size the timed sample from one step's cost so the run stays within the budget
+    t0 = time.perf_counter()
+    p = args.warmup % wl.seq_len
+    m.forward(int(toks[p]), p)
+    one = time.perf_counter() - t0
+    k = max(1, min(args.steps, int(args.reference_budget / max(one, 1e-6))))
+    t0 = time.perf_counter()
+    for i in range(k):
+        p = (args.warmup + 1 + i) % wl.seq_len
+        if p == 0:
+            m.key_cache[0][:] = 0
+            m.value_cache[0][:] = 0
+        m.forward(int(toks[p]), p)
+    el = time.perf_counter() - t0
+    value = k / el
+    threads = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    sample = (f"{k} teacher-forced oracle steps of {wl.name} at positions "
+              f"{args.warmup + 1}..{args.warmup + k} (of {args.steps} requested), after {args.warmup + 1} untimed")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": k, "warmup": args.warmup, "ms_per_step": 1000.0 * el / k, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64-accumulate/f32-storage", "data": "synthetic",
+            "config": config_of(wl),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, wl):
+    import torch
+    import torch.distributed as dist
+
+    import llama_transformer_decode_gb300 as pkg
+
+    rank, local_rank, world = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local_rank)
+    pkg._native.load()
+    uuid = str(torch.cuda.get_device_properties(local_rank).uuid)
+
+    cpu_leg = rank == 0 and world == 1 and not args.no_cpu
+    w_dev, host_w = load_weights_device(wl, keep_host=cpu_leg)
+    stream = torch.cuda.Stream()
+    dec = pkg.Decoder(wl.config_tuple(), w_dev, stream=stream)
+    S = wl.seq_len
+    toks = synth.token_stream(wl, 0, S)
+    out = torch.empty(wl.vocab_size, device="cuda")
+    kern = dec.kernels_per_step(1)
+
+    def positions(n, start):
+        return [(start + i) % S for i in range(n)]
+
+    def run_steps(pos_list, host_out=None):
+        for p in pos_list:
+            if p == 0:
+                dec.reset()
+            if host_out is None:
+                dec.forward(int(toks[p]), p, out)
+            else:
+                dec.forward_host(int(toks[p]), p, host_out)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    def max_over_ranks(v: float) -> float:
+        if world == 1:
+            return v
+        t = torch.tensor([v], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    warm = positions(args.warmup, 0)
+    timed = positions(args.steps, args.warmup)
+    run_steps(warm)
+    dec.sync()
+
+    # ---- device-resident timed region ----
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(uuid) as clocks:
+        ev0.record(stream)
+        run_steps(timed)
+        ev1.record(stream)
+        ev1.synchronize()
+    torch.cuda.synchronize()
+    barrier()
+    dec.sync()
+    ms = max_over_ranks(ev0.elapsed_time(ev1))
+    value = world * args.steps / (ms / 1000.0)
+    bytes_total = sum(weight_bytes(wl) + kv_bytes(wl, p) for p in timed)
+    step_gbs = bytes_total / (ms / 1000.0) / 1e9
+
+    # ---- end to end through the host-buffer call ----
+    host_logits = np.empty(wl.vocab_size, np.float32)
+    dec.reset()
+    run_steps(warm, host_logits)
+    barrier()
+    t0 = time.perf_counter()
+    run_steps(timed, host_logits)
+    e2e_s = max_over_ranks(time.perf_counter() - t0)
+    e2e = {"value": world * args.steps / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": dec.step_input_bytes(),
+           "d2h_bytes_per_step": 4 * wl.vocab_size}
+
+    # ---- dominant kernel (rmsnorm + W1/W3 + SwiGLU) timed alone, layers cycled ----
+    peaks = measured_peaks()
+    hbm = peaks.get("hbm_gbs")
+    peak_src = "of measured" if hbm else "of fallback"
+    hbm = hbm or FALLBACK_HBM_GBS
+    reps = max(1, 64 // wl.n_layers)
+    dec.launch_op("w13", 0, 1)
+    k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    k0.record(stream)
+    for _ in range(reps):
+        for layer in range(wl.n_layers):
+            dec.launch_op("w13", layer, 1)
+    k1.record(stream)
+    k1.synchronize()
+    w13_ms = k0.elapsed_time(k1) / (reps * wl.n_layers)
+    achieved = w13_bytes(wl) / (w13_ms / 1000.0) / 1e9
+    traffic = None
+    if W13_NCU_TRAFFIC is not None:
+        src = open(os.path.join(ROOT, "llama_transformer_decode_gb300", "csrc", "gemv.cu"), "rb").read()
+        if hashlib.sha256(src).hexdigest().startswith(W13_NCU_TRAFFIC[1]):
+            traffic = W13_NCU_TRAFFIC[0]
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                "traffic": traffic, "kernel": "gemv_kernel<GEMV_W13> (rmsnorm + W1/W3 + SwiGLU)",
+                "bytes_per_launch": w13_bytes(wl), "us_per_launch": w13_ms * 1000.0,
+                "timing": "CUDA events around standalone launches on the decoder's stream, layers cycled",
+                "peak_source": peak_src + " (MEASURED_PEAKS.json hbm_gbs, copy bandwidth)"}
+    dec.sync()
+
+    # ---- CPU baseline: the oracle on this host's cores ----
+    cpu = None
+    if cpu_leg:
+        n, el, threads = oracle_rate(wl, host_w, toks, args.cpu_budget)
+        cpu = {"value": n / el, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+               "sample": f"{n} teacher-forced oracle steps of {wl.name} at positions 0..{n - 1}"}
+
+    clk = clocks.summary()
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded random weights and tokens)",
+        "config": dict(config_of(wl), positions=f"{timed[0]}..{timed[-1]}" if timed else ""),
+        "hbm_roofline": {"achieved_gbs": step_gbs, "frac_of_8tbs": step_gbs / NOMINAL_HBM_GBS,
+                         "frac_of_measured": step_gbs / hbm,
+                         "bytes_per_step_avg": bytes_total / max(1, len(timed))},
+        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": kern * args.steps, "clocks": {k: clk[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
+    }
+    dec.close()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None, help="timed steps (default: to the end of the context)")
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default="llama2_7b", choices=sorted(WORKLOADS))
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-baseline leg")
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time for the CPU baseline")
+    ap.add_argument("--reference-budget", type=float, default=90.0,
+                    help="seconds of timed oracle work in --impl reference")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    wl = WORKLOADS[args.workload]
+    if args.steps is None:
+        args.steps = max(1, wl.seq_len - args.warmup)
+    if args.impl == "reference":
+        return run_reference(args, wl)
+    return run_ours(args, wl)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,189 @@
+/*
+ * l2decode -- single-token Llama-2 decode step on one GB300 (sm_103a), fp32.
+ *
+ * The operation is llama2.c's forward(token, pos) -> logits, as stated by
+ * the page "run.c" (play_with_baby_llama2 mirror of llama2.c), function
+ * transformer(), and by the page "run.c 逐行解讀" (line-by-line walkthrough
+ * of the later run.c), §4 forward() steps 1-3:
+ *   x = emb[token];
+ *   per layer l: xb = rmsnorm(x, rms_att[l]); q = Wq xb; k = Wk xb; v = Wv xb;
+ *     RoPE(q over dim, k over kv_dim; theta = pos*10000^(-(i mod hs)/hs));
+ *     K[l][pos] = k; V[l][pos] = v;
+ *     per query head h with KV head g(h): softmax(q_h.K_t/sqrt(hs), t<=pos)
+ *       weighted sum of V_t -> xb;
+ *     x += Wo xb; xb = rmsnorm(x, rms_ffn[l]);
+ *     x += W2 (silu(W1 xb) * (W3 xb));
+ *   logits = Wcls rmsnorm(x, rms_final).
+ * g(h) = floor(h * n_kv_heads / n_heads), which is the pages' h / kv_mul
+ * whenever n_heads is a multiple of n_kv_heads.
+ *
+ * Conventions for every entry point:
+ *   - Calls return an L2_* status; they never exit or abort the process.
+ *     After a failure, l2_last_error() describes it.
+ *   - Device pointers are borrowed: the caller keeps them alive and
+ *     unchanged until l2_destroy().  The handle owns everything it
+ *     allocates (KV cache, activations, workspaces, CUDA graphs, pinned
+ *     staging) and frees it in l2_destroy().
+ *   - Work is enqueued on the stream given to l2_create() and the call
+ *     returns without waiting, except where a function says it blocks.
+ *   - One handle must not be used from two host threads at once.
+ */
+#ifndef L2_DECODE_H
+#define L2_DECODE_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes. */
+#define L2_OK 0
+#define L2_EINVAL (-1)   /* invalid argument (config, pointer, token, pos, batch, slot) */
+#define L2_ESTATE (-2)   /* KV-cache precondition violated: pos beyond the written rows */
+#define L2_ENOMEM (-3)   /* a device or pinned allocation failed */
+#define L2_ECUDA (-4)    /* a CUDA runtime call failed */
+#define L2_EDEVICE (-5)  /* a kernel reported an error through the device error word */
+#define L2_ETIMEOUT (-6) /* a bounded device-side wait gave up */
+
+/* l2_create flags. */
+#define L2_FLAG_DEBUG 0x1u    /* keep per-layer attention probabilities (l2_debug_attention) */
+#define L2_FLAG_NO_GRAPH 0x2u /* launch the step's kernels one by one instead of a CUDA graph */
+#define L2_FLAG_NO_PDL 0x4u   /* no programmatic dependent launch between the step's kernels */
+
+/* Model shape: the pages' Config struct ("run.c", Config; walkthrough §2).
+ * head_size = dim / n_heads, kv_dim = dim * n_kv_heads / n_heads. */
+typedef struct {
+    int dim;        /* transformer width */
+    int hidden_dim; /* FFN width */
+    int n_layers;
+    int n_heads;    /* query heads */
+    int n_kv_heads; /* key/value heads, 1 <= n_kv_heads <= n_heads */
+    int vocab_size;
+    int seq_len;    /* KV-cache capacity in positions */
+} L2Config;
+
+/* Weights: the pages' TransformerWeights (walkthrough §2), fp32, row-major
+ * [out][in], layers stacked first.  All are DEVICE pointers, 16-byte
+ * aligned.  wcls may equal token_embedding_table (a shared classifier). */
+typedef struct {
+    const float *token_embedding_table; /* [vocab_size][dim] */
+    const float *rms_att_weight;        /* [n_layers][dim] */
+    const float *rms_ffn_weight;        /* [n_layers][dim] */
+    const float *wq;                    /* [n_layers][dim][dim] */
+    const float *wk;                    /* [n_layers][kv_dim][dim] */
+    const float *wv;                    /* [n_layers][kv_dim][dim] */
+    const float *wo;                    /* [n_layers][dim][dim] */
+    const float *w1;                    /* [n_layers][hidden_dim][dim] */
+    const float *w2;                    /* [n_layers][dim][hidden_dim] */
+    const float *w3;                    /* [n_layers][hidden_dim][dim] */
+    const float *rms_final_weight;      /* [dim] */
+    const float *wcls;                  /* [vocab_size][dim] */
+} L2Weights;
+
+typedef struct l2_ctx l2_ctx;
+
+/*
+ * Creates a decoder on the current CUDA device.  max_batch (1..64) is the
+ * number of independent sequences ("slots"), each with its own KV cache of
+ * seq_len positions.  cuda_stream is a cudaStream_t (NULL: the library
+ * creates its own stream).  The shape limits of this implementation, on top
+ * of the pages' own (dim % n_heads == 0, even head_size): dim, hidden_dim and
+ * head_size are multiples of 4, head_size <= 128, and at most 8 query heads
+ * share one KV head.  Blocks while it allocates and uploads the RoPE table.
+ * Returns L2_EINVAL, L2_ENOMEM or L2_ECUDA on failure (then *out is NULL).
+ */
+int l2_create(const L2Config *config, const L2Weights *weights, int max_batch, unsigned flags,
+              void *cuda_stream, l2_ctx **out);
+
+/* Rewinds the KV cache of one slot (-1: all slots) to zero written rows.
+ * Host bookkeeping only; no device work.  L2_EINVAL on a bad slot. */
+int l2_reset(l2_ctx *ctx, int slot);
+
+/*
+ * One decode step of slot 0: enqueues forward(token, pos) and writes the
+ * vocab_size logits to logits_out (a DEVICE pointer, or NULL to keep them
+ * only in the handle's buffer, see l2_logits).  Preconditions checked on
+ * the host: 0 <= token < vocab_size, 0 <= pos < seq_len, and pos <= the
+ * number of rows already written to the slot's cache (rows 0..pos-1 must
+ * exist).  After the call the slot holds rows 0..pos; rows beyond pos are
+ * stale.  L2_EINVAL / L2_ESTATE on a failed check (nothing enqueued).
+ */
+int l2_forward(l2_ctx *ctx, int token, int pos, float *logits_out);
+
+/*
+ * One decode step of slots 0..B-1 at once (1 <= B <= max_batch).  tokens and
+ * pos are HOST arrays of B entries; slot b steps tokens[b] at pos[b] under the
+ * same checks as l2_forward.  logits_out is a DEVICE array [B][vocab_size]
+ * or NULL.  Every weight is read once per call for all B sequences.
+ */
+int l2_forward_batch(l2_ctx *ctx, int B, const int *tokens, const int *pos, float *logits_out);
+
+/* l2_forward for callers without device buffers: logits_host is HOST memory
+ * (vocab_size floats).  Blocks until the logits have arrived. */
+int l2_forward_host(l2_ctx *ctx, int token, int pos, float *logits_host);
+
+/* Device pointer to the handle's logits buffer [max_batch][vocab_size],
+ * holding the last step's logits.  NULL on a bad handle. */
+const float *l2_logits(const l2_ctx *ctx);
+
+/* Number of cache rows written for a slot (the next pos it may step), or
+ * L2_EINVAL. */
+int l2_position(const l2_ctx *ctx, int slot);
+
+/*
+ * Attention probabilities of the last step of `slot` at `layer`: the
+ * softmax outputs (not the scores) as a HOST array [n_heads][pos+1], where
+ * pos is that step's position.  Needs L2_FLAG_DEBUG.  Blocks.
+ */
+int l2_debug_attention(l2_ctx *ctx, int slot, int layer, float *att_out);
+
+/*
+ * KV-cache transfer in the pages' layout ([pos][kv_dim] per layer; K after
+ * RoPE).  Both block.
+ * l2_kv_export copies rows 0..n_pos-1 of one layer of a slot into HOST
+ * arrays k_out, v_out [n_pos][kv_dim]; n_pos <= l2_position(slot).
+ * l2_kv_import writes HOST arrays k_in, v_in [n_layers][n_pos][kv_dim] into
+ * rows 0..n_pos-1 of every layer of a slot and sets its position to n_pos.
+ */
+int l2_kv_export(l2_ctx *ctx, int slot, int layer, int n_pos, float *k_out, float *v_out);
+int l2_kv_import(l2_ctx *ctx, int slot, int n_pos, const float *k_in, const float *v_in);
+
+/* Waits for the handle's stream and reports asynchronous failures:
+ * L2_ECUDA for a CUDA error, L2_EDEVICE / L2_ETIMEOUT for a kernel that set
+ * the device error word (the word is cleared).  Blocks. */
+int l2_sync(l2_ctx *ctx);
+
+/* Text of the last failure on this handle ("" if none).  With a NULL
+ * handle, the last failure of l2_create on this thread. */
+const char *l2_last_error(const l2_ctx *ctx);
+
+/* Frees everything the handle owns.  Waits for its stream first. */
+void l2_destroy(l2_ctx *ctx);
+
+/*
+ * Profiling hook: enqueues `count` launches of one kernel of the step,
+ * exactly as the step launches it, for timing it alone.  op: 0 = fused
+ * rmsnorm+QKV+RoPE+KV write, 1 = attention, 2 = Wo+residual, 3 = rmsnorm +
+ * W1/W3 + SwiGLU, 4 = W2+residual, 5 = final rmsnorm + classifier.  Uses
+ * slot 0's last token and position.  It overwrites activations and the
+ * cache row at that position, so re-run the step afterwards if its result
+ * matters.
+ */
+int l2_launch_op(l2_ctx *ctx, int op, int layer, int count);
+
+/* Number of kernel launches one step of batch B enqueues, or L2_EINVAL. */
+int l2_kernels_per_step(const l2_ctx *ctx, int B);
+
+/* Bytes each step copies from host to device (the step's token, position and
+ * output-pointer block). */
+int l2_step_input_bytes(void);
+
+/*
+ * Fault injection for tests: makes the n-th device allocation from now on
+ * (n >= 1) fail as if out of memory; 0 disables.  Process-wide.
+ */
+void l2_debug_fail_alloc_at(int n);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* L2_DECODE_H */

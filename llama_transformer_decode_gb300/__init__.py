@@ -1,0 +1,189 @@
+"""GB300-native llama2.c decode step: Python binding of the C ABI in ``include/l2.h``.
+
+The binding only marshals arguments: every step of forward(token, pos) ->
+logits runs in the CUDA kernels of ``libl2decode.so``.  PyTorch supplies the
+device memory (weights, output buffers) and the stream.  There is no CPU
+fallback: if the library is missing or no GPU is present, calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import numpy as np
+
+from . import _native
+from ._native import EXPORTS, WEIGHT_FIELDS, L2Config, L2Weights, build  # noqa: F401
+
+L2_OK, L2_EINVAL, L2_ESTATE, L2_ENOMEM, L2_ECUDA, L2_EDEVICE, L2_ETIMEOUT = 0, -1, -2, -3, -4, -5, -6
+L2_FLAG_DEBUG, L2_FLAG_NO_GRAPH, L2_FLAG_NO_PDL = 0x1, 0x2, 0x4
+
+OPS = {"qkv": 0, "attention": 1, "wo": 2, "w13": 3, "w2": 4, "cls": 5}
+
+# weight dict key (as in synth / the pages' TransformerWeights) -> C struct field
+_KEYS = {"emb": "token_embedding_table", "rms_att": "rms_att_weight", "rms_ffn": "rms_ffn_weight",
+         "wq": "wq", "wk": "wk", "wv": "wv", "wo": "wo", "w1": "w1", "w2": "w2", "w3": "w3",
+         "rms_final": "rms_final_weight", "wcls": "wcls"}
+
+
+class L2Error(RuntimeError):
+    def __init__(self, code: int, message: str):
+        super().__init__(f"[{code}] {message}")
+        self.code = code
+
+
+def lib():
+    return _native.load()
+
+
+def _ptr(t) -> int:
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("expected a torch tensor")
+    if not t.is_cuda or t.dtype != torch.float32 or not t.is_contiguous():
+        raise ValueError("expected a contiguous float32 CUDA tensor")
+    return t.data_ptr()
+
+
+class Decoder:
+    """One decoder handle (``l2_ctx``).
+
+    ``config``: (dim, hidden_dim, n_layers, n_heads, n_kv_heads, vocab_size, seq_len).
+    ``weights``: dict of contiguous float32 CUDA tensors keyed like
+    ``synth.Workload.tensor_names()``; they are borrowed and kept alive here.
+    ``stream``: a ``torch.cuda.Stream`` (default: a new one).
+    """
+
+    def __init__(self, config, weights: dict, max_batch: int = 1, flags: int = 0, stream=None):
+        import torch
+        self._lib = lib()
+        self.config = tuple(int(v) for v in config)
+        self.dim, self.hidden_dim, self.n_layers, self.n_heads, self.n_kv_heads, self.vocab_size, \
+            self.seq_len = self.config
+        self.kv_dim = self.dim * self.n_kv_heads // self.n_heads
+        self.max_batch = max_batch
+        self.flags = flags
+        self.stream = stream if stream is not None else torch.cuda.Stream()
+        self._weights = dict(weights)
+        w = L2Weights(**{_KEYS[k]: _ptr(v) for k, v in self._weights.items()})
+        cfg = L2Config(*self.config)
+        h = ctypes.c_void_p()
+        rc = self._lib.l2_create(ctypes.byref(cfg), ctypes.byref(w), max_batch, flags,
+                                 ctypes.c_void_p(self.stream.cuda_stream), ctypes.byref(h))
+        if rc != L2_OK:
+            raise L2Error(rc, self._lib.l2_last_error(None).decode())
+        self._h = h
+
+    # -- helpers -------------------------------------------------------------
+    def _check(self, rc: int) -> int:
+        if rc < 0:
+            raise L2Error(rc, self._lib.l2_last_error(self._h).decode())
+        return rc
+
+    @property
+    def handle(self):
+        return self._h
+
+    def close(self):
+        if getattr(self, "_h", None):
+            self._lib.l2_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    # -- API -----------------------------------------------------------------
+    def forward(self, token: int, pos: int, out=None):
+        """Enqueue one step of slot 0; ``out`` is a CUDA tensor of vocab_size floats (or None)."""
+        self._check(self._lib.l2_forward(self._h, int(token), int(pos),
+                                         ctypes.c_void_p(_ptr(out) if out is not None else 0)))
+        return out
+
+    def forward_batch(self, tokens, pos, out=None):
+        toks = np.ascontiguousarray(tokens, dtype=np.int32)
+        ps = np.ascontiguousarray(pos, dtype=np.int32)
+        if toks.size != ps.size:
+            raise ValueError("tokens and pos differ in length")
+        ip = ctypes.POINTER(ctypes.c_int)
+        self._check(self._lib.l2_forward_batch(
+            self._h, int(toks.size), toks.ctypes.data_as(ip), ps.ctypes.data_as(ip),
+            ctypes.c_void_p(_ptr(out) if out is not None else 0)))
+        return out
+
+    def forward_host(self, token: int, pos: int, out: np.ndarray | None = None) -> np.ndarray:
+        """Blocking step of slot 0 returning the logits in host memory."""
+        if out is None:
+            out = np.empty(self.vocab_size, np.float32)
+        assert out.dtype == np.float32 and out.flags.c_contiguous and out.size >= self.vocab_size
+        self._check(self._lib.l2_forward_host(self._h, int(token), int(pos), ctypes.c_void_p(out.ctypes.data)))
+        return out
+
+    def logits_ptr(self) -> int:
+        return int(self._lib.l2_logits(self._h) or 0)
+
+    def reset(self, slot: int = -1):
+        self._check(self._lib.l2_reset(self._h, int(slot)))
+
+    def position(self, slot: int = 0) -> int:
+        return self._check(self._lib.l2_position(self._h, int(slot)))
+
+    def sync(self):
+        self._check(self._lib.l2_sync(self._h))
+
+    def debug_attention(self, layer: int, slot: int = 0) -> np.ndarray:
+        n = self.position(slot)
+        out = np.empty((self.n_heads, n), np.float32)
+        self._check(self._lib.l2_debug_attention(self._h, int(slot), int(layer), ctypes.c_void_p(out.ctypes.data)))
+        return out
+
+    def kv_export(self, layer: int, n_pos: int | None = None, slot: int = 0):
+        n = self.position(slot) if n_pos is None else int(n_pos)
+        k = np.empty((n, self.kv_dim), np.float32)
+        v = np.empty((n, self.kv_dim), np.float32)
+        self._check(self._lib.l2_kv_export(self._h, int(slot), int(layer), n, ctypes.c_void_p(k.ctypes.data),
+                                           ctypes.c_void_p(v.ctypes.data)))
+        return k, v
+
+    def kv_import(self, k: np.ndarray, v: np.ndarray, slot: int = 0):
+        """k, v: (n_layers, n_pos, kv_dim) float32 host arrays."""
+        k = np.ascontiguousarray(k, np.float32)
+        v = np.ascontiguousarray(v, np.float32)
+        assert k.shape == v.shape and k.ndim == 3 and k.shape[0] == self.n_layers and k.shape[2] == self.kv_dim
+        self._check(self._lib.l2_kv_import(self._h, int(slot), int(k.shape[1]), ctypes.c_void_p(k.ctypes.data),
+                                           ctypes.c_void_p(v.ctypes.data)))
+
+    def launch_op(self, op, layer: int = 0, count: int = 1):
+        self._check(self._lib.l2_launch_op(self._h, OPS.get(op, op), int(layer), int(count)))
+
+    def step_input_bytes(self) -> int:
+        return int(self._lib.l2_step_input_bytes())
+
+    def kernels_per_step(self, batch: int = 1) -> int:
+        return self._check(self._lib.l2_kernels_per_step(self._h, int(batch)))
+
+
+def fail_alloc_at(n: int):
+    """Fault injection: the n-th device allocation from now on fails (0 disables)."""
+    lib().l2_debug_fail_alloc_at(int(n))
+
+
+def to_device(weights: dict, device="cuda") -> dict:
+    """Copy host (numpy) weights to contiguous float32 CUDA tensors, keeping a
+    shared classifier shared."""
+    import torch
+    out, seen = {}, {}
+    for k, v in weights.items():
+        if id(v) in seen:
+            out[k] = out[seen[id(v)]]
+            continue
+        seen[id(v)] = k
+        out[k] = torch.from_numpy(np.ascontiguousarray(v, np.float32)).to(device)
+    return out

@@ -1,0 +1,400 @@
+// Fused streaming matrix-vector kernels of the decode step (batch 1).
+//
+// Every weight matmul of llama2.c's forward step ("run.c", matmul(): W (d,n)
+// @ x (n,) -> (d,), rows split across threads) is one launch of gemv_kernel,
+// with the neighbouring elementwise work fused in:
+//   GEMV_QKV   rmsnorm(x) -> Wq|Wk|Wv -> RoPE -> q, and K/V rows written into
+//              the cache (walkthrough §4 forward() steps 2a-2d)
+//   GEMV_RESID x += W v for Wo (step 2f) and W2 (step 2h)
+//   GEMV_W13   rmsnorm(x) -> W1, W3 -> hb = silu(h1) * h3 (steps 2g-2h)
+//   GEMV_CLS   rmsnorm(x) -> logits = Wcls x (step 3)
+//
+// Design.  The kernel is HBM-bound (0.5 flop per weight byte), so it is built
+// around moving the weights at full bandwidth:
+//   - the grid is one CTA per SM; CTA c owns a contiguous, balanced range of
+//     output rows, i.e. one contiguous range of weight memory per matrix;
+//   - that range is split evenly, at 16-byte granularity and regardless of row
+//     boundaries, across the CTA's warps;
+//   - each warp streams its range through a private ring of shared-memory
+//     buffers filled by 1-D bulk async copies (TMA) completing on mbarriers,
+//     so several KB per warp are always in flight;
+//   - lanes read 16-byte words of the weights and of the input vector (held in
+//     shared memory) and accumulate with FMAs; a row finished by one warp is
+//     reduced with shuffles, and a row shared by neighbouring warps is summed
+//     from their partials in warp order, so results are deterministic;
+//   - the weight copies for the first stages are issued before
+//     griddepcontrol.wait, so under programmatic dependent launch they overlap
+//     the tail of the previous kernel.
+#include <cuda_runtime.h>
+
+#include "l2_device.cuh"
+#include "l2_kernels.h"
+
+namespace l2 {
+
+namespace {
+
+struct Piece {
+    const float4 *src;  // first weight word of the piece
+    long long f0;       // offset of the piece in the CTA's word stream
+    int rows;           // whole rows of n floats
+    int yoff;           // local output index of the piece's first row
+};
+
+template <int NW, int STAGES>
+struct GemvFixed {
+    uint64_t bars[NW * STAGES];
+    float head_val[NW];
+    float tail_val[NW];
+    int head_row[NW];
+    int tail_row[NW];
+    float red[NW];
+    float scalar;
+    int npieces;
+    int failed;
+    Piece pieces[3];
+};
+
+__host__ __device__ constexpr size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+template <int NW, int STAGES>
+__host__ __device__ constexpr size_t fixed_bytes() {
+    return align_up(sizeof(GemvFixed<NW, STAGES>), 128);
+}
+
+__device__ __forceinline__ float silu(float v) { return v / (1.0f + expf(-v)); }
+
+}  // namespace
+
+template <int NW, int STAGES, int CH4, int MODE>
+__global__ void __launch_bounds__(NW * 32, 1) gemv_kernel(const GemvParams p) {
+    constexpr int NT = NW * 32;
+    extern __shared__ __align__(128) unsigned char smem[];
+    auto &fx = *reinterpret_cast<GemvFixed<NW, STAGES> *>(smem);
+    float4 *ring = reinterpret_cast<float4 *>(smem + fixed_bytes<NW, STAGES>());
+    const int n4 = p.n >> 2;
+    float4 *xs = ring + NW * STAGES * CH4;
+    float *ys = reinterpret_cast<float *>(xs + n4);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    // ---- this CTA's rows: a balanced share of the units ----
+    const long long u0 = (long long)blockIdx.x * p.total_units / gridDim.x;
+    const long long u1 = (long long)(blockIdx.x + 1) * p.total_units / gridDim.x;
+    const int vr0 = (int)(u0 * p.unit_rows);
+    const int R = (int)((u1 - u0) * p.unit_rows);
+
+    if (tid == 0) {
+        int np = 0;
+        long long f = 0;
+        if (R > 0) {
+            if (MODE == GEMV_QKV) {
+                const float *mats[3] = {p.mat0, p.mat1, p.mat2};
+                const int rws[3] = {p.rows0, p.rows1, p.rows2};
+                int b0 = 0;
+                for (int m = 0; m < 3; ++m) {
+                    int lo = max(vr0, b0), hi = min(vr0 + R, b0 + rws[m]);
+                    if (lo < hi) {
+                        fx.pieces[np] = {reinterpret_cast<const float4 *>(mats[m] + (size_t)(lo - b0) * p.n), f,
+                                         hi - lo, lo - vr0};
+                        f += (long long)(hi - lo) * n4;
+                        ++np;
+                    }
+                    b0 += rws[m];
+                }
+            } else if (MODE == GEMV_W13) {
+                fx.pieces[0] = {reinterpret_cast<const float4 *>(p.mat0 + (size_t)vr0 * p.n), 0, R, 0};
+                fx.pieces[1] = {reinterpret_cast<const float4 *>(p.mat1 + (size_t)vr0 * p.n), (long long)R * n4, R,
+                                R};
+                np = 2;
+            } else {
+                fx.pieces[0] = {reinterpret_cast<const float4 *>(p.mat0 + (size_t)vr0 * p.n), 0, R, 0};
+                np = 1;
+            }
+        }
+        fx.npieces = np;
+        fx.failed = 0;
+        for (int i = 0; i < NW * STAGES; ++i) mbar_init(&fx.bars[i], 1);
+        fence_barrier_init();
+    }
+    if (lane == 0) {
+        fx.head_row[warp] = -1;
+        fx.tail_row[warp] = -1;
+    }
+    __syncthreads();
+
+    const int np = fx.npieces;
+    long long F = 0;
+    for (int i = 0; i < np; ++i) F += (long long)fx.pieces[i].rows * n4;
+    const long long fb = F * warp / NW, fe = F * (warp + 1) / NW;
+
+    // The chunk that starts at word f of the stream: its piece and length.
+    auto chunk_at = [&](long long f, int &pi, int &len) {
+        pi = 0;
+        while (pi + 1 < np && f >= fx.pieces[pi + 1].f0) ++pi;
+        const long long pend = fx.pieces[pi].f0 + (long long)fx.pieces[pi].rows * n4;
+        long long l = fe - f;
+        if (pend - f < l) l = pend - f;
+        if (l > CH4) l = CH4;
+        len = (int)l;
+    };
+
+    const uint64_t pol = policy_evict_first();
+    const bool hint = p.evict_first != 0;
+    uint64_t *bars = &fx.bars[warp * STAGES];
+    float4 *wring = ring + (size_t)warp * STAGES * CH4;
+    long long fi = fb;  // next word to request
+    int n_issued = 0;   // chunks requested so far
+    auto issue = [&](int stage) {
+        int pi, len;
+        chunk_at(fi, pi, len);
+        if (lane == 0) {
+            const Piece &pc = fx.pieces[pi];
+            mbar_arrive_expect_tx(&bars[stage], (uint32_t)len * 16u);
+            if (hint)
+                bulk_g2s(wring + (size_t)stage * CH4, pc.src + (fi - pc.f0), (uint32_t)len * 16u, &bars[stage], pol);
+            else
+                bulk_g2s_nohint(wring + (size_t)stage * CH4, pc.src + (fi - pc.f0), (uint32_t)len * 16u, &bars[stage]);
+        }
+        fi += len;
+        ++n_issued;
+    };
+
+    // Weights do not depend on the previous kernel: start streaming them now.
+#pragma unroll 1
+    for (int s = 0; s < STAGES && fi < fe; ++s) issue(s);
+
+    pdl_launch_dependents();
+    pdl_wait();
+
+    // ---- input vector into shared memory (with RMSNorm where the mode has one) ----
+    if (MODE == GEMV_RESID) {
+        const float4 *in4 = reinterpret_cast<const float4 *>(p.in_vec);
+        for (int i = tid; i < n4; i += NT) xs[i] = in4[i];
+    } else {
+        const float *src = p.x;
+        if (MODE == GEMV_QKV && p.layer == 0) src = p.emb + (size_t)p.step->token[0] * p.dim;
+        const float4 *s4 = reinterpret_cast<const float4 *>(src);
+        float ss = 0.f;
+        for (int i = tid; i < n4; i += NT) {
+            float4 v = s4[i];
+            xs[i] = v;
+            ss = fmaf(v.x, v.x, ss);
+            ss = fmaf(v.y, v.y, ss);
+            ss = fmaf(v.z, v.z, ss);
+            ss = fmaf(v.w, v.w, ss);
+        }
+        if (MODE == GEMV_QKV && p.layer == 0 && blockIdx.x == 0) {
+            float4 *x4 = reinterpret_cast<float4 *>(p.x);
+            for (int i = tid; i < n4; i += NT) x4[i] = s4[i];
+        }
+        ss = warp_sum(ss);
+        if (lane == 0) fx.red[warp] = ss;
+        __syncthreads();
+        if (tid == 0) {
+            float t = 0.f;
+            for (int w = 0; w < NW; ++w) t += fx.red[w];
+            fx.scalar = 1.0f / sqrtf(t / (float)p.n + 1e-5f);
+        }
+        __syncthreads();
+        const float inv = fx.scalar;
+        const float4 *g4 = reinterpret_cast<const float4 *>(p.norm_w);
+        for (int i = tid; i < n4; i += NT) {
+            float4 v = xs[i], g = g4[i];
+            xs[i] = make_float4(g.x * (inv * v.x), g.y * (inv * v.y), g.z * (inv * v.z), g.w * (inv * v.w));
+        }
+    }
+    __syncthreads();
+
+    // ---- stream this warp's weight words ----
+    float acc = 0.f;
+    bool started = false;  // this warp began the current row at its first word
+    bool pending = false;  // acc holds words of a row not yet deposited
+    int cur_row = -1;
+    long long fc = fb;
+    // Row walk state within the current piece: row r spans local words [rs, re).
+    int cpi = -1, r = 0, rs = 0, re = 0;
+    bool ok = true;
+    int k = 0;
+#pragma unroll 1
+    for (; fc < fe; ++k) {
+        const int s = k % STAGES;
+        int pi, len;
+        chunk_at(fc, pi, len);
+        if (!mbar_wait(&bars[s], (uint32_t)(k / STAGES) & 1u, p.err)) {
+            ok = false;
+            break;
+        }
+        const Piece &pc = fx.pieces[pi];
+        const float4 *buf = wring + (size_t)s * CH4;
+        const int lf = (int)(fc - pc.f0), lend = lf + len;
+        if (pi != cpi) {
+            cpi = pi;
+            r = lf / n4;
+            rs = r * n4;
+            re = rs + n4;
+        }
+        int a = lf;
+        while (a < lend) {
+            if (a == re) {
+                ++r;
+                rs = re;
+                re += n4;
+            }
+            const int b = lend < re ? lend : re;
+            if (a == rs) started = true;
+            cur_row = pc.yoff + r;
+            const float4 *wr = buf + (a - lf);
+            const float4 *xr = xs + (a - rs);
+            const int cnt = b - a;
+#pragma unroll 4
+            for (int i = lane; i < cnt; i += 32) acc = dot4(wr[i], xr[i], acc);
+            pending = true;
+            if (b == re) {
+                const float v = warp_sum(acc);
+                if (lane == 0) {
+                    if (started) {
+                        ys[cur_row] = v;
+                    } else {
+                        fx.head_row[warp] = cur_row;
+                        fx.head_val[warp] = v;
+                    }
+                }
+                acc = 0.f;
+                pending = false;
+                started = true;
+            }
+            a = b;
+        }
+        __syncwarp();
+        fc += len;
+        if (fi < fe) {
+            if (lane == 0) fence_proxy_async_smem();
+            issue(s);
+        }
+    }
+    if (!ok) {
+        // Let the copies still in flight land before the CTA's memory is released;
+        // the CTA then skips its epilogue (the host sees the device error word).
+        for (int j = k + 1; j < n_issued; ++j) (void)mbar_wait(&bars[j % STAGES], (uint32_t)(j / STAGES) & 1u, p.err);
+        if (lane == 0) fx.failed = 1;
+        pending = false;
+    }
+    if (pending) {
+        const float v = warp_sum(acc);
+        if (lane == 0) {
+            if (started) {
+                fx.tail_row[warp] = cur_row;
+                fx.tail_val[warp] = v;
+            } else {
+                fx.head_row[warp] = cur_row;
+                fx.head_val[warp] = v;
+            }
+        }
+    }
+    __syncthreads();
+    if (fx.failed) return;
+    if (tid == 0) {
+        for (int w = 0; w < NW; ++w) {
+            if (fx.head_row[w] >= 0) ys[fx.head_row[w]] += fx.head_val[w];
+            if (fx.tail_row[w] >= 0) ys[fx.tail_row[w]] = fx.tail_val[w];
+        }
+    }
+    __syncthreads();
+
+    // ---- epilogue ----
+    if (MODE == GEMV_QKV) {
+        const int pos = p.step->pos[0];
+        const int hs = p.head_size, half = hs >> 1;
+        const float2 *rr = p.rope + (size_t)pos * half;
+        for (int i = tid; i < (R >> 1); i += NT) {
+            const int j = 2 * i, v = vr0 + j;
+            const float y0 = ys[j], y1 = ys[j + 1];
+            if (v < p.dim) {
+                const float2 cs = rr[(v % hs) >> 1];
+                p.q[v] = y0 * cs.x - y1 * cs.y;
+                p.q[v + 1] = y0 * cs.y + y1 * cs.x;
+            } else {
+                const bool is_k = v < p.dim + p.kv_dim;
+                const int c = is_k ? v - p.dim : v - p.dim - p.kv_dim;
+                const int g = c / hs, d = c % hs;
+                const size_t idx = (((size_t)p.layer * p.n_kv_heads + g) * p.seq_len + pos) * hs + d;
+                if (is_k) {
+                    const float2 cs = rr[d >> 1];
+                    p.kcache[idx] = y0 * cs.x - y1 * cs.y;
+                    p.kcache[idx + 1] = y0 * cs.y + y1 * cs.x;
+                } else {
+                    p.vcache[idx] = y0;
+                    p.vcache[idx + 1] = y1;
+                }
+            }
+        }
+    } else if (MODE == GEMV_RESID) {
+        for (int j = tid; j < R; j += NT) p.x[vr0 + j] += ys[j];
+    } else if (MODE == GEMV_W13) {
+        for (int j = tid; j < R; j += NT) p.hb[vr0 + j] = silu(ys[j]) * ys[R + j];
+    } else {
+        float *user = p.step->logits_out;
+        for (int j = tid; j < R; j += NT) {
+            p.logits[vr0 + j] = ys[j];
+            if (user) user[vr0 + j] = ys[j];
+        }
+    }
+}
+
+// ---------------------------------------------------------------- host side
+
+namespace {
+constexpr int kNW = 8, kStages = 4, kCH4 = 128;  // 8 warps, 4 x 2 KB buffers per warp
+
+template <int MODE>
+cudaError_t set_attr() {
+    return cudaFuncSetAttribute(gemv_kernel<kNW, kStages, kCH4, MODE>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+}
+
+template <int MODE>
+void *kernel_ptr() {
+    return reinterpret_cast<void *>(gemv_kernel<kNW, kStages, kCH4, MODE>);
+}
+}  // namespace
+
+int gemv_threads() { return kNW * 32; }
+
+size_t gemv_smem_bytes(int n, int ymax) {
+    return fixed_bytes<kNW, kStages>() + (size_t)kNW * kStages * kCH4 * 16 + (size_t)n * 4 +
+           align_up((size_t)ymax * 4, 16);
+}
+
+cudaError_t gemv_init() {
+    cudaError_t e;
+    if ((e = set_attr<GEMV_QKV>()) != cudaSuccess) return e;
+    if ((e = set_attr<GEMV_RESID>()) != cudaSuccess) return e;
+    if ((e = set_attr<GEMV_W13>()) != cudaSuccess) return e;
+    return set_attr<GEMV_CLS>();
+}
+
+cudaError_t launch_gemv(int mode, const GemvParams &p, int grid, size_t smem, cudaStream_t stream, bool pdl) {
+    void *fn = nullptr;
+    switch (mode) {
+        case GEMV_QKV: fn = kernel_ptr<GEMV_QKV>(); break;
+        case GEMV_RESID: fn = kernel_ptr<GEMV_RESID>(); break;
+        case GEMV_W13: fn = kernel_ptr<GEMV_W13>(); break;
+        case GEMV_CLS: fn = kernel_ptr<GEMV_CLS>(); break;
+        default: return cudaErrorInvalidValue;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kNW * 32);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    void *args[] = {const_cast<GemvParams *>(&p)};
+    return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
+}  // namespace l2

@@ -1,0 +1,639 @@
+// Host side of the C ABI declared in include/l2.h: argument checks, device
+// memory, the per-step orchestration and its CUDA graphs.
+//
+// One step of batch B is 5 * n_layers + 1 kernel launches (per layer: fused
+// rmsnorm+QKV+RoPE+KV write, attention, Wo+residual, rmsnorm+W1/W3+SwiGLU,
+// W2+residual; then the final rmsnorm+classifier), linked by programmatic
+// dependent launch.  They are captured once per batch size into a CUDA graph
+// and replayed.  The step's inputs (tokens, positions, output pointer) are
+// not baked into the graph: each call writes them into a pinned ring slot and
+// copies them to a device struct that every kernel reads, so one graph serves
+// every position.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstddef>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "../../include/l2.h"
+#include "l2_kernels.h"
+#include "l2_params.h"
+
+using namespace l2;
+
+namespace {
+
+constexpr int kRing = 64;      // pinned step-input slots in flight
+constexpr int kMinChunk = 32;  // fewest cache positions per attention CTA
+
+thread_local std::string g_create_error;
+int g_fail_alloc_at = 0;  // fault injection: fail the n-th device allocation
+
+struct GemvPlan {
+    int mode;
+    int grid;
+    size_t smem;
+    GemvParams base;  // layer-independent fields
+};
+
+}  // namespace
+
+struct l2_ctx {
+    L2Config cfg{};
+    L2Weights w{};
+    int max_batch = 1;
+    unsigned flags = 0;
+    int device = 0, num_sms = 0;
+    int head_size = 0, kv_dim = 0;
+    cudaStream_t stream = nullptr, cap_stream = nullptr;
+    bool own_stream = false;
+
+    std::vector<void *> dev_allocs;
+    float *x = nullptr, *xb = nullptr, *q = nullptr, *hb = nullptr, *logits = nullptr;
+    float *kcache = nullptr, *vcache = nullptr, *ws_ml = nullptr, *ws_acc = nullptr, *dbg = nullptr;
+    unsigned *tickets = nullptr;
+    float2 *rope = nullptr;
+    StepDev *step_dev = nullptr;
+    int *err = nullptr;
+
+    StepDev *step_host = nullptr;  // pinned ring
+    cudaEvent_t ring_ev[kRing] = {};
+    bool ring_used[kRing] = {};
+    int ring_next = 0;
+
+    cudaGraphExec_t graph[kMaxBatch + 1] = {};
+
+    AttnLaunch attn{};
+    int attn_chunks = 1;
+    GemvPlan plan_qkv{}, plan_wo{}, plan_w13{}, plan_w2{}, plan_cls{};
+    bool evict_first = false;
+
+    std::vector<int> written;  // cache rows written per slot
+    std::string error;
+};
+
+namespace {
+
+int fail(l2_ctx *c, int code, const char *fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    if (c)
+        c->error = buf;
+    else
+        g_create_error = buf;
+    return code;
+}
+
+int cuda_fail(l2_ctx *c, cudaError_t e, const char *what) {
+    return fail(c, L2_ECUDA, "%s: %s (%s)", what, cudaGetErrorString(e), cudaGetErrorName(e));
+}
+
+#define L2_CUDA(ctx, call)                                      \
+    do {                                                        \
+        cudaError_t e_ = (call);                                \
+        if (e_ != cudaSuccess) return cuda_fail(ctx, e_, #call); \
+    } while (0)
+
+int dev_alloc(l2_ctx *c, void **p, size_t bytes, const char *what) {
+    *p = nullptr;
+    if (g_fail_alloc_at > 0 && --g_fail_alloc_at == 0)
+        return fail(c, L2_ENOMEM, "allocation of %s (%zu bytes) failed (injected)", what, bytes);
+    if (bytes == 0) bytes = 16;
+    cudaError_t e = cudaMalloc(p, bytes);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        *p = nullptr;
+        return fail(c, L2_ENOMEM, "cudaMalloc of %s (%zu bytes) failed: %s", what, bytes, cudaGetErrorString(e));
+    }
+    c->dev_allocs.push_back(*p);
+    return L2_OK;
+}
+
+template <typename T>
+int alloc_n(l2_ctx *c, T **p, size_t n, const char *what) {
+    return dev_alloc(c, reinterpret_cast<void **>(p), n * sizeof(T), what);
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+void free_all(l2_ctx *c) {
+    if (c->stream) cudaStreamSynchronize(c->stream);
+    for (auto &g : c->graph)
+        if (g) {
+            cudaGraphExecDestroy(g);
+            g = nullptr;
+        }
+    for (auto &e : c->ring_ev)
+        if (e) {
+            cudaEventDestroy(e);
+            e = nullptr;
+        }
+    for (void *p : c->dev_allocs) cudaFree(p);
+    c->dev_allocs.clear();
+    if (c->step_host) cudaFreeHost(c->step_host);
+    c->step_host = nullptr;
+    if (c->cap_stream) cudaStreamDestroy(c->cap_stream);
+    c->cap_stream = nullptr;
+    if (c->own_stream && c->stream) cudaStreamDestroy(c->stream);
+    c->stream = nullptr;
+}
+
+int check_config(const L2Config &p) {
+    if (p.dim <= 0 || p.hidden_dim <= 0 || p.n_layers <= 0 || p.n_heads <= 0 || p.n_kv_heads <= 0 ||
+        p.vocab_size <= 0 || p.seq_len <= 0)
+        return fail(nullptr, L2_EINVAL, "every Config field must be positive");
+    if (p.dim % p.n_heads) return fail(nullptr, L2_EINVAL, "dim (%d) must be a multiple of n_heads (%d)", p.dim, p.n_heads);
+    if (p.n_kv_heads > p.n_heads)
+        return fail(nullptr, L2_EINVAL, "n_kv_heads (%d) exceeds n_heads (%d)", p.n_kv_heads, p.n_heads);
+    const int hs = p.dim / p.n_heads;
+    if (hs % 2) return fail(nullptr, L2_EINVAL, "head_size (%d) must be even for RoPE pairs", hs);
+    if ((long long)p.dim * p.n_kv_heads % p.n_heads)
+        return fail(nullptr, L2_EINVAL, "dim * n_kv_heads must be a multiple of n_heads");
+    if (p.dim % 4 || p.hidden_dim % 4 || hs % 4)
+        return fail(nullptr, L2_EINVAL, "this implementation needs dim, hidden_dim and head_size to be multiples of 4");
+    if (hs > 128) return fail(nullptr, L2_EINVAL, "this implementation supports head_size <= 128 (got %d)", hs);
+    if ((p.n_heads + p.n_kv_heads - 1) / p.n_kv_heads > 8)
+        return fail(nullptr, L2_EINVAL, "this implementation supports at most 8 query heads per KV head");
+    return L2_OK;
+}
+
+int check_weights(const L2Weights &w) {
+    const float *ptrs[] = {w.token_embedding_table, w.rms_att_weight, w.rms_ffn_weight, w.wq, w.wk, w.wv,
+                           w.wo,                    w.w1,           w.w2,           w.w3, w.rms_final_weight, w.wcls};
+    for (const float *p : ptrs) {
+        if (!p) return fail(nullptr, L2_EINVAL, "a weight pointer is NULL");
+        if (!aligned16(p)) return fail(nullptr, L2_EINVAL, "weight pointers must be 16-byte aligned");
+        cudaPointerAttributes a{};
+        if (cudaPointerGetAttributes(&a, p) != cudaSuccess || a.type != cudaMemoryTypeDevice) {
+            cudaGetLastError();
+            return fail(nullptr, L2_EINVAL, "weight pointers must be device memory");
+        }
+    }
+    return L2_OK;
+}
+
+int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
+
+void make_plans(l2_ctx *c) {
+    const L2Config &p = c->cfg;
+    const int G = c->num_sms;
+    auto plan = [&](GemvPlan &pl, int mode, int n, int unit_rows, int units, int ymax_factor) {
+        pl.mode = mode;
+        pl.grid = units < G ? units : G;
+        const int per = ceil_div(units, pl.grid);
+        pl.smem = gemv_smem_bytes(n, per * unit_rows * ymax_factor);
+        GemvParams &b = pl.base;
+        memset(&b, 0, sizeof(b));
+        b.n = n;
+        b.unit_rows = unit_rows;
+        b.total_units = units;
+        b.emb = c->w.token_embedding_table;
+        b.x = c->x;
+        b.q = c->q;
+        b.kcache = c->kcache;
+        b.vcache = c->vcache;
+        b.rope = c->rope;
+        b.hb = c->hb;
+        b.logits = c->logits;
+        b.step = c->step_dev;
+        b.err = c->err;
+        b.dim = p.dim;
+        b.kv_dim = c->kv_dim;
+        b.head_size = c->head_size;
+        b.seq_len = p.seq_len;
+        b.n_kv_heads = p.n_kv_heads;
+        b.n_layers = p.n_layers;
+        b.vocab = p.vocab_size;
+        b.evict_first = c->evict_first ? 1 : 0;
+    };
+    plan(c->plan_qkv, GEMV_QKV, p.dim, 2, (p.dim + 2 * c->kv_dim) / 2, 1);
+    plan(c->plan_wo, GEMV_RESID, p.dim, 1, p.dim, 1);
+    plan(c->plan_w13, GEMV_W13, p.dim, 1, p.hidden_dim, 2);
+    plan(c->plan_w2, GEMV_RESID, p.hidden_dim, 1, p.dim, 1);
+    plan(c->plan_cls, GEMV_CLS, p.dim, 1, p.vocab_size, 1);
+    c->plan_qkv.base.rows0 = p.dim;
+    c->plan_qkv.base.rows1 = c->kv_dim;
+    c->plan_qkv.base.rows2 = c->kv_dim;
+    c->plan_wo.base.in_vec = c->xb;
+    c->plan_w2.base.in_vec = c->hb;
+    c->plan_cls.base.mat0 = c->w.wcls;
+    c->plan_cls.base.norm_w = c->w.rms_final_weight;
+}
+
+GemvParams layer_params(const l2_ctx *c, const GemvPlan &pl, int layer) {
+    const L2Config &p = c->cfg;
+    GemvParams g = pl.base;
+    g.layer = layer;
+    const size_t l = (size_t)layer;
+    const size_t dd = (size_t)p.dim * p.dim, kd = (size_t)c->kv_dim * p.dim, hd = (size_t)p.hidden_dim * p.dim;
+    if (&pl == &c->plan_qkv) {
+        g.mat0 = c->w.wq + l * dd;
+        g.mat1 = c->w.wk + l * kd;
+        g.mat2 = c->w.wv + l * kd;
+        g.norm_w = c->w.rms_att_weight + l * p.dim;
+    } else if (&pl == &c->plan_wo) {
+        g.mat0 = c->w.wo + l * dd;
+    } else if (&pl == &c->plan_w13) {
+        g.mat0 = c->w.w1 + l * hd;
+        g.mat1 = c->w.w3 + l * hd;
+        g.norm_w = c->w.rms_ffn_weight + l * p.dim;
+    } else if (&pl == &c->plan_w2) {
+        g.mat0 = c->w.w2 + l * hd;
+    }
+    return g;
+}
+
+AttnParams attn_params(const l2_ctx *c, int layer, int batch) {
+    const L2Config &p = c->cfg;
+    AttnParams a{};
+    a.q = c->q;
+    a.kcache = c->kcache;
+    a.vcache = c->vcache;
+    a.out = c->xb;
+    a.ws_ml = c->ws_ml;
+    a.ws_acc = c->ws_acc;
+    a.tickets = c->tickets;
+    a.dbg = c->dbg;
+    a.step = c->step_dev;
+    a.err = c->err;
+    a.layer = layer;
+    a.n_layers = p.n_layers;
+    a.n_heads = p.n_heads;
+    a.n_kv_heads = p.n_kv_heads;
+    a.head_size = c->head_size;
+    a.seq_len = p.seq_len;
+    a.dim = p.dim;
+    int nc = ceil_div(2LL * c->num_sms, (long long)p.n_kv_heads * batch);
+    const int cap = ceil_div(p.seq_len, kMinChunk);
+    if (nc > cap) nc = cap;
+    if (nc > c->attn_chunks) nc = c->attn_chunks;
+    if (nc < 1) nc = 1;
+    a.n_chunks = nc;
+    a.min_chunk = kMinChunk;
+    a.scale = (float)(1.0 / std::sqrt((double)c->head_size));
+    return a;
+}
+
+cudaError_t launch_op(l2_ctx *c, int op, int layer, int batch, cudaStream_t s, bool pdl) {
+    switch (op) {
+        case 0: {
+            GemvParams g = layer_params(c, c->plan_qkv, layer);
+            return launch_gemv(GEMV_QKV, g, c->plan_qkv.grid, c->plan_qkv.smem, s, pdl);
+        }
+        case 1: {
+            AttnParams a = attn_params(c, layer, batch);
+            return launch_attn(c->attn, a, batch, s, pdl);
+        }
+        case 2: {
+            GemvParams g = layer_params(c, c->plan_wo, layer);
+            return launch_gemv(GEMV_RESID, g, c->plan_wo.grid, c->plan_wo.smem, s, pdl);
+        }
+        case 3: {
+            GemvParams g = layer_params(c, c->plan_w13, layer);
+            return launch_gemv(GEMV_W13, g, c->plan_w13.grid, c->plan_w13.smem, s, pdl);
+        }
+        case 4: {
+            GemvParams g = layer_params(c, c->plan_w2, layer);
+            return launch_gemv(GEMV_RESID, g, c->plan_w2.grid, c->plan_w2.smem, s, pdl);
+        }
+        case 5: {
+            GemvParams g = layer_params(c, c->plan_cls, 0);
+            return launch_gemv(GEMV_CLS, g, c->plan_cls.grid, c->plan_cls.smem, s, pdl);
+        }
+    }
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t enqueue_step(l2_ctx *c, int batch, cudaStream_t s) {
+    const bool pdl = !(c->flags & L2_FLAG_NO_PDL);
+    cudaError_t e;
+    for (int l = 0; l < c->cfg.n_layers; ++l)
+        for (int op = 0; op < 5; ++op)
+            if ((e = launch_op(c, op, l, batch, s, pdl)) != cudaSuccess) return e;
+    return launch_op(c, 5, 0, batch, s, pdl);
+}
+
+int get_graph(l2_ctx *c, int batch, cudaGraphExec_t *out) {
+    if (c->graph[batch]) {
+        *out = c->graph[batch];
+        return L2_OK;
+    }
+    cudaGraph_t g = nullptr;
+    L2_CUDA(c, cudaStreamBeginCapture(c->cap_stream, cudaStreamCaptureModeThreadLocal));
+    cudaError_t e = enqueue_step(c, batch, c->cap_stream);
+    cudaError_t e2 = cudaStreamEndCapture(c->cap_stream, &g);
+    if (e != cudaSuccess) {
+        if (g) cudaGraphDestroy(g);
+        return cuda_fail(c, e, "kernel launch during graph capture");
+    }
+    if (e2 != cudaSuccess) return cuda_fail(c, e2, "cudaStreamEndCapture");
+    cudaGraphExec_t ex = nullptr;
+    e = cudaGraphInstantiate(&ex, g, 0);
+    cudaGraphDestroy(g);
+    if (e != cudaSuccess) return cuda_fail(c, e, "cudaGraphInstantiate");
+    c->graph[batch] = ex;
+    *out = ex;
+    return L2_OK;
+}
+
+int submit(l2_ctx *c, int B, const int *tokens, const int *pos, float *logits_out) {
+    if (B < 1 || B > c->max_batch) return fail(c, L2_EINVAL, "batch %d outside 1..%d", B, c->max_batch);
+    if (B > 1) return fail(c, L2_EINVAL, "batches of more than one sequence are not supported by this build");
+    for (int b = 0; b < B; ++b) {
+        if (tokens[b] < 0 || tokens[b] >= c->cfg.vocab_size)
+            return fail(c, L2_EINVAL, "token %d of slot %d outside [0, %d)", tokens[b], b, c->cfg.vocab_size);
+        if (pos[b] < 0 || pos[b] >= c->cfg.seq_len)
+            return fail(c, L2_EINVAL, "pos %d of slot %d outside [0, %d)", pos[b], b, c->cfg.seq_len);
+        if (pos[b] > c->written[b])
+            return fail(c, L2_ESTATE, "pos %d of slot %d skips cache rows (only %d written)", pos[b], b, c->written[b]);
+    }
+    if (logits_out && !aligned16(logits_out)) return fail(c, L2_EINVAL, "logits_out must be 16-byte aligned");
+
+    const int i = c->ring_next;
+    c->ring_next = (i + 1) % kRing;
+    if (c->ring_used[i]) L2_CUDA(c, cudaEventSynchronize(c->ring_ev[i]));
+    StepDev &sh = c->step_host[i];
+    for (int b = 0; b < B; ++b) {
+        sh.token[b] = tokens[b];
+        sh.pos[b] = pos[b];
+    }
+    sh.logits_out = logits_out;
+    sh.B = B;
+    L2_CUDA(c, cudaMemcpyAsync(c->step_dev, &sh, sizeof(StepDev), cudaMemcpyHostToDevice, c->stream));
+    L2_CUDA(c, cudaEventRecord(c->ring_ev[i], c->stream));
+    c->ring_used[i] = true;
+
+    if (c->flags & L2_FLAG_NO_GRAPH) {
+        L2_CUDA(c, enqueue_step(c, B, c->stream));
+    } else {
+        cudaGraphExec_t g = nullptr;
+        int rc = get_graph(c, B, &g);
+        if (rc != L2_OK) return rc;
+        L2_CUDA(c, cudaGraphLaunch(g, c->stream));
+    }
+    for (int b = 0; b < B; ++b) c->written[b] = pos[b] + 1;
+    return L2_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int l2_create(const L2Config *config, const L2Weights *weights, int max_batch, unsigned flags, void *cuda_stream,
+              l2_ctx **out) {
+    g_create_error.clear();
+    if (!out) return fail(nullptr, L2_EINVAL, "out is NULL");
+    *out = nullptr;
+    if (!config || !weights) return fail(nullptr, L2_EINVAL, "config and weights must not be NULL");
+    if (max_batch < 1 || max_batch > kMaxBatch)
+        return fail(nullptr, L2_EINVAL, "max_batch %d outside 1..%d", max_batch, kMaxBatch);
+    if (flags & ~(L2_FLAG_DEBUG | L2_FLAG_NO_GRAPH | L2_FLAG_NO_PDL))
+        return fail(nullptr, L2_EINVAL, "unknown flags 0x%x", flags);
+    int rc = check_config(*config);
+    if (rc) return rc;
+    rc = check_weights(*weights);
+    if (rc) return rc;
+
+    l2_ctx *c = new l2_ctx();
+    c->cfg = *config;
+    c->w = *weights;
+    c->max_batch = max_batch;
+    c->flags = flags;
+    const L2Config &p = c->cfg;
+    c->head_size = p.dim / p.n_heads;
+    c->kv_dim = p.dim * p.n_kv_heads / p.n_heads;
+    c->written.assign(max_batch, 0);
+
+    auto bail = [&](int code) {
+        g_create_error = c->error;
+        free_all(c);
+        delete c;
+        return code;
+    };
+#define CREATE_CUDA(call)                                 \
+    do {                                                  \
+        cudaError_t e_ = (call);                          \
+        if (e_ != cudaSuccess) return bail(cuda_fail(c, e_, #call)); \
+    } while (0)
+
+    CREATE_CUDA(cudaGetDevice(&c->device));
+    CREATE_CUDA(cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device));
+    int l2_bytes = 0;
+    CREATE_CUDA(cudaDeviceGetAttribute(&l2_bytes, cudaDevAttrL2CacheSize, c->device));
+    c->attn = attn_plan(c->head_size, p.n_heads, p.n_kv_heads);
+    if (!c->attn.ok) return bail(fail(c, L2_EINVAL, "unsupported head_size / GQA grouping"));
+    CREATE_CUDA(gemv_init());
+    CREATE_CUDA(attn_init());
+
+    if (cuda_stream) {
+        c->stream = static_cast<cudaStream_t>(cuda_stream);
+    } else {
+        CREATE_CUDA(cudaStreamCreateWithFlags(&c->stream, cudaStreamNonBlocking));
+        c->own_stream = true;
+    }
+    CREATE_CUDA(cudaStreamCreateWithFlags(&c->cap_stream, cudaStreamNonBlocking));
+
+    const size_t B = (size_t)max_batch, L = p.n_layers, S = p.seq_len, hs = c->head_size;
+    const size_t cache = B * L * p.n_kv_heads * S * hs;
+    c->attn_chunks = 1;
+    {
+        int nc = ceil_div(2LL * c->num_sms, p.n_kv_heads);
+        const int cap = ceil_div(p.seq_len, kMinChunk);
+        c->attn_chunks = nc < cap ? nc : cap;
+        if (c->attn_chunks < 1) c->attn_chunks = 1;
+    }
+    const size_t ws = B * p.n_heads * (size_t)c->attn_chunks;
+    if ((rc = alloc_n(c, &c->x, B * p.dim, "x")) || (rc = alloc_n(c, &c->xb, B * p.dim, "xb")) ||
+        (rc = alloc_n(c, &c->q, B * p.dim, "q")) || (rc = alloc_n(c, &c->hb, B * p.hidden_dim, "hb")) ||
+        (rc = alloc_n(c, &c->logits, B * p.vocab_size, "logits")) || (rc = alloc_n(c, &c->kcache, cache, "key cache")) ||
+        (rc = alloc_n(c, &c->vcache, cache, "value cache")) || (rc = alloc_n(c, &c->ws_ml, ws * 2, "attention workspace")) ||
+        (rc = alloc_n(c, &c->ws_acc, ws * hs, "attention workspace")) ||
+        (rc = alloc_n(c, &c->tickets, B * p.n_kv_heads, "attention tickets")) ||
+        (rc = alloc_n(c, &c->rope, S * (hs / 2), "RoPE table")) || (rc = alloc_n(c, &c->step_dev, 1, "step inputs")) ||
+        (rc = alloc_n(c, &c->err, 1, "error word")))
+        return bail(rc);
+    if (flags & L2_FLAG_DEBUG) {
+        if ((rc = alloc_n(c, &c->dbg, B * L * p.n_heads * S, "attention probabilities"))) return bail(rc);
+        CREATE_CUDA(cudaMemset(c->dbg, 0, B * L * p.n_heads * S * sizeof(float)));
+    }
+    CREATE_CUDA(cudaMemset(c->tickets, 0, B * p.n_kv_heads * sizeof(unsigned)));
+    CREATE_CUDA(cudaMemset(c->err, 0, sizeof(int)));
+    CREATE_CUDA(cudaMemset(c->kcache, 0, cache * sizeof(float)));
+    CREATE_CUDA(cudaMemset(c->vcache, 0, cache * sizeof(float)));
+    CREATE_CUDA(cudaMemset(c->x, 0, B * p.dim * sizeof(float)));
+    CREATE_CUDA(cudaMemset(c->step_dev, 0, sizeof(StepDev)));
+
+    // RoPE table: theta = pos * 10000^(-2j/head_size) for pair j of a head,
+    // evaluated in double and rounded once to fp32.
+    {
+        std::vector<float2> tab(S * (hs / 2));
+        for (size_t t = 0; t < S; ++t)
+            for (size_t j = 0; j < hs / 2; ++j) {
+                const double inv_freq = std::pow(10000.0, -(double)(2 * j) / (double)hs);
+                const double th = (double)t * inv_freq;
+                tab[t * (hs / 2) + j] = make_float2((float)std::cos(th), (float)std::sin(th));
+            }
+        CREATE_CUDA(cudaMemcpy(c->rope, tab.data(), tab.size() * sizeof(float2), cudaMemcpyHostToDevice));
+    }
+    CREATE_CUDA(cudaMallocHost(reinterpret_cast<void **>(&c->step_host), sizeof(StepDev) * kRing));
+    memset(c->step_host, 0, sizeof(StepDev) * kRing);
+    for (auto &e : c->ring_ev) CREATE_CUDA(cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
+
+    // Stream the weights with an evict-first L2 hint only when they cannot stay
+    // resident in L2 between steps anyway.
+    const double wbytes = 4.0 * ((double)L * (2.0 * p.dim * p.dim + 2.0 * c->kv_dim * p.dim + 3.0 * p.dim * p.hidden_dim) +
+                                 (double)p.vocab_size * p.dim);
+    c->evict_first = wbytes > 0.75 * (double)l2_bytes;
+    make_plans(c);
+    for (const GemvPlan *pl : {&c->plan_qkv, &c->plan_wo, &c->plan_w13, &c->plan_w2, &c->plan_cls})
+        if (pl->smem > 227 * 1024)
+            return bail(fail(c, L2_EINVAL, "a GEMV stage needs %zu bytes of shared memory (> 227 KB); dim or hidden_dim too large",
+                             pl->smem));
+    if (c->attn.smem > 227 * 1024) return bail(fail(c, L2_EINVAL, "attention needs too much shared memory"));
+    CREATE_CUDA(cudaDeviceSynchronize());
+#undef CREATE_CUDA
+    *out = c;
+    return L2_OK;
+}
+
+int l2_reset(l2_ctx *c, int slot) {
+    if (!c) return L2_EINVAL;
+    if (slot < -1 || slot >= c->max_batch) return fail(c, L2_EINVAL, "slot %d outside -1..%d", slot, c->max_batch - 1);
+    if (slot < 0)
+        for (int &w : c->written) w = 0;
+    else
+        c->written[slot] = 0;
+    return L2_OK;
+}
+
+int l2_forward(l2_ctx *c, int token, int pos, float *logits_out) {
+    if (!c) return L2_EINVAL;
+    return submit(c, 1, &token, &pos, logits_out);
+}
+
+int l2_forward_batch(l2_ctx *c, int B, const int *tokens, const int *pos, float *logits_out) {
+    if (!c) return L2_EINVAL;
+    if (!tokens || !pos) return fail(c, L2_EINVAL, "tokens and pos must not be NULL");
+    return submit(c, B, tokens, pos, logits_out);
+}
+
+int l2_forward_host(l2_ctx *c, int token, int pos, float *logits_host) {
+    if (!c) return L2_EINVAL;
+    if (!logits_host) return fail(c, L2_EINVAL, "logits_host must not be NULL");
+    int rc = submit(c, 1, &token, &pos, nullptr);
+    if (rc) return rc;
+    L2_CUDA(c, cudaMemcpyAsync(logits_host, c->logits, sizeof(float) * c->cfg.vocab_size, cudaMemcpyDeviceToHost,
+                               c->stream));
+    L2_CUDA(c, cudaStreamSynchronize(c->stream));
+    return L2_OK;
+}
+
+const float *l2_logits(const l2_ctx *c) { return c ? c->logits : nullptr; }
+
+int l2_position(const l2_ctx *c, int slot) {
+    if (!c || slot < 0 || slot >= c->max_batch) return L2_EINVAL;
+    return c->written[slot];
+}
+
+int l2_debug_attention(l2_ctx *c, int slot, int layer, float *att_out) {
+    if (!c) return L2_EINVAL;
+    if (!(c->flags & L2_FLAG_DEBUG)) return fail(c, L2_EINVAL, "created without L2_FLAG_DEBUG");
+    if (slot < 0 || slot >= c->max_batch || layer < 0 || layer >= c->cfg.n_layers || !att_out)
+        return fail(c, L2_EINVAL, "bad slot, layer or output pointer");
+    const int n = c->written[slot];
+    if (n == 0) return fail(c, L2_ESTATE, "slot %d has no step yet", slot);
+    const size_t S = c->cfg.seq_len, H = c->cfg.n_heads;
+    const float *src = c->dbg + (((size_t)slot * c->cfg.n_layers + layer) * H) * S;
+    L2_CUDA(c, cudaMemcpy2DAsync(att_out, n * sizeof(float), src, S * sizeof(float), n * sizeof(float), H,
+                                 cudaMemcpyDeviceToHost, c->stream));
+    L2_CUDA(c, cudaStreamSynchronize(c->stream));
+    return L2_OK;
+}
+
+int l2_kv_export(l2_ctx *c, int slot, int layer, int n_pos, float *k_out, float *v_out) {
+    if (!c) return L2_EINVAL;
+    if (slot < 0 || slot >= c->max_batch || layer < 0 || layer >= c->cfg.n_layers || !k_out || !v_out)
+        return fail(c, L2_EINVAL, "bad slot, layer or output pointer");
+    if (n_pos < 0 || n_pos > c->written[slot]) return fail(c, L2_ESTATE, "only %d rows written", c->written[slot]);
+    if (n_pos == 0) return L2_OK;
+    const size_t S = c->cfg.seq_len, hs = c->head_size, KV = c->cfg.n_kv_heads;
+    for (size_t g = 0; g < KV; ++g) {
+        const size_t off = (((size_t)slot * c->cfg.n_layers + layer) * KV + g) * S * hs;
+        L2_CUDA(c, cudaMemcpy2DAsync(k_out + g * hs, c->kv_dim * sizeof(float), c->kcache + off, hs * sizeof(float),
+                                     hs * sizeof(float), n_pos, cudaMemcpyDeviceToHost, c->stream));
+        L2_CUDA(c, cudaMemcpy2DAsync(v_out + g * hs, c->kv_dim * sizeof(float), c->vcache + off, hs * sizeof(float),
+                                     hs * sizeof(float), n_pos, cudaMemcpyDeviceToHost, c->stream));
+    }
+    L2_CUDA(c, cudaStreamSynchronize(c->stream));
+    return L2_OK;
+}
+
+int l2_kv_import(l2_ctx *c, int slot, int n_pos, const float *k_in, const float *v_in) {
+    if (!c) return L2_EINVAL;
+    if (slot < 0 || slot >= c->max_batch || !k_in || !v_in) return fail(c, L2_EINVAL, "bad slot or input pointer");
+    if (n_pos < 0 || n_pos > c->cfg.seq_len) return fail(c, L2_EINVAL, "n_pos %d outside 0..seq_len", n_pos);
+    const size_t S = c->cfg.seq_len, hs = c->head_size, KV = c->cfg.n_kv_heads, L = c->cfg.n_layers;
+    for (size_t l = 0; l < L && n_pos > 0; ++l)
+        for (size_t g = 0; g < KV; ++g) {
+            const size_t off = (((size_t)slot * L + l) * KV + g) * S * hs;
+            const size_t src = l * (size_t)n_pos * c->kv_dim + g * hs;
+            L2_CUDA(c, cudaMemcpy2DAsync(c->kcache + off, hs * sizeof(float), k_in + src, c->kv_dim * sizeof(float),
+                                         hs * sizeof(float), n_pos, cudaMemcpyHostToDevice, c->stream));
+            L2_CUDA(c, cudaMemcpy2DAsync(c->vcache + off, hs * sizeof(float), v_in + src, c->kv_dim * sizeof(float),
+                                         hs * sizeof(float), n_pos, cudaMemcpyHostToDevice, c->stream));
+        }
+    L2_CUDA(c, cudaStreamSynchronize(c->stream));
+    c->written[slot] = n_pos;
+    return L2_OK;
+}
+
+int l2_sync(l2_ctx *c) {
+    if (!c) return L2_EINVAL;
+    L2_CUDA(c, cudaStreamSynchronize(c->stream));
+    int word = 0;
+    L2_CUDA(c, cudaMemcpy(&word, c->err, sizeof(int), cudaMemcpyDeviceToHost));
+    if (word) {
+        L2_CUDA(c, cudaMemset(c->err, 0, sizeof(int)));
+        if (word & L2_DEV_ERR_TIMEOUT) return fail(c, L2_ETIMEOUT, "a device-side wait gave up (error word 0x%x)", word);
+        return fail(c, L2_EDEVICE, "a kernel reported an error (error word 0x%x)", word);
+    }
+    return L2_OK;
+}
+
+const char *l2_last_error(const l2_ctx *c) { return c ? c->error.c_str() : g_create_error.c_str(); }
+
+void l2_destroy(l2_ctx *c) {
+    if (!c) return;
+    free_all(c);
+    delete c;
+}
+
+int l2_launch_op(l2_ctx *c, int op, int layer, int count) {
+    if (!c) return L2_EINVAL;
+    if (op < 0 || op > 5 || layer < 0 || layer >= c->cfg.n_layers || count < 0)
+        return fail(c, L2_EINVAL, "bad op, layer or count");
+    if (c->written[0] == 0) return fail(c, L2_ESTATE, "run a step first");
+    // Standalone launches write the classifier's output only to the handle's buffer.
+    L2_CUDA(c, cudaMemsetAsync(reinterpret_cast<char *>(c->step_dev) + offsetof(StepDev, logits_out), 0,
+                               sizeof(float *), c->stream));
+    for (int i = 0; i < count; ++i) L2_CUDA(c, launch_op(c, op, layer, 1, c->stream, false));
+    return L2_OK;
+}
+
+int l2_kernels_per_step(const l2_ctx *c, int B) {
+    if (!c || B < 1 || B > c->max_batch) return L2_EINVAL;
+    return 5 * c->cfg.n_layers + 1;
+}
+
+int l2_step_input_bytes(void) { return (int)sizeof(StepDev); }
+
+void l2_debug_fail_alloc_at(int n) { g_fail_alloc_at = n > 0 ? n : 0; }
+
+}  // extern "C"

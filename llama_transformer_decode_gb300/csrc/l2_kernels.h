@@ -1,0 +1,29 @@
+// Launch entry points of the decode kernels (host side).
+#pragma once
+#include <cstddef>
+#include <cuda_runtime.h>
+
+#include "l2_params.h"
+
+namespace l2 {
+
+// Fused streaming GEMV (gemv.cu).
+cudaError_t gemv_init();
+int gemv_threads();
+// Dynamic shared memory of one CTA for input length n and at most ymax local outputs.
+size_t gemv_smem_bytes(int n, int ymax);
+cudaError_t launch_gemv(int mode, const GemvParams &p, int grid, size_t smem, cudaStream_t stream, bool pdl);
+
+// Flash-decoding attention (attention.cu).
+struct AttnLaunch {
+    int lp;       // lanes per cache row (power of two)
+    int gq;       // query heads per KV head, rounded up to a power of two
+    int threads;
+    size_t smem;
+    bool ok;      // this head size / grouping is supported
+};
+AttnLaunch attn_plan(int head_size, int n_heads, int n_kv_heads);
+cudaError_t attn_init();
+cudaError_t launch_attn(const AttnLaunch &a, const AttnParams &p, int batch, cudaStream_t stream, bool pdl);
+
+}  // namespace l2

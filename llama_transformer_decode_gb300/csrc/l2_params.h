@@ -1,0 +1,70 @@
+// Kernel parameter blocks shared by the host orchestrator and the kernels.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace l2 {
+
+constexpr int kMaxBatch = 64;
+// A bounded device-side wait gives up after this much wall time.
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+
+// Bits of the device error word.
+enum : int { L2_DEV_ERR_TIMEOUT = 1, L2_DEV_ERR_BOUNDS = 2 };
+
+// Per-step inputs, filled by one host->device copy before each step.
+struct StepDev {
+    int token[kMaxBatch];
+    int pos[kMaxBatch];
+    float *logits_out;  // caller's device buffer [B][vocab] or nullptr
+    int B;
+    int pad_[3];
+};
+
+// The fused GEMV kernel's modes (prologue / epilogue around y = W v).
+enum GemvMode : int {
+    GEMV_QKV = 0,    // v = rmsnorm(x); rows of Wq|Wk|Wv; RoPE; q out, K/V rows into the cache
+    GEMV_RESID = 1,  // v = an activation vector; x += y
+    GEMV_W13 = 2,    // v = rmsnorm(x); rows of W1 and W3; hb = silu(h1) * h3
+    GEMV_CLS = 3,    // v = rmsnorm(x); logits = y
+};
+
+struct GemvParams {
+    int n;            // row length = input vector length
+    int unit_rows;    // rows per unit of the CTA split (2 keeps RoPE pairs together)
+    int total_units;  // units split evenly across the grid
+    int layer;
+    const float *mat0, *mat1, *mat2;  // this layer's matrices, row-major [rows][n]
+    int rows0, rows1, rows2;
+    const float *in_vec;  // GEMV_RESID input (xb or hb), [B][n]
+    const float *norm_w;  // rmsnorm gain [n]
+    const float *emb;     // embedding table (layer-0 QKV reads x from it)
+    float *x;             // residual stream [B][dim]
+    float *q;             // [B][dim]
+    float *kcache, *vcache;  // [slot][layer][kv_head][seq_len][head_size]
+    const float2 *rope;      // [seq_len][head_size/2] (cos, sin)
+    float *hb;               // [B][hidden_dim]
+    float *logits;           // handle's logits buffer [B][vocab]
+    const StepDev *step;
+    int *err;
+    int dim, kv_dim, head_size, seq_len, n_kv_heads, n_layers, vocab;
+    int evict_first;  // stream the weights with an L2 evict-first hint
+};
+
+struct AttnParams {
+    const float *q;                  // [B][dim]
+    const float *kcache, *vcache;    // [slot][layer][kv_head][seq_len][head_size]
+    float *out;                      // [B][dim]
+    float *ws_ml;                    // [B][n_heads][n_chunks][2] (running max, sum)
+    float *ws_acc;                   // [B][n_heads][n_chunks][head_size]
+    unsigned *tickets;               // [B][n_kv_heads], zero between launches
+    float *dbg;                      // [B][n_layers][n_heads][seq_len] scores -> probabilities, or nullptr
+    const StepDev *step;
+    int *err;
+    int layer, n_layers, n_heads, n_kv_heads, head_size, seq_len, dim;
+    int n_chunks;   // grid.x: CTAs per (slot, KV head)
+    int min_chunk;  // fewest positions a CTA takes before more CTAs join
+    float scale;    // 1 / sqrt(head_size)
+};
+
+}  // namespace l2

@@ -84,6 +84,28 @@ def fill_tensor(wl: Workload, name: str, out: np.ndarray, seed: int | None = Non
     return out
 
 
+def fill_range(wl: Workload, name: str, start: int, out: np.ndarray, seed: int | None = None) -> np.ndarray:
+    """Elements [start, start + out.size) of tensor ``name``'s flat stream
+    (the same values ``fill_tensor`` produces there), for streaming a large
+    tensor through a small host buffer."""
+    seed = wl.seed if seed is None else seed
+    tid = TENSOR_IDS[name]
+    flat = out.reshape(-1)
+    mean, std_fn = wl.recipe(name)
+    if name not in wl.layered:
+        return normal(seed, tid, start, flat.size, mean, std_fn(0), flat)
+    shape = wl.shape(name)
+    per = int(np.prod(shape[1:]))
+    done = 0
+    while done < flat.size:
+        i = start + done
+        l = i // per
+        n = min(flat.size - done, (l + 1) * per - i)
+        normal(seed, tid, i, n, mean, std_fn(l), flat[done:done + n])
+        done += n
+    return out
+
+
 def make_weights(wl: Workload, seed: int | None = None) -> dict:
     """All weight tensors of a workload as float32 numpy arrays, row-major [out][in].
 

@@ -1,0 +1,72 @@
+"""The C-ABI library builds, loads, and exports every entry point that
+include/l2.h declares.  Host-only checks: no kernel runs here."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import llama_transformer_decode_gb300 as pkg
+from llama_transformer_decode_gb300 import _native
+
+HEADER = os.path.join(_native.ROOT, "include", "l2.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(l2_[a-z_0-9]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    try:
+        return _native.load()
+    except OSError as e:  # libcudart not loadable on this host
+        pytest.skip(f"cannot load the CUDA runtime here: {e}")
+
+
+def test_header_declares_the_binding_exports():
+    assert declared_functions() == sorted(_native.EXPORTS)
+
+
+def test_library_exports_every_declared_function(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_struct_layouts_match_header():
+    assert ctypes.sizeof(_native.L2Config) == 7 * 4
+    assert ctypes.sizeof(_native.L2Weights) == 12 * ctypes.sizeof(ctypes.c_void_p)
+    text = open(HEADER).read()
+    for field in _native.WEIGHT_FIELDS:
+        assert re.search(r"\*%s;" % field, text), field
+
+
+def test_create_rejects_bad_arguments_on_the_host(lib):
+    cfg = _native.L2Config(64, 172, 5, 8, 4, 512, 512)
+    w = _native.L2Weights()
+    h = ctypes.c_void_p()
+    assert lib.l2_create(None, ctypes.byref(w), 1, 0, None, ctypes.byref(h)) == pkg.L2_EINVAL
+    assert lib.l2_create(ctypes.byref(cfg), ctypes.byref(w), 0, 0, None, ctypes.byref(h)) == pkg.L2_EINVAL
+    assert lib.l2_create(ctypes.byref(cfg), ctypes.byref(w), 65, 0, None, ctypes.byref(h)) == pkg.L2_EINVAL
+    assert b"max_batch" in lib.l2_last_error(None)
+    assert lib.l2_create(ctypes.byref(cfg), ctypes.byref(w), 1, 0x100, None, ctypes.byref(h)) == pkg.L2_EINVAL
+    for bad in [(64, 172, 5, 7, 4, 512, 512), (64, 172, 5, 8, 9, 512, 512), (64, 170, 5, 8, 4, 512, 512),
+                (0, 172, 5, 8, 4, 512, 512), (544, 172, 5, 2, 2, 512, 512), (64, 172, 5, 16, 1, 512, 512)]:
+        c = _native.L2Config(*bad)
+        assert lib.l2_create(ctypes.byref(c), ctypes.byref(w), 1, 0, None, ctypes.byref(h)) == pkg.L2_EINVAL
+    # a valid config with NULL weight pointers is refused before any device work
+    assert lib.l2_create(ctypes.byref(cfg), ctypes.byref(w), 1, 0, None, ctypes.byref(h)) == pkg.L2_EINVAL
+    assert b"NULL" in lib.l2_last_error(None)
+    assert not h.value
+
+
+def test_null_handle_calls_fail_cleanly(lib):
+    assert lib.l2_forward(None, 0, 0, None) == pkg.L2_EINVAL
+    assert lib.l2_reset(None, 0) == pkg.L2_EINVAL
+    assert lib.l2_sync(None) == pkg.L2_EINVAL
+    assert lib.l2_position(None, 0) == pkg.L2_EINVAL
+    assert lib.l2_kernels_per_step(None, 1) == pkg.L2_EINVAL
+    assert lib.l2_logits(None) is None
+    lib.l2_destroy(None)

@@ -1,0 +1,215 @@
+"""CUDA path against the oracle, element by element, on seeded inputs.
+
+Small workloads are checked at every teacher-forced step (logits) and, with
+the debug export, every layer's attention probabilities.  Bounds: per step
+max|d logit| <= 2e-3 and <= 1e-4 * max|oracle logit|; probabilities within
+1e-5.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from synth import WORKLOADS
+from tests.gpu_util import ATT_ABS, check_logits, decoder_for, gpu_decode
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("no CUDA device", allow_module_level=True)
+
+import llama_transformer_decode_gb300 as pkg  # noqa: E402
+
+
+def run_pair(wl, n_steps, att_every=1, flags=pkg.L2_FLAG_DEBUG, weights=None):
+    w = weights if weights is not None else synth.make_weights(wl)
+    toks = synth.token_stream(wl, 0, n_steps)
+    ref = oracle.Model(wl.config_tuple(), w)
+    dec = decoder_for(wl, pkg.to_device(w), flags=flags)
+    out = torch.empty((n_steps, wl.vocab_size), device="cuda")
+    ref_logits = np.empty((n_steps, wl.vocab_size), np.float32)
+    worst_att = 0.0
+    for t, tok in enumerate(toks):
+        check_att = (flags & pkg.L2_FLAG_DEBUG) and (t % att_every == 0 or t == n_steps - 1)
+        dec.forward(int(tok), t, out[t])
+        if check_att:
+            ref_logits[t], att = ref.forward(int(tok), t, want_att=True)
+            dec.sync()
+            for layer in range(wl.n_layers):
+                ga = dec.debug_attention(layer)
+                assert ga.shape == (wl.n_heads, t + 1)
+                d = float(np.abs(ga - att[layer, :, : t + 1]).max())
+                worst_att = max(worst_att, d)
+                assert d <= ATT_ABS, f"step {t} layer {layer}: attention differs by {d:.3e}"
+        else:
+            ref_logits[t] = ref.forward(int(tok), t)
+    dec.sync()
+    rel = check_logits(out.cpu().numpy(), ref_logits, wl.name)
+    return dec, ref, rel, worst_att
+
+
+def test_tiny_all_steps():
+    wl = WORKLOADS["tiny"]
+    _, _, rel, att = run_pair(wl, wl.steps)
+    print(f"tiny: worst relative logit error {rel:.2e}, attention {att:.2e}")
+
+
+def test_gqa_small_all_steps():
+    # 6 query heads on 4 KV heads: the non-integer group map 0,0,1,2,2,3
+    wl = WORKLOADS["gqa_small"]
+    _, _, rel, att = run_pair(wl, wl.steps, att_every=8)
+    print(f"gqa_small: worst relative logit error {rel:.2e}, attention {att:.2e}")
+
+
+def test_mid_all_steps():
+    wl = WORKLOADS["mid"]
+    _, _, rel, att = run_pair(wl, wl.steps, att_every=128)
+    print(f"mid: worst relative logit error {rel:.2e}, attention {att:.2e}")
+
+
+@pytest.mark.parametrize("name,sharp", [("tiny", 12.0), ("gqa_small", 6.0)])
+def test_sharp_attention(name, sharp):
+    # wq and wk scaled so scores spread over O(5) and the top probability nears 1:
+    # exercises the online-softmax rescaling.  Sharper scaling makes the check
+    # ill-conditioned: at x25 (tiny) a 2e-7 relative change of wq alone moves
+    # the oracle's probabilities by 1.5e-5.
+    wl = WORKLOADS[name].replace(std_scale=(("wq", sharp), ("wk", sharp)))
+    _, ref, rel, att = run_pair(wl, 64, att_every=4)
+    # the attention really is peaked
+    _, a = ref.forward(int(synth.token_stream(wl, 0, 65)[64]), 64, want_att=True)
+    assert a[:, :, :65].max() > 0.3
+
+
+def test_ragged_shapes():
+    # head_size 12 (3 of 4 lanes per row), rows not multiples of any tile, 5 heads on 2 KV heads
+    wl = WORKLOADS["tiny"].replace(name="ragged", dim=60, hidden_dim=92, n_layers=3, n_heads=5,
+                                   n_kv_heads=2, vocab_size=301, seq_len=70, shared_wcls=False,
+                                   seed_override=77, std_scale=(("wq", 8.0), ("wk", 8.0)))
+    run_pair(wl, 70, att_every=3)
+
+
+def test_pos0_attention_is_exactly_one():
+    wl = WORKLOADS["gqa_small"]
+    w = synth.make_weights(wl)
+    dec = decoder_for(wl, pkg.to_device(w), flags=pkg.L2_FLAG_DEBUG)
+    dec.forward(5, 0)
+    dec.sync()
+    for layer in range(wl.n_layers):
+        assert np.all(dec.debug_attention(layer) == 1.0)
+
+
+def test_kv_cache_rows_match_oracle():
+    wl = WORKLOADS["gqa_small"]
+    w = synth.make_weights(wl)
+    toks = synth.token_stream(wl, 0, 40)
+    ref = oracle.Model(wl.config_tuple(), w)
+    ref.decode(toks)
+    dec = decoder_for(wl, pkg.to_device(w))
+    gpu_decode(dec, toks)
+    for layer in (0, wl.n_layers - 1):
+        k, v = dec.kv_export(layer)
+        rk = ref.key_cache[0][layer, :40]
+        rv = ref.value_cache[0][layer, :40]
+        assert np.abs(k - rk).max() <= 1e-4 * np.abs(rk).max()
+        assert np.abs(v - rv).max() <= 1e-4 * np.abs(rv).max()
+
+
+def test_graph_eager_and_no_pdl_agree_bitwise():
+    wl = WORKLOADS["gqa_small"]
+    w = pkg.to_device(synth.make_weights(wl))
+    toks = synth.token_stream(wl, 0, 24)
+    base = gpu_decode(decoder_for(wl, w), toks)
+    again = gpu_decode(decoder_for(wl, w), toks)
+    eager = gpu_decode(decoder_for(wl, w, flags=pkg.L2_FLAG_NO_GRAPH), toks)
+    nopdl = gpu_decode(decoder_for(wl, w, flags=pkg.L2_FLAG_NO_PDL), toks)
+    assert np.array_equal(base, again)
+    assert np.array_equal(base, eager)
+    assert np.array_equal(base, nopdl)
+
+
+def test_reset_and_rewrite_positions():
+    wl = WORKLOADS["tiny"]
+    w = synth.make_weights(wl)
+    toks = synth.token_stream(wl, 0, 20)
+    dec = decoder_for(wl, pkg.to_device(w))
+    first = gpu_decode(dec, toks)
+    assert dec.position() == 20
+    dec.reset()
+    assert dec.position() == 0
+    second = gpu_decode(dec, toks)
+    assert np.array_equal(first, second)
+    # rewriting position 10 with another token, then continuing from there
+    other = toks.copy()
+    other[10] = (other[10] + 1) % wl.vocab_size
+    tail = gpu_decode(dec, other[10:], pos0=10)
+    ref = oracle.Model(wl.config_tuple(), w).decode(other)
+    check_logits(tail, ref[10:], "rewrite")
+
+
+def test_forward_host_matches_device_output():
+    wl = WORKLOADS["gqa_small"]
+    w = pkg.to_device(synth.make_weights(wl))
+    toks = synth.token_stream(wl, 0, 6)
+    a = gpu_decode(decoder_for(wl, w), toks)
+    dec = decoder_for(wl, w)
+    b = np.stack([dec.forward_host(int(t), i) for i, t in enumerate(toks)])
+    assert np.array_equal(a, b)
+
+
+def test_host_side_argument_checks():
+    wl = WORKLOADS["tiny"]
+    dec = decoder_for(wl, pkg.to_device(synth.make_weights(wl)), flags=pkg.L2_FLAG_DEBUG)
+    for tok, pos, code in [(-1, 0, pkg.L2_EINVAL), (wl.vocab_size, 0, pkg.L2_EINVAL),
+                           (0, -1, pkg.L2_EINVAL), (0, wl.seq_len, pkg.L2_EINVAL),
+                           (0, 1, pkg.L2_ESTATE)]:
+        with pytest.raises(pkg.L2Error) as e:
+            dec.forward(tok, pos)
+        assert e.value.code == code
+    with pytest.raises(pkg.L2Error):
+        dec.debug_attention(0)  # no step yet
+    with pytest.raises(pkg.L2Error):
+        dec.reset(5)
+    dec.forward(1, 0)
+    dec.sync()
+    with pytest.raises(pkg.L2Error):
+        dec.debug_attention(wl.n_layers)
+
+
+def test_create_rejects_bad_configs():
+    wl = WORKLOADS["tiny"]
+    w = pkg.to_device(synth.make_weights(wl))
+    bad = [
+        (64, 172, 5, 7, 4, 512, 512),    # dim not a multiple of n_heads
+        (64, 172, 5, 8, 9, 512, 512),    # more KV heads than heads
+        (64, 170, 5, 8, 4, 512, 512),    # hidden_dim not a multiple of 4
+        (64, 172, 0, 8, 4, 512, 512),    # no layers
+        (544, 172, 5, 2, 2, 512, 512),   # head_size 272 > 128
+    ]
+    for cfg in bad:
+        with pytest.raises(pkg.L2Error) as e:
+            pkg.Decoder(cfg, w)
+        assert e.value.code == pkg.L2_EINVAL
+    host = {k: v.cpu() for k, v in w.items()}
+    with pytest.raises((pkg.L2Error, ValueError)):
+        pkg.Decoder(wl.config_tuple(), host)
+
+
+def test_injected_allocation_failure_reports_enomem_without_leak():
+    wl = WORKLOADS["gqa_small"]
+    w = pkg.to_device(synth.make_weights(wl))
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    for n in (1, 3, 7):
+        pkg.fail_alloc_at(n)
+        with pytest.raises(pkg.L2Error) as e:
+            pkg.Decoder(wl.config_tuple(), w)
+        assert e.value.code == pkg.L2_ENOMEM
+    pkg.fail_alloc_at(0)
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert abs(free0 - free1) < 64 << 20
+    d = pkg.Decoder(wl.config_tuple(), w)  # and a normal create still works
+    d.close()
