@@ -354,7 +354,8 @@ int submit(l2_ctx *c, int B, const int *tokens, const int *pos, float *logits_ou
         if (pos[b] > c->written[b])
             return fail(c, L2_ESTATE, "pos %d of slot %d skips cache rows (only %d written)", pos[b], b, c->written[b]);
     }
-    if (logits_out && !aligned16(logits_out)) return fail(c, L2_EINVAL, "logits_out must be 16-byte aligned");
+    if (logits_out && (reinterpret_cast<uintptr_t>(logits_out) & 3u))
+        return fail(c, L2_EINVAL, "logits_out must be 4-byte aligned");
 
     const int i = c->ring_next;
     c->ring_next = (i + 1) % kRing;

@@ -42,21 +42,24 @@ uint64_t synth_draw_u64(uint64_t seed, uint64_t tensor_id, uint64_t n) {
     return draw(stream_key(seed, tensor_id), n);
 }
 
-/* out[k] = mean + std * z(start + k), k in [0, count). */
+/* out[k] = mean + std * z(start + k), k in [0, count).  Works pair by pair:
+ * both normals of a Box-Muller pair come from one (u1, u2). */
 void synth_normal_f32(uint64_t seed, uint64_t tensor_id, uint64_t start, uint64_t count,
                       double mean, double std, float *out) {
+    if (count == 0) return;
     const uint64_t key = stream_key(seed, tensor_id);
     const double two_pi = 6.283185307179586476925286766559;
-    long long n = (long long)count;
+    const long long j0 = (long long)(start >> 1), j1 = (long long)((start + count - 1) >> 1);
 #pragma omp parallel for schedule(static)
-    for (long long k = 0; k < n; k++) {
-        uint64_t i = start + (uint64_t)k;
-        uint64_t j = i >> 1;
-        double u1 = unit_open0(draw(key, 2 * j));
-        double u2 = unit_open0(draw(key, 2 * j + 1));
+    for (long long j = j0; j <= j1; j++) {
+        double u1 = unit_open0(draw(key, 2 * (uint64_t)j));
+        double u2 = unit_open0(draw(key, 2 * (uint64_t)j + 1));
         double rad = sqrt(-2.0 * log(u1));
-        double z = (i & 1ULL) ? rad * sin(two_pi * u2) : rad * cos(two_pi * u2);
-        out[k] = (float)(mean + std * z);
+        double z[2] = {rad * cos(two_pi * u2), rad * sin(two_pi * u2)};
+        for (int e = 0; e < 2; e++) {
+            uint64_t i = 2 * (uint64_t)j + (uint64_t)e;
+            if (i >= start && i < start + count) out[i - start] = (float)(mean + std * z[e]);
+        }
     }
 }
 
