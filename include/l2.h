@@ -178,6 +178,29 @@ int l2_kernels_per_step(const l2_ctx *ctx, int B);
 int l2_step_input_bytes(void);
 
 /*
+ * l2_forward without allocating anything, for callers that cannot call
+ * cudaMalloc once decoding has started: a serving process that handed all of
+ * the device memory to its own pool at start-up, or a latency-critical loop
+ * that must not hit the implicit device synchronisation an allocation or a
+ * free may cause.  (l2_forward may build a CUDA graph on its first call for a
+ * batch size, and building one allocates.)  The pages have no counterpart of
+ * this entry point.
+ * Same arguments, checks, status codes and result as l2_forward, for slot 0.
+ * The step's kernels are launched one by one, and the attention kernel keeps
+ * its cross-CTA partial results and tickets in one static device array of
+ * 1 MiB (262144 floats) compiled into the library, which every GPU that
+ * loads the library holds until the process exits.  A handle whose attention
+ * needs more, n_heads * n_chunks * (head_size + 2) + n_kv_heads floats with
+ * n_chunks = min(ceil(2 * SMs / n_kv_heads), ceil(seq_len / 32)), is refused
+ * with L2_EINVAL before anything is enqueued.  The first call on a device
+ * looks up the array's device address; make that first call before any
+ * stream capture.  The handle's device must be current.  Every call shares
+ * the array and clears its tickets first: calls whose kernels overlap on the
+ * GPU (handles on different streams) race and give wrong results.
+ */
+int l2_forward_static(l2_ctx *ctx, int token, int pos, float *logits_out);
+
+/*
  * Fault injection for tests: makes the n-th device allocation from now on
  * (n >= 1) fail as if out of memory; 0 disables.  Process-wide.
  */

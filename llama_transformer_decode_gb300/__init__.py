@@ -107,6 +107,12 @@ class Decoder:
                                          ctypes.c_void_p(_ptr(out) if out is not None else 0)))
         return out
 
+    def forward_static(self, token: int, pos: int, out=None):
+        """Like forward(), with nothing allocated on the path (l2_forward_static)."""
+        self._check(self._lib.l2_forward_static(self._h, int(token), int(pos),
+                                                ctypes.c_void_p(_ptr(out) if out is not None else 0)))
+        return out
+
     def forward_batch(self, tokens, pos, out=None):
         toks = np.ascontiguousarray(tokens, dtype=np.int32)
         ps = np.ascontiguousarray(pos, dtype=np.int32)

@@ -80,7 +80,7 @@ class L2Weights(ctypes.Structure):
 EXPORTS = ("l2_create", "l2_reset", "l2_forward", "l2_forward_batch", "l2_forward_host", "l2_logits",
            "l2_position", "l2_debug_attention", "l2_kv_export", "l2_kv_import", "l2_sync",
            "l2_last_error", "l2_destroy", "l2_launch_op", "l2_kernels_per_step",
-           "l2_step_input_bytes", "l2_debug_fail_alloc_at")
+           "l2_step_input_bytes", "l2_forward_static", "l2_debug_fail_alloc_at")
 
 _lib = None
 
@@ -107,13 +107,14 @@ def declare(lib):
     lib.l2_destroy.restype = None
     lib.l2_launch_op.argtypes = [vp, i, i, i]
     lib.l2_kernels_per_step.argtypes = [vp, i]
+    lib.l2_forward_static.argtypes = [vp, i, i, fp]
     lib.l2_step_input_bytes.argtypes = []
     lib.l2_step_input_bytes.restype = i
     lib.l2_debug_fail_alloc_at.argtypes = [i]
     lib.l2_debug_fail_alloc_at.restype = None
     for name in ("l2_create", "l2_reset", "l2_forward", "l2_forward_batch", "l2_forward_host",
                  "l2_position", "l2_debug_attention", "l2_kv_export", "l2_kv_import", "l2_sync",
-                 "l2_launch_op", "l2_kernels_per_step"):
+                 "l2_launch_op", "l2_kernels_per_step", "l2_forward_static"):
         getattr(lib, name).restype = i
     return lib
 

@@ -638,3 +638,99 @@ int l2_step_input_bytes(void) { return (int)sizeof(StepDev); }
 void l2_debug_fail_alloc_at(int n) { g_fail_alloc_at = n > 0 ? n : 0; }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// l2_forward_static: the decode step with nothing allocated on its path, for
+// callers that cannot call cudaMalloc once decoding has started (a serving
+// process that handed all device memory to its own pool at start-up, or a
+// latency-critical loop that must not hit the implicit device synchronisation
+// an allocation or free may cause).  l2_forward may build a CUDA graph on its
+// first call for a batch size, which allocates; this entry point launches the
+// kernels one by one instead, and gives the one kernel that needs scratch
+// memory -- attention, for its cross-CTA partial results and tickets -- a
+// static device array in place of the handle's workspace.
+
+// Attention scratch of l2_forward_static: accumulators, (max, sum) pairs and
+// tickets, 1 MiB.  Every GPU that loads the library holds it until exit.  In
+// host code this name is only a stand-in: kernels get the address that
+// cudaGetSymbolAddress returns for the current device.
+constexpr size_t kStaticScratchFloats = size_t(1) << 18;
+static __device__ __align__(256) float g_static_scratch[kStaticScratchFloats];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+float *g_static_scratch_ptr[kMaxDevices] = {};  // device address, per device
+
+// Looks up the array's device address on the current device (once per device).
+int static_scratch(l2_ctx *c, float **out) {
+    if (c->device < 0 || c->device >= kMaxDevices) return fail(c, L2_EINVAL, "device index %d too large", c->device);
+    if (!g_static_scratch_ptr[c->device]) {
+        void *p = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
+        if (e != cudaSuccess) return cuda_fail(c, e, "cudaGetSymbolAddress(static attention scratch)");
+        g_static_scratch_ptr[c->device] = static_cast<float *>(p);
+    }
+    *out = g_static_scratch_ptr[c->device];
+    return L2_OK;
+}
+
+}  // namespace
+
+extern "C" int l2_forward_static(l2_ctx *c, int token, int pos, float *logits_out) {
+    if (!c) return L2_EINVAL;
+    int dev = -1;
+    L2_CUDA(c, cudaGetDevice(&dev));
+    if (dev != c->device) return fail(c, L2_EINVAL, "the handle's device (%d) must be current (is %d)", c->device, dev);
+    if (token < 0 || token >= c->cfg.vocab_size)
+        return fail(c, L2_EINVAL, "token %d outside [0, %d)", token, c->cfg.vocab_size);
+    if (pos < 0 || pos >= c->cfg.seq_len) return fail(c, L2_EINVAL, "pos %d outside [0, %d)", pos, c->cfg.seq_len);
+    if (pos > c->written[0]) return fail(c, L2_ESTATE, "pos %d skips cache rows (only %d written)", pos, c->written[0]);
+    if (logits_out && (reinterpret_cast<uintptr_t>(logits_out) & 3u))
+        return fail(c, L2_EINVAL, "logits_out must be 4-byte aligned");
+
+    // Scratch layout: accumulators [n_heads][n_chunks][head_size] (16-byte
+    // aligned), then (max, sum) pairs [n_heads][n_chunks][2], then one ticket
+    // per KV head.
+    const AttnParams probe = attn_params(c, 0, 1);
+    const size_t slots = (size_t)c->cfg.n_heads * probe.n_chunks;
+    const size_t acc_f = slots * c->head_size, ml_f = slots * 2, tick_f = (size_t)c->cfg.n_kv_heads;
+    const size_t need = acc_f + ml_f + tick_f;
+    if (need > kStaticScratchFloats)
+        return fail(c, L2_EINVAL,
+                    "attention needs %zu floats of scratch; l2_forward_static has a static array of %zu floats",
+                    need, kStaticScratchFloats);
+    float *scratch = nullptr;
+    int rc = static_scratch(c, &scratch);
+    if (rc) return rc;
+    float *ws_acc = scratch, *ws_ml = scratch + acc_f;
+    unsigned *tickets = reinterpret_cast<unsigned *>(scratch + acc_f + ml_f);
+
+    const int i = c->ring_next;
+    c->ring_next = (i + 1) % kRing;
+    if (c->ring_used[i]) L2_CUDA(c, cudaEventSynchronize(c->ring_ev[i]));
+    StepDev &sh = c->step_host[i];
+    sh.token[0] = token;
+    sh.pos[0] = pos;
+    sh.logits_out = logits_out;
+    sh.B = 1;
+    L2_CUDA(c, cudaMemcpyAsync(c->step_dev, &sh, sizeof(StepDev), cudaMemcpyHostToDevice, c->stream));
+    L2_CUDA(c, cudaEventRecord(c->ring_ev[i], c->stream));
+    c->ring_used[i] = true;
+    // The array keeps the previous call's contents: the tickets must start at zero.
+    L2_CUDA(c, cudaMemsetAsync(tickets, 0, tick_f * sizeof(unsigned), c->stream));
+
+    const bool pdl = !(c->flags & L2_FLAG_NO_PDL);
+    for (int l = 0; l < c->cfg.n_layers; ++l) {
+        L2_CUDA(c, launch_op(c, 0, l, 1, c->stream, pdl));
+        AttnParams a = attn_params(c, l, 1);
+        a.ws_acc = ws_acc;
+        a.ws_ml = ws_ml;
+        a.tickets = tickets;
+        L2_CUDA(c, launch_attn(c->attn, a, 1, c->stream, pdl));
+        for (int op = 2; op < 5; ++op) L2_CUDA(c, launch_op(c, op, l, 1, c->stream, pdl));
+    }
+    L2_CUDA(c, launch_op(c, 5, 0, 1, c->stream, pdl));
+    c->written[0] = pos + 1;
+    return L2_OK;
+}
