@@ -363,6 +363,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default="llama2_7b", choices=sorted(WORKLOADS))
+    ap.add_argument("--layers", type=int, default=None,
+                    help="decode only the first N layers of the workload (a smaller case, e.g. for profiling)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-baseline leg")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time for the CPU baseline")
     ap.add_argument("--reference-budget", type=float, default=90.0,
@@ -371,6 +373,10 @@ def main(argv=None):
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     wl = WORKLOADS[args.workload]
+    if args.layers is not None:
+        if not 1 <= args.layers <= wl.n_layers:
+            ap.error(f"--layers must be in 1..{wl.n_layers}")
+        wl = wl.replace(n_layers=args.layers, name=f"{wl.name} ({args.layers} layers)")
     if args.steps is None:
         args.steps = max(1, wl.seq_len - args.warmup)
     if args.impl == "reference":

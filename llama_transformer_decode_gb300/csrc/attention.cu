@@ -216,6 +216,33 @@ __global__ void __launch_bounds__(kNWA * 32) attn_kernel(const AttnParams p) {
 
     // merge the warps in warp order and publish this CTA's partial
     const int NC = p.n_chunks;
+    if (n_active == 1) {
+        // The only chunk: normalise and write the output directly.
+        for (int idx = tid; idx < nq * hs4; idx += NT) {
+            const int j = idx / hs4, w4 = idx % hs4;
+            float mm = -CUDART_INF_F, ll = 0.f;
+            float4 aa = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int w = 0; w < kNWA; ++w)
+                merge_state(mm, ll, aa, mrg[(w * GQ + j) * 2], mrg[(w * GQ + j) * 2 + 1],
+                            accs[(size_t)(w * GQ + j) * hs4 + w4]);
+            const float inv = 1.0f / ll;
+            reinterpret_cast<float4 *>(p.out + (size_t)b * p.dim + (size_t)(h0 + j) * hs)[w4] =
+                make_float4(aa.x * inv, aa.y * inv, aa.z * inv, aa.w * inv);
+            if (w4 == 0) {
+                fin[j * 2] = mm;
+                fin[j * 2 + 1] = ll;
+            }
+        }
+        if (dbg) {
+            __syncthreads();
+            for (int idx = tid; idx < nq * P; idx += NT) {
+                const int j = idx / P, t = idx % P;
+                float *cell = dbg + (size_t)j * p.seq_len + t;
+                *cell = expf(*cell - fin[j * 2]) / fin[j * 2 + 1];
+            }
+        }
+        return;
+    }
     for (int idx = tid; idx < nq * hs4; idx += NT) {
         const int j = idx / hs4, w4 = idx % hs4;
         float mm = -CUDART_INF_F, ll = 0.f;

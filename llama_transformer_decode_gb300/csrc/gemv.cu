@@ -30,6 +30,25 @@
 #include "l2_device.cuh"
 #include "l2_kernels.h"
 
+// Launch shape (compile-time): warps per CTA, ring buffers per warp, 16-byte
+// words per buffer.  Measured on GB300 (7B shape): 8 KB copies reach ~6 TB/s
+// where 2 KB copies with the same bytes in flight stay near 3.7 TB/s, so the
+// per-copy cost, not the depth of the ring, sets the rate.  L2_GEMV_FENCE adds
+// a generic->async proxy fence before a buffer is refilled (not needed: the
+// warp's reads of the buffer have completed when it issues the refill).
+#ifndef L2_GEMV_WARPS
+#define L2_GEMV_WARPS 8
+#endif
+#ifndef L2_GEMV_STAGES
+#define L2_GEMV_STAGES 2
+#endif
+#ifndef L2_GEMV_CHUNK_WORDS
+#define L2_GEMV_CHUNK_WORDS 512
+#endif
+#ifndef L2_GEMV_FENCE
+#define L2_GEMV_FENCE 0
+#endif
+
 namespace l2 {
 
 namespace {
@@ -126,7 +145,10 @@ __global__ void __launch_bounds__(NW * 32, 1) gemv_kernel(const GemvParams p) {
     const int np = fx.npieces;
     long long F = 0;
     for (int i = 0; i < np; ++i) F += (long long)fx.pieces[i].rows * n4;
-    const long long fb = F * warp / NW, fe = F * (warp + 1) / NW;
+    // Warp ranges start on 128-byte boundaries of the stream (whole cache lines
+    // whenever the pieces themselves start on one).
+    const long long fb = (F * warp / NW) & ~7LL;
+    const long long fe = warp == NW - 1 ? F : (F * (warp + 1) / NW) & ~7LL;
 
     // The chunk that starts at word f of the stream: its piece and length.
     auto chunk_at = [&](long long f, int &pi, int &len) {
@@ -269,7 +291,9 @@ __global__ void __launch_bounds__(NW * 32, 1) gemv_kernel(const GemvParams p) {
         __syncwarp();
         fc += len;
         if (fi < fe) {
+#if L2_GEMV_FENCE
             if (lane == 0) fence_proxy_async_smem();
+#endif
             issue(s);
         }
     }
@@ -344,8 +368,9 @@ __global__ void __launch_bounds__(NW * 32, 1) gemv_kernel(const GemvParams p) {
 
 // ---------------------------------------------------------------- host side
 
+
 namespace {
-constexpr int kNW = 8, kStages = 4, kCH4 = 128;  // 8 warps, 4 x 2 KB buffers per warp
+constexpr int kNW = L2_GEMV_WARPS, kStages = L2_GEMV_STAGES, kCH4 = L2_GEMV_CHUNK_WORDS;
 
 template <int MODE>
 cudaError_t set_attr() {
