@@ -41,7 +41,7 @@ FALLBACK_HBM_GBS = 6800.0
 # the dominant kernel, from the ncu capture summarised in
 # profiles/gemv_w13_llama2_7b.md, valid only for the kernel source whose
 # sha256 prefix is recorded beside it.
-W13_NCU_TRAFFIC = None  # (bytes per launch, gemv.cu sha256 prefix)
+W13_NCU_TRAFFIC = (364068608, "13f432b0754ca229")  # (bytes per launch, gemv.cu sha256 prefix)
 
 
 def weight_bytes(wl) -> int:
@@ -223,6 +223,13 @@ def run_reference(args, wl):
     return 0
 
 
+def fp32_alu_peak_tflops(props) -> float:
+    """fp32 FMA peak: SMs x 128 lanes x 2 flop x the maximum SM clock."""
+    peaks = measured_peaks()
+    mhz = peaks.get("sm_max_mhz", 2070.0)
+    return props.multi_processor_count * 128 * 2 * mhz * 1e6 / 1e12
+
+
 def run_ours(args, wl):
     import torch
     import torch.distributed as dist
@@ -234,28 +241,51 @@ def run_ours(args, wl):
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     torch.cuda.set_device(local_rank)
     pkg._native.load()
-    uuid = str(torch.cuda.get_device_properties(local_rank).uuid)
+    props = torch.cuda.get_device_properties(local_rank)
+    uuid = str(props.uuid)
+    B = args.batch
 
     cpu_leg = rank == 0 and world == 1 and not args.no_cpu
     w_dev, host_w = load_weights_device(wl, keep_host=cpu_leg)
     stream = torch.cuda.Stream()
-    dec = pkg.Decoder(wl.config_tuple(), w_dev, stream=stream)
+    dec = pkg.Decoder(wl.config_tuple(), w_dev, max_batch=B, stream=stream)
     S = wl.seq_len
-    toks = synth.token_stream(wl, 0, S)
-    out = torch.empty(wl.vocab_size, device="cuda")
-    kern = dec.kernels_per_step(1)
+    streams = [synth.token_stream(wl, b, S) for b in range(B)]
+    out = torch.empty((B, wl.vocab_size), device="cuda")
+    kern = dec.kernels_per_step(B)
+    peaks = measured_peaks()
+    hbm = peaks.get("hbm_gbs")
+    peak_src = "of measured" if hbm else "of fallback"
+    hbm = hbm or FALLBACK_HBM_GBS
 
-    def positions(n, start):
-        return [(start + i) % S for i in range(n)]
+    # Slot b starts at floor(b * S / B) (0 for a batch of one) and wraps to 0,
+    # with its cache rewound, at the end of the context.
+    offsets = [b * S // B for b in range(B)]
+    for b in range(B):
+        if offsets[b]:
+            # rows before the offset stand for tokens decoded earlier; their
+            # values do not change a step's cost, so they are imported
+            dec.kv_import(synth.kv_rows(wl, b, offsets[b], "k"), synth.kv_rows(wl, b, offsets[b], "v"), slot=b)
 
-    def run_steps(pos_list, host_out=None):
-        for p in pos_list:
-            if p == 0:
-                dec.reset()
-            if host_out is None:
-                dec.forward(int(toks[p]), p, out)
+    def positions(step):
+        return [(offsets[b] + step) % S for b in range(B)]
+
+    def run_steps(first, n, host_out=None):
+        for s in range(first, first + n):
+            pos = positions(s)
+            for b in range(B):
+                if pos[b] == 0 and dec.position(b) > 0:
+                    dec.reset(b)
+            if B == 1:
+                if host_out is None:
+                    dec.forward(int(streams[0][pos[0]]), pos[0], out[0])
+                else:
+                    dec.forward_host(int(streams[0][pos[0]]), pos[0], host_out)
             else:
-                dec.forward_host(int(toks[p]), p, host_out)
+                dec.forward_batch([int(streams[b][pos[b]]) for b in range(B)], pos, out)
+                if host_out is not None:
+                    stream.synchronize()
+                    host_out[...] = out.cpu().numpy()
 
     def barrier():
         if world > 1:
@@ -268,9 +298,7 @@ def run_ours(args, wl):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         return float(t.item())
 
-    warm = positions(args.warmup, 0)
-    timed = positions(args.steps, args.warmup)
-    run_steps(warm)
+    run_steps(0, args.warmup)
     dec.sync()
 
     # ---- device-resident timed region ----
@@ -279,72 +307,91 @@ def run_ours(args, wl):
     torch.cuda.synchronize()
     with ClockSampler(uuid) as clocks:
         ev0.record(stream)
-        run_steps(timed)
+        run_steps(args.warmup, args.steps)
         ev1.record(stream)
         ev1.synchronize()
     torch.cuda.synchronize()
     barrier()
     dec.sync()
     ms = max_over_ranks(ev0.elapsed_time(ev1))
-    value = world * args.steps / (ms / 1000.0)
-    bytes_total = sum(weight_bytes(wl) + kv_bytes(wl, p) for p in timed)
+    value = world * B * args.steps / (ms / 1000.0)
+    timed_pos = [positions(s) for s in range(args.warmup, args.warmup + args.steps)]
+    bytes_total = sum(weight_bytes(wl) + sum(kv_bytes(wl, p) for p in pos) for pos in timed_pos)
     step_gbs = bytes_total / (ms / 1000.0) / 1e9
 
-    # ---- end to end through the host-buffer call ----
-    host_logits = np.empty(wl.vocab_size, np.float32)
+    # ---- end to end through the public call with host output ----
+    host_logits = np.empty(wl.vocab_size if B == 1 else (B, wl.vocab_size), np.float32)
     dec.reset()
-    run_steps(warm, host_logits)
+    for b in range(B):
+        if offsets[b]:
+            dec.kv_import(synth.kv_rows(wl, b, offsets[b], "k"), synth.kv_rows(wl, b, offsets[b], "v"), slot=b)
+    run_steps(0, args.warmup, host_logits)
     barrier()
     t0 = time.perf_counter()
-    run_steps(timed, host_logits)
+    run_steps(args.warmup, args.steps, host_logits)
     e2e_s = max_over_ranks(time.perf_counter() - t0)
-    e2e = {"value": world * args.steps / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": dec.step_input_bytes(),
-           "d2h_bytes_per_step": 4 * wl.vocab_size}
+    e2e = {"value": world * B * args.steps / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": dec.step_input_bytes(),
+           "d2h_bytes_per_step": 4 * wl.vocab_size * B}
 
-    # ---- dominant kernel (rmsnorm + W1/W3 + SwiGLU) timed alone, layers cycled ----
-    peaks = measured_peaks()
-    hbm = peaks.get("hbm_gbs")
-    peak_src = "of measured" if hbm else "of fallback"
-    hbm = hbm or FALLBACK_HBM_GBS
-    reps = max(1, 64 // wl.n_layers)
-    dec.launch_op("w13", 0, 1)
-    k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    k0.record(stream)
-    for _ in range(reps):
-        for layer in range(wl.n_layers):
-            dec.launch_op("w13", layer, 1)
-    k1.record(stream)
-    k1.synchronize()
-    w13_ms = k0.elapsed_time(k1) / (reps * wl.n_layers)
-    achieved = w13_bytes(wl) / (w13_ms / 1000.0) / 1e9
-    traffic = None
-    if W13_NCU_TRAFFIC is not None:
-        src = open(os.path.join(ROOT, "llama_transformer_decode_gb300", "csrc", "gemv.cu"), "rb").read()
-        if hashlib.sha256(src).hexdigest().startswith(W13_NCU_TRAFFIC[1]):
-            traffic = W13_NCU_TRAFFIC[0]
-    roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                "traffic": traffic, "kernel": "gemv_kernel<GEMV_W13> (rmsnorm + W1/W3 + SwiGLU)",
-                "bytes_per_launch": w13_bytes(wl), "us_per_launch": w13_ms * 1000.0,
-                "timing": "CUDA events around standalone launches on the decoder's stream, layers cycled",
-                "peak_source": peak_src + " (MEASURED_PEAKS.json hbm_gbs, copy bandwidth)"}
+    # ---- roofline ----
+    if B == 1:
+        # dominant kernel (rmsnorm + W1/W3 + SwiGLU) timed alone, layers cycled
+        reps = max(1, 64 // wl.n_layers)
+        dec.launch_op("w13", 0, 1)
+        k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        k0.record(stream)
+        for _ in range(reps):
+            for layer in range(wl.n_layers):
+                dec.launch_op("w13", layer, 1)
+        k1.record(stream)
+        k1.synchronize()
+        w13_ms = k0.elapsed_time(k1) / (reps * wl.n_layers)
+        achieved = w13_bytes(wl) / (w13_ms / 1000.0) / 1e9
+        traffic = None
+        if W13_NCU_TRAFFIC is not None and (wl.dim, wl.hidden_dim) == (4096, 11008):
+            src = open(os.path.join(ROOT, "llama_transformer_decode_gb300", "csrc", "gemv.cu"), "rb").read()
+            if hashlib.sha256(src).hexdigest().startswith(W13_NCU_TRAFFIC[1]):
+                traffic = W13_NCU_TRAFFIC[0]
+        roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                    "traffic": traffic, "kernel": "gemv_kernel<GEMV_W13> (rmsnorm + W1/W3 + SwiGLU)",
+                    "bytes_per_launch": w13_bytes(wl), "us_per_launch": w13_ms * 1000.0,
+                    "timing": "CUDA events around standalone launches on the decoder's stream, layers cycled",
+                    "peak_source": peak_src + " (MEASURED_PEAKS.json hbm_gbs, copy bandwidth)"}
+    else:
+        # whole batched step: B/2 flop per weight byte
+        flops = 2.0 * B * (weight_bytes(wl) / 4.0) * args.steps
+        tflops = flops / (ms / 1000.0) / 1e12
+        alu = fp32_alu_peak_tflops(props)
+        if B / 2.0 < alu * 1e3 / hbm:  # B/2 flop per weight byte, below the fp32 ridge point
+            roofline = {"bound": "hbm", "achieved": step_gbs, "peak": hbm, "unit": "GB/s", "frac": step_gbs / hbm,
+                        "traffic": None, "kernel": "whole batched step (all kernels)",
+                        "peak_source": peak_src + " (MEASURED_PEAKS.json hbm_gbs)"}
+        else:
+            roofline = {"bound": "alu", "achieved": tflops, "peak": alu, "unit": "TFLOP/s", "frac": tflops / alu,
+                        "traffic": None, "kernel": "whole batched step (all kernels)",
+                        "peak_source": "fp32 FMA peak derived: SMs x 128 lanes x 2 flop x max SM clock"}
     dec.sync()
 
     # ---- CPU baseline: the oracle on this host's cores ----
     cpu = None
     if cpu_leg:
-        n, el, threads = oracle_rate(wl, host_w, toks, args.cpu_budget)
+        n, el, threads = oracle_rate(wl, host_w, streams[0], args.cpu_budget)
         cpu = {"value": n / el, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-               "sample": f"{n} teacher-forced oracle steps of {wl.name} at positions 0..{n - 1}"}
+               "sample": f"{n} teacher-forced oracle steps of {wl.name} (one sequence) at positions 0..{n - 1}"}
 
     clk = clocks.summary()
+    cfg = config_of(wl, B)
+    cfg["positions"] = (f"{timed_pos[0][0]}..{timed_pos[-1][0]}" if B == 1 else
+                        f"slot b from floor(b*{S}/{B}) + {args.warmup}, {args.steps} steps, wrapping at {S}")
     line = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "metric": METRIC if B == 1 else METRIC.replace("at batch 1", f"at batch {B}"),
+        "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded random weights and tokens)",
-        "config": dict(config_of(wl), positions=f"{timed[0]}..{timed[-1]}" if timed else ""),
+        "config": cfg,
         "hbm_roofline": {"achieved_gbs": step_gbs, "frac_of_8tbs": step_gbs / NOMINAL_HBM_GBS,
                          "frac_of_measured": step_gbs / hbm,
-                         "bytes_per_step_avg": bytes_total / max(1, len(timed))},
+                         "bytes_per_step_avg": bytes_total / max(1, len(timed_pos))},
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": kern * args.steps, "clocks": {k: clk[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
     }
@@ -363,6 +410,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default="llama2_7b", choices=sorted(WORKLOADS))
+    ap.add_argument("--batch", type=int, default=1,
+                    help="independent sequences per step at staggered positions (batched_1b: 16 or 64)")
     ap.add_argument("--layers", type=int, default=None,
                     help="decode only the first N layers of the workload (a smaller case, e.g. for profiling)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-baseline leg")
@@ -372,6 +421,8 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if not 1 <= args.batch <= 64:
+        ap.error("--batch must be in 1..64")
     wl = WORKLOADS[args.workload]
     if args.layers is not None:
         if not 1 <= args.layers <= wl.n_layers:

@@ -37,7 +37,8 @@ struct GemvPlan {
     int mode;
     int grid;
     size_t smem;
-    GemvParams base;  // layer-independent fields
+    int units, unit_rows, factor;  // work split: units of unit_rows rows; factor rows per row for W1/W3
+    GemvParams base;               // layer-independent fields
 };
 
 }  // namespace
@@ -59,6 +60,7 @@ struct l2_ctx {
     float2 *rope = nullptr;
     StepDev *step_dev = nullptr;
     int *err = nullptr;
+    float *ss_part = nullptr;  // batched steps: partial sums of x^2 [kMaxParts][max_batch]
 
     StepDev *step_host = nullptr;  // pinned ring
     cudaEvent_t ring_ev[kRing] = {};
@@ -186,6 +188,9 @@ void make_plans(l2_ctx *c) {
     const int G = c->num_sms;
     auto plan = [&](GemvPlan &pl, int mode, int n, int unit_rows, int units, int ymax_factor) {
         pl.mode = mode;
+        pl.units = units;
+        pl.unit_rows = unit_rows;
+        pl.factor = ymax_factor;
         pl.grid = units < G ? units : G;
         const int per = ceil_div(units, pl.grid);
         pl.smem = gemv_smem_bytes(n, per * unit_rows * ymax_factor);
@@ -281,7 +286,41 @@ AttnParams attn_params(const l2_ctx *c, int layer, int batch) {
     return a;
 }
 
+// Grid, shared memory and ring depth of a batched GEMV launch.
+struct BatchedShape {
+    int grid;
+    size_t smem;
+    int stages;
+};
+
+BatchedShape batched_shape(const l2_ctx *c, const GemvPlan &pl, int batch) {
+    BatchedShape bs{};
+    int G = pl.units < c->num_sms ? pl.units : c->num_sms;
+    for (;;) {
+        const int rows_max = ceil_div(pl.units, G) * pl.unit_rows * pl.factor;
+        if (gemv_batched_rows_ok(rows_max, batch) || G >= pl.units) {
+            bs.grid = G;
+            bs.smem = gemv_batched_smem(rows_max, batch, &bs.stages);
+            return bs;
+        }
+        G = 2 * G < pl.units ? 2 * G : pl.units;
+    }
+}
+
+cudaError_t launch_batched(l2_ctx *c, const GemvPlan &pl, int layer, int batch, cudaStream_t s, bool pdl) {
+    GemvParams g = layer_params(c, pl, layer);
+    g.batch = batch;
+    g.ss_part = c->ss_part;
+    g.ss_parts = batched_shape(c, c->plan_wo, batch).grid;
+    const BatchedShape bs = batched_shape(c, pl, batch);
+    return launch_gemv_batched(pl.mode, g, bs.grid, bs.smem, bs.stages, s, pdl);
+}
+
 cudaError_t launch_op(l2_ctx *c, int op, int layer, int batch, cudaStream_t s, bool pdl) {
+    if (batch > 1 && op != 1) {
+        const GemvPlan *pl[] = {&c->plan_qkv, nullptr, &c->plan_wo, &c->plan_w13, &c->plan_w2, &c->plan_cls};
+        return launch_batched(c, *pl[op], op == 5 ? 0 : layer, batch, s, pdl);
+    }
     switch (op) {
         case 0: {
             GemvParams g = layer_params(c, c->plan_qkv, layer);
@@ -345,7 +384,6 @@ int get_graph(l2_ctx *c, int batch, cudaGraphExec_t *out) {
 
 int submit(l2_ctx *c, int B, const int *tokens, const int *pos, float *logits_out) {
     if (B < 1 || B > c->max_batch) return fail(c, L2_EINVAL, "batch %d outside 1..%d", B, c->max_batch);
-    if (B > 1) return fail(c, L2_EINVAL, "batches of more than one sequence are not supported by this build");
     for (int b = 0; b < B; ++b) {
         if (tokens[b] < 0 || tokens[b] >= c->cfg.vocab_size)
             return fail(c, L2_EINVAL, "token %d of slot %d outside [0, %d)", tokens[b], b, c->cfg.vocab_size);
@@ -431,6 +469,7 @@ int l2_create(const L2Config *config, const L2Weights *weights, int max_batch, u
     c->attn = attn_plan(c->head_size, p.n_heads, p.n_kv_heads);
     if (!c->attn.ok) return bail(fail(c, L2_EINVAL, "unsupported head_size / GQA grouping"));
     CREATE_CUDA(gemv_init());
+    CREATE_CUDA(gemv_batched_init());
     CREATE_CUDA(attn_init());
 
     if (cuda_stream) {
@@ -458,7 +497,8 @@ int l2_create(const L2Config *config, const L2Weights *weights, int max_batch, u
         (rc = alloc_n(c, &c->ws_acc, ws * hs, "attention workspace")) ||
         (rc = alloc_n(c, &c->tickets, B * p.n_kv_heads, "attention tickets")) ||
         (rc = alloc_n(c, &c->rope, S * (hs / 2), "RoPE table")) || (rc = alloc_n(c, &c->step_dev, 1, "step inputs")) ||
-        (rc = alloc_n(c, &c->err, 1, "error word")))
+        (rc = alloc_n(c, &c->err, 1, "error word")) ||
+        (rc = alloc_n(c, &c->ss_part, (size_t)kMaxParts * B, "sum-of-squares partials")))
         return bail(rc);
     if (flags & L2_FLAG_DEBUG) {
         if ((rc = alloc_n(c, &c->dbg, B * L * p.n_heads * S, "attention probabilities"))) return bail(rc);
@@ -498,6 +538,12 @@ int l2_create(const L2Config *config, const L2Weights *weights, int max_batch, u
             return bail(fail(c, L2_EINVAL, "a GEMV stage needs %zu bytes of shared memory (> 227 KB); dim or hidden_dim too large",
                              pl->smem));
     if (c->attn.smem > 227 * 1024) return bail(fail(c, L2_EINVAL, "attention needs too much shared memory"));
+    for (int b = 2; b <= max_batch; ++b)
+        for (const GemvPlan *pl : {&c->plan_qkv, &c->plan_wo, &c->plan_w13, &c->plan_w2, &c->plan_cls}) {
+            const BatchedShape bs = batched_shape(c, *pl, b);
+            if (bs.smem > 227 * 1024 || bs.grid > kMaxParts)
+                return bail(fail(c, L2_EINVAL, "a batched GEMV of %d sequences does not fit one CTA's shared memory", b));
+        }
     CREATE_CUDA(cudaDeviceSynchronize());
 #undef CREATE_CUDA
     *out = c;

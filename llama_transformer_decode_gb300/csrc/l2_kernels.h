@@ -14,6 +14,16 @@ int gemv_threads();
 size_t gemv_smem_bytes(int n, int ymax);
 cudaError_t launch_gemv(int mode, const GemvParams &p, int grid, size_t smem, cudaStream_t stream, bool pdl);
 
+// Batched fused GEMV, B >= 2 sequences per step (gemv_batched.cu).
+cudaError_t gemv_batched_init();
+// Dynamic shared memory for at most rows_max local rows and `batch` sequences;
+// *stages receives the ring depth that fits.
+size_t gemv_batched_smem(int rows_max, int batch, int *stages);
+// Whether one CTA can hold rows_max rows for `batch` sequences in registers.
+int gemv_batched_rows_ok(int rows_max, int batch);
+cudaError_t launch_gemv_batched(int mode, const GemvParams &p, int grid, size_t smem, int stages, cudaStream_t stream,
+                                bool pdl);
+
 // Flash-decoding attention (attention.cu).
 struct AttnLaunch {
     int lp;       // lanes per cache row (power of two)

@@ -121,6 +121,19 @@ def make_weights(wl: Workload, seed: int | None = None) -> dict:
     return w
 
 
+def kv_rows(wl: Workload, slot: int, n_pos: int, which: str, std: float = 1.0,
+            seed: int | None = None) -> np.ndarray:
+    """A synthetic KV-cache prefix (n_layers, n_pos, kv_dim) ~ N(0, std^2) for
+    slot ``slot``; ``which`` is "k" or "v".  Stands in for rows 0..n_pos-1 that
+    earlier steps would have written."""
+    seed = wl.seed if seed is None else seed
+    tid = (200 if which == "k" else 300) + slot
+    out = np.empty((wl.n_layers, n_pos, wl.kv_dim), np.float32)
+    if out.size:
+        normal(seed, tid, 0, out.size, 0.0, std, out.reshape(-1))
+    return out
+
+
 def token_stream(wl: Workload, slot: int, count: int, start: int = 0, seed: int | None = None) -> np.ndarray:
     seed = wl.seed if seed is None else seed
     return tokens(seed, token_stream_id(slot), start, count, wl.vocab_size)
