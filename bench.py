@@ -319,6 +319,26 @@ def run_ours(args, wl):
     bytes_total = sum(weight_bytes(wl) + sum(kv_bytes(wl, p) for p in pos) for pos in timed_pos)
     step_gbs = bytes_total / (ms / 1000.0) / 1e9
 
+    # ---- rate at chosen positions (cache rows before them imported) ----
+    per_pos = {}
+    if B == 1 and not args.no_positions:
+        for p0 in (0, S // 4 - 1, S - 9):
+            dec.reset()
+            if p0:
+                dec.kv_import(synth.kv_rows(wl, 0, p0, "k"), synth.kv_rows(wl, 0, p0, "v"))
+            for p in range(p0, p0 + 2):
+                dec.forward(int(streams[0][p]), p, out[0])
+            a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a0.record(stream)
+            for p in range(p0 + 2, p0 + 8):
+                dec.forward(int(streams[0][p]), p, out[0])
+            a1.record(stream)
+            a1.synchronize()
+            t = a0.elapsed_time(a1) / 6
+            gb = sum(weight_bytes(wl) + kv_bytes(wl, p) for p in range(p0 + 2, p0 + 8)) / 6
+            per_pos[str(p0 + 2)] = {"tokens_per_s": 1000.0 / t, "ms_per_step": t, "gbs": gb / t / 1e6}
+        dec.sync()
+
     # ---- end to end through the public call with host output ----
     host_logits = np.empty(wl.vocab_size if B == 1 else (B, wl.vocab_size), np.float32)
     dec.reset()
@@ -392,7 +412,7 @@ def run_ours(args, wl):
         "hbm_roofline": {"achieved_gbs": step_gbs, "frac_of_8tbs": step_gbs / NOMINAL_HBM_GBS,
                          "frac_of_measured": step_gbs / hbm,
                          "bytes_per_step_avg": bytes_total / max(1, len(timed_pos))},
-        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "per_position": per_pos or None,
         "gpu_launches": kern * args.steps, "clocks": {k: clk[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
     }
     dec.close()
@@ -415,6 +435,7 @@ def main(argv=None):
     ap.add_argument("--layers", type=int, default=None,
                     help="decode only the first N layers of the workload (a smaller case, e.g. for profiling)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-baseline leg")
+    ap.add_argument("--no-positions", action="store_true", help="skip the per-position rates")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time for the CPU baseline")
     ap.add_argument("--reference-budget", type=float, default=90.0,
                     help="seconds of timed oracle work in --impl reference")

@@ -7,18 +7,22 @@
 // arithmetic intensity is B/2 flop per weight byte: at B = 16 the step is
 // still bandwidth-bound, at B = 64 it is bound by the fp32 CUDA cores.
 //
-// Design.  CTA c owns a balanced range of output rows (all pieces of it, e.g.
-// its W1 rows and the same W3 rows).  The K dimension is walked in tiles of
-// 64 columns: per tile, the CTA's row segments (256 B each) and the B input
-// segments land in shared memory by 1-D bulk async copies (TMA) on one
-// mbarrier per ring stage.  Each thread owns 4 rows x 8 sequences of the
-// output (32 accumulators, two such tiles at most) for a subset of the tile's
-// 16-byte column words; per word it loads 4 weight and 8 input words and does
-// 128 FMAs.  Partial sums of the column groups are added in a fixed order at
-// the end, so results do not depend on timing.  RMSNorm: the gain is applied
-// to the input tile in shared memory, the 1/rms factor of each sequence to its
-// outputs; the sums of squares come from the residual kernels' epilogues
-// (per-CTA partials added in CTA order), so no CTA re-reads all of x.
+// Design.  CTA c owns a balanced range of rows of one matrix (for W1/W3 the
+// same rows of both).  K is walked in tiles of up to 256 columns: per tile,
+// one 2-D tensor copy (TMA, cp.async.bulk.tensor) brings the CTA's rows x tile
+// columns of each weight matrix into shared memory and one brings the B input
+// rows x tile columns, all completing on one mbarrier per ring stage.  (Copies
+// per row would be many small TMA operations, and the operation count, not the
+// bytes, then limits the rate.)  Each warp owns an output tile of 8 rows x 8
+// sequences (64 accumulators per lane); its lanes split the columns, so every
+// shared-memory read is 32 consecutive 16-byte words of one row, and per word
+// a lane loads 8 weight and 8 input words for 256 FMAs.  A CTA holds at most
+// 8 tiles, so the host sizes the row ranges (and the grid) from the batch.
+// Lane partials are reduced with shuffles in a fixed order.  RMSNorm: the gain
+// scales the input tile in shared memory, 1/rms scales the outputs, and the
+// sums of squares come from the residual kernels' epilogues (per-CTA partials
+// added in CTA order), so no CTA re-reads the whole of x.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "l2_device.cuh"
@@ -28,24 +32,14 @@ namespace l2 {
 
 namespace {
 
-constexpr int kBT = 256;        // threads
-constexpr int kTK = 64;         // K columns per tile
-constexpr int kTKP = kTK + 4;   // padded shared-memory row (floats): rows start 16 B apart in bank terms
-constexpr int kRR = 4;          // rows per thread tile
-constexpr int kBB = 8;          // sequences per thread tile
-constexpr int kMT = 2;          // thread tiles per thread at most
+constexpr int kBT = 256;             // threads
+constexpr int kTR = 8;               // rows per warp tile
+constexpr int kTB = 8;               // sequences per warp tile
+constexpr int kMaxTiles = kBT / 32;  // one warp tile per warp
 constexpr int kMaxStages = 4;
-
-struct BPiece {
-    const float *src;  // first row of the piece
-    int rows;
-    int yoff;          // local row of the piece's first row
-};
 
 struct BatchFixed {
     uint64_t bars[kMaxStages];
-    BPiece pieces[3];
-    int npieces;
     int failed;
     float inv[kMaxBatch];
 };
@@ -54,114 +48,102 @@ __host__ __device__ constexpr size_t fixed_b_bytes() { return (sizeof(BatchFixed
 
 __device__ __forceinline__ float silu_b(float v) { return v / (1.0f + expf(-v)); }
 
-__host__ __device__ inline int kgroups_for(int tiles) {
-    int kg = 1;
-    while (kg < 16 && tiles * kg * 2 <= kBT) kg <<= 1;
-    return kg;
+// Raises the bytes a barrier phase waits for, without arriving on it.
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+// 2-D tiled tensor copy global -> shared; coordinates {column, row}.
+__device__ __forceinline__ void tensor_g2s(void *dst, const CUtensorMap *map, int c0, int c1, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+        : "memory");
 }
 
 }  // namespace
 
 template <int MODE>
-__global__ void __launch_bounds__(kBT, 1) gemv_batched_kernel(const GemvParams p, int stages) {
+__global__ void __launch_bounds__(kBT, 1) gemv_batched_kernel(const __grid_constant__ BatchParams bp) {
+    const GemvParams &p = bp.g;
     extern __shared__ __align__(128) unsigned char smem[];
     auto &fx = *reinterpret_cast<BatchFixed *>(smem);
     float *region = reinterpret_cast<float *>(smem + fixed_b_bytes());
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int B = p.batch, n = p.n;
+    const int B = p.batch, n = p.n, tk = bp.tk, RB = bp.rows_box, stages = bp.stages;
 
-    const long long u0 = (long long)blockIdx.x * p.total_units / gridDim.x;
-    const long long u1 = (long long)(blockIdx.x + 1) * p.total_units / gridDim.x;
-    const int vr0 = (int)(u0 * p.unit_rows);
-    const int R = (int)((u1 - u0) * p.unit_rows);
-    const int RT = (MODE == GEMV_W13) ? 2 * R : R;
-    const int stage_floats = (RT + B) * kTKP;
-    const int NKT = (n + kTK - 1) / kTK;
+    // ---- this CTA's matrix and rows ----
+    int m = 0, cta = blockIdx.x;
+    while (m < 2 && cta >= bp.part_ctas[m]) cta -= bp.part_ctas[m++];
+    const int units = bp.part_units[m], nct = bp.part_ctas[m];
+    const long long u0 = (long long)cta * units / nct, u1 = (long long)(cta + 1) * units / nct;
+    const int r0 = (int)(u0 * p.unit_rows);        // first row within matrix m
+    const int R = (int)((u1 - u0) * p.unit_rows);  // rows of this CTA (<= RB)
+    const int npc = (MODE == GEMV_W13) ? 2 : 1;    // weight pieces (W1 and W3 share rows)
+    const int SR = npc * RB;                       // weight rows in a stage (piece pc at row pc*RB)
+    const int mrows = (MODE == GEMV_QKV) ? (m == 0 ? p.rows0 : p.rows1) : p.total_units * p.unit_rows;
+    const int wrow0 = (MODE == GEMV_CLS ? 0 : p.layer * mrows) + r0;  // tensor-map row of the first row
+    const int stage_floats = (SR + B) * tk;
+    const int NKT = (n + tk - 1) / tk;
+    const bool emb_rows = (MODE == GEMV_QKV && p.layer == 0);  // inputs gathered from the embedding table
 
     if (tid == 0) {
-        int np = 0;
-        if (R > 0) {
-            if (MODE == GEMV_QKV) {
-                const float *mats[3] = {p.mat0, p.mat1, p.mat2};
-                const int rws[3] = {p.rows0, p.rows1, p.rows2};
-                int b0 = 0;
-                for (int m = 0; m < 3; ++m) {
-                    const int lo = max(vr0, b0), hi = min(vr0 + R, b0 + rws[m]);
-                    if (lo < hi) fx.pieces[np++] = {mats[m] + (size_t)(lo - b0) * n, hi - lo, lo - vr0};
-                    b0 += rws[m];
-                }
-            } else if (MODE == GEMV_W13) {
-                fx.pieces[0] = {p.mat0 + (size_t)vr0 * n, R, 0};
-                fx.pieces[1] = {p.mat1 + (size_t)vr0 * n, R, R};
-                np = 2;
-            } else {
-                fx.pieces[0] = {p.mat0 + (size_t)vr0 * n, R, 0};
-                np = 1;
-            }
-        }
-        fx.npieces = np;
         fx.failed = 0;
         for (int i = 0; i < stages; ++i) mbar_init(&fx.bars[i], 1);
         fence_barrier_init();
     }
     __syncthreads();
-    if (RT == 0) return;
+    if (R <= 0) return;
 
-    // Global address of local weight row i.
-    auto row_src = [&](int i) -> const float * {
-        int pi = 0;
-        while (pi + 1 < fx.npieces && i >= fx.pieces[pi + 1].yoff) ++pi;
-        return fx.pieces[pi].src + (size_t)(i - fx.pieces[pi].yoff) * n;
-    };
-    // Global address of sequence b's input vector.
-    auto in_src = [&](int b) -> const float * {
-        if (MODE == GEMV_RESID) return p.in_vec + (size_t)b * n;
-        if (MODE == GEMV_QKV && p.layer == 0) return p.emb + (size_t)p.step->token[b] * p.dim;
-        return p.x + (size_t)b * n;
-    };
-    const bool in_ready_early = (MODE == GEMV_QKV && p.layer == 0);  // embedding rows: read-only
-
-    // Issue K tile kt into stage s (warp 0).  With `weights_only`, only the
-    // weight rows (which do not depend on the previous kernel).
-    auto issue = [&](int kt, int s, bool weights_only, bool inputs_only) {
-        const int k0 = kt * kTK, len = min(kTK, n - k0);
-        const uint32_t bytes = (uint32_t)len * 4u;
-        float *W = region + (size_t)s * stage_floats;
-        float *X = W + (size_t)RT * kTKP;
+    // Requests for K tile kt into stage s, by lane 0 of warp 0 (lanes of warp 0
+    // for the embedding rows).  The weight half only raises the expected bytes;
+    // the input half arrives, so a stage cannot complete before both halves
+    // have been requested.  The weights do not depend on the previous kernel
+    // and are requested before waiting on it.
+    auto issue_weights = [&](int kt, int s) {
         if (lane == 0) {
-            // One arrival per stage use.  A weights-only request only raises the
-            // expected bytes, so the stage cannot complete before the inputs'
-            // request (which arrives) has been made.
-            if (weights_only)
-                asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(&fx.bars[s])),
-                             "r"((uint32_t)RT * bytes)
-                             : "memory");
-            else
-                mbar_arrive_expect_tx(&fx.bars[s], (inputs_only ? 0u : (uint32_t)RT * bytes) + (uint32_t)B * bytes);
+            float *W = region + (size_t)s * stage_floats;
+            mbar_expect_tx(&fx.bars[s], (uint32_t)(SR * tk * 4));
+            for (int pc = 0; pc < npc; ++pc)
+                tensor_g2s(W + (size_t)pc * RB * tk, &bp.wmap[MODE == GEMV_QKV ? m : pc], kt * tk, wrow0, &fx.bars[s]);
         }
-        __syncwarp();
-        if (!inputs_only)
-            for (int i = lane; i < RT; i += 32) bulk_g2s_nohint(W + (size_t)i * kTKP, row_src(i) + k0, bytes, &fx.bars[s]);
-        if (!weights_only)
-            for (int b = lane; b < B; b += 32) bulk_g2s_nohint(X + (size_t)b * kTKP, in_src(b) + k0, bytes, &fx.bars[s]);
+    };
+    auto issue_inputs = [&](int kt, int s) {
+        float *X = region + (size_t)s * stage_floats + (size_t)SR * tk;
+        const int k0 = kt * tk, len = min(tk, n - k0);
+        if (emb_rows) {
+            // one embedding row per sequence; columns past n stay unused
+            if (lane == 0) mbar_arrive_expect_tx(&fx.bars[s], (uint32_t)(B * len * 4));
+            __syncwarp();
+            for (int b = lane; b < B; b += 32)
+                bulk_g2s_nohint(X + (size_t)b * tk, p.emb + (size_t)p.step->token[b] * p.dim + k0, (uint32_t)len * 4u,
+                                &fx.bars[s]);
+        } else if (lane == 0) {
+            mbar_arrive_expect_tx(&fx.bars[s], (uint32_t)(B * tk * 4));
+            tensor_g2s(X, &bp.xmap, k0, 0, &fx.bars[s]);
+        }
     };
 
-    // Weights of the first stages before waiting on the previous kernel.
     const int pre = min(stages, NKT);
     if (warp == 0)
-        for (int kt = 0; kt < pre; ++kt) issue(kt, kt, !in_ready_early, false);
+        for (int kt = 0; kt < pre; ++kt) {
+            issue_weights(kt, kt);
+            if (emb_rows) issue_inputs(kt, kt);  // the embedding table is read-only
+        }
 
     pdl_launch_dependents();
     pdl_wait();
 
-    if (warp == 0 && !in_ready_early)
-        for (int kt = 0; kt < pre; ++kt) issue(kt, kt, false, true);
+    if (warp == 0 && !emb_rows)
+        for (int kt = 0; kt < pre; ++kt) issue_inputs(kt, kt);
 
     // 1/rms of each sequence
     if (MODE != GEMV_RESID) {
-        if (MODE == GEMV_QKV && p.layer == 0) {
+        if (emb_rows) {
             for (int b = warp; b < B; b += kBT / 32) {
-                const float4 *e4 = reinterpret_cast<const float4 *>(in_src(b));
+                const float4 *e4 = reinterpret_cast<const float4 *>(p.emb + (size_t)p.step->token[b] * p.dim);
                 float ss = 0.f;
                 for (int i = lane; i < n / 4; i += 32) {
                     const float4 v = e4[i];
@@ -178,25 +160,26 @@ __global__ void __launch_bounds__(kBT, 1) gemv_batched_kernel(const GemvParams p
                 }
             }
         } else {
-            for (int b = tid; b < B; b += kBT) {
+            // a warp per sequence; lanes add strided partials, then a fixed-order reduction
+            for (int b = warp; b < B; b += kBT / 32) {
                 float ss = 0.f;
-                for (int i = 0; i < p.ss_parts; ++i) ss += __ldcg(p.ss_part + (size_t)i * B + b);
-                fx.inv[b] = 1.0f / sqrtf(ss / (float)n + 1e-5f);
+                for (int i = lane; i < p.ss_parts; i += 32) ss += __ldcg(p.ss_part + (size_t)i * B + b);
+                ss = warp_sum(ss);
+                if (lane == 0) fx.inv[b] = 1.0f / sqrtf(ss / (float)n + 1e-5f);
             }
         }
     }
 
-    // thread tiles
-    const int TRG = (RT + kRR - 1) / kRR, TBG = (B + kBB - 1) / kBB, T = TRG * TBG;
-    const int KG = kgroups_for(T);
-    const int kg = tid % KG, t0 = tid / KG, tstride = kBT / KG;
-    float acc[kMT][kRR][kBB];
+    // Warp w owns the output tile of stage rows 8*(w % TRG).. and sequences
+    // 8*(w / TRG)..; its 32 lanes split the tile's columns.
+    const int TRG = (SR + kTR - 1) / kTR, TBG = (B + kTB - 1) / kTB, T = TRG * TBG;
+    const bool busy = warp < T;
+    const int rg = warp % TRG, bg = warp / TRG;
+    float acc[kTR][kTB];
 #pragma unroll
-    for (int m = 0; m < kMT; ++m)
+    for (int i = 0; i < kTR; ++i)
 #pragma unroll
-        for (int i = 0; i < kRR; ++i)
-#pragma unroll
-            for (int j = 0; j < kBB; ++j) acc[m][i][j] = 0.f;
+        for (int j = 0; j < kTB; ++j) acc[i][j] = 0.f;
 
     bool ok = true;
 #pragma unroll 1
@@ -211,45 +194,53 @@ __global__ void __launch_bounds__(kBT, 1) gemv_batched_kernel(const GemvParams p
             ok = false;
             break;
         }
-        const int k0 = kt * kTK, len = min(kTK, n - k0), len4 = len >> 2;
+        const int k0 = kt * tk, len = min(tk, n - k0), len4 = len >> 2;
         const float *W = region + (size_t)s * stage_floats;
-        float *X = const_cast<float *>(W) + (size_t)RT * kTKP;
+        float *X = const_cast<float *>(W) + (size_t)SR * tk;
         if (MODE != GEMV_RESID) {
-            for (int e = tid; e < B * len; e += kBT) {
-                const int b = e / len, k = e - b * len;
-                X[(size_t)b * kTKP + k] *= __ldg(p.norm_w + k0 + k);
+            // the RMSNorm gain, applied to the input tile in place
+            const float4 *g4 = reinterpret_cast<const float4 *>(p.norm_w + k0);
+            for (int f = lane; f < len4; f += 32) {
+                const float4 g = __ldg(g4 + f);
+                for (int b = warp; b < B; b += kBT / 32) {
+                    float4 *xv = reinterpret_cast<float4 *>(X + (size_t)b * tk) + f;
+                    float4 v = *xv;
+                    v.x *= g.x;
+                    v.y *= g.y;
+                    v.z *= g.z;
+                    v.w *= g.w;
+                    *xv = v;
+                }
             }
             __syncthreads();
         }
+        if (busy) {
+            const float4 *wr[kTR];
+            const float4 *xr[kTB];
 #pragma unroll
-        for (int m = 0; m < kMT; ++m) {
-            const int t = t0 + m * tstride;
-            if (t < T) {
-                const int rg = t % TRG, bg = t / TRG;
-                const float4 *wr[kRR];
-                const float4 *xr[kBB];
+            for (int i = 0; i < kTR; ++i)
+                wr[i] = reinterpret_cast<const float4 *>(W + (size_t)min(rg * kTR + i, SR - 1) * tk);
 #pragma unroll
-                for (int i = 0; i < kRR; ++i)
-                    wr[i] = reinterpret_cast<const float4 *>(W + (size_t)min(rg * kRR + i, RT - 1) * kTKP);
-#pragma unroll
-                for (int j = 0; j < kBB; ++j)
-                    xr[j] = reinterpret_cast<const float4 *>(X + (size_t)min(bg * kBB + j, B - 1) * kTKP);
+            for (int j = 0; j < kTB; ++j)
+                xr[j] = reinterpret_cast<const float4 *>(X + (size_t)min(bg * kTB + j, B - 1) * tk);
 #pragma unroll 1
-                for (int k4 = kg; k4 < len4; k4 += KG) {
-                    float4 w4[kRR], x4[kBB];
+            for (int f = lane; f < len4; f += 32) {
+                float4 w4[kTR], x4[kTB];
 #pragma unroll
-                    for (int i = 0; i < kRR; ++i) w4[i] = wr[i][k4];
+                for (int i = 0; i < kTR; ++i) w4[i] = wr[i][f];
 #pragma unroll
-                    for (int j = 0; j < kBB; ++j) x4[j] = xr[j][k4];
+                for (int j = 0; j < kTB; ++j) x4[j] = xr[j][f];
 #pragma unroll
-                    for (int i = 0; i < kRR; ++i)
+                for (int i = 0; i < kTR; ++i)
 #pragma unroll
-                        for (int j = 0; j < kBB; ++j) acc[m][i][j] = dot4(w4[i], x4[j], acc[m][i][j]);
-                }
+                    for (int j = 0; j < kTB; ++j) acc[i][j] = dot4(w4[i], x4[j], acc[i][j]);
             }
         }
         __syncthreads();
-        if (warp == 0 && kt + stages < NKT) issue(kt + stages, s, false, false);
+        if (warp == 0 && kt + stages < NKT) {
+            issue_weights(kt + stages, s);
+            issue_inputs(kt + stages, s);
+        }
     }
     if (!ok) {
         // Let the copies already requested land (bounded waits) before leaving.
@@ -258,53 +249,40 @@ __global__ void __launch_bounds__(kBT, 1) gemv_batched_kernel(const GemvParams p
         return;
     }
 
-    // add up the column groups in a fixed order
-    float *red = region;  // [KG][RT][B]
+    // reduce each output over the lanes; ys[stage row][sequence] in shared memory
+    float *ys = region;
+    if (busy) {
 #pragma unroll
-    for (int m = 0; m < kMT; ++m) {
-        const int t = t0 + m * tstride;
-        if (t < T) {
-            const int rg = t % TRG, bg = t / TRG;
+        for (int i = 0; i < kTR; ++i)
 #pragma unroll
-            for (int i = 0; i < kRR; ++i)
-#pragma unroll
-                for (int j = 0; j < kBB; ++j) {
-                    const int r = rg * kRR + i, b = bg * kBB + j;
-                    if (r < RT && b < B) red[((size_t)kg * RT + r) * B + b] = acc[m][i][j];
-                }
-        }
-    }
-    __syncthreads();
-    float *ys = region + (size_t)KG * RT * B;  // [RT][B]
-    for (int e = tid; e < RT * B; e += kBT) {
-        float v = 0.f;
-        for (int g = 0; g < KG; ++g) v += red[(size_t)g * RT * B + e];
-        if (MODE != GEMV_RESID) v *= fx.inv[e % B];
-        ys[e] = v;
+            for (int j = 0; j < kTB; ++j) {
+                const float v = warp_sum(acc[i][j]);
+                const int r = rg * kTR + i, b = bg * kTB + j;
+                if (lane == 0 && r < SR && b < B) ys[(size_t)r * B + b] = (MODE != GEMV_RESID) ? v * fx.inv[b] : v;
+            }
     }
     __syncthreads();
 
-    // ---- epilogue ----
+    // ---- epilogue (rows 0..R-1 of each piece) ----
     if (MODE == GEMV_QKV) {
         const int hs = p.head_size, half = hs >> 1;
         for (int e = tid; e < (R >> 1) * B; e += kBT) {
             const int pi = e / B, b = e - pi * B;
-            const int j = 2 * pi, v = vr0 + j;
+            const int j = 2 * pi;
             const float y0 = ys[(size_t)j * B + b], y1 = ys[(size_t)(j + 1) * B + b];
             const int pos = p.step->pos[b];
             const float2 *rr = p.rope + (size_t)pos * half;
-            if (v < p.dim) {
+            const int v = r0 + j;  // row within matrix m
+            if (m == 0) {
                 const float2 cs = rr[(v % hs) >> 1];
                 float *q = p.q + (size_t)b * p.dim;
                 q[v] = y0 * cs.x - y1 * cs.y;
                 q[v + 1] = y0 * cs.y + y1 * cs.x;
             } else {
-                const bool is_k = v < p.dim + p.kv_dim;
-                const int c = is_k ? v - p.dim : v - p.dim - p.kv_dim;
-                const int g = c / hs, d = c % hs;
+                const int g = v / hs, d = v % hs;
                 const size_t idx =
                     ((((size_t)b * p.n_layers + p.layer) * p.n_kv_heads + g) * p.seq_len + pos) * hs + d;
-                if (is_k) {
+                if (m == 1) {
                     const float2 cs = rr[d >> 1];
                     p.kcache[idx] = y0 * cs.x - y1 * cs.y;
                     p.kcache[idx + 1] = y0 * cs.y + y1 * cs.x;
@@ -318,13 +296,13 @@ __global__ void __launch_bounds__(kBT, 1) gemv_batched_kernel(const GemvParams p
         const int hidden = p.total_units;
         for (int e = tid; e < R * B; e += kBT) {
             const int r = e / B, b = e - r * B;
-            p.hb[(size_t)b * hidden + vr0 + r] = silu_b(ys[e]) * ys[(size_t)(R + r) * B + b];
+            p.hb[(size_t)b * hidden + r0 + r] = silu_b(ys[e]) * ys[(size_t)(RB + r) * B + b];
         }
     } else if (MODE == GEMV_RESID) {
         const int dim = p.total_units;
         for (int e = tid; e < R * B; e += kBT) {
             const int r = e / B, b = e - r * B;
-            float *xp = p.x + (size_t)b * dim + vr0 + r;
+            float *xp = p.x + (size_t)b * dim + r0 + r;
             const float nv = *xp + ys[e];
             *xp = nv;
             ys[e] = nv;
@@ -340,30 +318,29 @@ __global__ void __launch_bounds__(kBT, 1) gemv_batched_kernel(const GemvParams p
         const int V = p.total_units;
         for (int e = tid; e < R * B; e += kBT) {
             const int r = e / B, b = e - r * B;
-            p.logits[(size_t)b * V + vr0 + r] = ys[e];
-            if (user) user[(size_t)b * V + vr0 + r] = ys[e];
+            p.logits[(size_t)b * V + r0 + r] = ys[e];
+            if (user) user[(size_t)b * V + r0 + r] = ys[e];
         }
     }
 }
 
 // ---------------------------------------------------------------- host side
 
-size_t gemv_batched_smem(int rows_max, int batch, int *stages) {
-    const size_t stage = (size_t)(rows_max + batch) * kTKP * 4;
-    int st = kMaxStages;
+int gemv_batched_rows_cap(int batch) { return kTR * (kMaxTiles / ((batch + kTB - 1) / kTB)); }
+
+size_t gemv_batched_smem(int stage_rows, int batch, int n, int *stages, int *tk) {
+    // The widest K tile (fewer, bigger copies and fewer barriers) that still
+    // leaves three ring stages; two stages of 64 columns at the least.
     const size_t limit = 227 * 1024 - fixed_b_bytes();
+    int t = 256;
+    while (t > 64 && (3 * (size_t)(stage_rows + batch) * t * 4 > limit || t >= 2 * n)) t >>= 1;
+    const size_t stage = (size_t)(stage_rows + batch) * t * 4;
+    int st = kMaxStages;
     while (st > 2 && st * stage > limit) --st;
     *stages = st;
-    // After the K loop the same memory holds the column-group partials
-    // [KG][RT][B] and the sums [RT][B]; KG*RT <= max(1024, RT) for any RT.
-    const size_t rb = (size_t)rows_max * batch;
-    const size_t red = 4 * ((rb > 8192 ? rb : 8192) + rb);
-    return fixed_b_bytes() + (st * stage > red ? st * stage : red);
-}
-
-int gemv_batched_rows_ok(int rows_max, int batch) {
-    const int T = ((rows_max + kRR - 1) / kRR) * ((batch + kBB - 1) / kBB);
-    return T <= kMT * kBT && batch <= kMaxBatch;
+    *tk = t;
+    const size_t ys = (size_t)stage_rows * batch * 4;  // reuses the ring after the K loop
+    return fixed_b_bytes() + (st * stage > ys ? st * stage : ys);
 }
 
 cudaError_t gemv_batched_init() {
@@ -378,8 +355,7 @@ cudaError_t gemv_batched_init() {
     return cudaSuccess;
 }
 
-cudaError_t launch_gemv_batched(int mode, const GemvParams &p, int grid, size_t smem, int stages, cudaStream_t stream,
-                                bool pdl) {
+cudaError_t launch_gemv_batched(int mode, const BatchParams &bp, int grid, size_t smem, cudaStream_t stream, bool pdl) {
     void *fn = nullptr;
     switch (mode) {
         case GEMV_QKV: fn = reinterpret_cast<void *>(gemv_batched_kernel<GEMV_QKV>); break;
@@ -398,7 +374,7 @@ cudaError_t launch_gemv_batched(int mode, const GemvParams &p, int grid, size_t 
     attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    void *args[] = {const_cast<GemvParams *>(&p), &stages};
+    void *args[] = {const_cast<BatchParams *>(&bp)};
     return cudaLaunchKernelExC(&cfg, fn, args);
 }
 

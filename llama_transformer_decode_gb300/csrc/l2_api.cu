@@ -33,6 +33,17 @@ constexpr int kMinChunk = 32;  // fewest cache positions per attention CTA
 thread_local std::string g_create_error;
 int g_fail_alloc_at = 0;  // fault injection: fail the n-th device allocation
 
+struct BatchPlan {
+    BatchParams bp;  // tensor maps, partition, tiles (layer fields filled per launch)
+    int grid;
+    size_t smem;
+};
+
+struct BatchSet {
+    bool built = false;
+    BatchPlan plan[5];  // QKV, Wo, W1/W3, W2, classifier
+};
+
 struct GemvPlan {
     int mode;
     int grid;
@@ -72,6 +83,7 @@ struct l2_ctx {
     AttnLaunch attn{};
     int attn_chunks = 1;
     GemvPlan plan_qkv{}, plan_wo{}, plan_w13{}, plan_w2{}, plan_cls{};
+    std::vector<BatchSet> bsets;  // batched GEMV plans, indexed by batch size
     bool evict_first = false;
 
     std::vector<int> written;  // cache rows written per slot
@@ -255,6 +267,19 @@ GemvParams layer_params(const l2_ctx *c, const GemvPlan &pl, int layer) {
     return g;
 }
 
+// Attention CTAs per (slot, KV head): as many as fill every SM with the
+// CTAs that fit on it, in one wave, and no more than one per kMinChunk
+// positions of the cache.
+int attn_chunks_for(const l2_ctx *c, int batch) {
+    int per_sm = (int)((227 * 1024) / (c->attn.smem + 1024));
+    if (per_sm > 4) per_sm = 4;
+    if (per_sm < 1) per_sm = 1;
+    int nc = (int)(((long long)per_sm * c->num_sms) / ((long long)c->cfg.n_kv_heads * batch));
+    const int cap = ceil_div(c->cfg.seq_len, kMinChunk);
+    if (nc > cap) nc = cap;
+    return nc < 1 ? 1 : nc;
+}
+
 AttnParams attn_params(const l2_ctx *c, int layer, int batch) {
     const L2Config &p = c->cfg;
     AttnParams a{};
@@ -275,51 +300,144 @@ AttnParams attn_params(const l2_ctx *c, int layer, int batch) {
     a.head_size = c->head_size;
     a.seq_len = p.seq_len;
     a.dim = p.dim;
-    int nc = ceil_div(2LL * c->num_sms, (long long)p.n_kv_heads * batch);
-    const int cap = ceil_div(p.seq_len, kMinChunk);
-    if (nc > cap) nc = cap;
+    int nc = attn_chunks_for(c, batch);
     if (nc > c->attn_chunks) nc = c->attn_chunks;
-    if (nc < 1) nc = 1;
     a.n_chunks = nc;
     a.min_chunk = kMinChunk;
     a.scale = (float)(1.0 / std::sqrt((double)c->head_size));
     return a;
 }
 
-// Grid, shared memory and ring depth of a batched GEMV launch.
-struct BatchedShape {
-    int grid;
-    size_t smem;
-    int stages;
-};
+// ---- batched GEMV plans: grid, tensor maps and tiles per batch size ----
 
-BatchedShape batched_shape(const l2_ctx *c, const GemvPlan &pl, int batch) {
-    BatchedShape bs{};
-    int G = pl.units < c->num_sms ? pl.units : c->num_sms;
-    for (;;) {
-        const int rows_max = ceil_div(pl.units, G) * pl.unit_rows * pl.factor;
-        if (gemv_batched_rows_ok(rows_max, batch) || G >= pl.units) {
-            bs.grid = G;
-            bs.smem = gemv_batched_smem(rows_max, batch, &bs.stages);
-            return bs;
-        }
-        G = 2 * G < pl.units ? 2 * G : pl.units;
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
     }
+    return fn;
 }
 
-cudaError_t launch_batched(l2_ctx *c, const GemvPlan &pl, int layer, int batch, cudaStream_t s, bool pdl) {
-    GemvParams g = layer_params(c, pl, layer);
-    g.batch = batch;
-    g.ss_part = c->ss_part;
-    g.ss_parts = batched_shape(c, c->plan_wo, batch).grid;
-    const BatchedShape bs = batched_shape(c, pl, batch);
-    return launch_gemv_batched(pl.mode, g, bs.grid, bs.smem, bs.stages, s, pdl);
+// Row-major fp32 matrix [rows][cols] seen as 2-D tiles of box_rows x box_cols.
+bool encode_matrix(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows, uint32_t box_cols,
+                   uint32_t box_rows) {
+    EncodeTiledFn fn = encode_tiled();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols * 4};
+    const cuuint32_t box[2] = {box_cols, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Builds the five batched GEMV plans (QKV, Wo, W1/W3, W2, classifier) for
+// `batch` sequences.  Returns L2_OK or an error code.
+int build_batch_set(l2_ctx *c, int batch) {
+    const L2Config &p = c->cfg;
+    BatchSet &set = c->bsets[batch];
+    const int cap = gemv_batched_rows_cap(batch);
+    const GemvPlan *plans[5] = {&c->plan_qkv, &c->plan_wo, &c->plan_w13, &c->plan_w2, &c->plan_cls};
+    const size_t L = p.n_layers;
+    for (int k = 0; k < 5; ++k) {
+        const GemvPlan &pl = *plans[k];
+        BatchPlan &bpl = set.plan[k];
+        BatchParams &bp = bpl.bp;
+        memset(&bp, 0, sizeof(bp));
+        const int npc = pl.mode == GEMV_W13 ? 2 : 1;
+        int upc = cap / (pl.unit_rows * npc);  // units per CTA at most
+        if (upc < 1) upc = 1;
+        int rows_box = 0, grid = 0;
+        if (pl.mode == GEMV_QKV) {
+            const int u[3] = {p.dim / 2, c->kv_dim / 2, c->kv_dim / 2};
+            const int total = u[0] + u[1] + u[2];
+            int target = ceil_div(u[0], upc) + ceil_div(u[1], upc) + ceil_div(u[2], upc);
+            if (target < c->num_sms) target = c->num_sms;
+            for (int m = 0; m < 3; ++m) {
+                int g = (int)(((long long)target * u[m] + total / 2) / total);
+                if (g < ceil_div(u[m], upc)) g = ceil_div(u[m], upc);
+                if (g > u[m]) g = u[m];
+                if (g < 1) g = 1;
+                bp.part_ctas[m] = g;
+                bp.part_units[m] = u[m];
+                grid += g;
+                const int rb = ceil_div(u[m], g) * 2;
+                if (rb > rows_box) rows_box = rb;
+            }
+        } else {
+            grid = pl.units < c->num_sms ? pl.units : c->num_sms;
+            if (ceil_div(pl.units, upc) > grid) grid = ceil_div(pl.units, upc);
+            bp.part_ctas[0] = grid;
+            bp.part_units[0] = pl.units;
+            rows_box = ceil_div(pl.units, grid) * pl.unit_rows;
+        }
+        bp.rows_box = rows_box;
+        bpl.grid = grid;
+        bpl.smem = gemv_batched_smem(npc * rows_box, batch, pl.base.n, &bp.stages, &bp.tk);
+        if (bpl.smem > 227 * 1024 || npc * rows_box > cap)
+            return fail(c, L2_EINVAL, "a batched GEMV of %d sequences does not fit one CTA", batch);
+        if (pl.mode == GEMV_RESID && grid > kMaxParts)
+            return fail(c, L2_EINVAL, "a batched residual GEMV of %d sequences needs too many CTAs", batch);
+        // weight tensor maps: all layers stacked as one tall matrix
+        const uint32_t tk = (uint32_t)bp.tk, rb = (uint32_t)rows_box;
+        bool ok = true;
+        const uint64_t D = p.dim, H = p.hidden_dim, KVD = c->kv_dim;
+        switch (k) {
+            case 0:
+                ok = encode_matrix(&bp.wmap[0], c->w.wq, D, L * D, tk, rb) &&
+                     encode_matrix(&bp.wmap[1], c->w.wk, D, L * KVD, tk, rb) &&
+                     encode_matrix(&bp.wmap[2], c->w.wv, D, L * KVD, tk, rb) &&
+                     encode_matrix(&bp.xmap, c->x, D, c->max_batch, tk, batch);
+                break;
+            case 1:
+                ok = encode_matrix(&bp.wmap[0], c->w.wo, D, L * D, tk, rb) &&
+                     encode_matrix(&bp.xmap, c->xb, D, c->max_batch, tk, batch);
+                break;
+            case 2:
+                ok = encode_matrix(&bp.wmap[0], c->w.w1, D, L * H, tk, rb) &&
+                     encode_matrix(&bp.wmap[1], c->w.w3, D, L * H, tk, rb) &&
+                     encode_matrix(&bp.xmap, c->x, D, c->max_batch, tk, batch);
+                break;
+            case 3:
+                ok = encode_matrix(&bp.wmap[0], c->w.w2, H, L * D, tk, rb) &&
+                     encode_matrix(&bp.xmap, c->hb, H, c->max_batch, tk, batch);
+                break;
+            case 4:
+                ok = encode_matrix(&bp.wmap[0], c->w.wcls, D, (uint64_t)p.vocab_size, tk, rb) &&
+                     encode_matrix(&bp.xmap, c->x, D, c->max_batch, tk, batch);
+                break;
+        }
+        if (!ok) return fail(c, L2_ECUDA, "cuTensorMapEncodeTiled failed for a batched GEMV plan");
+    }
+    set.built = true;
+    return L2_OK;
+}
+
+cudaError_t launch_batched(l2_ctx *c, int k, const GemvPlan &pl, int layer, int batch, cudaStream_t s, bool pdl) {
+    const BatchPlan &bpl = c->bsets[batch].plan[k];
+    BatchParams bp = bpl.bp;
+    bp.g = layer_params(c, pl, layer);
+    bp.g.batch = batch;
+    bp.g.ss_part = c->ss_part;
+    bp.g.ss_parts = c->bsets[batch].plan[1].grid;  // the residual kernels' grid
+    return launch_gemv_batched(pl.mode, bp, bpl.grid, bpl.smem, s, pdl);
 }
 
 cudaError_t launch_op(l2_ctx *c, int op, int layer, int batch, cudaStream_t s, bool pdl) {
     if (batch > 1 && op != 1) {
         const GemvPlan *pl[] = {&c->plan_qkv, nullptr, &c->plan_wo, &c->plan_w13, &c->plan_w2, &c->plan_cls};
-        return launch_batched(c, *pl[op], op == 5 ? 0 : layer, batch, s, pdl);
+        const int k = op == 0 ? 0 : op - 1;  // index into the batch set's plans
+        return launch_batched(c, k, *pl[op], op == 5 ? 0 : layer, batch, s, pdl);
     }
     switch (op) {
         case 0: {
@@ -482,13 +600,7 @@ int l2_create(const L2Config *config, const L2Weights *weights, int max_batch, u
 
     const size_t B = (size_t)max_batch, L = p.n_layers, S = p.seq_len, hs = c->head_size;
     const size_t cache = B * L * p.n_kv_heads * S * hs;
-    c->attn_chunks = 1;
-    {
-        int nc = ceil_div(2LL * c->num_sms, p.n_kv_heads);
-        const int cap = ceil_div(p.seq_len, kMinChunk);
-        c->attn_chunks = nc < cap ? nc : cap;
-        if (c->attn_chunks < 1) c->attn_chunks = 1;
-    }
+    c->attn_chunks = attn_chunks_for(c, 1);
     const size_t ws = B * p.n_heads * (size_t)c->attn_chunks;
     if ((rc = alloc_n(c, &c->x, B * p.dim, "x")) || (rc = alloc_n(c, &c->xb, B * p.dim, "xb")) ||
         (rc = alloc_n(c, &c->q, B * p.dim, "q")) || (rc = alloc_n(c, &c->hb, B * p.hidden_dim, "hb")) ||
@@ -538,12 +650,9 @@ int l2_create(const L2Config *config, const L2Weights *weights, int max_batch, u
             return bail(fail(c, L2_EINVAL, "a GEMV stage needs %zu bytes of shared memory (> 227 KB); dim or hidden_dim too large",
                              pl->smem));
     if (c->attn.smem > 227 * 1024) return bail(fail(c, L2_EINVAL, "attention needs too much shared memory"));
+    c->bsets.resize(max_batch + 1);
     for (int b = 2; b <= max_batch; ++b)
-        for (const GemvPlan *pl : {&c->plan_qkv, &c->plan_wo, &c->plan_w13, &c->plan_w2, &c->plan_cls}) {
-            const BatchedShape bs = batched_shape(c, *pl, b);
-            if (bs.smem > 227 * 1024 || bs.grid > kMaxParts)
-                return bail(fail(c, L2_EINVAL, "a batched GEMV of %d sequences does not fit one CTA's shared memory", b));
-        }
+        if ((rc = build_batch_set(c, b))) return bail(rc);
     CREATE_CUDA(cudaDeviceSynchronize());
 #undef CREATE_CUDA
     *out = c;

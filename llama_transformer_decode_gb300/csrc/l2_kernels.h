@@ -16,13 +16,12 @@ cudaError_t launch_gemv(int mode, const GemvParams &p, int grid, size_t smem, cu
 
 // Batched fused GEMV, B >= 2 sequences per step (gemv_batched.cu).
 cudaError_t gemv_batched_init();
-// Dynamic shared memory for at most rows_max local rows and `batch` sequences;
-// *stages receives the ring depth that fits.
-size_t gemv_batched_smem(int rows_max, int batch, int *stages);
-// Whether one CTA can hold rows_max rows for `batch` sequences in registers.
-int gemv_batched_rows_ok(int rows_max, int batch);
-cudaError_t launch_gemv_batched(int mode, const GemvParams &p, int grid, size_t smem, int stages, cudaStream_t stream,
-                                bool pdl);
+// Most weight rows (all pieces) one CTA holds in registers for `batch` sequences.
+int gemv_batched_rows_cap(int batch);
+// Dynamic shared memory for stage_rows weight rows, `batch` sequences and
+// rows of n floats; *stages and *tk receive the ring depth and K-tile width.
+size_t gemv_batched_smem(int stage_rows, int batch, int n, int *stages, int *tk);
+cudaError_t launch_gemv_batched(int mode, const BatchParams &bp, int grid, size_t smem, cudaStream_t stream, bool pdl);
 
 // Flash-decoding attention (attention.cu).
 struct AttnLaunch {

@@ -1,6 +1,7 @@
 // Kernel parameter blocks shared by the host orchestrator and the kernels.
 #pragma once
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace l2 {
@@ -56,6 +57,19 @@ struct GemvParams {
 };
 
 constexpr int kMaxParts = 1024;
+
+// Batched GEMV launch (gemv_batched.cu): tensor maps for 2-D tile copies of
+// the weights (rows x columns boxes) and of the B input rows.
+struct alignas(64) BatchParams {
+    CUtensorMap wmap[3];  // QKV: Wq, Wk, Wv; W1/W3: W1, W3; otherwise [0]
+    CUtensorMap xmap;     // input activations [slots][n], box = tk columns x batch rows
+    GemvParams g;
+    int part_ctas[3];     // CTAs per matrix (QKV), or [0] = grid
+    int part_units[3];    // units per matrix
+    int rows_box;         // rows per weight box (the most rows any CTA owns)
+    int tk;               // columns per K tile
+    int stages;           // ring depth
+};
 
 struct AttnParams {
     const float *q;                  // [B][dim]
