@@ -33,6 +33,7 @@ namespace {
 constexpr int kNWA = 4;              // warps per CTA
 constexpr int kAttStages = 3;        // ring depth per warp
 constexpr int kStageFloats = 1024;   // K + V floats per stage (4 KB)
+constexpr int kPPG = 4;              // positions a lane group scores before one softmax update
 
 __device__ __forceinline__ void merge_state(float &m, float &l, float4 &acc, float m2, float l2v, float4 acc2) {
     const float M = fmaxf(m, m2);
@@ -65,7 +66,15 @@ __global__ void __launch_bounds__(kNWA * 32) attn_kernel(const AttnParams p) {
     const int c = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
     const int pos = p.step->pos[b];
     const int P = pos + 1;
-    int n_active = (P + p.min_chunk - 1) / p.min_chunk;
+    int chunk = p.min_chunk;
+    if (p.capacity > 0) {
+        // spread the positions of every slot over the resident CTAs
+        long long total = 0;
+        for (int b2 = 0; b2 < (int)gridDim.z; ++b2) total += p.step->pos[b2] + 1;
+        const long long per = (total * p.n_kv_heads + p.capacity - 1) / p.capacity;
+        if (per > chunk) chunk = (int)per;
+    }
+    int n_active = (P + chunk - 1) / chunk;
     if (n_active > p.n_chunks) n_active = p.n_chunks;
     if (c >= n_active) return;  // too few positions for this CTA to join
 
@@ -146,31 +155,54 @@ __global__ void __launch_bounds__(kNWA * 32) attn_kernel(const AttnParams p) {
         const float4 *Ks = wring + (size_t)s * (kStageFloats / 4);
         const float4 *Vs = Ks + (size_t)TP * hs4;
 #pragma unroll 1
-        for (int tt = 0; tt < np; tt += RPI) {
-            const int tl = tt + rg;
-            const bool row_on = tl < np;
-            float4 kv = make_float4(0.f, 0.f, 0.f, 0.f), vv = kv;
-            if (row_on && lane_on) {
-                kv = Ks[tl * hs4 + c4];
-                vv = Vs[tl * hs4 + c4];
+        // Up to kPPG positions per lane group at a time: all their scores
+        // first (independent dot products and shuffles), then one online-
+        // softmax update per head (one rescale per group of positions).
+        for (int tt = 0; tt < np; tt += RPI * kPPG) {
+            float sc[kPPG][GQ];
+            float4 vv[kPPG];
+#pragma unroll
+            for (int u = 0; u < kPPG; ++u) {
+                const int tl = tt + u * RPI + rg;
+                const bool row_on = tl < np;
+                float4 kv = make_float4(0.f, 0.f, 0.f, 0.f);
+                vv[u] = kv;
+                if (row_on && lane_on) {
+                    kv = Ks[tl * hs4 + c4];
+                    vv[u] = Vs[tl * hs4 + c4];
+                }
+#pragma unroll
+                for (int j = 0; j < GQ; ++j) {
+                    float d = dot4(q4[j], kv, 0.f);
+#pragma unroll
+                    for (int o = LP / 2; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+                    sc[u][j] = row_on ? d * p.scale : -CUDART_INF_F;
+                    if (dbg && row_on && c4 == 0 && j < nq) dbg[(size_t)j * p.seq_len + tc + tl] = sc[u][j];
+                }
             }
 #pragma unroll
             for (int j = 0; j < GQ; ++j) {
-                float d = dot4(q4[j], kv, 0.f);
+                if (j >= nq) continue;
+                float mx = sc[0][j];
 #pragma unroll
-                for (int o = LP / 2; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
-                if (j < nq && row_on) {
-                    const float sc = d * p.scale;
-                    if (dbg && c4 == 0) dbg[(size_t)j * p.seq_len + tc + tl] = sc;
-                    const float mn = fmaxf(m[j], sc);
-                    const float corr = expf(m[j] - mn), pe = expf(sc - mn);
-                    l[j] = l[j] * corr + pe;
-                    acc[j].x = acc[j].x * corr + pe * vv.x;
-                    acc[j].y = acc[j].y * corr + pe * vv.y;
-                    acc[j].z = acc[j].z * corr + pe * vv.z;
-                    acc[j].w = acc[j].w * corr + pe * vv.w;
-                    m[j] = mn;
+                for (int u = 1; u < kPPG; ++u) mx = fmaxf(mx, sc[u][j]);
+                const float mn = fmaxf(m[j], mx);
+                if (mn == -CUDART_INF_F) continue;  // no position of this group
+                const float corr = expf(m[j] - mn);
+                float ps = 0.f;
+                float4 a = make_float4(acc[j].x * corr, acc[j].y * corr, acc[j].z * corr, acc[j].w * corr);
+#pragma unroll
+                for (int u = 0; u < kPPG; ++u) {
+                    const float pe = expf(sc[u][j] - mn);
+                    ps += pe;
+                    a.x = fmaf(pe, vv[u].x, a.x);
+                    a.y = fmaf(pe, vv[u].y, a.y);
+                    a.z = fmaf(pe, vv[u].z, a.z);
+                    a.w = fmaf(pe, vv[u].w, a.w);
                 }
+                l[j] = l[j] * corr + ps;
+                acc[j] = a;
+                m[j] = mn;
             }
         }
         __syncwarp();
@@ -361,6 +393,16 @@ AttnLaunch attn_plan(int head_size, int n_heads, int n_kv_heads) {
     a.smem = hdr + (size_t)kNWA * kAttStages * kStageFloats * 4 + (size_t)kNWA * a.gq * hs4 * 16;
     a.ok = a.lp <= 32 && a.gq <= 8 && head_size % 4 == 0 && 2 * head_size <= kStageFloats;
     return a;
+}
+
+int attn_ctas_per_sm(const AttnLaunch &a) {
+    int n = 0;
+    AttnFn fn = pick(a.lp, a.gq);
+    if (!fn || cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, a.threads, a.smem) != cudaSuccess) {
+        cudaGetLastError();
+        return 1;
+    }
+    return n < 1 ? 1 : n;
 }
 
 cudaError_t attn_init() {

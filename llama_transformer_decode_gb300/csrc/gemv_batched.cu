@@ -8,7 +8,8 @@
 // still bandwidth-bound, at B = 64 it is bound by the fp32 CUDA cores.
 //
 // Design.  CTA c owns a balanced range of rows of one matrix (for W1/W3 the
-// same rows of both).  K is walked in tiles of up to 256 columns: per tile,
+// same rows of both), walked in blocks of a few rows; each block walks K in
+// tiles of up to 256 columns, and the ring runs on across blocks.  Per tile,
 // one 2-D tensor copy (TMA, cp.async.bulk.tensor) brings the CTA's rows x tile
 // columns of each weight matrix into shared memory and one brings the B input
 // rows x tile columns, all completing on one mbarrier per ring stage.  (Copies
@@ -70,23 +71,28 @@ __global__ void __launch_bounds__(kBT, 1) gemv_batched_kernel(const __grid_const
     const GemvParams &p = bp.g;
     extern __shared__ __align__(128) unsigned char smem[];
     auto &fx = *reinterpret_cast<BatchFixed *>(smem);
-    float *region = reinterpret_cast<float *>(smem + fixed_b_bytes());
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int B = p.batch, n = p.n, tk = bp.tk, RB = bp.rows_box, stages = bp.stages;
+    const int npc = (MODE == GEMV_W13) ? 2 : 1;  // weight pieces (W1 and W3 share rows)
+    const int SR = npc * RB;                     // weight rows in a stage (piece pc at row pc*RB)
+    // shared memory: fixed | gain [n] | ys [SR][B] | ring of stages [(SR + B) * tk]
+    float *gain = reinterpret_cast<float *>(smem + fixed_b_bytes());
+    float *ys = gain + ((MODE == GEMV_RESID) ? 0 : ((n + 31) & ~31));
+    float *region = ys + (((size_t)SR * B + 31) & ~(size_t)31);
 
-    // ---- this CTA's matrix and rows ----
+    // ---- this CTA's matrix and rows, walked in blocks of RB rows ----
     int m = 0, cta = blockIdx.x;
     while (m < 2 && cta >= bp.part_ctas[m]) cta -= bp.part_ctas[m++];
     const int units = bp.part_units[m], nct = bp.part_ctas[m];
     const long long u0 = (long long)cta * units / nct, u1 = (long long)(cta + 1) * units / nct;
     const int r0 = (int)(u0 * p.unit_rows);        // first row within matrix m
-    const int R = (int)((u1 - u0) * p.unit_rows);  // rows of this CTA (<= RB)
-    const int npc = (MODE == GEMV_W13) ? 2 : 1;    // weight pieces (W1 and W3 share rows)
-    const int SR = npc * RB;                       // weight rows in a stage (piece pc at row pc*RB)
+    const int R = (int)((u1 - u0) * p.unit_rows);  // rows of this CTA
     const int mrows = (MODE == GEMV_QKV) ? (m == 0 ? p.rows0 : p.rows1) : p.total_units * p.unit_rows;
     const int wrow0 = (MODE == GEMV_CLS ? 0 : p.layer * mrows) + r0;  // tensor-map row of the first row
     const int stage_floats = (SR + B) * tk;
     const int NKT = (n + tk - 1) / tk;
+    const int NB = (R + RB - 1) / RB;  // row blocks
+    const int NQ = NB * NKT;           // K tiles over all blocks
     const bool emb_rows = (MODE == GEMV_QKV && p.layer == 0);  // inputs gathered from the embedding table
 
     if (tid == 0) {
@@ -97,22 +103,24 @@ __global__ void __launch_bounds__(kBT, 1) gemv_batched_kernel(const __grid_const
     __syncthreads();
     if (R <= 0) return;
 
-    // Requests for K tile kt into stage s, by lane 0 of warp 0 (lanes of warp 0
-    // for the embedding rows).  The weight half only raises the expected bytes;
-    // the input half arrives, so a stage cannot complete before both halves
-    // have been requested.  The weights do not depend on the previous kernel
-    // and are requested before waiting on it.
-    auto issue_weights = [&](int kt, int s) {
+    // Requests for tile q (block q / NKT, K tile q % NKT) into stage s, by
+    // warp 0.  The weight half only raises the expected bytes; the input half
+    // arrives, so a stage cannot complete before both halves are requested.
+    // The weights do not depend on the previous kernel and are requested
+    // before waiting on it.
+    auto issue_weights = [&](int q, int s) {
         if (lane == 0) {
             float *W = region + (size_t)s * stage_floats;
+            const int blk = q / NKT, kt = q - blk * NKT;
             mbar_expect_tx(&fx.bars[s], (uint32_t)(SR * tk * 4));
             for (int pc = 0; pc < npc; ++pc)
-                tensor_g2s(W + (size_t)pc * RB * tk, &bp.wmap[MODE == GEMV_QKV ? m : pc], kt * tk, wrow0, &fx.bars[s]);
+                tensor_g2s(W + (size_t)pc * RB * tk, &bp.wmap[MODE == GEMV_QKV ? m : pc], kt * tk, wrow0 + blk * RB,
+                           &fx.bars[s]);
         }
     };
-    auto issue_inputs = [&](int kt, int s) {
+    auto issue_inputs = [&](int q, int s) {
         float *X = region + (size_t)s * stage_floats + (size_t)SR * tk;
-        const int k0 = kt * tk, len = min(tk, n - k0);
+        const int kt = q % NKT, k0 = kt * tk, len = min(tk, n - k0);
         if (emb_rows) {
             // one embedding row per sequence; columns past n stay unused
             if (lane == 0) mbar_arrive_expect_tx(&fx.bars[s], (uint32_t)(B * len * 4));
@@ -126,21 +134,23 @@ __global__ void __launch_bounds__(kBT, 1) gemv_batched_kernel(const __grid_const
         }
     };
 
-    const int pre = min(stages, NKT);
+    const int pre = min(stages, NQ);
     if (warp == 0)
-        for (int kt = 0; kt < pre; ++kt) {
-            issue_weights(kt, kt);
-            if (emb_rows) issue_inputs(kt, kt);  // the embedding table is read-only
+        for (int q = 0; q < pre; ++q) {
+            issue_weights(q, q);
+            if (emb_rows) issue_inputs(q, q);  // the embedding table is read-only
         }
 
     pdl_launch_dependents();
     pdl_wait();
 
     if (warp == 0 && !emb_rows)
-        for (int kt = 0; kt < pre; ++kt) issue_inputs(kt, kt);
+        for (int q = 0; q < pre; ++q) issue_inputs(q, q);
 
-    // 1/rms of each sequence
+    // RMSNorm: the gain vector into shared memory, 1/rms of each sequence
     if (MODE != GEMV_RESID) {
+        for (int i = tid; i < n / 4; i += kBT)
+            reinterpret_cast<float4 *>(gain)[i] = __ldg(reinterpret_cast<const float4 *>(p.norm_w) + i);
         if (emb_rows) {
             for (int b = warp; b < B; b += kBT / 32) {
                 const float4 *e4 = reinterpret_cast<const float4 *>(p.emb + (size_t)p.step->token[b] * p.dim);
@@ -168,7 +178,10 @@ __global__ void __launch_bounds__(kBT, 1) gemv_batched_kernel(const __grid_const
                 if (lane == 0) fx.inv[b] = 1.0f / sqrtf(ss / (float)n + 1e-5f);
             }
         }
+    } else {
+        for (int b = tid; b < B; b += kBT) fx.inv[b] = 0.f;  // sum of squares of the CTA's new x rows
     }
+    __syncthreads();
 
     // Warp w owns the output tile of stage rows 8*(w % TRG).. and sequences
     // 8*(w / TRG)..; its 32 lanes split the tile's columns.
@@ -181,40 +194,15 @@ __global__ void __launch_bounds__(kBT, 1) gemv_batched_kernel(const __grid_const
 #pragma unroll
         for (int j = 0; j < kTB; ++j) acc[i][j] = 0.f;
 
-    bool ok = true;
 #pragma unroll 1
-    for (int kt = 0; kt < NKT; ++kt) {
-        const int s = kt % stages;
-        if (!mbar_wait(&fx.bars[s], (uint32_t)(kt / stages) & 1u, p.err)) {
-            ok = false;
-            fx.failed = 1;
-        }
-        __syncthreads();
-        if (fx.failed) {
-            ok = false;
-            break;
-        }
+    for (int q = 0; q < NQ; ++q) {
+        const int s = q % stages;
+        const int blk = q / NKT, kt = q - blk * NKT;
+        if (!mbar_wait(&fx.bars[s], (uint32_t)(q / stages) & 1u, p.err)) fx.failed = 1;
         const int k0 = kt * tk, len = min(tk, n - k0), len4 = len >> 2;
         const float *W = region + (size_t)s * stage_floats;
-        float *X = const_cast<float *>(W) + (size_t)SR * tk;
-        if (MODE != GEMV_RESID) {
-            // the RMSNorm gain, applied to the input tile in place
-            const float4 *g4 = reinterpret_cast<const float4 *>(p.norm_w + k0);
-            for (int f = lane; f < len4; f += 32) {
-                const float4 g = __ldg(g4 + f);
-                for (int b = warp; b < B; b += kBT / 32) {
-                    float4 *xv = reinterpret_cast<float4 *>(X + (size_t)b * tk) + f;
-                    float4 v = *xv;
-                    v.x *= g.x;
-                    v.y *= g.y;
-                    v.z *= g.z;
-                    v.w *= g.w;
-                    *xv = v;
-                }
-            }
-            __syncthreads();
-        }
-        if (busy) {
+        const float *X = W + (size_t)SR * tk;
+        if (busy && !fx.failed) {
             const float4 *wr[kTR];
             const float4 *xr[kTB];
 #pragma unroll
@@ -223,115 +211,147 @@ __global__ void __launch_bounds__(kBT, 1) gemv_batched_kernel(const __grid_const
 #pragma unroll
             for (int j = 0; j < kTB; ++j)
                 xr[j] = reinterpret_cast<const float4 *>(X + (size_t)min(bg * kTB + j, B - 1) * tk);
+            const float4 *g4 = reinterpret_cast<const float4 *>(gain + k0);
 #pragma unroll 1
             for (int f = lane; f < len4; f += 32) {
                 float4 w4[kTR], x4[kTB];
 #pragma unroll
                 for (int i = 0; i < kTR; ++i) w4[i] = wr[i][f];
+                if (MODE != GEMV_RESID) {
+                    const float4 g = g4[f];
+#pragma unroll
+                    for (int i = 0; i < kTR; ++i) {
+                        w4[i].x *= g.x;
+                        w4[i].y *= g.y;
+                        w4[i].z *= g.z;
+                        w4[i].w *= g.w;
+                    }
+                }
 #pragma unroll
                 for (int j = 0; j < kTB; ++j) x4[j] = xr[j][f];
+                // component-major order: 64 independent FMAs per component
 #pragma unroll
                 for (int i = 0; i < kTR; ++i)
 #pragma unroll
-                    for (int j = 0; j < kTB; ++j) acc[i][j] = dot4(w4[i], x4[j], acc[i][j]);
+                    for (int j = 0; j < kTB; ++j) acc[i][j] = fmaf(w4[i].x, x4[j].x, acc[i][j]);
+#pragma unroll
+                for (int i = 0; i < kTR; ++i)
+#pragma unroll
+                    for (int j = 0; j < kTB; ++j) acc[i][j] = fmaf(w4[i].y, x4[j].y, acc[i][j]);
+#pragma unroll
+                for (int i = 0; i < kTR; ++i)
+#pragma unroll
+                    for (int j = 0; j < kTB; ++j) acc[i][j] = fmaf(w4[i].z, x4[j].z, acc[i][j]);
+#pragma unroll
+                for (int i = 0; i < kTR; ++i)
+#pragma unroll
+                    for (int j = 0; j < kTB; ++j) acc[i][j] = fmaf(w4[i].w, x4[j].w, acc[i][j]);
             }
         }
         __syncthreads();
-        if (warp == 0 && kt + stages < NKT) {
-            issue_weights(kt + stages, s);
-            issue_inputs(kt + stages, s);
+        if (fx.failed) {
+            // Let the copies already requested land (bounded waits) before leaving.
+            if (tid == 0)
+                for (int j = q + 1; j < NQ && j < q + stages; ++j)
+                    (void)mbar_wait(&fx.bars[j % stages], (uint32_t)(j / stages) & 1u, p.err);
+            return;
         }
-    }
-    if (!ok) {
-        // Let the copies already requested land (bounded waits) before leaving.
-        if (tid == 0)
-            for (int j = 0; j < NKT && j < stages; ++j) (void)mbar_wait(&fx.bars[j], 0u, p.err);
-        return;
-    }
+        if (warp == 0 && q + stages < NQ) {
+            issue_weights(q + stages, s);
+            issue_inputs(q + stages, s);
+        }
+        if (kt != NKT - 1) continue;
 
-    // reduce each output over the lanes; ys[stage row][sequence] in shared memory
-    float *ys = region;
-    if (busy) {
+        // ---- end of a row block: reduce over the lanes, then the epilogue ----
+        if (busy) {
 #pragma unroll
-        for (int i = 0; i < kTR; ++i)
+            for (int i = 0; i < kTR; ++i)
 #pragma unroll
-            for (int j = 0; j < kTB; ++j) {
-                const float v = warp_sum(acc[i][j]);
-                const int r = rg * kTR + i, b = bg * kTB + j;
-                if (lane == 0 && r < SR && b < B) ys[(size_t)r * B + b] = (MODE != GEMV_RESID) ? v * fx.inv[b] : v;
-            }
-    }
-    __syncthreads();
-
-    // ---- epilogue (rows 0..R-1 of each piece) ----
-    if (MODE == GEMV_QKV) {
-        const int hs = p.head_size, half = hs >> 1;
-        for (int e = tid; e < (R >> 1) * B; e += kBT) {
-            const int pi = e / B, b = e - pi * B;
-            const int j = 2 * pi;
-            const float y0 = ys[(size_t)j * B + b], y1 = ys[(size_t)(j + 1) * B + b];
-            const int pos = p.step->pos[b];
-            const float2 *rr = p.rope + (size_t)pos * half;
-            const int v = r0 + j;  // row within matrix m
-            if (m == 0) {
-                const float2 cs = rr[(v % hs) >> 1];
-                float *q = p.q + (size_t)b * p.dim;
-                q[v] = y0 * cs.x - y1 * cs.y;
-                q[v + 1] = y0 * cs.y + y1 * cs.x;
-            } else {
-                const int g = v / hs, d = v % hs;
-                const size_t idx =
-                    ((((size_t)b * p.n_layers + p.layer) * p.n_kv_heads + g) * p.seq_len + pos) * hs + d;
-                if (m == 1) {
-                    const float2 cs = rr[d >> 1];
-                    p.kcache[idx] = y0 * cs.x - y1 * cs.y;
-                    p.kcache[idx + 1] = y0 * cs.y + y1 * cs.x;
+                for (int j = 0; j < kTB; ++j) {
+                    const float v = warp_sum(acc[i][j]);
+                    const int r = rg * kTR + i, b = bg * kTB + j;
+                    if (lane == 0 && r < SR && b < B) ys[(size_t)r * B + b] = (MODE != GEMV_RESID) ? v * fx.inv[b] : v;
+                    acc[i][j] = 0.f;
+                }
+        }
+        __syncthreads();
+        const int rb0 = blk * RB;                  // block's first row within the CTA
+        const int RR = min(RB, R - rb0);           // rows of this block
+        const int rr0 = r0 + rb0;                  // block's first row within matrix m
+        if (MODE == GEMV_QKV) {
+            const int hs = p.head_size, half = hs >> 1;
+            for (int e = tid; e < (RR >> 1) * B; e += kBT) {
+                const int pi = e / B, b = e - pi * B;
+                const int j = 2 * pi;
+                const float y0 = ys[(size_t)j * B + b], y1 = ys[(size_t)(j + 1) * B + b];
+                const int pos = p.step->pos[b];
+                const float2 *rr = p.rope + (size_t)pos * half;
+                const int v = rr0 + j;  // row within matrix m
+                if (m == 0) {
+                    const float2 cs = rr[(v % hs) >> 1];
+                    float *qv = p.q + (size_t)b * p.dim;
+                    qv[v] = y0 * cs.x - y1 * cs.y;
+                    qv[v + 1] = y0 * cs.y + y1 * cs.x;
                 } else {
-                    p.vcache[idx] = y0;
-                    p.vcache[idx + 1] = y1;
+                    const int g = v / hs, d = v % hs;
+                    const size_t idx =
+                        ((((size_t)b * p.n_layers + p.layer) * p.n_kv_heads + g) * p.seq_len + pos) * hs + d;
+                    if (m == 1) {
+                        const float2 cs = rr[d >> 1];
+                        p.kcache[idx] = y0 * cs.x - y1 * cs.y;
+                        p.kcache[idx + 1] = y0 * cs.y + y1 * cs.x;
+                    } else {
+                        p.vcache[idx] = y0;
+                        p.vcache[idx + 1] = y1;
+                    }
                 }
             }
-        }
-    } else if (MODE == GEMV_W13) {
-        const int hidden = p.total_units;
-        for (int e = tid; e < R * B; e += kBT) {
-            const int r = e / B, b = e - r * B;
-            p.hb[(size_t)b * hidden + r0 + r] = silu_b(ys[e]) * ys[(size_t)(RB + r) * B + b];
-        }
-    } else if (MODE == GEMV_RESID) {
-        const int dim = p.total_units;
-        for (int e = tid; e < R * B; e += kBT) {
-            const int r = e / B, b = e - r * B;
-            float *xp = p.x + (size_t)b * dim + r0 + r;
-            const float nv = *xp + ys[e];
-            *xp = nv;
-            ys[e] = nv;
+        } else if (MODE == GEMV_W13) {
+            const int hidden = p.total_units;
+            for (int e = tid; e < RR * B; e += kBT) {
+                const int r = e / B, b = e - r * B;
+                p.hb[(size_t)b * hidden + rr0 + r] = silu_b(ys[e]) * ys[(size_t)(RB + r) * B + b];
+            }
+        } else if (MODE == GEMV_RESID) {
+            const int dim = p.total_units;
+            for (int e = tid; e < RR * B; e += kBT) {
+                const int r = e / B, b = e - r * B;
+                float *xp = p.x + (size_t)b * dim + rr0 + r;
+                const float nv = *xp + ys[e];
+                *xp = nv;
+                ys[e] = nv;
+            }
+            __syncthreads();
+            for (int b = tid; b < B; b += kBT) {
+                float ss = fx.inv[b];
+                for (int r = 0; r < RR; ++r) ss = fmaf(ys[(size_t)r * B + b], ys[(size_t)r * B + b], ss);
+                fx.inv[b] = ss;
+            }
+        } else {
+            float *user = p.step->logits_out;
+            const int V = p.total_units;
+            for (int e = tid; e < RR * B; e += kBT) {
+                const int r = e / B, b = e - r * B;
+                p.logits[(size_t)b * V + rr0 + r] = ys[e];
+                if (user) user[(size_t)b * V + rr0 + r] = ys[e];
+            }
         }
         __syncthreads();
-        for (int b = tid; b < B; b += kBT) {
-            float ss = 0.f;
-            for (int r = 0; r < R; ++r) ss = fmaf(ys[(size_t)r * B + b], ys[(size_t)r * B + b], ss);
-            p.ss_part[(size_t)blockIdx.x * B + b] = ss;
-        }
-    } else {
-        float *user = p.step->logits_out;
-        const int V = p.total_units;
-        for (int e = tid; e < R * B; e += kBT) {
-            const int r = e / B, b = e - r * B;
-            p.logits[(size_t)b * V + r0 + r] = ys[e];
-            if (user) user[(size_t)b * V + r0 + r] = ys[e];
-        }
     }
+    if (MODE == GEMV_RESID)
+        for (int b = tid; b < B; b += kBT) p.ss_part[(size_t)blockIdx.x * B + b] = fx.inv[b];
 }
 
 // ---------------------------------------------------------------- host side
 
 int gemv_batched_rows_cap(int batch) { return kTR * (kMaxTiles / ((batch + kTB - 1) / kTB)); }
 
-size_t gemv_batched_smem(int stage_rows, int batch, int n, int *stages, int *tk) {
+size_t gemv_batched_smem(int stage_rows, int batch, int n, bool norm, int *stages, int *tk) {
     // The widest K tile (fewer, bigger copies and fewer barriers) that still
     // leaves three ring stages; two stages of 64 columns at the least.
-    const size_t limit = 227 * 1024 - fixed_b_bytes();
+    const size_t head = fixed_b_bytes() + (norm ? (size_t)((n + 31) & ~31) * 4 : 0) +
+                        (((size_t)stage_rows * batch + 31) & ~(size_t)31) * 4;
+    const size_t limit = 227 * 1024 - head;
     int t = 256;
     while (t > 64 && (3 * (size_t)(stage_rows + batch) * t * 4 > limit || t >= 2 * n)) t >>= 1;
     const size_t stage = (size_t)(stage_rows + batch) * t * 4;
@@ -339,8 +359,7 @@ size_t gemv_batched_smem(int stage_rows, int batch, int n, int *stages, int *tk)
     while (st > 2 && st * stage > limit) --st;
     *stages = st;
     *tk = t;
-    const size_t ys = (size_t)stage_rows * batch * 4;  // reuses the ring after the K loop
-    return fixed_b_bytes() + (st * stage > ys ? st * stage : ys);
+    return head + st * stage;
 }
 
 cudaError_t gemv_batched_init() {

@@ -82,6 +82,7 @@ struct l2_ctx {
 
     AttnLaunch attn{};
     int attn_chunks = 1;
+    int attn_per_sm = 1;  // attention CTAs resident per SM
     GemvPlan plan_qkv{}, plan_wo{}, plan_w13{}, plan_w2{}, plan_cls{};
     std::vector<BatchSet> bsets;  // batched GEMV plans, indexed by batch size
     bool evict_first = false;
@@ -271,9 +272,8 @@ GemvParams layer_params(const l2_ctx *c, const GemvPlan &pl, int layer) {
 // CTAs that fit on it, in one wave, and no more than one per kMinChunk
 // positions of the cache.
 int attn_chunks_for(const l2_ctx *c, int batch) {
-    int per_sm = (int)((227 * 1024) / (c->attn.smem + 1024));
+    int per_sm = c->attn_per_sm;
     if (per_sm > 4) per_sm = 4;
-    if (per_sm < 1) per_sm = 1;
     int nc = (int)(((long long)per_sm * c->num_sms) / ((long long)c->cfg.n_kv_heads * batch));
     const int cap = ceil_div(c->cfg.seq_len, kMinChunk);
     if (nc > cap) nc = cap;
@@ -301,6 +301,12 @@ AttnParams attn_params(const l2_ctx *c, int layer, int batch) {
     a.seq_len = p.seq_len;
     a.dim = p.dim;
     int nc = attn_chunks_for(c, batch);
+    a.capacity = 0;
+    if (batch > 1) {
+        // slots sit at different positions: size the chunks on the device
+        nc = ceil_div(p.seq_len, kMinChunk);
+        a.capacity = c->attn_per_sm * c->num_sms;
+    }
     if (nc > c->attn_chunks) nc = c->attn_chunks;
     a.n_chunks = nc;
     a.min_chunk = kMinChunk;
@@ -355,35 +361,36 @@ int build_batch_set(l2_ctx *c, int batch) {
         BatchParams &bp = bpl.bp;
         memset(&bp, 0, sizeof(bp));
         const int npc = pl.mode == GEMV_W13 ? 2 : 1;
-        int upc = cap / (pl.unit_rows * npc);  // units per CTA at most
-        if (upc < 1) upc = 1;
-        int rows_box = 0, grid = 0;
+        // one CTA per SM, each owning a balanced row range that it walks in
+        // blocks of at most cap / npc rows (whole units)
+        int grid = 0, rows_max = 0;
         if (pl.mode == GEMV_QKV) {
             const int u[3] = {p.dim / 2, c->kv_dim / 2, c->kv_dim / 2};
             const int total = u[0] + u[1] + u[2];
-            int target = ceil_div(u[0], upc) + ceil_div(u[1], upc) + ceil_div(u[2], upc);
-            if (target < c->num_sms) target = c->num_sms;
+            const int target = c->num_sms > 3 ? c->num_sms : 3;
             for (int m = 0; m < 3; ++m) {
                 int g = (int)(((long long)target * u[m] + total / 2) / total);
-                if (g < ceil_div(u[m], upc)) g = ceil_div(u[m], upc);
                 if (g > u[m]) g = u[m];
                 if (g < 1) g = 1;
                 bp.part_ctas[m] = g;
                 bp.part_units[m] = u[m];
                 grid += g;
-                const int rb = ceil_div(u[m], g) * 2;
-                if (rb > rows_box) rows_box = rb;
+                const int r = ceil_div(u[m], g) * 2;
+                if (r > rows_max) rows_max = r;
             }
         } else {
             grid = pl.units < c->num_sms ? pl.units : c->num_sms;
-            if (ceil_div(pl.units, upc) > grid) grid = ceil_div(pl.units, upc);
             bp.part_ctas[0] = grid;
             bp.part_units[0] = pl.units;
-            rows_box = ceil_div(pl.units, grid) * pl.unit_rows;
+            rows_max = ceil_div(pl.units, grid) * pl.unit_rows;
         }
+        int block_cap = (cap / npc) / pl.unit_rows * pl.unit_rows;  // whole units per block
+        if (block_cap < pl.unit_rows) block_cap = pl.unit_rows;
+        const int nblocks = ceil_div(rows_max, block_cap);
+        int rows_box = ceil_div(ceil_div(rows_max, nblocks), pl.unit_rows) * pl.unit_rows;
         bp.rows_box = rows_box;
         bpl.grid = grid;
-        bpl.smem = gemv_batched_smem(npc * rows_box, batch, pl.base.n, &bp.stages, &bp.tk);
+        bpl.smem = gemv_batched_smem(npc * rows_box, batch, pl.base.n, pl.mode != GEMV_RESID, &bp.stages, &bp.tk);
         if (bpl.smem > 227 * 1024 || npc * rows_box > cap)
             return fail(c, L2_EINVAL, "a batched GEMV of %d sequences does not fit one CTA", batch);
         if (pl.mode == GEMV_RESID && grid > kMaxParts)
@@ -589,6 +596,7 @@ int l2_create(const L2Config *config, const L2Weights *weights, int max_batch, u
     CREATE_CUDA(gemv_init());
     CREATE_CUDA(gemv_batched_init());
     CREATE_CUDA(attn_init());
+    c->attn_per_sm = attn_ctas_per_sm(c->attn);
 
     if (cuda_stream) {
         c->stream = static_cast<cudaStream_t>(cuda_stream);
@@ -601,6 +609,7 @@ int l2_create(const L2Config *config, const L2Weights *weights, int max_batch, u
     const size_t B = (size_t)max_batch, L = p.n_layers, S = p.seq_len, hs = c->head_size;
     const size_t cache = B * L * p.n_kv_heads * S * hs;
     c->attn_chunks = attn_chunks_for(c, 1);
+    if (max_batch > 1 && ceil_div(p.seq_len, kMinChunk) > c->attn_chunks) c->attn_chunks = ceil_div(p.seq_len, kMinChunk);
     const size_t ws = B * p.n_heads * (size_t)c->attn_chunks;
     if ((rc = alloc_n(c, &c->x, B * p.dim, "x")) || (rc = alloc_n(c, &c->xb, B * p.dim, "xb")) ||
         (rc = alloc_n(c, &c->q, B * p.dim, "q")) || (rc = alloc_n(c, &c->hb, B * p.hidden_dim, "hb")) ||

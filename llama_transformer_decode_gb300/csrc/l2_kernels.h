@@ -18,9 +18,10 @@ cudaError_t launch_gemv(int mode, const GemvParams &p, int grid, size_t smem, cu
 cudaError_t gemv_batched_init();
 // Most weight rows (all pieces) one CTA holds in registers for `batch` sequences.
 int gemv_batched_rows_cap(int batch);
-// Dynamic shared memory for stage_rows weight rows, `batch` sequences and
-// rows of n floats; *stages and *tk receive the ring depth and K-tile width.
-size_t gemv_batched_smem(int stage_rows, int batch, int n, int *stages, int *tk);
+// Dynamic shared memory for stage_rows weight rows per block, `batch`
+// sequences and rows of n floats (norm: the mode has an RMSNorm prologue);
+// *stages and *tk receive the ring depth and K-tile width.
+size_t gemv_batched_smem(int stage_rows, int batch, int n, bool norm, int *stages, int *tk);
 cudaError_t launch_gemv_batched(int mode, const BatchParams &bp, int grid, size_t smem, cudaStream_t stream, bool pdl);
 
 // Flash-decoding attention (attention.cu).
@@ -33,6 +34,8 @@ struct AttnLaunch {
 };
 AttnLaunch attn_plan(int head_size, int n_heads, int n_kv_heads);
 cudaError_t attn_init();
+// Attention CTAs that can be resident on one SM (registers, shared memory, threads).
+int attn_ctas_per_sm(const AttnLaunch &a);
 cudaError_t launch_attn(const AttnLaunch &a, const AttnParams &p, int batch, cudaStream_t stream, bool pdl);
 
 }  // namespace l2

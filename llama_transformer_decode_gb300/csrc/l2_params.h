@@ -66,7 +66,7 @@ struct alignas(64) BatchParams {
     GemvParams g;
     int part_ctas[3];     // CTAs per matrix (QKV), or [0] = grid
     int part_units[3];    // units per matrix
-    int rows_box;         // rows per weight box (the most rows any CTA owns)
+    int rows_box;         // rows per weight box = rows per block (a CTA walks its rows in blocks)
     int tk;               // columns per K tile
     int stages;           // ring depth
 };
@@ -84,6 +84,8 @@ struct AttnParams {
     int layer, n_layers, n_heads, n_kv_heads, head_size, seq_len, dim;
     int n_chunks;   // grid.x: CTAs per (slot, KV head)
     int min_chunk;  // fewest positions a CTA takes before more CTAs join
+    int capacity;   // batches: CTAs resident at once; the chunk grows so the
+                    // positions of all slots fill about that many (0: fixed chunk)
     float scale;    // 1 / sqrt(head_size)
 };
 
