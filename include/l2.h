@@ -191,7 +191,7 @@ int l2_step_input_bytes(void);
  * 1 MiB (262144 floats) compiled into the library, which every GPU that
  * loads the library holds until the process exits.  A handle whose attention
  * needs more, n_heads * n_chunks * (head_size + 2) + n_kv_heads floats with
- * n_chunks = min(floor(c * SMs / n_kv_heads), ceil(seq_len / 32)) and c the
+ * n_chunks = min(floor(c * SMs / n_kv_heads), ceil(seq_len / 128)) and c the
  * attention CTAs that fit on one SM (at most 4), is refused
  * with L2_EINVAL before anything is enqueued.  The first call on a device
  * looks up the array's device address; make that first call before any

@@ -28,7 +28,16 @@ using namespace l2;
 namespace {
 
 constexpr int kRing = 64;      // pinned step-input slots in flight
-constexpr int kMinChunk = 32;  // fewest cache positions per attention CTA
+#ifndef L2_ATTN_MIN_CHUNK
+#define L2_ATTN_MIN_CHUNK 128
+#endif
+#ifndef L2_ATTN_MAX_PER_SM
+#define L2_ATTN_MAX_PER_SM 4
+#endif
+// Fewest cache positions per attention CTA.  Measured on GB300 (7B shape):
+// 128 beats 32 and 64 at positions up to ~2000 (fewer chunks to merge, a
+// single CTA per head below 128 positions) and ties above.
+constexpr int kMinChunk = L2_ATTN_MIN_CHUNK;
 
 thread_local std::string g_create_error;
 int g_fail_alloc_at = 0;  // fault injection: fail the n-th device allocation
@@ -273,7 +282,7 @@ GemvParams layer_params(const l2_ctx *c, const GemvPlan &pl, int layer) {
 // positions of the cache.
 int attn_chunks_for(const l2_ctx *c, int batch) {
     int per_sm = c->attn_per_sm;
-    if (per_sm > 4) per_sm = 4;
+    if (per_sm > L2_ATTN_MAX_PER_SM) per_sm = L2_ATTN_MAX_PER_SM;
     int nc = (int)(((long long)per_sm * c->num_sms) / ((long long)c->cfg.n_kv_heads * batch));
     const int cap = ceil_div(c->cfg.seq_len, kMinChunk);
     if (nc > cap) nc = cap;

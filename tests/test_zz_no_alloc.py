@@ -47,11 +47,11 @@ def test_static_scratch_step_matches_forward_on_two_calls():
 
 
 def test_static_scratch_limit_is_enforced():
-    # 32 heads of 128 on 4 KV heads with a 4096-position cache need more
+    # 32 heads of 128 on 4 KV heads with a 16384-position cache need more
     # attention scratch than the 262144 floats of the static array.
-    cfg = (4096, 16, 1, 32, 4, 16, 4096)
+    cfg = (4096, 16, 1, 32, 4, 16, 16384)
     wl = WORKLOADS["tiny"].replace(dim=4096, hidden_dim=16, n_layers=1, n_heads=32, n_kv_heads=4,
-                                   vocab_size=16, seq_len=4096, shared_wcls=False)
+                                   vocab_size=16, seq_len=16384, shared_wcls=False)
     w = {k: torch.zeros(wl.shape(k), device="cuda") for k in wl.tensor_names()}
     dec = pkg.Decoder(cfg, w)
     lib = pkg.lib()
