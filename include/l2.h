@@ -188,12 +188,14 @@ int l2_step_input_bytes(void);
  * Same arguments, checks, status codes and result as l2_forward, for slot 0.
  * The step's kernels are launched one by one, and the attention kernel keeps
  * its cross-CTA partial results and tickets in one static device array of
- * 1 MiB (262144 floats) compiled into the library, which every GPU that
+ * 512 KiB (131072 floats) compiled into the library, which every GPU that
  * loads the library holds until the process exits.  A handle whose attention
  * needs more, n_heads * n_chunks * (head_size + 2) + n_kv_heads floats with
  * n_chunks = min(floor(c * SMs / n_kv_heads), ceil(seq_len / 128)) and c the
  * attention CTAs that fit on one SM (at most 4), is refused
- * with L2_EINVAL before anything is enqueued.  The first call on a device
+ * with L2_EINVAL before anything is enqueued.  (With one attention CTA per
+ * SM on 152 SMs: 16.6 k floats at the Llama-2-7B shape; 8 query heads per KV
+ * head of size 128 need 158 k and are refused.)  The first call on a device
  * looks up the array's device address; make that first call before any
  * stream capture.  The handle's device must be current.  Every call shares
  * the array and clears its tickets first: calls whose kernels overlap on the

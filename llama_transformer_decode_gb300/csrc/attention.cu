@@ -27,12 +27,25 @@
 #include "l2_device.cuh"
 #include "l2_kernels.h"
 
+// Launch shape (compile-time): warps per CTA, ring buffers per warp, K + V
+// floats per ring buffer (a buffer holds stage_floats / (2 head_size) cache
+// positions; K and V arrive as one copy each).
+#ifndef L2_ATTN_WARPS
+#define L2_ATTN_WARPS 8
+#endif
+#ifndef L2_ATTN_STAGES
+#define L2_ATTN_STAGES 2
+#endif
+#ifndef L2_ATTN_STAGE_FLOATS
+#define L2_ATTN_STAGE_FLOATS 2048
+#endif
+
 namespace l2 {
 
 namespace {
-constexpr int kNWA = 4;              // warps per CTA
-constexpr int kAttStages = 3;        // ring depth per warp
-constexpr int kStageFloats = 1024;   // K + V floats per stage (4 KB)
+constexpr int kNWA = L2_ATTN_WARPS;
+constexpr int kAttStages = L2_ATTN_STAGES;
+constexpr int kStageFloats = L2_ATTN_STAGE_FLOATS;
 constexpr int kPPG = 4;              // positions a lane group scores before one softmax update
 
 __device__ __forceinline__ void merge_state(float &m, float &l, float4 &acc, float m2, float l2v, float4 acc2) {

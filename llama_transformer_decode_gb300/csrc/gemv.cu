@@ -30,20 +30,38 @@
 #include "l2_device.cuh"
 #include "l2_kernels.h"
 
-// Launch shape (compile-time): warps per CTA, ring buffers per warp, 16-byte
-// words per buffer.  Measured on GB300 (7B shape): 8 KB copies reach ~6 TB/s
-// where 2 KB copies with the same bytes in flight stay near 3.7 TB/s, so the
-// per-copy cost, not the depth of the ring, sets the rate.  L2_GEMV_FENCE adds
-// a generic->async proxy fence before a buffer is refilled (not needed: the
+// Launch shapes (compile-time): warps per CTA, ring buffers per warp, 16-byte
+// words per buffer.  A plan takes the first shape whose shared memory (ring +
+// input vector) fits: A, else B (for long rows such as W2's), else C.
+// Measured on GB300 (7B shape): 8 KB copies reach ~6 TB/s where 2 KB copies
+// with the same bytes in flight stay near 3.7 TB/s, so the per-copy cost sets
+// the rate; and a pure read stream of 8 KB copies reaches ~7.3 TB/s, so the
+// compute between a buffer's arrival and its refill matters.  With three or
+// more stages (L2_GEMV_ISSUE_AHEAD) a warp therefore refills the buffer it
+// finished in the previous iteration as soon as its wait returns, keeping
+// stages - 1 copies in flight while it computes.  L2_GEMV_FENCE adds a
+// generic->async proxy fence before a buffer is refilled (not needed: the
 // warp's reads of the buffer have completed when it issues the refill).
 #ifndef L2_GEMV_WARPS
 #define L2_GEMV_WARPS 8
 #endif
 #ifndef L2_GEMV_STAGES
-#define L2_GEMV_STAGES 2
+#define L2_GEMV_STAGES 3
 #endif
 #ifndef L2_GEMV_CHUNK_WORDS
 #define L2_GEMV_CHUNK_WORDS 512
+#endif
+#ifndef L2_GEMV_WARPS_B
+#define L2_GEMV_WARPS_B 7
+#endif
+#ifndef L2_GEMV_STAGES_B
+#define L2_GEMV_STAGES_B 3
+#endif
+#ifndef L2_GEMV_CHUNK_WORDS_B
+#define L2_GEMV_CHUNK_WORDS_B 512
+#endif
+#ifndef L2_GEMV_ISSUE_AHEAD
+#define L2_GEMV_ISSUE_AHEAD 1
 #endif
 #ifndef L2_GEMV_FENCE
 #define L2_GEMV_FENCE 0
@@ -183,8 +201,9 @@ __global__ void __launch_bounds__(NW * 32, 1) gemv_kernel(const GemvParams p) {
     };
 
     // Weights do not depend on the previous kernel: start streaming them now.
+    constexpr bool AHEAD = L2_GEMV_ISSUE_AHEAD && STAGES >= 3;
 #pragma unroll 1
-    for (int s = 0; s < STAGES && fi < fe; ++s) issue(s);
+    for (int s = 0; s < (AHEAD ? STAGES - 1 : STAGES) && fi < fe; ++s) issue(s);
 
     pdl_launch_dependents();
     pdl_wait();
@@ -247,6 +266,8 @@ __global__ void __launch_bounds__(NW * 32, 1) gemv_kernel(const GemvParams p) {
             ok = false;
             break;
         }
+        // chunk k + STAGES - 1 goes into the buffer finished in iteration k - 1
+        if (AHEAD && fi < fe) issue((k + STAGES - 1) % STAGES);
         const Piece &pc = fx.pieces[pi];
         const float4 *buf = wring + (size_t)s * CH4;
         const int lf = (int)(fc - pc.f0), lend = lf + len;
@@ -290,7 +311,7 @@ __global__ void __launch_bounds__(NW * 32, 1) gemv_kernel(const GemvParams p) {
         }
         __syncwarp();
         fc += len;
-        if (fi < fe) {
+        if (!AHEAD && fi < fe) {
 #if L2_GEMV_FENCE
             if (lane == 0) fence_proxy_async_smem();
 #endif
@@ -370,47 +391,85 @@ __global__ void __launch_bounds__(NW * 32, 1) gemv_kernel(const GemvParams p) {
 
 
 namespace {
-constexpr int kNW = L2_GEMV_WARPS, kStages = L2_GEMV_STAGES, kCH4 = L2_GEMV_CHUNK_WORDS;
+struct Shape {
+    int nw, stages, ch4;
+};
+constexpr Shape kShapes[kGemvShapes] = {{L2_GEMV_WARPS, L2_GEMV_STAGES, L2_GEMV_CHUNK_WORDS},
+                                        {L2_GEMV_WARPS_B, L2_GEMV_STAGES_B, L2_GEMV_CHUNK_WORDS_B},
+                                        {8, 2, 512}};
 
-template <int MODE>
-cudaError_t set_attr() {
-    return cudaFuncSetAttribute(gemv_kernel<kNW, kStages, kCH4, MODE>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+template <int S, int MODE>
+void *kernel_ptr() {
+    return reinterpret_cast<void *>(gemv_kernel<kShapes[S].nw, kShapes[S].stages, kShapes[S].ch4, MODE>);
 }
 
-template <int MODE>
-void *kernel_ptr() {
-    return reinterpret_cast<void *>(gemv_kernel<kNW, kStages, kCH4, MODE>);
+template <int S>
+void *kernel_for(int mode) {
+    switch (mode) {
+        case GEMV_QKV: return kernel_ptr<S, GEMV_QKV>();
+        case GEMV_RESID: return kernel_ptr<S, GEMV_RESID>();
+        case GEMV_W13: return kernel_ptr<S, GEMV_W13>();
+        case GEMV_CLS: return kernel_ptr<S, GEMV_CLS>();
+    }
+    return nullptr;
+}
+
+void *kernel_for(int shape, int mode) {
+    switch (shape) {
+        case 0: return kernel_for<0>(mode);
+        case 1: return kernel_for<1>(mode);
+        case 2: return kernel_for<2>(mode);
+    }
+    return nullptr;
+}
+
+template <int S>
+size_t fixed_of() {
+    return fixed_bytes<kShapes[S].nw, kShapes[S].stages>();
+}
+
+size_t fixed_of(int shape) {
+    switch (shape) {
+        case 0: return fixed_of<0>();
+        case 1: return fixed_of<1>();
+        default: return fixed_of<2>();
+    }
 }
 }  // namespace
 
-int gemv_threads() { return kNW * 32; }
+int gemv_threads(int shape) { return kShapes[shape].nw * 32; }
 
-size_t gemv_smem_bytes(int n, int ymax) {
-    return fixed_bytes<kNW, kStages>() + (size_t)kNW * kStages * kCH4 * 16 + (size_t)n * 4 +
-           align_up((size_t)ymax * 4, 16);
+size_t gemv_smem_bytes(int shape, int n, int ymax) {
+    const Shape &sh = kShapes[shape];
+    return fixed_of(shape) + (size_t)sh.nw * sh.stages * sh.ch4 * 16 + (size_t)n * 4 + align_up((size_t)ymax * 4, 16);
+}
+
+int gemv_pick_shape(int n, int ymax, size_t *smem) {
+    for (int sh = 0; sh < kGemvShapes; ++sh) {
+        *smem = gemv_smem_bytes(sh, n, ymax);
+        if (*smem <= 227 * 1024) return sh;
+    }
+    return -1;
 }
 
 cudaError_t gemv_init() {
-    cudaError_t e;
-    if ((e = set_attr<GEMV_QKV>()) != cudaSuccess) return e;
-    if ((e = set_attr<GEMV_RESID>()) != cudaSuccess) return e;
-    if ((e = set_attr<GEMV_W13>()) != cudaSuccess) return e;
-    return set_attr<GEMV_CLS>();
+    for (int sh = 0; sh < kGemvShapes; ++sh)
+        for (int mode = GEMV_QKV; mode <= GEMV_CLS; ++mode) {
+            cudaError_t e =
+                cudaFuncSetAttribute(kernel_for(sh, mode), cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+            if (e != cudaSuccess) return e;
+        }
+    return cudaSuccess;
 }
 
-cudaError_t launch_gemv(int mode, const GemvParams &p, int grid, size_t smem, cudaStream_t stream, bool pdl) {
-    void *fn = nullptr;
-    switch (mode) {
-        case GEMV_QKV: fn = kernel_ptr<GEMV_QKV>(); break;
-        case GEMV_RESID: fn = kernel_ptr<GEMV_RESID>(); break;
-        case GEMV_W13: fn = kernel_ptr<GEMV_W13>(); break;
-        case GEMV_CLS: fn = kernel_ptr<GEMV_CLS>(); break;
-        default: return cudaErrorInvalidValue;
-    }
+cudaError_t launch_gemv(int mode, int shape, const GemvParams &p, int grid, size_t smem, cudaStream_t stream,
+                        bool pdl) {
+    if (shape < 0 || shape >= kGemvShapes) return cudaErrorInvalidValue;
+    void *fn = kernel_for(shape, mode);
+    if (!fn) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kNW * 32);
+    cfg.blockDim = dim3(gemv_threads(shape));
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];

@@ -55,6 +55,7 @@ struct BatchSet {
 
 struct GemvPlan {
     int mode;
+    int shape;  // GEMV launch shape (-1: none fits in shared memory)
     int grid;
     size_t smem;
     int units, unit_rows, factor;  // work split: units of unit_rows rows; factor rows per row for W1/W3
@@ -215,7 +216,7 @@ void make_plans(l2_ctx *c) {
         pl.factor = ymax_factor;
         pl.grid = units < G ? units : G;
         const int per = ceil_div(units, pl.grid);
-        pl.smem = gemv_smem_bytes(n, per * unit_rows * ymax_factor);
+        pl.shape = gemv_pick_shape(n, per * unit_rows * ymax_factor, &pl.smem);
         GemvParams &b = pl.base;
         memset(&b, 0, sizeof(b));
         b.n = n;
@@ -458,7 +459,7 @@ cudaError_t launch_op(l2_ctx *c, int op, int layer, int batch, cudaStream_t s, b
     switch (op) {
         case 0: {
             GemvParams g = layer_params(c, c->plan_qkv, layer);
-            return launch_gemv(GEMV_QKV, g, c->plan_qkv.grid, c->plan_qkv.smem, s, pdl);
+            return launch_gemv(GEMV_QKV, c->plan_qkv.shape, g, c->plan_qkv.grid, c->plan_qkv.smem, s, pdl);
         }
         case 1: {
             AttnParams a = attn_params(c, layer, batch);
@@ -466,19 +467,19 @@ cudaError_t launch_op(l2_ctx *c, int op, int layer, int batch, cudaStream_t s, b
         }
         case 2: {
             GemvParams g = layer_params(c, c->plan_wo, layer);
-            return launch_gemv(GEMV_RESID, g, c->plan_wo.grid, c->plan_wo.smem, s, pdl);
+            return launch_gemv(GEMV_RESID, c->plan_wo.shape, g, c->plan_wo.grid, c->plan_wo.smem, s, pdl);
         }
         case 3: {
             GemvParams g = layer_params(c, c->plan_w13, layer);
-            return launch_gemv(GEMV_W13, g, c->plan_w13.grid, c->plan_w13.smem, s, pdl);
+            return launch_gemv(GEMV_W13, c->plan_w13.shape, g, c->plan_w13.grid, c->plan_w13.smem, s, pdl);
         }
         case 4: {
             GemvParams g = layer_params(c, c->plan_w2, layer);
-            return launch_gemv(GEMV_RESID, g, c->plan_w2.grid, c->plan_w2.smem, s, pdl);
+            return launch_gemv(GEMV_RESID, c->plan_w2.shape, g, c->plan_w2.grid, c->plan_w2.smem, s, pdl);
         }
         case 5: {
             GemvParams g = layer_params(c, c->plan_cls, 0);
-            return launch_gemv(GEMV_CLS, g, c->plan_cls.grid, c->plan_cls.smem, s, pdl);
+            return launch_gemv(GEMV_CLS, c->plan_cls.shape, g, c->plan_cls.grid, c->plan_cls.smem, s, pdl);
         }
     }
     return cudaErrorInvalidValue;
@@ -664,7 +665,7 @@ int l2_create(const L2Config *config, const L2Weights *weights, int max_batch, u
     c->evict_first = wbytes > 0.75 * (double)l2_bytes;
     make_plans(c);
     for (const GemvPlan *pl : {&c->plan_qkv, &c->plan_wo, &c->plan_w13, &c->plan_w2, &c->plan_cls})
-        if (pl->smem > 227 * 1024)
+        if (pl->shape < 0)
             return bail(fail(c, L2_EINVAL, "a GEMV stage needs %zu bytes of shared memory (> 227 KB); dim or hidden_dim too large",
                              pl->smem));
     if (c->attn.smem > 227 * 1024) return bail(fail(c, L2_EINVAL, "attention needs too much shared memory"));
@@ -824,10 +825,10 @@ void l2_debug_fail_alloc_at(int n) { g_fail_alloc_at = n > 0 ? n : 0; }
 // static device array in place of the handle's workspace.
 
 // Attention scratch of l2_forward_static: accumulators, (max, sum) pairs and
-// tickets, 1 MiB.  Every GPU that loads the library holds it until exit.  In
+// tickets, 512 KiB.  Every GPU that loads the library holds it until exit.  In
 // host code this name is only a stand-in: kernels get the address that
 // cudaGetSymbolAddress returns for the current device.
-constexpr size_t kStaticScratchFloats = size_t(1) << 18;
+constexpr size_t kStaticScratchFloats = size_t(1) << 17;
 static __device__ __align__(256) float g_static_scratch[kStaticScratchFloats];
 
 namespace {

@@ -7,12 +7,17 @@
 
 namespace l2 {
 
-// Fused streaming GEMV (gemv.cu).
+// Fused streaming GEMV (gemv.cu), in one of kGemvShapes launch shapes.
+constexpr int kGemvShapes = 3;
 cudaError_t gemv_init();
-int gemv_threads();
+int gemv_threads(int shape);
 // Dynamic shared memory of one CTA for input length n and at most ymax local outputs.
-size_t gemv_smem_bytes(int n, int ymax);
-cudaError_t launch_gemv(int mode, const GemvParams &p, int grid, size_t smem, cudaStream_t stream, bool pdl);
+size_t gemv_smem_bytes(int shape, int n, int ymax);
+// The first launch shape whose shared memory fits (its size in *smem), or -1
+// (*smem then holds the smallest shape's need).
+int gemv_pick_shape(int n, int ymax, size_t *smem);
+cudaError_t launch_gemv(int mode, int shape, const GemvParams &p, int grid, size_t smem, cudaStream_t stream,
+                        bool pdl);
 
 // Batched fused GEMV, B >= 2 sequences per step (gemv_batched.cu).
 cudaError_t gemv_batched_init();

@@ -48,7 +48,8 @@ def test_static_scratch_step_matches_forward_on_two_calls():
 
 def test_static_scratch_limit_is_enforced():
     # 32 heads of 128 on 4 KV heads with a 16384-position cache need more
-    # attention scratch than the 262144 floats of the static array.
+    # attention scratch than the 131072 floats of the static array (on 152
+    # SMs with one attention CTA per SM: 32 * 38 * 130 + 4 = 158084 floats).
     cfg = (4096, 16, 1, 32, 4, 16, 16384)
     wl = WORKLOADS["tiny"].replace(dim=4096, hidden_dim=16, n_layers=1, n_heads=32, n_kv_heads=4,
                                    vocab_size=16, seq_len=16384, shared_wcls=False)
