@@ -48,6 +48,13 @@ extern "C" {
 #define L2_FLAG_DEBUG 0x1u    /* keep per-layer attention probabilities (l2_debug_attention) */
 #define L2_FLAG_NO_GRAPH 0x2u /* launch the step's kernels one by one instead of a CUDA graph */
 #define L2_FLAG_NO_PDL 0x4u   /* no programmatic dependent launch between the step's kernels */
+/* Run batch-1 steps as ONE persistent cooperative kernel (one CTA per SM,
+ * grid-wide barriers between the phases of a layer) instead of one kernel
+ * per matmul group and one attention kernel per layer.  Used when the device
+ * supports cooperative launch and the shape fits (l2_kernels_per_step then
+ * reports 1); ignored with L2_FLAG_DEBUG.  Measured on GB300 it is slower
+ * than the default graph of kernels with programmatic dependent launch. */
+#define L2_FLAG_PERSIST 0x8u
 
 /* Model shape: the pages' Config struct ("run.c", Config; walkthrough §2).
  * head_size = dim / n_heads, kv_dim = dim * n_kv_heads / n_heads. */

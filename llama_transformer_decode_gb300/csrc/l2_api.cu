@@ -11,6 +11,7 @@
 // every position.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstddef>
@@ -33,6 +34,14 @@ constexpr int kRing = 64;      // pinned step-input slots in flight
 #endif
 #ifndef L2_ATTN_MAX_PER_SM
 #define L2_ATTN_MAX_PER_SM 4
+#endif
+// Ring of the persistent step kernel: buffers per warp, and the largest
+// buffer in 16-byte words (the host fills the free shared memory up to it).
+#ifndef L2_STEP_STAGES
+#define L2_STEP_STAGES 3
+#endif
+#ifndef L2_STEP_MAX_CHUNK_WORDS
+#define L2_STEP_MAX_CHUNK_WORDS 512
 #endif
 // Fewest cache positions per attention CTA.  Measured on GB300 (7B shape):
 // 128 beats 32 and 64 at positions up to ~2000 (fewer chunks to merge, a
@@ -94,6 +103,10 @@ struct l2_ctx {
     int attn_chunks = 1;
     int attn_per_sm = 1;  // attention CTAs resident per SM
     GemvPlan plan_qkv{}, plan_wo{}, plan_w13{}, plan_w2{}, plan_cls{};
+    bool persist = false;  // batch-1 steps run as the persistent step kernel
+    int persist_gq = 1;
+    size_t persist_smem = 0;
+    StepKParams sp{};
     std::vector<BatchSet> bsets;  // batched GEMV plans, indexed by batch size
     bool evict_first = false;
 
@@ -450,6 +463,96 @@ cudaError_t launch_batched(l2_ctx *c, int k, const GemvPlan &pl, int layer, int 
     return launch_gemv_batched(pl.mode, bp, bpl.grid, bpl.smem, s, pdl);
 }
 
+// The persistent batch-1 step kernel (L2_FLAG_PERSIST): used when the device
+// launches cooperative kernels, one CTA per SM fits (shared memory for the
+// largest phase), the attention items of a step fit the grid and two cache
+// rows fit one ring buffer; not with L2_FLAG_DEBUG (it keeps no
+// probabilities).
+int plan_persistent(l2_ctx *c) {
+    c->persist = false;
+    if (!(c->flags & L2_FLAG_PERSIST) || (c->flags & L2_FLAG_DEBUG)) return L2_OK;
+    const L2Config &p = c->cfg;
+    const int G = c->num_sms;
+    int coop = 0;
+    if (cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, c->device) != cudaSuccess) {
+        cudaGetLastError();
+        return L2_OK;
+    }
+    if (!coop || p.n_kv_heads > G) return L2_OK;
+    auto per_cta = [&](int units) { return ceil_div(units, G); };
+    int ys = 2 * per_cta((p.dim + 2 * c->kv_dim) / 2);
+    ys = std::max(ys, per_cta(p.dim));
+    ys = std::max(ys, 2 * per_cta(p.hidden_dim));
+    ys = std::max(ys, per_cta(p.vocab_size));
+    const int xs = std::max(p.dim, p.hidden_dim);
+    const int gq = c->attn.gq;
+    int stages = L2_STEP_STAGES, ch4 = step_kernel_ring(gq, c->head_size, xs, ys, stages, L2_STEP_MAX_CHUNK_WORDS);
+    if (!ch4) {
+        stages = 2;
+        ch4 = step_kernel_ring(gq, c->head_size, xs, ys, stages, L2_STEP_MAX_CHUNK_WORDS);
+    }
+    if (!ch4) return L2_OK;
+    const size_t smem = step_kernel_smem(gq, c->head_size, xs, ys, stages, ch4);
+    if (smem > 227 * 1024) return L2_OK;
+    cudaError_t e = step_kernel_init();
+    if (e != cudaSuccess) return cuda_fail(c, e, "step_kernel_init()");
+    if (step_kernel_ctas_per_sm(gq, smem) < 1) return L2_OK;
+    int nc = G / p.n_kv_heads;
+    nc = std::min(nc, ceil_div(p.seq_len, kMinChunk));
+    nc = std::min(nc, c->attn_chunks);
+    if (nc < 1) return L2_OK;
+
+    StepKParams &k = c->sp;
+    k = StepKParams{};
+    k.emb = c->w.token_embedding_table;
+    k.rms_att = c->w.rms_att_weight;
+    k.rms_ffn = c->w.rms_ffn_weight;
+    k.rms_final = c->w.rms_final_weight;
+    k.wq = c->w.wq;
+    k.wk = c->w.wk;
+    k.wv = c->w.wv;
+    k.wo = c->w.wo;
+    k.w1 = c->w.w1;
+    k.w2 = c->w.w2;
+    k.w3 = c->w.w3;
+    k.wcls = c->w.wcls;
+    k.x = c->x;
+    k.xb = c->xb;
+    k.q = c->q;
+    k.hb = c->hb;
+    k.logits = c->logits;
+    k.kcache = c->kcache;
+    k.vcache = c->vcache;
+    k.rope = c->rope;
+    k.ws_ml = c->ws_ml;
+    k.ws_acc = c->ws_acc;
+    k.tickets = c->tickets;
+    k.step = c->step_dev;
+    k.err = c->err;
+    k.dim = p.dim;
+    k.hidden_dim = p.hidden_dim;
+    k.n_layers = p.n_layers;
+    k.n_heads = p.n_heads;
+    k.n_kv_heads = p.n_kv_heads;
+    k.head_size = c->head_size;
+    k.kv_dim = c->kv_dim;
+    k.vocab = p.vocab_size;
+    k.seq_len = p.seq_len;
+    k.n_chunks = nc;
+    k.min_chunk = kMinChunk;
+    k.lp = c->attn.lp;
+    k.xs_floats = xs;
+    k.ys_floats = ys;
+    k.evict_first = c->evict_first ? 1 : 0;
+    k.stages = stages;
+    k.ch4 = ch4;
+    k.scale = (float)(1.0 / std::sqrt((double)c->head_size));
+    c->persist_gq = gq;
+    c->persist_smem = smem;
+    c->persist = true;
+    return L2_OK;
+}
+
 cudaError_t launch_op(l2_ctx *c, int op, int layer, int batch, cudaStream_t s, bool pdl) {
     if (batch > 1 && op != 1) {
         const GemvPlan *pl[] = {&c->plan_qkv, nullptr, &c->plan_wo, &c->plan_w13, &c->plan_w2, &c->plan_cls};
@@ -540,11 +643,14 @@ int submit(l2_ctx *c, int B, const int *tokens, const int *pos, float *logits_ou
     }
     sh.logits_out = logits_out;
     sh.B = B;
+    sh.sync_count = 0;
     L2_CUDA(c, cudaMemcpyAsync(c->step_dev, &sh, sizeof(StepDev), cudaMemcpyHostToDevice, c->stream));
     L2_CUDA(c, cudaEventRecord(c->ring_ev[i], c->stream));
     c->ring_used[i] = true;
 
-    if (c->flags & L2_FLAG_NO_GRAPH) {
+    if (B == 1 && c->persist) {
+        L2_CUDA(c, launch_step_kernel(c->persist_gq, c->sp, c->num_sms, c->persist_smem, c->stream));
+    } else if (c->flags & L2_FLAG_NO_GRAPH) {
         L2_CUDA(c, enqueue_step(c, B, c->stream));
     } else {
         cudaGraphExec_t g = nullptr;
@@ -568,7 +674,7 @@ int l2_create(const L2Config *config, const L2Weights *weights, int max_batch, u
     if (!config || !weights) return fail(nullptr, L2_EINVAL, "config and weights must not be NULL");
     if (max_batch < 1 || max_batch > kMaxBatch)
         return fail(nullptr, L2_EINVAL, "max_batch %d outside 1..%d", max_batch, kMaxBatch);
-    if (flags & ~(L2_FLAG_DEBUG | L2_FLAG_NO_GRAPH | L2_FLAG_NO_PDL))
+    if (flags & ~(L2_FLAG_DEBUG | L2_FLAG_NO_GRAPH | L2_FLAG_NO_PDL | L2_FLAG_PERSIST))
         return fail(nullptr, L2_EINVAL, "unknown flags 0x%x", flags);
     int rc = check_config(*config);
     if (rc) return rc;
@@ -672,6 +778,7 @@ int l2_create(const L2Config *config, const L2Weights *weights, int max_batch, u
     c->bsets.resize(max_batch + 1);
     for (int b = 2; b <= max_batch; ++b)
         if ((rc = build_batch_set(c, b))) return bail(rc);
+    if ((rc = plan_persistent(c))) return bail(rc);
     CREATE_CUDA(cudaDeviceSynchronize());
 #undef CREATE_CUDA
     *out = c;
@@ -804,6 +911,7 @@ int l2_launch_op(l2_ctx *c, int op, int layer, int count) {
 
 int l2_kernels_per_step(const l2_ctx *c, int B) {
     if (!c || B < 1 || B > c->max_batch) return L2_EINVAL;
+    if (B == 1 && c->persist) return 1;
     return 5 * c->cfg.n_layers + 1;
 }
 

@@ -29,6 +29,18 @@ int gemv_batched_rows_cap(int batch);
 size_t gemv_batched_smem(int stage_rows, int batch, int n, bool norm, int *stages, int *tk);
 cudaError_t launch_gemv_batched(int mode, const BatchParams &bp, int grid, size_t smem, cudaStream_t stream, bool pdl);
 
+// Persistent step kernel for batch 1 (step_kernel.cu), one CTA per SM,
+// launched cooperatively.
+int step_kernel_threads();
+size_t step_kernel_smem(int gq, int head_size, int xs_floats, int ys_floats, int stages, int ch4);
+// 16-byte words per ring buffer (a multiple of 8, at most max_ch4) that fill
+// the shared memory left by the largest phase with `stages` buffers per warp,
+// or 0 if two cache rows do not fit one buffer.
+int step_kernel_ring(int gq, int head_size, int xs_floats, int ys_floats, int stages, int max_ch4);
+cudaError_t step_kernel_init();
+int step_kernel_ctas_per_sm(int gq, size_t smem);
+cudaError_t launch_step_kernel(int gq, const StepKParams &p, int grid, size_t smem, cudaStream_t stream);
+
 // Flash-decoding attention (attention.cu).
 struct AttnLaunch {
     int lp;       // lanes per cache row (power of two)

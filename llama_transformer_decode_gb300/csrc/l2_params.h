@@ -19,7 +19,8 @@ struct StepDev {
     int pos[kMaxBatch];
     float *logits_out;  // caller's device buffer [B][vocab] or nullptr
     int B;
-    int pad_[3];
+    unsigned sync_count;  // grid-barrier arrivals of the persistent step kernel (zero at the copy)
+    int pad_[2];
 };
 
 // The fused GEMV kernel's modes (prologue / epilogue around y = W v).
@@ -69,6 +70,31 @@ struct alignas(64) BatchParams {
     int rows_box;         // rows per weight box = rows per block (a CTA walks its rows in blocks)
     int tk;               // columns per K tile
     int stages;           // ring depth
+};
+
+// Persistent step kernel (step_kernel.cu, batch 1): everything one step
+// reads and writes.  Weights are the model's base pointers (layer l of a
+// per-layer tensor starts l * its per-layer size further on).
+struct StepKParams {
+    const float *emb, *rms_att, *rms_ffn, *rms_final;
+    const float *wq, *wk, *wv, *wo, *w1, *w2, *w3, *wcls;
+    float *x, *xb, *q, *hb, *logits;
+    float *kcache, *vcache;   // slot 0: [layer][kv_head][seq_len][head_size]
+    const float2 *rope;
+    float *ws_ml, *ws_acc;    // attention partials [n_heads][n_chunks][2] / [..][head_size]
+    unsigned *tickets;        // [n_kv_heads], zero between steps
+    StepDev *step;
+    int *err;
+    int dim, hidden_dim, n_layers, n_heads, n_kv_heads, head_size, kv_dim, vocab, seq_len;
+    int n_chunks;    // most attention CTAs per KV head (n_chunks * n_kv_heads <= grid)
+    int min_chunk;   // fewest cache positions per attention CTA
+    int lp;          // lanes per cache row (power of two >= head_size / 4)
+    int xs_floats;   // shared input-vector region (largest row length)
+    int ys_floats;   // shared output region (most outputs one CTA produces in a phase)
+    int evict_first;
+    int stages;      // ring buffers per warp (<= 4)
+    int ch4;         // 16-byte words per ring buffer (a multiple of 8)
+    float scale;     // 1 / sqrt(head_size)
 };
 
 struct AttnParams {

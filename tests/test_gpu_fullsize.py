@@ -1,5 +1,6 @@
 """Parity at the full workload sizes, in the launch configuration bench.py
-times (CUDA graph + programmatic dependent launch).
+times (CUDA graph + programmatic dependent launch), and for the 7B shape also
+with the opt-in persistent step kernel.
 
 7B shape: the first 8 teacher-forced steps against the oracle, then one run
 to position 4095 whose steps at positions {255, 1023, 2047, 4095} are each
@@ -49,12 +50,18 @@ def test_llama7b_first_steps(llama7b):
     dec.close()
 
 
-def test_llama7b_sampled_positions(llama7b):
+@pytest.mark.parametrize("path", ["per_kernel_debug", "persistent"])
+def test_llama7b_sampled_positions(llama7b, path):
+    # per_kernel_debug: one kernel per matmul (the path bench.py times) with
+    # the attention probabilities exported; persistent: the opt-in persistent
+    # step kernel (logits)
     wl, w, dev = llama7b
     samples = (255, 1023, 2047, 4095)
-    layers = (0, 15, 31)
+    debug = path == "per_kernel_debug"
+    layers = (0, 15, 31) if debug else ()
     toks = synth.token_stream(wl, 0, wl.seq_len)
-    dec = pkg.Decoder(wl.config_tuple(), dev, flags=pkg.L2_FLAG_DEBUG)
+    dec = pkg.Decoder(wl.config_tuple(), dev, flags=pkg.L2_FLAG_DEBUG if debug else pkg.L2_FLAG_PERSIST)
+    assert (dec.kernels_per_step() == 1) == (not debug)
     out = torch.empty(wl.vocab_size, device="cuda")
     got, att = {}, {}
     for p in range(wl.seq_len):
@@ -71,7 +78,7 @@ def test_llama7b_sampled_positions(llama7b):
     for p in samples:
         # the oracle's cache rows 0..p-1 are the GPU run's; row p is recomputed
         r, ra = ref.forward(int(toks[p]), p, want_att=True)
-        rel = check_logits(got[p], r, f"llama2_7b pos {p}")
+        rel = check_logits(got[p], r, f"llama2_7b pos {p} ({path})")
         for l in layers:
             d = float(np.abs(att[p][l] - ra[l, :, : p + 1]).max())
             assert d <= ATT_ABS, f"pos {p} layer {l}: attention differs by {d:.3e}"
