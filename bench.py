@@ -41,7 +41,7 @@ FALLBACK_HBM_GBS = 6800.0
 # the dominant kernel, from the ncu capture summarised in
 # profiles/gemv_w13_llama2_7b.md, valid only for the kernel source whose
 # sha256 prefix is recorded beside it.
-W13_NCU_TRAFFIC = (364068608, "13f432b0754ca229")  # (bytes per launch, gemv.cu sha256 prefix)
+W13_NCU_TRAFFIC = (364313344, "08026df8323ddb77")  # (bytes per launch, gemv.cu sha256 prefix)
 
 
 def weight_bytes(wl) -> int:
@@ -373,7 +373,7 @@ def run_ours(args, wl):
             if hashlib.sha256(src).hexdigest().startswith(W13_NCU_TRAFFIC[1]):
                 traffic = W13_NCU_TRAFFIC[0]
         roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                    "traffic": traffic, "kernel": "gemv_kernel<GEMV_W13> (rmsnorm + W1/W3 + SwiGLU)",
+                    "traffic": traffic, "kernel": "gemv_kernel<8,3,512,GEMV_W13> (rmsnorm + W1/W3 + SwiGLU)",
                     "bytes_per_launch": w13_bytes(wl), "us_per_launch": w13_ms * 1000.0,
                     "timing": "CUDA events around standalone launches on the decoder's stream, layers cycled",
                     "peak_source": peak_src + " (MEASURED_PEAKS.json hbm_gbs, copy bandwidth)"}

@@ -1,7 +1,8 @@
 """ORACLE -- test infrastructure, not part of the product.
 
 Python access (ctypes) to ``l2_oracle.c``, the plain CPU statement of the
-llama2.c decode step.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+llama2.c decode step, and to ``sampler_oracle.c``, the statement of its
+token sampler.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
 benchmark's CPU-baseline leg may import this package; the library under
 ``llama_transformer_decode_gb300`` never does, and the two share no code.
 
@@ -20,7 +21,10 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "l2_oracle.c")
 _OUT = os.path.join(_HERE, "_build", "liboracle.so")
+_SSRC = os.path.join(_HERE, "sampler_oracle.c")
+_SOUT = os.path.join(_HERE, "_build", "libsampler_oracle.so")
 _lib = None
+_slib = None
 
 _FP = ctypes.POINTER(ctypes.c_float)
 
@@ -46,9 +50,67 @@ def compile_oracle(src: str, out: str, extra: tuple = ()) -> str:
 
 
 def build(force: bool = False) -> str:
+    build_sampler(force)
     if not force and os.path.exists(_OUT) and os.path.getmtime(_OUT) >= os.path.getmtime(_SRC):
         return _OUT
     return compile_oracle(_SRC, _OUT)
+
+
+def build_sampler(force: bool = False) -> str:
+    """The sampler's statement is built without contraction of a*b+c into one
+    fused operation, so every fp32 operation is the one written."""
+    if not force and os.path.exists(_SOUT) and os.path.getmtime(_SOUT) >= os.path.getmtime(_SSRC):
+        return _SOUT
+    os.makedirs(os.path.dirname(_SOUT), exist_ok=True)
+    tmp = _SOUT + f".tmp{os.getpid()}"
+    subprocess.check_call(["gcc", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared", _SSRC,
+                           "-o", tmp, "-lm"])
+    os.replace(tmp, _SOUT)
+    return _SOUT
+
+
+def load_sampler():
+    global _slib
+    if _slib is None:
+        lib = ctypes.CDLL(build_sampler())
+        u64p = ctypes.POINTER(ctypes.c_uint64)
+        lib.oracle_random_u32.argtypes = [u64p]
+        lib.oracle_random_u32.restype = ctypes.c_uint32
+        lib.oracle_sampler_exp.argtypes = [ctypes.c_float]
+        lib.oracle_sampler_exp.restype = ctypes.c_float
+        lib.oracle_argmax.argtypes = [ctypes.c_void_p, ctypes.c_int]
+        lib.oracle_argmax.restype = ctypes.c_int
+        lib.oracle_sample.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_float, u64p, u64p, u64p]
+        lib.oracle_sample.restype = ctypes.c_int
+        _slib = lib
+    return _slib
+
+
+def random_u32(state: int):
+    """One xorshift* draw: (value, next state)."""
+    st = ctypes.c_uint64(state)
+    v = load_sampler().oracle_random_u32(ctypes.byref(st))
+    return int(v), int(st.value)
+
+
+def sampler_exp(x: float) -> float:
+    return float(load_sampler().oracle_sampler_exp(float(x)))
+
+
+def argmax(v) -> int:
+    v = np.ascontiguousarray(v, dtype=np.float32)
+    return int(load_sampler().oracle_argmax(v.ctypes.data, v.size))
+
+
+def sample(logits, temperature: float, topp: float, state: int):
+    """One token from fp32 logits: (index, next state, total S or P, scaled coin r)."""
+    x = np.ascontiguousarray(logits, dtype=np.float32)
+    st, tot, r = ctypes.c_uint64(state), ctypes.c_uint64(0), ctypes.c_uint64(0)
+    idx = load_sampler().oracle_sample(x.ctypes.data, x.size, float(temperature), float(topp), ctypes.byref(st),
+                                       ctypes.byref(tot), ctypes.byref(r))
+    if idx < 0:
+        raise ValueError("oracle_sample rejected its input")
+    return int(idx), int(st.value), int(tot.value), int(r.value)
 
 
 def _declare(lib):
