@@ -69,10 +69,11 @@ def build_sampler(force: bool = False) -> str:
     return _SOUT
 
 
-def load_sampler():
+def load_sampler(path: str | None = None):
+    """The sampler oracle (built on first use); ``path`` loads another build of it."""
     global _slib
-    if _slib is None:
-        lib = ctypes.CDLL(build_sampler())
+    if path is not None or _slib is None:
+        lib = ctypes.CDLL(path or build_sampler())
         u64p = ctypes.POINTER(ctypes.c_uint64)
         lib.oracle_random_u32.argtypes = [u64p]
         lib.oracle_random_u32.restype = ctypes.c_uint32
@@ -82,32 +83,34 @@ def load_sampler():
         lib.oracle_argmax.restype = ctypes.c_int
         lib.oracle_sample.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_float, u64p, u64p, u64p]
         lib.oracle_sample.restype = ctypes.c_int
+        if path is not None:
+            return lib
         _slib = lib
     return _slib
 
 
-def random_u32(state: int):
+def random_u32(state: int, lib=None):
     """One xorshift* draw: (value, next state)."""
     st = ctypes.c_uint64(state)
-    v = load_sampler().oracle_random_u32(ctypes.byref(st))
+    v = (lib or load_sampler()).oracle_random_u32(ctypes.byref(st))
     return int(v), int(st.value)
 
 
-def sampler_exp(x: float) -> float:
-    return float(load_sampler().oracle_sampler_exp(float(x)))
+def sampler_exp(x: float, lib=None) -> float:
+    return float((lib or load_sampler()).oracle_sampler_exp(float(x)))
 
 
-def argmax(v) -> int:
+def argmax(v, lib=None) -> int:
     v = np.ascontiguousarray(v, dtype=np.float32)
-    return int(load_sampler().oracle_argmax(v.ctypes.data, v.size))
+    return int((lib or load_sampler()).oracle_argmax(v.ctypes.data, v.size))
 
 
-def sample(logits, temperature: float, topp: float, state: int):
+def sample(logits, temperature: float, topp: float, state: int, lib=None):
     """One token from fp32 logits: (index, next state, total S or P, scaled coin r)."""
     x = np.ascontiguousarray(logits, dtype=np.float32)
     st, tot, r = ctypes.c_uint64(state), ctypes.c_uint64(0), ctypes.c_uint64(0)
-    idx = load_sampler().oracle_sample(x.ctypes.data, x.size, float(temperature), float(topp), ctypes.byref(st),
-                                       ctypes.byref(tot), ctypes.byref(r))
+    idx = (lib or load_sampler()).oracle_sample(x.ctypes.data, x.size, float(temperature), float(topp),
+                                                ctypes.byref(st), ctypes.byref(tot), ctypes.byref(r))
     if idx < 0:
         raise ValueError("oracle_sample rejected its input")
     return int(idx), int(st.value), int(tot.value), int(r.value)
