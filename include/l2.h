@@ -211,6 +211,37 @@ int l2_step_input_bytes(void);
 int l2_forward_static(l2_ctx *ctx, int token, int pos, float *logits_out);
 
 /*
+ * Next-token sampling on the device: the sampler of the generation loop on
+ * the pages ("run.c": argmax(), sample() and the main loop; "run.c 逐行解讀"
+ * §6 Sampler: random_u32() xorshift* and sample() with temperature and
+ * top-p).  For each of B sequences, from logits[b][0..vocab_size):
+ *   temperature == 0: the index of the first maximum; rng_state[b] unchanged;
+ *   temperature > 0: one xorshift* draw from rng_state[b] (advanced in
+ *     place), its top 24 bits k the coin; the tempered softmax weights
+ *     q_i = floor(E(l_i / T - max_j l_j / T) * 2^48), E a specified fp32
+ *     exponential (Cody-Waite reduction, degree-7 Taylor polynomial, within
+ *     1 ulp of exp, 0 below -87); the first index whose running total of q
+ *     exceeds floor(k * total / 2^24);
+ *   0 < topp < 1: the same draw restricted to the nucleus, the shortest
+ *     prefix of the weights sorted descending (ties: lower index first)
+ *     whose total P has P * 2^24 >= floor(topp * 2^24) * total, walked in
+ *     that order against floor(k * P / 2^24).
+ * All sums are exact integer arithmetic, so the result is a function of the
+ * inputs alone (bit-for-bit reproducible).  Tokens whose weight is below
+ * 2^-48 of the largest are never drawn.
+ * logits (fp32, row-major [B][vocab_size], 4-byte aligned), rng_state
+ * ([B] 64-bit states, non-zero) and tokens_out ([B] ints) are DEVICE
+ * pointers owned by the caller; rows of logits are not modified.  The work
+ * is enqueued on cuda_stream (NULL: the legacy default stream) and the call
+ * returns without waiting.  L2_EINVAL for NULL pointers, host pointers,
+ * B < 1, vocab_size outside 1..49152, a negative or non-finite temperature
+ * or a non-finite topp (l2_last_error(NULL) describes it); L2_ECUDA if the
+ * launch fails.  Not for logits containing NaN.
+ */
+int l2_sample(const float *logits, int B, int vocab_size, float temperature, float topp,
+              unsigned long long *rng_state, int *tokens_out, void *cuda_stream);
+
+/*
  * Fault injection for tests: makes the n-th device allocation from now on
  * (n >= 1) fail as if out of memory; 0 disables.  Process-wide.
  */

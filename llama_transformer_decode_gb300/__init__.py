@@ -176,6 +176,29 @@ class Decoder:
         return self._check(self._lib.l2_kernels_per_step(self._h, int(batch)))
 
 
+def sample(logits, temperature: float, topp: float, rng_state, out=None, stream=None):
+    """Next token of each row of ``logits`` (CUDA fp32 [B][vocab]) with the
+    pages' sampler (l2_sample): argmax at temperature 0, otherwise one
+    xorshift* draw per row from ``rng_state`` (CUDA uint64/int64 [B], advanced
+    in place), restricted to the top-p nucleus when 0 < topp < 1.  Returns
+    ``out`` (CUDA int32 [B]); enqueued on ``stream`` (default: torch's current)."""
+    import torch
+    logits = logits if logits.dim() == 2 else logits.reshape(1, -1)
+    B, V = logits.shape
+    assert logits.dtype == torch.float32 and logits.is_cuda and logits.is_contiguous()
+    assert rng_state.is_cuda and rng_state.numel() >= B and rng_state.element_size() == 8 and rng_state.is_contiguous()
+    if out is None:
+        out = torch.empty(B, dtype=torch.int32, device=logits.device)
+    assert out.dtype == torch.int32 and out.is_cuda and out.numel() >= B
+    st = stream if stream is not None else torch.cuda.current_stream()
+    rc = lib().l2_sample(ctypes.c_void_p(logits.data_ptr()), B, V, float(temperature), float(topp),
+                         ctypes.c_void_p(rng_state.data_ptr()), ctypes.c_void_p(out.data_ptr()),
+                         ctypes.c_void_p(st.cuda_stream))
+    if rc != L2_OK:
+        raise L2Error(rc, lib().l2_last_error(None).decode())
+    return out
+
+
 def fail_alloc_at(n: int):
     """Fault injection: the n-th device allocation from now on fails (0 disables)."""
     lib().l2_debug_fail_alloc_at(int(n))

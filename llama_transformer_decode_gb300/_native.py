@@ -12,7 +12,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libl2decode.so")
-SOURCES = ("gemv.cu", "gemv_batched.cu", "attention.cu", "step_kernel.cu", "l2_api.cu")
+SOURCES = ("gemv.cu", "gemv_batched.cu", "attention.cu", "step_kernel.cu", "sample.cu", "l2_api.cu")
 HEADERS = ("l2_device.cuh", "l2_params.h", "l2_kernels.h")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-lineinfo", "-O3", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O3"]
@@ -80,7 +80,7 @@ class L2Weights(ctypes.Structure):
 EXPORTS = ("l2_create", "l2_reset", "l2_forward", "l2_forward_batch", "l2_forward_host", "l2_logits",
            "l2_position", "l2_debug_attention", "l2_kv_export", "l2_kv_import", "l2_sync",
            "l2_last_error", "l2_destroy", "l2_launch_op", "l2_kernels_per_step",
-           "l2_step_input_bytes", "l2_forward_static", "l2_debug_fail_alloc_at")
+           "l2_step_input_bytes", "l2_forward_static", "l2_debug_fail_alloc_at", "l2_sample")
 
 _lib = None
 
@@ -112,6 +112,8 @@ def declare(lib):
     lib.l2_step_input_bytes.restype = i
     lib.l2_debug_fail_alloc_at.argtypes = [i]
     lib.l2_debug_fail_alloc_at.restype = None
+    lib.l2_sample.argtypes = [fp, i, i, ctypes.c_float, ctypes.c_float, vp, vp, vp]
+    lib.l2_sample.restype = i
     for name in ("l2_create", "l2_reset", "l2_forward", "l2_forward_batch", "l2_forward_host",
                  "l2_position", "l2_debug_attention", "l2_kv_export", "l2_kv_import", "l2_sync",
                  "l2_launch_op", "l2_kernels_per_step", "l2_forward_static"):

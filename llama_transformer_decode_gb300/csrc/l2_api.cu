@@ -909,6 +909,38 @@ int l2_launch_op(l2_ctx *c, int op, int layer, int count) {
     return L2_OK;
 }
 
+int l2_sample(const float *logits, int B, int vocab_size, float temperature, float topp,
+              unsigned long long *rng_state, int *tokens_out, void *cuda_stream) {
+    if (!logits || !rng_state || !tokens_out) return fail(nullptr, L2_EINVAL, "l2_sample: NULL pointer");
+    if (B < 1 || B > 65535) return fail(nullptr, L2_EINVAL, "l2_sample: B = %d outside 1..65535", B);
+    if (vocab_size < 1 || vocab_size > sample_max_vocab())
+        return fail(nullptr, L2_EINVAL, "l2_sample: vocab_size %d outside 1..%d", vocab_size, sample_max_vocab());
+    if (!(temperature >= 0.0f) || !std::isfinite(temperature))
+        return fail(nullptr, L2_EINVAL, "l2_sample: temperature must be finite and >= 0");
+    if (!std::isfinite(topp)) return fail(nullptr, L2_EINVAL, "l2_sample: topp must be finite");
+    if (reinterpret_cast<uintptr_t>(logits) & 3u) return fail(nullptr, L2_EINVAL, "l2_sample: logits not 4-byte aligned");
+    for (const void *ptr : {(const void *)logits, (const void *)rng_state, (const void *)tokens_out}) {
+        cudaPointerAttributes a{};
+        if (cudaPointerGetAttributes(&a, ptr) != cudaSuccess ||
+            (a.type != cudaMemoryTypeDevice && a.type != cudaMemoryTypeManaged)) {
+            cudaGetLastError();
+            return fail(nullptr, L2_EINVAL, "l2_sample: pointers must be device memory");
+        }
+    }
+    cudaError_t e = sample_init();
+    if (e != cudaSuccess) return cuda_fail(nullptr, e, "sample_init()");
+    SampleParams sp{};
+    sp.logits = logits;
+    sp.rng = rng_state;
+    sp.out = tokens_out;
+    sp.vocab = vocab_size;
+    sp.temperature = temperature;
+    sp.topp = topp;
+    e = launch_sample(sp, B, static_cast<cudaStream_t>(cuda_stream));
+    if (e != cudaSuccess) return cuda_fail(nullptr, e, "sample launch");
+    return L2_OK;
+}
+
 int l2_kernels_per_step(const l2_ctx *c, int B) {
     if (!c || B < 1 || B > c->max_batch) return L2_EINVAL;
     if (B == 1 && c->persist) return 1;

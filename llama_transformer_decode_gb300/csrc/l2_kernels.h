@@ -41,6 +41,12 @@ cudaError_t step_kernel_init();
 int step_kernel_ctas_per_sm(int gq, size_t smem);
 cudaError_t launch_step_kernel(int gq, const StepKParams &p, int grid, size_t smem, cudaStream_t stream);
 
+// Token sampler (sample.cu).
+int sample_max_vocab();
+size_t sample_smem_bytes(int vocab);
+cudaError_t sample_init();
+cudaError_t launch_sample(const SampleParams &p, int batch, cudaStream_t stream);
+
 // Flash-decoding attention (attention.cu).
 struct AttnLaunch {
     int lp;       // lanes per cache row (power of two)

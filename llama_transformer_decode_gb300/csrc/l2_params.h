@@ -97,6 +97,17 @@ struct StepKParams {
     float scale;     // 1 / sqrt(head_size)
 };
 
+// Token sampler (sample.cu): one CTA per sequence.
+struct SampleParams {
+    const float *logits;       // [B][vocab]
+    unsigned long long *rng;   // [B] xorshift* states, advanced by one draw when temperature > 0
+    int *out;                  // [B] sampled token ids
+    int vocab;
+    float temperature;         // 0: argmax
+    float topp;                // in (0, 1): nucleus sampling; otherwise none
+    int cand_cap;              // top-p candidate list capacity (set at launch)
+};
+
 struct AttnParams {
     const float *q;                  // [B][dim]
     const float *kcache, *vcache;    // [slot][layer][kv_head][seq_len][head_size]

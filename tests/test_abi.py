@@ -70,3 +70,23 @@ def test_null_handle_calls_fail_cleanly(lib):
     assert lib.l2_kernels_per_step(None, 1) == pkg.L2_EINVAL
     assert lib.l2_logits(None) is None
     lib.l2_destroy(None)
+
+
+def test_sample_rejects_bad_arguments_on_the_host(lib):
+    f = ctypes.c_void_p
+    buf = (ctypes.c_float * 16)()
+    st = (ctypes.c_uint64 * 2)(1, 2)
+    out = (ctypes.c_int * 2)()
+    p, s, o = ctypes.cast(buf, f), ctypes.cast(st, f), ctypes.cast(out, f)
+    assert lib.l2_sample(None, 1, 16, 1.0, 0.9, s, o, None) == pkg.L2_EINVAL
+    assert b"NULL" in lib.l2_last_error(None)
+    assert lib.l2_sample(p, 0, 16, 1.0, 0.9, s, o, None) == pkg.L2_EINVAL
+    assert lib.l2_sample(p, 1, 0, 1.0, 0.9, s, o, None) == pkg.L2_EINVAL
+    assert lib.l2_sample(p, 1, 49153, 1.0, 0.9, s, o, None) == pkg.L2_EINVAL
+    assert b"vocab_size" in lib.l2_last_error(None)
+    for t in (-1.0, float("inf"), float("nan")):
+        assert lib.l2_sample(p, 1, 16, t, 0.9, s, o, None) == pkg.L2_EINVAL
+    assert lib.l2_sample(p, 1, 16, 1.0, float("nan"), s, o, None) == pkg.L2_EINVAL
+    # host memory is refused before any launch
+    assert lib.l2_sample(p, 1, 16, 1.0, 0.9, s, o, None) == pkg.L2_EINVAL
+    assert b"device memory" in lib.l2_last_error(None)
