@@ -177,6 +177,18 @@ void l2_destroy(l2_ctx *ctx);
  */
 int l2_launch_op(l2_ctx *ctx, int op, int layer, int count);
 
+/*
+ * l2_forward_batch with the tokens read from DEVICE memory when the step
+ * runs (for instance the tokens_out of the previous l2_sample), so a
+ * generation loop need not wait for the host: tokens_dev [B] ints on the
+ * device, pos [B] host ints (checked on the host as in l2_forward_batch).
+ * A token outside [0, vocab_size) cannot be checked on the host: the step
+ * then uses token 0 for that slot and the next l2_sync returns L2_EDEVICE.
+ * Enqueues one extra one-thread kernel before the step.  The pages have no
+ * counterpart (their loop keeps the token on the host).
+ */
+int l2_forward_dev_tokens(l2_ctx *ctx, int B, const int *tokens_dev, const int *pos, float *logits_out);
+
 /* Number of kernel launches one step of batch B enqueues, or L2_EINVAL. */
 int l2_kernels_per_step(const l2_ctx *ctx, int B);
 

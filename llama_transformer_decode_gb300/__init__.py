@@ -124,6 +124,18 @@ class Decoder:
             ctypes.c_void_p(_ptr(out) if out is not None else 0)))
         return out
 
+    def forward_dev_tokens(self, tokens_dev, pos, out=None):
+        """One step whose tokens are read from ``tokens_dev`` (CUDA int32 [B])
+        when it runs; ``pos`` an int (B = 1) or a list of B ints."""
+        import torch
+        pos = [int(pos)] if isinstance(pos, int) else [int(v) for v in pos]
+        B = len(pos)
+        assert tokens_dev.is_cuda and tokens_dev.dtype == torch.int32 and tokens_dev.numel() >= B
+        parr = (ctypes.c_int * B)(*pos)
+        self._check(self._lib.l2_forward_dev_tokens(self._h, B, ctypes.c_void_p(tokens_dev.data_ptr()), parr,
+                                                    ctypes.c_void_p(_ptr(out) if out is not None else None)))
+        return out
+
     def forward_host(self, token: int, pos: int, out: np.ndarray | None = None) -> np.ndarray:
         """Blocking step of slot 0 returning the logits in host memory."""
         if out is None:

@@ -620,10 +620,27 @@ int get_graph(l2_ctx *c, int batch, cudaGraphExec_t *out) {
     return L2_OK;
 }
 
-int submit(l2_ctx *c, int B, const int *tokens, const int *pos, float *logits_out) {
+// Copies B tokens from device memory into the step block, each checked
+// against the vocabulary (an out-of-range token sets L2_DEV_ERR_BOUNDS in the
+// error word and token 0 is used in its place).
+__global__ void set_step_tokens(StepDev *step, const int *tokens, int B, int vocab, int *err) {
+    const int b = threadIdx.x;
+    if (b < B) {
+        int t = tokens[b];
+        if (t < 0 || t >= vocab) {
+            atomicOr(err, L2_DEV_ERR_BOUNDS);
+            t = 0;
+        }
+        step->token[b] = t;
+    }
+}
+
+// tokens_dev: when not NULL, the step's tokens are read from this device
+// array when the step runs (tokens is then ignored).
+int submit(l2_ctx *c, int B, const int *tokens, const int *pos, float *logits_out, const int *tokens_dev = nullptr) {
     if (B < 1 || B > c->max_batch) return fail(c, L2_EINVAL, "batch %d outside 1..%d", B, c->max_batch);
     for (int b = 0; b < B; ++b) {
-        if (tokens[b] < 0 || tokens[b] >= c->cfg.vocab_size)
+        if (!tokens_dev && (tokens[b] < 0 || tokens[b] >= c->cfg.vocab_size))
             return fail(c, L2_EINVAL, "token %d of slot %d outside [0, %d)", tokens[b], b, c->cfg.vocab_size);
         if (pos[b] < 0 || pos[b] >= c->cfg.seq_len)
             return fail(c, L2_EINVAL, "pos %d of slot %d outside [0, %d)", pos[b], b, c->cfg.seq_len);
@@ -638,7 +655,7 @@ int submit(l2_ctx *c, int B, const int *tokens, const int *pos, float *logits_ou
     if (c->ring_used[i]) L2_CUDA(c, cudaEventSynchronize(c->ring_ev[i]));
     StepDev &sh = c->step_host[i];
     for (int b = 0; b < B; ++b) {
-        sh.token[b] = tokens[b];
+        sh.token[b] = tokens_dev ? 0 : tokens[b];
         sh.pos[b] = pos[b];
     }
     sh.logits_out = logits_out;
@@ -647,6 +664,10 @@ int submit(l2_ctx *c, int B, const int *tokens, const int *pos, float *logits_ou
     L2_CUDA(c, cudaMemcpyAsync(c->step_dev, &sh, sizeof(StepDev), cudaMemcpyHostToDevice, c->stream));
     L2_CUDA(c, cudaEventRecord(c->ring_ev[i], c->stream));
     c->ring_used[i] = true;
+    if (tokens_dev) {
+        set_step_tokens<<<1, kMaxBatch, 0, c->stream>>>(c->step_dev, tokens_dev, B, c->cfg.vocab_size, c->err);
+        L2_CUDA(c, cudaGetLastError());
+    }
 
     if (B == 1 && c->persist) {
         L2_CUDA(c, launch_step_kernel(c->persist_gq, c->sp, c->num_sms, c->persist_smem, c->stream));
@@ -804,6 +825,18 @@ int l2_forward_batch(l2_ctx *c, int B, const int *tokens, const int *pos, float 
     if (!c) return L2_EINVAL;
     if (!tokens || !pos) return fail(c, L2_EINVAL, "tokens and pos must not be NULL");
     return submit(c, B, tokens, pos, logits_out);
+}
+
+int l2_forward_dev_tokens(l2_ctx *c, int B, const int *tokens_dev, const int *pos, float *logits_out) {
+    if (!c) return L2_EINVAL;
+    if (!tokens_dev || !pos) return fail(c, L2_EINVAL, "tokens_dev and pos must not be NULL");
+    cudaPointerAttributes a{};
+    if (cudaPointerGetAttributes(&a, tokens_dev) != cudaSuccess ||
+        (a.type != cudaMemoryTypeDevice && a.type != cudaMemoryTypeManaged)) {
+        cudaGetLastError();
+        return fail(c, L2_EINVAL, "tokens_dev must be device memory");
+    }
+    return submit(c, B, nullptr, pos, logits_out, tokens_dev);
 }
 
 int l2_forward_host(l2_ctx *c, int token, int pos, float *logits_host) {

@@ -116,3 +116,64 @@ def test_greedy_generation_loop_on_device():
         else:  # a near tie: both continuations are valid; stop comparing
             break
     assert pos >= 8, "the generation ended in a near tie too early to be a test"
+
+
+def test_device_resident_generation_loop():
+    """forward (token read from device memory) -> l2_sample -> forward ...,
+    with no host round trip inside the loop; greedy: the oracle's own greedy
+    sequence (compared while its top-two margin exceeds the logit tolerance);
+    temperature 0.8, top-p 0.9: the same tokens as the host-driven loop."""
+    wl = WORKLOADS["gqa_small"]
+    w = synth.make_weights(wl)
+    dw = pkg.to_device(w)
+    n = 40
+
+    def device_loop(temperature, topp):
+        dec = pkg.Decoder(wl.config_tuple(), dw)
+        seq = torch.zeros(n + 1, dtype=torch.int32, device="cuda")
+        seq[0] = 1
+        st = torch.tensor([0x9E3779B97F4A7C15 & (2**63 - 1)], dtype=torch.int64, device="cuda")
+        out = torch.empty(wl.vocab_size, device="cuda")
+        torch.cuda.synchronize()
+        for pos in range(n):
+            dec.forward_dev_tokens(seq[pos:pos + 1], pos, out)
+            pkg.sample(out, temperature, topp, st, seq[pos + 1:pos + 2], stream=dec.stream)
+        dec.sync()
+        return seq.cpu().numpy()
+
+    def host_loop(temperature, topp):
+        dec = pkg.Decoder(wl.config_tuple(), dw)
+        st = torch.tensor([0x9E3779B97F4A7C15 & (2**63 - 1)], dtype=torch.int64, device="cuda")
+        out = torch.empty(wl.vocab_size, device="cuda")
+        nxt = torch.empty(1, dtype=torch.int32, device="cuda")
+        toks = [1]
+        for pos in range(n):
+            dec.forward(toks[-1], pos, out)
+            pkg.sample(out, temperature, topp, st, nxt, stream=dec.stream)
+            dec.sync()
+            toks.append(int(nxt.cpu()[0]))
+        return np.array(toks, np.int32)
+
+    greedy = device_loop(0.0, 0.0)
+    ref = oracle.Model(wl.config_tuple(), w)
+    tok = 1
+    for pos in range(n):
+        r = ref.forward(tok, pos)
+        top2 = np.sort(r)[-2:]
+        tok = int(np.argmax(r))
+        if top2[1] - top2[0] <= LOGIT_ABS:
+            break
+        assert greedy[pos + 1] == tok, f"pos {pos}: device {greedy[pos + 1]}, oracle {tok}"
+    assert pos >= 8
+    assert np.array_equal(device_loop(0.8, 0.9), host_loop(0.8, 0.9))
+
+
+def test_out_of_range_device_token_is_reported():
+    wl = WORKLOADS["tiny"]
+    dec = pkg.Decoder(wl.config_tuple(), pkg.to_device(synth.make_weights(wl)))
+    bad = torch.tensor([wl.vocab_size + 5], dtype=torch.int32, device="cuda")
+    dec.forward_dev_tokens(bad, 0)
+    with pytest.raises(pkg.L2Error) as e:
+        dec.sync()
+    assert e.value.code == pkg.L2_EDEVICE
+    dec.sync()  # the error word was cleared
