@@ -178,6 +178,23 @@ void l2_destroy(l2_ctx *ctx);
 int l2_launch_op(l2_ctx *ctx, int op, int layer, int count);
 
 /*
+ * Prefill: the T tokens of a prompt, at positions pos0..pos0+T-1 of one
+ * sequence (KV-cache slot `slot`), with the pages' causal attention (token
+ * i attends to positions 0..pos0+i).  Cache rows pos0.. of the slot are
+ * written; rows before pos0 must exist (pos0 <= l2_position(slot), else
+ * L2_ESTATE); pos0 + T <= seq_len and every token in [0, vocab_size), else
+ * L2_EINVAL.  logits_out (DEVICE, [T][vocab_size], or NULL) receives the
+ * logits after each token, each equal to what l2_forward gives for that
+ * token at that position.  The tokens are processed max_batch at a time as
+ * one batched step each (the rows of a chunk share the weights read and
+ * read the cache rows the chunk's earlier rows write), so a handle created
+ * with max_batch 1 runs one step per token.  The pages have no counterpart
+ * (their loop feeds a prompt one token per step); the R/Keras page's
+ * full-sequence causal forward computes the same values.
+ */
+int l2_prefill(l2_ctx *ctx, int slot, int T, const int *tokens, int pos0, float *logits_out);
+
+/*
  * l2_forward_batch with the tokens read from DEVICE memory when the step
  * runs (for instance the tokens_out of the previous l2_sample), so a
  * generation loop need not wait for the host: tokens_dev [B] ints on the

@@ -124,6 +124,15 @@ class Decoder:
             ctypes.c_void_p(_ptr(out) if out is not None else 0)))
         return out
 
+    def prefill(self, tokens, pos0: int = 0, slot: int = 0, out=None):
+        """The prompt ``tokens`` at positions pos0.. of ``slot`` (l2_prefill);
+        ``out`` a CUDA tensor [T][vocab_size] for every token's logits, or None."""
+        toks = np.ascontiguousarray(tokens, dtype=np.int32)
+        self._check(self._lib.l2_prefill(self._h, int(slot), int(toks.size),
+                                         toks.ctypes.data_as(ctypes.POINTER(ctypes.c_int)), int(pos0),
+                                         ctypes.c_void_p(_ptr(out) if out is not None else 0)))
+        return out
+
     def forward_dev_tokens(self, tokens_dev, pos, out=None):
         """One step whose tokens are read from ``tokens_dev`` (CUDA int32 [B])
         when it runs; ``pos`` an int (B = 1) or a list of B ints."""

@@ -100,7 +100,7 @@ __global__ void __launch_bounds__(kNWA * 32) attn_kernel(const AttnParams p) {
     const int wt1 = t0 + (int)((long long)(t1 - t0) * (warp + 1) / kNWA);
     const int TP = kStageFloats / (2 * hs);  // positions per stage
 
-    const size_t head_base = (((size_t)b * p.n_layers + p.layer) * KV + g) * (size_t)p.seq_len * hs;
+    const size_t head_base = (((size_t)p.step->slot[b] * p.n_layers + p.layer) * KV + g) * (size_t)p.seq_len * hs;
     const float *kbase = p.kcache + head_base;
     const float *vbase = p.vcache + head_base;
 
@@ -128,10 +128,12 @@ __global__ void __launch_bounds__(kNWA * 32) attn_kernel(const AttnParams p) {
         ti += np;
         ++n_issued;
     };
-    // Rows before pos are not written during this step: fetch them before the
-    // previous kernel (which writes row pos) has finished.
+    // Rows before stable[b] (pos for an ordinary step, the chunk's first
+    // position in a prefill) are not written during this step: fetch them
+    // before the previous kernel (which writes the newer rows) has finished.
+    const int stable = p.step->stable[b];
 #pragma unroll 1
-    for (int s = 0; s < kAttStages && ti < wt1 && ti + min(TP, wt1 - ti) <= pos; ++s) issue(s);
+    for (int s = 0; s < kAttStages && ti < wt1 && ti + min(TP, wt1 - ti) <= stable; ++s) issue(s);
     pdl_launch_dependents();
     pdl_wait();
 #pragma unroll 1

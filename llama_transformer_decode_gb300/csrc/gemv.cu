@@ -363,7 +363,8 @@ __global__ void __launch_bounds__(NW * 32, 1) gemv_kernel(const GemvParams p) {
                 const bool is_k = v < p.dim + p.kv_dim;
                 const int c = is_k ? v - p.dim : v - p.dim - p.kv_dim;
                 const int g = c / hs, d = c % hs;
-                const size_t idx = (((size_t)p.layer * p.n_kv_heads + g) * p.seq_len + pos) * hs + d;
+                const size_t idx =
+                    ((((size_t)p.step->slot[0] * p.n_layers + p.layer) * p.n_kv_heads + g) * p.seq_len + pos) * hs + d;
                 if (is_k) {
                     const float2 cs = rr[d >> 1];
                     p.kcache[idx] = y0 * cs.x - y1 * cs.y;

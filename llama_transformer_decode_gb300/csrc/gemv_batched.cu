@@ -295,7 +295,8 @@ __global__ void __launch_bounds__(kBT, 1) gemv_batched_kernel(const __grid_const
                 } else {
                     const int g = v / hs, d = v % hs;
                     const size_t idx =
-                        ((((size_t)b * p.n_layers + p.layer) * p.n_kv_heads + g) * p.seq_len + pos) * hs + d;
+                        ((((size_t)p.step->slot[b] * p.n_layers + p.layer) * p.n_kv_heads + g) * p.seq_len + pos) * hs +
+                        d;
                     if (m == 1) {
                         const float2 cs = rr[d >> 1];
                         p.kcache[idx] = y0 * cs.x - y1 * cs.y;

@@ -636,12 +636,17 @@ __global__ void set_step_tokens(StepDev *step, const int *tokens, int B, int voc
 }
 
 // tokens_dev: when not NULL, the step's tokens are read from this device
-// array when the step runs (tokens is then ignored).
-int submit(l2_ctx *c, int B, const int *tokens, const int *pos, float *logits_out, const int *tokens_dev = nullptr) {
+// array when the step runs (tokens is then ignored).  prefill_slot >= 0: the
+// B rows are consecutive positions pos[0].. of that one slot (a prompt
+// chunk, checked by the caller) instead of one position of each of slots
+// 0..B-1.
+int submit(l2_ctx *c, int B, const int *tokens, const int *pos, float *logits_out, const int *tokens_dev = nullptr,
+           int prefill_slot = -1) {
     if (B < 1 || B > c->max_batch) return fail(c, L2_EINVAL, "batch %d outside 1..%d", B, c->max_batch);
     for (int b = 0; b < B; ++b) {
         if (!tokens_dev && (tokens[b] < 0 || tokens[b] >= c->cfg.vocab_size))
             return fail(c, L2_EINVAL, "token %d of slot %d outside [0, %d)", tokens[b], b, c->cfg.vocab_size);
+        if (prefill_slot >= 0) continue;
         if (pos[b] < 0 || pos[b] >= c->cfg.seq_len)
             return fail(c, L2_EINVAL, "pos %d of slot %d outside [0, %d)", pos[b], b, c->cfg.seq_len);
         if (pos[b] > c->written[b])
@@ -657,6 +662,8 @@ int submit(l2_ctx *c, int B, const int *tokens, const int *pos, float *logits_ou
     for (int b = 0; b < B; ++b) {
         sh.token[b] = tokens_dev ? 0 : tokens[b];
         sh.pos[b] = pos[b];
+        sh.slot[b] = prefill_slot >= 0 ? prefill_slot : b;
+        sh.stable[b] = prefill_slot >= 0 ? pos[0] : pos[b];
     }
     sh.logits_out = logits_out;
     sh.B = B;
@@ -669,7 +676,7 @@ int submit(l2_ctx *c, int B, const int *tokens, const int *pos, float *logits_ou
         L2_CUDA(c, cudaGetLastError());
     }
 
-    if (B == 1 && c->persist) {
+    if (B == 1 && c->persist && sh.slot[0] == 0) {
         L2_CUDA(c, launch_step_kernel(c->persist_gq, c->sp, c->num_sms, c->persist_smem, c->stream));
     } else if (c->flags & L2_FLAG_NO_GRAPH) {
         L2_CUDA(c, enqueue_step(c, B, c->stream));
@@ -679,7 +686,10 @@ int submit(l2_ctx *c, int B, const int *tokens, const int *pos, float *logits_ou
         if (rc != L2_OK) return rc;
         L2_CUDA(c, cudaGraphLaunch(g, c->stream));
     }
-    for (int b = 0; b < B; ++b) c->written[b] = pos[b] + 1;
+    if (prefill_slot >= 0)
+        c->written[prefill_slot] = pos[B - 1] + 1;
+    else
+        for (int b = 0; b < B; ++b) c->written[b] = pos[b] + 1;
     return L2_OK;
 }
 
@@ -825,6 +835,31 @@ int l2_forward_batch(l2_ctx *c, int B, const int *tokens, const int *pos, float 
     if (!c) return L2_EINVAL;
     if (!tokens || !pos) return fail(c, L2_EINVAL, "tokens and pos must not be NULL");
     return submit(c, B, tokens, pos, logits_out);
+}
+
+int l2_prefill(l2_ctx *c, int slot, int T, const int *tokens, int pos0, float *logits_out) {
+    if (!c) return L2_EINVAL;
+    if (!tokens) return fail(c, L2_EINVAL, "tokens must not be NULL");
+    if (slot < 0 || slot >= c->max_batch) return fail(c, L2_EINVAL, "slot %d outside 0..%d", slot, c->max_batch - 1);
+    if (T < 1) return fail(c, L2_EINVAL, "T must be >= 1 (got %d)", T);
+    if (pos0 < 0 || (long long)pos0 + T > c->cfg.seq_len)
+        return fail(c, L2_EINVAL, "positions %d..%lld outside [0, %d)", pos0, (long long)pos0 + T - 1, c->cfg.seq_len);
+    if (pos0 > c->written[slot])
+        return fail(c, L2_ESTATE, "pos0 %d of slot %d skips cache rows (only %d written)", pos0, slot, c->written[slot]);
+    if (logits_out && (reinterpret_cast<uintptr_t>(logits_out) & 3u))
+        return fail(c, L2_EINVAL, "logits_out must be 4-byte aligned");
+    for (int i = 0; i < T; ++i)
+        if (tokens[i] < 0 || tokens[i] >= c->cfg.vocab_size)
+            return fail(c, L2_EINVAL, "token %d at index %d outside [0, %d)", tokens[i], i, c->cfg.vocab_size);
+    int pos[kMaxBatch];
+    for (int i0 = 0; i0 < T; i0 += c->max_batch) {
+        const int n = std::min(c->max_batch, T - i0);
+        for (int b = 0; b < n; ++b) pos[b] = pos0 + i0 + b;
+        const int rc = submit(c, n, tokens + i0, pos, logits_out ? logits_out + (size_t)i0 * c->cfg.vocab_size : nullptr,
+                              nullptr, slot);
+        if (rc) return rc;
+    }
+    return L2_OK;
 }
 
 int l2_forward_dev_tokens(l2_ctx *c, int B, const int *tokens_dev, const int *pos, float *logits_out) {
@@ -1059,6 +1094,8 @@ extern "C" int l2_forward_static(l2_ctx *c, int token, int pos, float *logits_ou
     StepDev &sh = c->step_host[i];
     sh.token[0] = token;
     sh.pos[0] = pos;
+    sh.slot[0] = 0;
+    sh.stable[0] = pos;
     sh.logits_out = logits_out;
     sh.B = 1;
     L2_CUDA(c, cudaMemcpyAsync(c->step_dev, &sh, sizeof(StepDev), cudaMemcpyHostToDevice, c->stream));

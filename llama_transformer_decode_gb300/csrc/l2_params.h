@@ -17,6 +17,9 @@ enum : int { L2_DEV_ERR_TIMEOUT = 1, L2_DEV_ERR_BOUNDS = 2 };
 struct StepDev {
     int token[kMaxBatch];
     int pos[kMaxBatch];
+    int slot[kMaxBatch];    // KV-cache slot row b reads and writes (b for ordinary steps)
+    int stable[kMaxBatch];  // rows of that slot written before this step (pos[b] for
+                            // ordinary steps; the first position of a prefill chunk)
     float *logits_out;  // caller's device buffer [B][vocab] or nullptr
     int B;
     unsigned sync_count;  // grid-barrier arrivals of the persistent step kernel (zero at the copy)
