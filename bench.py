@@ -41,7 +41,7 @@ FALLBACK_HBM_GBS = 6800.0
 # the dominant kernel, from the ncu capture summarised in
 # profiles/gemv_w13_llama2_7b.md, valid only for the kernel source whose
 # sha256 prefix is recorded beside it.
-W13_NCU_TRAFFIC = (364313344, "08026df8323ddb77")  # (bytes per launch, gemv.cu sha256 prefix)
+W13_NCU_TRAFFIC = (364191744, "f749e57f10155989")  # (bytes per launch, gemv.cu sha256 prefix)
 
 
 def weight_bytes(wl) -> int:
