@@ -185,10 +185,11 @@ int l2_launch_op(l2_ctx *ctx, int op, int layer, int count);
  * L2_ESTATE); pos0 + T <= seq_len and every token in [0, vocab_size), else
  * L2_EINVAL.  logits_out (DEVICE, [T][vocab_size], or NULL) receives the
  * logits after each token, each equal to what l2_forward gives for that
- * token at that position.  The tokens are processed max_batch at a time as
- * one batched step each (the rows of a chunk share the weights read and
- * read the cache rows the chunk's earlier rows write), so a handle created
- * with max_batch 1 runs one step per token.  The pages have no counterpart
+ * token at that position.  The tokens are processed 64 at a time (max_batch
+ * at a time with L2_FLAG_DEBUG) as one batched step each: the rows of a
+ * chunk share the weights read and read the cache rows the chunk's earlier
+ * rows write.  Any handle can prefill in 64-row chunks: the per-row buffers
+ * are sized for 64 rows, the KV cache for max_batch slots.  The pages have no counterpart
  * (their loop feeds a prompt one token per step); the R/Keras page's
  * full-sequence causal forward computes the same values.
  */

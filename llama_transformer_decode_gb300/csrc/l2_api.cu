@@ -76,7 +76,8 @@ struct GemvPlan {
 struct l2_ctx {
     L2Config cfg{};
     L2Weights w{};
-    int max_batch = 1;
+    int max_batch = 1;  // sequences, each with its own KV-cache slot
+    int max_rows = 1;   // rows of a batched step: max_batch, or 64 for prompt chunks
     unsigned flags = 0;
     int device = 0, num_sms = 0;
     int head_size = 0, kv_dim = 0;
@@ -90,7 +91,7 @@ struct l2_ctx {
     float2 *rope = nullptr;
     StepDev *step_dev = nullptr;
     int *err = nullptr;
-    float *ss_part = nullptr;  // batched steps: partial sums of x^2 [kMaxParts][max_batch]
+    float *ss_part = nullptr;  // batched steps: partial sums of x^2 [kMaxParts][max_rows]
 
     StepDev *step_host = nullptr;  // pinned ring
     cudaEvent_t ring_ev[kRing] = {};
@@ -427,24 +428,24 @@ int build_batch_set(l2_ctx *c, int batch) {
                 ok = encode_matrix(&bp.wmap[0], c->w.wq, D, L * D, tk, rb) &&
                      encode_matrix(&bp.wmap[1], c->w.wk, D, L * KVD, tk, rb) &&
                      encode_matrix(&bp.wmap[2], c->w.wv, D, L * KVD, tk, rb) &&
-                     encode_matrix(&bp.xmap, c->x, D, c->max_batch, tk, batch);
+                     encode_matrix(&bp.xmap, c->x, D, c->max_rows, tk, batch);
                 break;
             case 1:
                 ok = encode_matrix(&bp.wmap[0], c->w.wo, D, L * D, tk, rb) &&
-                     encode_matrix(&bp.xmap, c->xb, D, c->max_batch, tk, batch);
+                     encode_matrix(&bp.xmap, c->xb, D, c->max_rows, tk, batch);
                 break;
             case 2:
                 ok = encode_matrix(&bp.wmap[0], c->w.w1, D, L * H, tk, rb) &&
                      encode_matrix(&bp.wmap[1], c->w.w3, D, L * H, tk, rb) &&
-                     encode_matrix(&bp.xmap, c->x, D, c->max_batch, tk, batch);
+                     encode_matrix(&bp.xmap, c->x, D, c->max_rows, tk, batch);
                 break;
             case 3:
                 ok = encode_matrix(&bp.wmap[0], c->w.w2, H, L * D, tk, rb) &&
-                     encode_matrix(&bp.xmap, c->hb, H, c->max_batch, tk, batch);
+                     encode_matrix(&bp.xmap, c->hb, H, c->max_rows, tk, batch);
                 break;
             case 4:
                 ok = encode_matrix(&bp.wmap[0], c->w.wcls, D, (uint64_t)p.vocab_size, tk, rb) &&
-                     encode_matrix(&bp.xmap, c->x, D, c->max_batch, tk, batch);
+                     encode_matrix(&bp.xmap, c->x, D, c->max_rows, tk, batch);
                 break;
         }
         if (!ok) return fail(c, L2_ECUDA, "cuTensorMapEncodeTiled failed for a batched GEMV plan");
@@ -642,7 +643,8 @@ __global__ void set_step_tokens(StepDev *step, const int *tokens, int B, int voc
 // 0..B-1.
 int submit(l2_ctx *c, int B, const int *tokens, const int *pos, float *logits_out, const int *tokens_dev = nullptr,
            int prefill_slot = -1) {
-    if (B < 1 || B > c->max_batch) return fail(c, L2_EINVAL, "batch %d outside 1..%d", B, c->max_batch);
+    const int cap = prefill_slot >= 0 ? c->max_rows : c->max_batch;
+    if (B < 1 || B > cap) return fail(c, L2_EINVAL, "batch %d outside 1..%d", B, cap);
     for (int b = 0; b < B; ++b) {
         if (!tokens_dev && (tokens[b] < 0 || tokens[b] >= c->cfg.vocab_size))
             return fail(c, L2_EINVAL, "token %d of slot %d outside [0, %d)", tokens[b], b, c->cfg.vocab_size);
@@ -716,6 +718,10 @@ int l2_create(const L2Config *config, const L2Weights *weights, int max_batch, u
     c->cfg = *config;
     c->w = *weights;
     c->max_batch = max_batch;
+    // Prompt chunks use up to 64 rows whatever max_batch is (the per-row
+    // buffers are small); with L2_FLAG_DEBUG the per-row probability export
+    // keeps them at max_batch.
+    c->max_rows = (flags & L2_FLAG_DEBUG) ? max_batch : kMaxBatch;
     c->flags = flags;
     const L2Config &p = c->cfg;
     c->head_size = p.dim / p.n_heads;
@@ -753,10 +759,10 @@ int l2_create(const L2Config *config, const L2Weights *weights, int max_batch, u
     }
     CREATE_CUDA(cudaStreamCreateWithFlags(&c->cap_stream, cudaStreamNonBlocking));
 
-    const size_t B = (size_t)max_batch, L = p.n_layers, S = p.seq_len, hs = c->head_size;
-    const size_t cache = B * L * p.n_kv_heads * S * hs;
+    const size_t B = (size_t)c->max_rows, L = p.n_layers, S = p.seq_len, hs = c->head_size;
+    const size_t cache = (size_t)max_batch * L * p.n_kv_heads * S * hs;
     c->attn_chunks = attn_chunks_for(c, 1);
-    if (max_batch > 1 && ceil_div(p.seq_len, kMinChunk) > c->attn_chunks) c->attn_chunks = ceil_div(p.seq_len, kMinChunk);
+    if (c->max_rows > 1 && ceil_div(p.seq_len, kMinChunk) > c->attn_chunks) c->attn_chunks = ceil_div(p.seq_len, kMinChunk);
     const size_t ws = B * p.n_heads * (size_t)c->attn_chunks;
     if ((rc = alloc_n(c, &c->x, B * p.dim, "x")) || (rc = alloc_n(c, &c->xb, B * p.dim, "xb")) ||
         (rc = alloc_n(c, &c->q, B * p.dim, "q")) || (rc = alloc_n(c, &c->hb, B * p.hidden_dim, "hb")) ||
@@ -806,9 +812,14 @@ int l2_create(const L2Config *config, const L2Weights *weights, int max_batch, u
             return bail(fail(c, L2_EINVAL, "a GEMV stage needs %zu bytes of shared memory (> 227 KB); dim or hidden_dim too large",
                              pl->smem));
     if (c->attn.smem > 227 * 1024) return bail(fail(c, L2_EINVAL, "attention needs too much shared memory"));
-    c->bsets.resize(max_batch + 1);
-    for (int b = 2; b <= max_batch; ++b)
-        if ((rc = build_batch_set(c, b))) return bail(rc);
+    c->bsets.resize(c->max_rows + 1);
+    for (int b = 2; b <= c->max_rows; ++b)
+        if ((rc = build_batch_set(c, b))) {
+            if (b <= max_batch) return bail(rc);
+            c->max_rows = b - 1;  // prompt chunks stop at the widest step that could be planned
+            c->error.clear();
+            break;
+        }
     if ((rc = plan_persistent(c))) return bail(rc);
     CREATE_CUDA(cudaDeviceSynchronize());
 #undef CREATE_CUDA
@@ -852,8 +863,8 @@ int l2_prefill(l2_ctx *c, int slot, int T, const int *tokens, int pos0, float *l
         if (tokens[i] < 0 || tokens[i] >= c->cfg.vocab_size)
             return fail(c, L2_EINVAL, "token %d at index %d outside [0, %d)", tokens[i], i, c->cfg.vocab_size);
     int pos[kMaxBatch];
-    for (int i0 = 0; i0 < T; i0 += c->max_batch) {
-        const int n = std::min(c->max_batch, T - i0);
+    for (int i0 = 0; i0 < T; i0 += c->max_rows) {
+        const int n = std::min(c->max_rows, T - i0);
         for (int b = 0; b < n; ++b) pos[b] = pos0 + i0 + b;
         const int rc = submit(c, n, tokens + i0, pos, logits_out ? logits_out + (size_t)i0 * c->cfg.vocab_size : nullptr,
                               nullptr, slot);

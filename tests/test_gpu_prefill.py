@@ -1,14 +1,15 @@
 """Prefill (l2_prefill) against the oracle, token by token.
 
 A prompt of T tokens at positions pos0.. of one slot is run as batched steps
-of up to max_batch rows; every row's logits must equal (within the parity
+of up to 64 rows (max_batch rows with L2_FLAG_DEBUG); every row's logits must equal (within the parity
 bounds) the oracle's logits for that token at that position after the
 tokens before it, i.e. the oracle's teacher-forced decode of the same
 stream.  Covered: one chunk, several chunks with a ragged last one, a
 one-token chunk (the batch-1 kernels writing a slot other than 0), a slot
 other than 0 while slot 0 keeps decoding, 8 query heads per KV head, 64-row
 chunks, the cache rows written, ordinary steps after a prefill, argument
-checks, and a handle running batch-1 steps as the persistent kernel.
+checks, a one-sequence handle, and ordinary steps after a prefill on a
+handle running batch-1 steps as the persistent kernel.
 """
 import numpy as np
 import pytest
@@ -60,7 +61,14 @@ def run_plan(wl, max_batch, plan, slot=0, flags=0, then_steps=0):
 
 
 def test_prefill_several_chunks_then_decode():
-    run_plan(WORKLOADS["gqa_small"], 16, [37], then_steps=5)
+    # 100 tokens: chunks of 64 and 36 rows on a handle of 2 sequences
+    run_plan(WORKLOADS["gqa_small"], 2, [100], then_steps=5)
+
+
+def test_prefill_on_a_one_sequence_handle_and_with_debug_export():
+    run_plan(WORKLOADS["mid"], 1, [70, 3], then_steps=3)
+    # with L2_FLAG_DEBUG the chunks are max_batch rows: 4 + 4 + 2
+    run_plan(WORKLOADS["tiny"], 4, [10], flags=pkg.L2_FLAG_DEBUG, then_steps=2)
 
 
 def test_prefill_in_pieces_and_a_single_token_in_slot_3():
@@ -93,7 +101,7 @@ def test_prefill_64_row_chunks():
     run_plan(WORKLOADS["mid"], 64, [64, 64, 10])
 
 
-def test_prefill_one_token_per_step_on_a_persistent_handle():
+def test_prefill_then_persistent_steps():
     run_plan(WORKLOADS["tiny"], 1, [7, 3], flags=pkg.L2_FLAG_PERSIST, then_steps=4)
 
 
