@@ -25,13 +25,14 @@
 // cached in shared memory (vocabularies up to kMaxVocab, one pad word per 32
 // against bank conflicts); sums are 64-bit integer CTA reductions.  The
 // plain draw finds the crossing with a blocked prefix sum over index order.
-// Top-p finds the weight v* at which the sorted running total reaches the
-// threshold by a bitwise search over weight values (sum of the weights >= a
-// candidate value, 49 rounds), takes as many tokens of weight v* (lowest
-// indices first) as needed, and finds the drawn token the same way inside
-// the nucleus: no sort is needed.  Only tokens above a proven lower bound of
-// v* can matter; when they fit a list of a few thousand, one warp runs both
-// searches over that list with shuffle reductions.
+// Top-p: no nucleus token weighs less than a proven lower bound; the tokens
+// above it are usually few, and then they are sorted (bitonic, in shared
+// memory: weight descending, index ascending) and walked with exact prefix
+// sums.  When they do not fit the list, the whole CTA instead finds the
+// weight v* at which the sorted running total reaches the threshold by a
+// bitwise search over weight values (sum of the weights >= a candidate, 49
+// rounds), takes as many tokens of weight v* (lowest indices first) as
+// needed, and finds the drawn token the same way inside the nucleus.
 #include <cuda_runtime.h>
 
 #include "l2_device.cuh"
@@ -270,52 +271,68 @@ __global__ void __launch_bounds__(kST, 1) sample_kernel(const SampleParams p) {
     __syncthreads();
     const u64 C = sc.bcast[1];
 
-    if (C <= (u64)p.cand_cap) {
-        // candidates in index order, then one warp does the rest
+    int Cp = 1;
+    while ((u64)Cp < C) Cp <<= 1;
+    if (Cp <= p.cand_cap) {
+        // Candidates in index order, padded to a power of two with -1, then
+        // a bitonic sort into the nucleus order: weight descending, index
+        // ascending (the padding last).
         int *cand = reinterpret_cast<int *>(ecache + slot(V) + 1);
         u64 k = cbase;
         for (int i = i0; i < i1; ++i)
             if (weight_of(ecache[slot(i)]) >= cutoff) cand[k++] = i;
+        for (int i = (int)C + tid; i < Cp; i += kST) cand[i] = -1;
         __syncthreads();
-        if (tid >= 32) return;
-        const int lane = tid, nc = (int)C;
-        auto G = [&](u64 t) {
-            u64 v = 0;
-            for (int j = lane; j < nc; j += 32) {
-                const u64 q = weight_of(ecache[slot(cand[j])]);
-                if (q >= t) v += q;
-            }
-            return warp_sum_u64(v);
+        auto before = [&](int a, int b) -> bool {
+            if (b < 0) return a >= 0;
+            if (a < 0) return false;
+            const u64 qa = weight_of(ecache[slot(a)]), qb = weight_of(ecache[slot(b)]);
+            return qa > qb || (qa == qb && a < b);
         };
-        u64 vstar = 0;
-        for (int bit = 48; bit >= 0; --bit) {
-            const u64 cnd = vstar | (1ull << bit);
-            if (((u128)G(cnd) << 24) >= need) vstar = cnd;
-        }
-        const u64 A = G(vstar + 1);
-        const u128 D = need - ((u128)A << 24);
-        const u64 Dh = (u64)(D >> 24), Dl = (u64)D & 0xFFFFFFull;
-        u64 c = Dh / vstar + ((Dh % vstar != 0 || Dl != 0) ? 1 : 0);
-        if (c < 1) c = 1;
-        const u64 P = A + c * vstar;
-        const u64 r = (u64)(((u128)k24 * P) >> 24);
-        u64 w = 0;
-        for (int bit = 48; bit >= 0; --bit) {
-            const u64 cnd = w | (1ull << bit);
-            if ((cnd > vstar ? G(cnd) : P) > r) w = cnd;
-        }
-        const u64 F = w + 1 > vstar ? G(w + 1) : P;
-        u64 jr = (r - F) / w;  // rank (by index) of the drawn token among those of weight w
-        for (int base = 0; base < nc; base += 32) {
-            const int j = base + lane;
-            const bool hit = j < nc && weight_of(ecache[slot(cand[j])]) == w;
-            const unsigned mask = __ballot_sync(0xffffffffu, hit);
-            const u64 n = (u64)__popc(mask);
-            if (jr < n) {
-                if (hit && (u64)__popc(mask & ((1u << lane) - 1u)) == jr) p.out[b] = cand[j];
-                break;
+        for (int kk = 2; kk <= Cp; kk <<= 1)
+            for (int j = kk >> 1; j > 0; j >>= 1) {
+                for (int i = tid; i < Cp; i += kST) {
+                    const int ixj = i ^ j;
+                    if (ixj > i) {
+                        const int a = cand[i], b = cand[ixj];
+                        if ((i & kk) == 0 ? before(b, a) : before(a, b)) {
+                            cand[i] = b;
+                            cand[ixj] = a;
+                        }
+                    }
+                }
+                __syncthreads();
             }
-            jr -= n;
+        // Running totals in that order (exact): the nucleus ends at the first
+        // position whose total P has P 2^24 >= need; the drawn token is the
+        // first whose total exceeds r = floor(k P / 2^24).
+        const int nc = (int)C, per = (nc + kST - 1) / kST;
+        const int j0 = min(nc, tid * per), j1 = min(nc, j0 + per);
+        u64 loc = 0;
+        for (int j = j0; j < j1; ++j) loc += weight_of(ecache[slot(cand[j])]);
+        const u64 base = cta_exclusive_scan(loc, sc);
+        if (j1 > j0 && ((u128)(base + loc) << 24) >= need && (j0 == 0 || ((u128)base << 24) < need)) {
+            u64 run = base;
+            for (int j = j0; j < j1; ++j) {
+                run += weight_of(ecache[slot(cand[j])]);
+                if (((u128)run << 24) >= need) {
+                    sc.bcast[2] = run;
+                    break;
+                }
+            }
+        }
+        __syncthreads();
+        const u64 P = sc.bcast[2];
+        const u64 r = (u64)(((u128)k24 * P) >> 24);
+        if (j1 > j0 && r >= base && r < base + loc) {
+            u64 run = base;
+            for (int j = j0; j < j1; ++j) {
+                run += weight_of(ecache[slot(cand[j])]);
+                if (r < run) {
+                    p.out[b] = cand[j];
+                    break;
+                }
+            }
         }
         return;
     }
