@@ -55,6 +55,11 @@ extern "C" {
  * reports 1); ignored with L2_FLAG_DEBUG.  Measured on GB300 it is slower
  * than the default graph of kernels with programmatic dependent launch. */
 #define L2_FLAG_PERSIST 0x8u
+/* Batched steps and prompt chunks of 16 or more rows normally run their
+ * matrix products on the tensor cores (tf32 with the 3-way split hi*hi +
+ * hi*lo + lo*hi, fp32-level accuracy); with this flag they stay on the CUDA
+ * cores. */
+#define L2_FLAG_NO_TC 0x10u
 
 /* Model shape: the pages' Config struct ("run.c", Config; walkthrough §2).
  * head_size = dim / n_heads, kv_dim = dim * n_kv_heads / n_heads. */

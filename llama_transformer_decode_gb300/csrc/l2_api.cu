@@ -43,6 +43,11 @@ constexpr int kRing = 64;      // pinned step-input slots in flight
 #ifndef L2_STEP_MAX_CHUNK_WORDS
 #define L2_STEP_MAX_CHUNK_WORDS 512
 #endif
+// Batched steps and prompt chunks of at least this many rows use the
+// tensor-core GEMV (gemv_tc.cu) unless L2_FLAG_NO_TC.
+#ifndef L2_TC_MIN_BATCH
+#define L2_TC_MIN_BATCH 16
+#endif
 // Fewest cache positions per attention CTA.  Measured on GB300 (7B shape):
 // 128 beats 32 and 64 at positions up to ~2000 (fewer chunks to merge, a
 // single CTA per head below 128 positions) and ties above.
@@ -60,6 +65,11 @@ struct BatchPlan {
 struct BatchSet {
     bool built = false;
     BatchPlan plan[5];  // QKV, Wo, W1/W3, W2, classifier
+    bool tc = false;    // the tensor-core plans below are used
+    TcParams tcp[5];
+    int tc_grid[5] = {};
+    size_t tc_ws_floats = 0;  // split-K workspace the plans need
+    int tc_tiles = 0;         // most tiles of a plan (tickets)
 };
 
 struct GemvPlan {
@@ -92,6 +102,9 @@ struct l2_ctx {
     StepDev *step_dev = nullptr;
     int *err = nullptr;
     float *ss_part = nullptr;  // batched steps: partial sums of x^2 [kMaxParts][max_rows]
+    float *tc_ws = nullptr;       // tensor-core GEMV split-K partial tiles
+    float *xg = nullptr;          // tensor-core path: x * gain of the next RMSNorm [max_rows][dim]
+    unsigned *tc_tickets = nullptr;
 
     StepDev *step_host = nullptr;  // pinned ring
     cudaEvent_t ring_ev[kRing] = {};
@@ -371,6 +384,89 @@ bool encode_matrix(CUtensorMap *m, const void *base, uint64_t cols, uint64_t row
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Row-major fp32 matrix [rows][cols] seen as tiles of box_rows x 32 columns
+// (128-byte lines) with the 128-byte swizzle the tensor-core operands use.
+bool encode_matrix_sw128(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows, uint32_t box_rows) {
+    EncodeTiledFn fn = encode_tiled();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols * 4};
+    const cuuint32_t box[2] = {32, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The tensor-core plans of a batch size (16..64 rows): tiles of 128 output
+// rows (64 of W1 over 64 of W3), K split so that the items fill the SMs.
+int build_tc_set(l2_ctx *c, int batch) {
+    const L2Config &p = c->cfg;
+    BatchSet &set = c->bsets[batch];
+    const uint64_t L = p.n_layers, D = p.dim, H = p.hidden_dim, KVD = c->kv_dim, V = p.vocab_size;
+    const int bpad = (batch + 15) / 16 * 16;
+    set.tc_ws_floats = 0;
+    set.tc_tiles = 0;
+    for (int k = 0; k < 5; ++k) {
+        TcParams &tp = set.tcp[k];
+        memset(&tp, 0, sizeof(tp));
+        tp.bpad = bpad;
+        bool ok = true;
+        int n = 0;
+        switch (k) {
+            case 0:
+                tp.mrows[0] = p.dim;
+                tp.mrows[1] = tp.mrows[2] = c->kv_dim;
+                for (int m = 0; m < 3; ++m) tp.tiles[m] = ceil_div(tp.mrows[m], 128);
+                ok = encode_matrix_sw128(&tp.wmap[0], c->w.wq, D, L * D, 128) &&
+                     encode_matrix_sw128(&tp.wmap[1], c->w.wk, D, L * KVD, 128) &&
+                     encode_matrix_sw128(&tp.wmap[2], c->w.wv, D, L * KVD, 128) &&
+                     encode_matrix_sw128(&tp.xmap, c->xg, D, c->max_rows, bpad);
+                n = p.dim;
+                break;
+            case 1:
+                tp.mrows[0] = p.dim;
+                tp.tiles[0] = ceil_div(p.dim, 128);
+                ok = encode_matrix_sw128(&tp.wmap[0], c->w.wo, D, L * D, 128) &&
+                     encode_matrix_sw128(&tp.xmap, c->xb, D, c->max_rows, bpad);
+                n = p.dim;
+                break;
+            case 2:
+                tp.mrows[0] = p.hidden_dim;
+                tp.tiles[0] = ceil_div(p.hidden_dim, 64);
+                ok = encode_matrix_sw128(&tp.wmap[0], c->w.w1, D, L * H, 64) &&
+                     encode_matrix_sw128(&tp.wmap[1], c->w.w3, D, L * H, 64) &&
+                     encode_matrix_sw128(&tp.xmap, c->xg, D, c->max_rows, bpad);
+                n = p.dim;
+                break;
+            case 3:
+                tp.mrows[0] = p.dim;
+                tp.tiles[0] = ceil_div(p.dim, 128);
+                ok = encode_matrix_sw128(&tp.wmap[0], c->w.w2, H, L * D, 128) &&
+                     encode_matrix_sw128(&tp.xmap, c->hb, H, c->max_rows, bpad);
+                n = p.hidden_dim;
+                break;
+            case 4:
+                tp.mrows[0] = p.vocab_size;
+                tp.tiles[0] = ceil_div(p.vocab_size, 128);
+                ok = encode_matrix_sw128(&tp.wmap[0], c->w.wcls, D, V, 128) &&
+                     encode_matrix_sw128(&tp.xmap, c->xg, D, c->max_rows, bpad);
+                n = p.dim;
+                break;
+        }
+        if (!ok) return fail(c, L2_ECUDA, "cuTensorMapEncodeTiled failed for a tensor-core GEMV plan");
+        tp.ntiles = tp.tiles[0] + tp.tiles[1] + tp.tiles[2];
+        tp.splits = gemv_tc_splits(tp.ntiles, n, c->num_sms);
+        const int items = tp.ntiles * tp.splits;
+        set.tc_grid[k] = items < c->num_sms ? items : c->num_sms;
+        if (tp.splits > 1) set.tc_ws_floats = std::max(set.tc_ws_floats, (size_t)items * 128 * bpad);
+        set.tc_tiles = std::max(set.tc_tiles, tp.ntiles);
+    }
+    if (set.tcp[1].ntiles > kMaxParts) return fail(c, L2_EINVAL, "too many residual tiles for the sum-of-squares parts");
+    set.tc = true;
+    return L2_OK;
+}
+
 // Builds the five batched GEMV plans (QKV, Wo, W1/W3, W2, classifier) for
 // `batch` sequences.  Returns L2_OK or an error code.
 int build_batch_set(l2_ctx *c, int batch) {
@@ -455,6 +551,27 @@ int build_batch_set(l2_ctx *c, int batch) {
 }
 
 cudaError_t launch_batched(l2_ctx *c, int k, const GemvPlan &pl, int layer, int batch, cudaStream_t s, bool pdl) {
+    const BatchSet &set = c->bsets[batch];
+    if (set.tc) {
+        TcParams tp = set.tcp[k];
+        tp.g = layer_params(c, pl, layer);
+        tp.g.batch = batch;
+        tp.g.ss_part = c->ss_part;
+        tp.g.ss_parts = (k == 0 && layer == 0) ? 1 : set.tcp[1].ntiles;  // the embedding, else the residual tiles
+        tp.ws = c->tc_ws;
+        tp.tickets = c->tc_tickets;
+        tp.xg = c->xg;
+        const L2Config &cf = c->cfg;
+        if (k == 1) tp.next_gain = c->w.rms_ffn_weight + (size_t)layer * cf.dim;
+        if (k == 3)
+            tp.next_gain = layer + 1 < cf.n_layers ? c->w.rms_att_weight + (size_t)(layer + 1) * cf.dim
+                                                   : c->w.rms_final_weight;
+        if (k == 0 && layer == 0) {
+            cudaError_t e = launch_tc_embed(tp, batch, s, pdl);
+            if (e != cudaSuccess) return e;
+        }
+        return launch_gemv_tc(pl.mode, tp, set.tc_grid[k], s, pdl);
+    }
     const BatchPlan &bpl = c->bsets[batch].plan[k];
     BatchParams bp = bpl.bp;
     bp.g = layer_params(c, pl, layer);
@@ -707,7 +824,7 @@ int l2_create(const L2Config *config, const L2Weights *weights, int max_batch, u
     if (!config || !weights) return fail(nullptr, L2_EINVAL, "config and weights must not be NULL");
     if (max_batch < 1 || max_batch > kMaxBatch)
         return fail(nullptr, L2_EINVAL, "max_batch %d outside 1..%d", max_batch, kMaxBatch);
-    if (flags & ~(L2_FLAG_DEBUG | L2_FLAG_NO_GRAPH | L2_FLAG_NO_PDL | L2_FLAG_PERSIST))
+    if (flags & ~(L2_FLAG_DEBUG | L2_FLAG_NO_GRAPH | L2_FLAG_NO_PDL | L2_FLAG_PERSIST | L2_FLAG_NO_TC))
         return fail(nullptr, L2_EINVAL, "unknown flags 0x%x", flags);
     int rc = check_config(*config);
     if (rc) return rc;
@@ -820,6 +937,24 @@ int l2_create(const L2Config *config, const L2Weights *weights, int max_batch, u
             c->error.clear();
             break;
         }
+    // tensor-core plans for 16..64 rows, with one workspace and ticket array for all
+    if (!(flags & L2_FLAG_NO_TC) && c->max_rows >= L2_TC_MIN_BATCH) {
+        CREATE_CUDA(gemv_tc_init());
+        if ((rc = alloc_n(c, &c->xg, (size_t)c->max_rows * p.dim, "x * gain"))) return bail(rc);
+        size_t ws = 0;
+        int tiles = 0;
+        for (int b = L2_TC_MIN_BATCH; b <= c->max_rows && b <= gemv_tc_max_batch(); ++b) {
+            if ((rc = build_tc_set(c, b))) return bail(rc);
+            ws = std::max(ws, c->bsets[b].tc_ws_floats);
+            tiles = std::max(tiles, c->bsets[b].tc_tiles);
+        }
+        if (tiles > 0) {
+            if ((rc = alloc_n(c, &c->tc_ws, ws ? ws : 1, "tensor-core GEMV workspace")) ||
+                (rc = alloc_n(c, &c->tc_tickets, (size_t)tiles, "tensor-core GEMV tickets")))
+                return bail(rc);
+            CREATE_CUDA(cudaMemset(c->tc_tickets, 0, (size_t)tiles * sizeof(unsigned)));
+        }
+    }
     if ((rc = plan_persistent(c))) return bail(rc);
     CREATE_CUDA(cudaDeviceSynchronize());
 #undef CREATE_CUDA
@@ -1023,7 +1158,7 @@ int l2_sample(const float *logits, int B, int vocab_size, float temperature, flo
 int l2_kernels_per_step(const l2_ctx *c, int B) {
     if (!c || B < 1 || B > c->max_batch) return L2_EINVAL;
     if (B == 1 && c->persist) return 1;
-    return 5 * c->cfg.n_layers + 1;
+    return 5 * c->cfg.n_layers + 1 + (B > 1 && c->bsets[B].tc ? 1 : 0);
 }
 
 int l2_step_input_bytes(void) { return (int)sizeof(StepDev); }
