@@ -8,10 +8,11 @@
 // hi the truncated tf32 part and lo = x - hi (the "3xTF32" split of Ootomo
 // and Yokota), accumulating in fp32 in tensor memory: the dropped lo*lo term
 // and the truncation of lo leave a relative error near 2^-21 per product,
-// fp32-level for these sums.  The raw fp32 tile serves as hi (the hardware
-// truncates); converter warps write lo beside it.  W*x_hi and W*x_lo are one
-// MMA of N = 2*bpad (the input rows followed by their lo rows), so the weight
-// tile is read twice per K step (W, W_lo) rather than three times.
+// fp32-level for these sums.  The raw fp32 tiles serve as hi (the hardware
+// truncates).  Converter warps write the inputs' lo rows beside the inputs
+// in shared memory, and the weights' lo parts into tensor memory (one row
+// per TMEM lane), where the MMA reads its A operand directly.  Per K step:
+// one MMA of N = 2*bpad, W * [x_hi; x_lo], and one of N = bpad, W_lo * x_hi.
 //
 // Inputs.  The RMSNorm modes read x * gain, written by the previous residual
 // kernel (or the embedding kernel) beside x, and scale the outputs by 1/rms
@@ -19,16 +20,21 @@
 //
 // Work.  An output tile is 128 weight rows (64 rows of W1 over the same 64
 // rows of W3, so SwiGLU pairs stay in one tile) by bpad sequences (B rounded
-// up to 16).  Items are (tile, K range); the host splits K so that the items
-// fill the SMs; with several ranges the partial tiles go to a workspace and
-// the last CTA of the tile (ticket) adds them in range order, so results do
-// not depend on timing.  Warp roles, all walking the CTA's items in order:
+// up to 16).  The (tile, K stage) pairs, tile-major, are split evenly over
+// the CTAs ("stream-K"): a CTA's range is whole tiles plus at most a partial
+// tile at each end.  Whole tiles are finished at once; partial ones go to a
+// workspace, and after its last tile -- with no copies of its own in flight,
+// so the one release it needs is cheap -- the CTA takes a ticket per partial
+// tile; the last CTA of a tile adds the parts in K order, so results do not
+// depend on timing.  Warp roles, all walking the CTA's range in order:
 //   warp 0      2-D tensor copies (TMA, 128-byte swizzle) of the weight and
-//               input tiles of 32 K columns into a 4-stage ring;
+//               input tiles of 64 K columns into a ring of 3 to 5 stages
+//               (as many as shared memory holds for the batch width);
 //   warp 1      the MMAs (M 128, K 8) of each converted stage, committed to
 //               the stage's "empty" barrier, and per item to an accumulator
 //               barrier; two accumulators in tensor memory alternate;
-//   warps 4-7   lo parts of each stage;
+//   warps 4-7   lo parts of each stage (weights into the stage's TMEM
+//               columns, inputs into shared memory);
 //   warps 8-11  epilogue: accumulator -> shared memory -> outputs, while the
 //               next item's MMAs run in the other accumulator.
 #include <algorithm>
@@ -44,37 +50,52 @@ namespace l2 {
 namespace {
 
 constexpr int kTT = 384;        // threads: 12 warps
-constexpr int kTS = 4;          // ring stages
-constexpr int kTK = 32;         // K columns per tile (128 bytes)
+constexpr int kMaxStages = 8;   // ring stages (fewer for wide batches)
+constexpr int kBK = 32;         // K columns of one tensor-copy box (128 bytes)
+constexpr int kSK = 2 * kBK;    // K columns per ring stage: two adjacent boxes
 constexpr int kTM = 128;        // output rows per tile
 constexpr int kTN = 64;         // most sequences
 constexpr int kConvWarp0 = 4;   // converter warps 4..7
 constexpr int kEpiWarp0 = 8;    // epilogue warps 8..11
 constexpr int kRoleThreads = 128;
-constexpr uint32_t kABytes = kTM * kTK * 4;          // 16 KB
-constexpr uint32_t kXBytes = 2 * kTN * kTK * 4;      // inputs and their lo rows, 16 KB
-constexpr uint32_t kStageBytes = 2 * kABytes + kXBytes;
-constexpr uint32_t kAccCols = 2 * kTN;                // one accumulator: columns [x_hi | x_lo]
-constexpr uint32_t kTmemCols = 2 * kAccCols;          // two accumulators
-constexpr int kYsStride = kTN + 1;                    // ys row stride bound (bpad + 1)
-constexpr int kMaxSplits = 16;                        // K ranges per tile
+constexpr uint32_t kABytes = kTM * kBK * 4;          // 16 KB: one box of weights (128 rows x 32)
+constexpr uint32_t kTmemCols = 512;                   // accumulators [0, 4 bpad), W_lo ring above
+constexpr size_t kSmemLimit = 227 * 1024;
+
+// A stage covers 64 K columns as two 32-column halves h: weights W_h (16 KB
+// each), then per half the bpad input rows X_h followed by their bpad lo
+// rows.  Whole stages move with one barrier phase: fewer, larger phases
+// stream from HBM markedly faster than twice as many 16 KB ones.
+__host__ __device__ constexpr uint32_t xbox_bytes(int bpad) { return (uint32_t)bpad * kBK * 4; }
+__host__ __device__ constexpr uint32_t stage_bytes(int bpad) { return 2 * kABytes + 4 * xbox_bytes(bpad); }
+// ys: the finished tile [128][bpad + 1] (odd stride: conflict-free columns)
+__host__ __device__ constexpr size_t ys_bytes(int bpad) { return (size_t)kTM * (bpad + 1) * 4; }
 
 struct TcFixed {
-    uint64_t full[kTS];     // copies landed
-    uint64_t conv[kTS];     // lo parts written
-    uint64_t empty[kTS];    // MMAs done with the stage
+    uint64_t full[kMaxStages];   // copies landed
+    uint64_t conv[kMaxStages];   // lo parts written
+    uint64_t empty[kMaxStages];  // MMAs done with the stage
     uint64_t acc_full[2];   // accumulator complete
     uint64_t acc_free[2];   // accumulator read out
     uint64_t fin;
     uint32_t tmem;
     int abort;
-    int last;
+    int last_w[2];
     float inv[kMaxBatch];
-    float red[kRoleThreads];
+    int pos[kMaxBatch];   // the step's positions and cache slots (QKV)
+    int slot[kMaxBatch];
 };
 
 __host__ __device__ constexpr size_t tc_fixed_bytes() { return (sizeof(TcFixed) + 1023) / 1024 * 1024; }
-__host__ __device__ constexpr size_t tc_ys_bytes() { return ((size_t)kTM * kYsStride * 4 + 1023) / 1024 * 1024; }
+
+// Ring stages for a batch width: what shared memory and the TMEM columns left
+// beside the two accumulators hold.
+__host__ __device__ constexpr int tc_stages(int bpad) {
+    const int by_smem = (int)((kSmemLimit - 1024 - tc_fixed_bytes() - ys_bytes(bpad)) / stage_bytes(bpad));
+    const int by_tmem = (int)((kTmemCols - 4u * (uint32_t)bpad) / kSK);
+    const int n = by_smem < by_tmem ? by_smem : by_tmem;
+    return n < kMaxStages ? n : kMaxStages;
+}
 
 __device__ __forceinline__ float silu_t(float v) { return v / (1.0f + expf(-v)); }
 __device__ __forceinline__ float tf32_lo(float x) { return x - __uint_as_float(__float_as_uint(x) & 0xFFFFE000u); }
@@ -124,6 +145,27 @@ __device__ __forceinline__ uint32_t elect_one() {
     return pred;
 }
 
+// A operand from tensor memory (one row per lane, K along the columns).
+__device__ __forceinline__ void mma_tf32_ta(uint32_t tmem, uint32_t ta, uint64_t db, uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem),
+        "r"(ta), "l"(db), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t addr, const uint32_t *v) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%"
+        "19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(addr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+        "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]),
+        "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]),
+        "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
 __device__ __forceinline__ void mma_commit(uint64_t *bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                  : "memory");
@@ -144,6 +186,16 @@ __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::
 
 // The 128 epilogue threads only.
 __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// Same barrier; every epilogue thread gets the OR of all their flags.
+__device__ __forceinline__ bool epi_sync_or(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, 1, 128, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v)
+        : "memory");
+    return r != 0;
+}
 
 __device__ __forceinline__ bool aborted(const TcFixed &fx) { return *reinterpret_cast<const volatile int *>(&fx.abort) != 0; }
 __device__ __forceinline__ void set_abort(TcFixed &fx) { *reinterpret_cast<volatile int *>(&fx.abort) = 1; }
@@ -193,17 +245,38 @@ __global__ void __launch_bounds__(kTT, 1) gemv_tc_kernel(const __grid_constant__
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     TcFixed &fx = *reinterpret_cast<TcFixed *>(smem);
-    float *ys = reinterpret_cast<float *>(smem + tc_fixed_bytes());  // [128][bpad + 1]
-    unsigned char *ring = smem + tc_fixed_bytes() + tc_ys_bytes();
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int B = p.batch, BP = tp.bpad, n = p.n;
+    const int NS = tp.stages;
+    const uint32_t SB = stage_bytes(BP);
+    unsigned char *ring = smem + tc_fixed_bytes();  // 1024-aligned stages, then ys
+    float *ys = reinterpret_cast<float *>(ring + (size_t)NS * SB);  // [128][bpad + 1]
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int YS = BP + 1;
-    const int KT = (n + kTK - 1) / kTK;
-    const int S = tp.splits;
-    const int items = tp.ntiles * S;
+    const int KT = (n + kSK - 1) / kSK;  // ring stages of 64 columns per tile
+    // Stream-K: the (tile, stage) pairs in tile-major order, split evenly over the CTAs.
+    const long long T = (long long)tp.ntiles * KT;
+    const int G = gridDim.x;
+    const long long s_begin = (long long)blockIdx.x * T / G, s_end = (long long)(blockIdx.x + 1) * T / G;
+    // the CTA holding stage x of the sequence
+    auto cta_of = [&](long long x) { return (int)(((x + 1) * G + T - 1) / T - 1); };
+    // the next segment (one tile's part of the CTA's range) at sequence position sq
+    auto segment = [&](long long sq, int &tile, int &k0, int &k1) {
+        tile = (int)(sq / KT);
+        k0 = (int)(sq - (long long)tile * KT);
+        k1 = (int)min((long long)KT, k0 + (s_end - sq));
+    };
+    // tile -> matrix, its first row within it, its tensor-map row
+    auto tile_geom = [&](int tile, int &m, int &r0, int &wrow) {
+        m = 0;
+        int t = tile;
+        if (MODE == GEMV_QKV)
+            while (m < 2 && t >= tp.tiles[m]) t -= tp.tiles[m++];
+        r0 = t * ((MODE == GEMV_W13) ? kTM / 2 : kTM);
+        wrow = (MODE == GEMV_CLS ? 0 : p.layer * tp.mrows[m]) + r0;
+    };
 
     if (tid == 0) {
-        for (int i = 0; i < kTS; ++i) {
+        for (int i = 0; i < NS; ++i) {
             mbar_init(&fx.full[i], 1);
             mbar_init(&fx.conv[i], kRoleThreads);
             mbar_init(&fx.empty[i], 1);
@@ -228,95 +301,98 @@ __global__ void __launch_bounds__(kTT, 1) gemv_tc_kernel(const __grid_constant__
     const uint32_t tmem = fx.tmem;
     pdl_launch_dependents();
 
-    // item -> matrix, first row within it, tensor-map row, K range, tile
-    auto item_geom = [&](int it, int &m, int &r0, int &wrow, int &k0t, int &k1t, int &tile) {
-        tile = it / S;
-        const int sp = it - tile * S;
-        m = 0;
-        int t = tile;
-        if (MODE == GEMV_QKV)
-            while (m < 2 && t >= tp.tiles[m]) t -= tp.tiles[m++];
-        r0 = t * ((MODE == GEMV_W13) ? kTM / 2 : kTM);
-        wrow = (MODE == GEMV_CLS ? 0 : p.layer * tp.mrows[m]) + r0;
-        k0t = (int)((long long)sp * KT / S);
-        k1t = (int)((long long)(sp + 1) * KT / S);
-    };
-    auto stage_ptr = [&](int s) { return ring + (size_t)s * kStageBytes; };
+    auto stage_ptr = [&](int s) { return ring + (size_t)s * SB; };
+    // stage s: W_0 | W_1 | X_0 | X_0 lo | X_1 | X_1 lo
+    auto wbox = [&](int s, int h) { return stage_ptr(s) + h * kABytes; };
+    auto xbox = [&](int s, int h) { return stage_ptr(s) + 2 * kABytes + 2 * h * xbox_bytes(BP); };
+    // TMEM: accumulator a at columns [2 bpad a, 2 bpad (a + 1)); stage s's W_lo at 4 bpad + 64 s
+    auto wlo_col = [&](int s) { return (uint32_t)(4 * BP + kSK * s); };
 
     if (warp == 0) {
         // ---------------- producer: tensor copies into the ring (whole warp, one lane issues) ----------------
-        const uint32_t stage_tx = kABytes + (uint32_t)BP * kTK * 4;
+        const uint32_t stage_tx = 2 * kABytes + 2 * xbox_bytes(BP);  // the lo rows are written here
         long long nl = 0;
         bool stop = false;
         auto issue_weights = [&](int s, int m, int wrow, int kt) {
-            unsigned char *st = stage_ptr(s);
             mbar_arrive_expect_tx(&fx.full[s], stage_tx);
-            if (MODE == GEMV_W13) {
-                tensor2d(st, &tp.wmap[0], kt * kTK, wrow, &fx.full[s]);
-                tensor2d(st + kABytes / 2, &tp.wmap[1], kt * kTK, wrow, &fx.full[s]);
-            } else {
-                tensor2d(st, &tp.wmap[MODE == GEMV_QKV ? m : 0], kt * kTK, wrow, &fx.full[s]);
+            for (int h = 0; h < 2; ++h) {
+                const int x = kt * kSK + h * kBK;
+                if (MODE == GEMV_W13) {
+                    tensor2d(wbox(s, h), &tp.wmap[0], x, wrow, &fx.full[s]);
+                    tensor2d(wbox(s, h) + kABytes / 2, &tp.wmap[1], x, wrow, &fx.full[s]);
+                } else {
+                    tensor2d(wbox(s, h), &tp.wmap[MODE == GEMV_QKV ? m : 0], x, wrow, &fx.full[s]);
+                }
             }
         };
         // the weights do not depend on the previous kernel: the first stages' tiles go out before the wait
         int npre = 0;
-        if ((int)blockIdx.x < items) {
-            int m, r0, wrow, k0t, k1t, tile;
-            item_geom(blockIdx.x, m, r0, wrow, k0t, k1t, tile);
-            npre = min(k1t - k0t, kTS);
+        if (s_begin < s_end) {
+            int tile, k0, k1, m, r0, wrow;
+            segment(s_begin, tile, k0, k1);
+            tile_geom(tile, m, r0, wrow);
+            npre = min(k1 - k0, NS);
             if (elect_one())
-                for (int i = 0; i < npre; ++i) issue_weights(i, m, wrow, k0t + i);
+                for (int i = 0; i < npre; ++i) issue_weights(i, m, wrow, k0 + i);
             __syncwarp();
         }
         pdl_wait();  // the inputs come from the previous kernel
-        for (int it = blockIdx.x; it < items && !stop; it += gridDim.x) {
-            int m, r0, wrow, k0t, k1t, tile;
-            item_geom(it, m, r0, wrow, k0t, k1t, tile);
-            for (int kt = k0t; kt < k1t; ++kt) {
-                const int s = (int)(nl % kTS);
-                const bool ok = nl < kTS || mbar_wait(&fx.empty[s], (uint32_t)(((nl / kTS) - 1) & 1), p.err);
+        for (long long sq = s_begin; sq < s_end && !stop;) {
+            int tile, k0, k1, m, r0, wrow;
+            segment(sq, tile, k0, k1);
+            tile_geom(tile, m, r0, wrow);
+            sq += k1 - k0;
+            for (int kt = k0; kt < k1; ++kt) {
+                const int s = (int)(nl % NS);
+                const bool ok = nl < NS || mbar_wait(&fx.empty[s], (uint32_t)(((nl / NS) - 1) & 1), p.err);
                 if ((stop = warp_stop(fx, ok))) break;
                 if (elect_one()) {
                     if (nl >= npre) issue_weights(s, m, wrow, kt);
-                    tensor2d(stage_ptr(s) + 2 * kABytes, &tp.xmap, kt * kTK, 0, &fx.full[s]);
+                    tensor2d(xbox(s, 0), &tp.xmap, kt * kSK, 0, &fx.full[s]);
+                    tensor2d(xbox(s, 1), &tp.xmap, kt * kSK + kBK, 0, &fx.full[s]);
                 }
                 __syncwarp();
                 ++nl;
             }
         }
         if (stop)  // the copies still in flight land before the CTA's memory goes
-            for (long long j = nl > kTS ? nl - kTS : 0; j < nl; ++j)
-                (void)mbar_wait(&fx.full[j % kTS], (uint32_t)((j / kTS) & 1), p.err);
+            for (long long j = nl > NS ? nl - NS : 0; j < nl; ++j)
+                (void)mbar_wait(&fx.full[j % NS], (uint32_t)((j / NS) & 1), p.err);
     } else if (warp == 1) {
         // ---------------- MMA issuer (whole warp, one lane issues) ----------------
         const uint32_t idesc2 = idesc_tf32(kTM, 2 * BP), idesc1 = idesc_tf32(kTM, BP);
         const uint64_t dring = desc_sw128(smem_u32(ring));  // stage 0's weight tile
         long long nc = 0, ni = 0;
         bool stop = false;
-        for (int it = blockIdx.x; it < items && !stop; it += gridDim.x, ++ni) {
-            int m, r0, wrow, k0t, k1t, tile;
-            item_geom(it, m, r0, wrow, k0t, k1t, tile);
+        for (long long sq = s_begin; sq < s_end && !stop; ++ni) {
+            int tile, k0, k1;
+            segment(sq, tile, k0, k1);
+            sq += k1 - k0;
             const int a = (int)(ni & 1);
             const bool ok = ni < 2 || mbar_wait(&fx.acc_free[a], (uint32_t)(((ni / 2) - 1) & 1), p.err);
             if ((stop = warp_stop(fx, ok))) break;
             tc_fence_after();
-            const uint32_t dacc = tmem + (uint32_t)a * kAccCols;
-            for (int kt = k0t; kt < k1t; ++kt, ++nc) {
-                const int s = (int)(nc % kTS);
-                const bool okc = mbar_wait(&fx.conv[s], (uint32_t)((nc / kTS) & 1), p.err);
+            const uint32_t dacc = tmem + (uint32_t)(2 * BP * a);
+            for (int kt = k0; kt < k1; ++kt, ++nc) {
+                const int s = (int)(nc % NS);
+                const bool okc = mbar_wait(&fx.conv[s], (uint32_t)((nc / NS) & 1), p.err);
                 if ((stop = warp_stop(fx, okc))) break;
                 tc_fence_after();
                 // descriptor start addresses are in 16-byte units; a K step of 8 is 32 bytes
-                const uint64_t dw = dring + (uint64_t)((uint32_t)s * (kStageBytes >> 4));
-                const uint64_t dwl = dw + (kABytes >> 4), dx = dw + ((2 * kABytes) >> 4);
-                const uint32_t first = kt == k0t ? 0u : 1u;
+                const uint64_t dw = dring + (uint64_t)((uint32_t)s * (SB >> 4));
+                const uint64_t dx = dw + ((2 * kABytes) >> 4), dxh = (2 * xbox_bytes(BP)) >> 4;
+                const uint32_t twl = tmem + wlo_col(s);
+                const uint32_t first = kt == k0 ? 0u : 1u;
                 if (elect_one()) {
 #pragma unroll
-                    for (int ks = 0; ks < kTK / 8; ++ks) {
-                        // columns [0, BP): W x_hi; [BP, 2 BP): W x_lo; then W_lo x_hi into [0, BP)
-                        mma_tf32(dacc, dw + 2 * ks, dx + 2 * ks, idesc2, ks == 0 ? first : 1u);
-                        mma_tf32(dacc, dwl + 2 * ks, dx + 2 * ks, idesc1, 1u);
-                    }
+                    for (int h = 0; h < 2; ++h)
+#pragma unroll
+                        for (int ks = 0; ks < kBK / 8; ++ks) {
+                            // columns [0, BP): W x_hi; [BP, 2 BP): W x_lo; then W_lo x_hi into [0, BP)
+                            const uint64_t a = dw + h * (kABytes >> 4) + 2 * ks, b = dx + h * dxh + 2 * ks;
+                            mma_tf32(dacc, a, b, idesc2, (h == 0 && ks == 0) ? first : 1u);
+                            mma_tf32_ta(dacc, twl + (uint32_t)(kBK * h + 8 * ks), b, idesc1, 1u);
+                        }
                     mma_commit(&fx.empty[s]);
                 }
                 __syncwarp();
@@ -330,27 +406,42 @@ __global__ void __launch_bounds__(kTT, 1) gemv_tc_kernel(const __grid_constant__
         __syncwarp();
         (void)mbar_wait(&fx.fin, 0u, p.err);
     } else if (warp >= kConvWarp0 && warp < kConvWarp0 + 4) {
-        // ---------------- converters: lo parts of weights and inputs ----------------
+        // ---------------- converters: lo parts of weights (-> TMEM) and inputs ----------------
         const int ct = tid - kConvWarp0 * 32;
+        const int q = warp & 3, row = 32 * q + lane;  // this thread's weight row = its TMEM lane
         long long nc = 0;
-        for (int it = blockIdx.x; it < items && !aborted(fx); it += gridDim.x) {
-            int m, r0, wrow, k0t, k1t, tile;
-            item_geom(it, m, r0, wrow, k0t, k1t, tile);
-            for (int kt = k0t; kt < k1t; ++kt, ++nc) {
-                const int s = (int)(nc % kTS);
-                if (!mbar_wait(&fx.full[s], (uint32_t)((nc / kTS) & 1), p.err)) set_abort(fx);
-                if (aborted(fx)) break;
-                float4 *A4 = reinterpret_cast<float4 *>(stage_ptr(s));
-                float4 *Alo4 = A4 + kTM * kTK / 4;
-                float4 *X4 = Alo4 + kTM * kTK / 4;
-                float4 *Xlo4 = X4 + BP * kTK / 4;  // right after the BP input rows
-                float4 a[kTM * kTK / 4 / kRoleThreads];
+        bool stop = false;
+        for (long long sq = s_begin; sq < s_end && !stop;) {
+            int tile, k0, k1;
+            segment(sq, tile, k0, k1);
+            sq += k1 - k0;
+            for (int kt = k0; kt < k1; ++kt, ++nc) {
+                const int s = (int)(nc % NS);
+                if ((stop = warp_stop(fx, mbar_wait(&fx.full[s], (uint32_t)((nc / NS) & 1), p.err)))) break;
+                tc_fence_after();  // after the MMAs that last read this stage's TMEM columns
 #pragma unroll
-                for (int i = 0; i < kTM * kTK / 4 / kRoleThreads; ++i) a[i] = A4[ct + i * kRoleThreads];
+                for (int h = 0; h < 2; ++h) {
+                    // the row's 8 16-byte chunks of half h, logical chunk j stored at j ^ (row % 8)
+                    const float4 *A4 = reinterpret_cast<const float4 *>(wbox(s, h)) + row * (kBK / 4);
+                    uint32_t v[kBK];
 #pragma unroll
-                for (int i = 0; i < kTM * kTK / 4 / kRoleThreads; ++i) Alo4[ct + i * kRoleThreads] = tf32_lo4(a[i]);
-                for (int i = ct; i < BP * kTK / 4; i += kRoleThreads) Xlo4[i] = tf32_lo4(X4[i]);
+                    for (int j = 0; j < kBK / 4; ++j) {
+                        const float4 a = tf32_lo4(A4[j ^ (row & 7)]);
+                        v[4 * j] = __float_as_uint(a.x);
+                        v[4 * j + 1] = __float_as_uint(a.y);
+                        v[4 * j + 2] = __float_as_uint(a.z);
+                        v[4 * j + 3] = __float_as_uint(a.w);
+                    }
+                    tmem_st32(tmem + ((uint32_t)(32 * q) << 16) + wlo_col(s) + (uint32_t)(kBK * h), v);
+                }
+                for (int h = 0; h < 2; ++h) {
+                    float4 *X4 = reinterpret_cast<float4 *>(xbox(s, h));
+                    float4 *Xlo4 = X4 + BP * kBK / 4;  // right after the BP input rows
+                    for (int i = ct; i < BP * kBK / 4; i += kRoleThreads) Xlo4[i] = tf32_lo4(X4[i]);
+                }
+                tmem_wait_st();
                 fence_proxy_async_smem();
+                tc_fence_before();
                 mbar_arrive(&fx.conv[s]);
             }
         }
@@ -358,6 +449,11 @@ __global__ void __launch_bounds__(kTT, 1) gemv_tc_kernel(const __grid_constant__
         // ---------------- epilogue ----------------
         const int et = tid - kEpiWarp0 * 32, q = warp & 3, row = 32 * q + lane;
         pdl_wait();  // sums of squares, x, the step's positions and slots
+        if (MODE == GEMV_QKV)
+            for (int b = et; b < B; b += kRoleThreads) {
+                fx.pos[b] = p.step->pos[b];
+                fx.slot[b] = p.step->slot[b];
+            }
         if (MODE != GEMV_RESID) {
             for (int b = et >> 5; b < B; b += kRoleThreads / 32) {
                 float ss = 0.f;
@@ -367,17 +463,122 @@ __global__ void __launch_bounds__(kTT, 1) gemv_tc_kernel(const __grid_constant__
             }
         }
         epi_sync();
+        // a finished tile in ys -> the outputs of rows r0.. of matrix m, sequences 0..B-1 (row index fastest)
+        auto finish = [&](int tile) {
+            int m, r0, wrow;
+            tile_geom(tile, m, r0, wrow);
+        if (MODE == GEMV_QKV) {
+            // pairs (j, j+1) of rows: RoPE on q and k, then the KV cache; the table reads of
+            // 8 pairs go out before their stores
+            const int hs = p.head_size, half = hs >> 1, mr = tp.mrows[m];
+            for (int e0 = et; e0 < (kTM / 2) * B; e0 += 8 * kRoleThreads) {
+                float2 cs[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int e = e0 + i * kRoleThreads, b = e / (kTM / 2), v = r0 + 2 * (e - b * (kTM / 2));
+                    cs[i] = make_float2(1.f, 0.f);
+                    if (m < 2 && e < (kTM / 2) * B && v < mr) cs[i] = p.rope[(size_t)fx.pos[b] * half + ((v % hs) >> 1)];
+                }
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int e = e0 + i * kRoleThreads, b = e / (kTM / 2), j = 2 * (e - b * (kTM / 2)), v = r0 + j;
+                    if (e >= (kTM / 2) * B || v >= mr) continue;
+                    const float y0 = ys[j * YS + b] * fx.inv[b], y1 = ys[(j + 1) * YS + b] * fx.inv[b];
+                    if (m == 0) {
+                        float *qv = p.q + (size_t)b * p.dim;
+                        qv[v] = y0 * cs[i].x - y1 * cs[i].y;
+                        qv[v + 1] = y0 * cs[i].y + y1 * cs[i].x;
+                    } else {
+                        const int g = v / hs, d = v % hs;
+                        const size_t idx =
+                            ((((size_t)fx.slot[b] * p.n_layers + p.layer) * p.n_kv_heads + g) * p.seq_len + fx.pos[b]) * hs +
+                            d;
+                        if (m == 1) {
+                            p.kcache[idx] = y0 * cs[i].x - y1 * cs[i].y;
+                            p.kcache[idx + 1] = y0 * cs[i].y + y1 * cs[i].x;
+                        } else {
+                            p.vcache[idx] = y0;
+                            p.vcache[idx + 1] = y1;
+                        }
+                    }
+                }
+            }
+        } else if (MODE == GEMV_W13) {
+            const int hidden = tp.mrows[0];
+            for (int e = et; e < (kTM / 2) * B; e += kRoleThreads) {
+                const int b = e / (kTM / 2), j = e - b * (kTM / 2);
+                if (r0 + j >= hidden) continue;
+                const float h1 = ys[j * YS + b] * fx.inv[b], h3 = ys[(j + kTM / 2) * YS + b] * fx.inv[b];
+                p.hb[(size_t)b * hidden + r0 + j] = silu_t(h1) * h3;
+            }
+        } else if (MODE == GEMV_RESID) {
+            const int dim = tp.mrows[0];
+            // thread = row j; x of 8 sequences loaded before any store
+            if (et < dim - r0) {
+                const int j = et;
+                const float g = __ldg(tp.next_gain + r0 + j);
+                for (int b0 = 0; b0 < B; b0 += 8) {
+                    float xv[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        if (b0 + i < B) xv[i] = p.x[(size_t)(b0 + i) * dim + r0 + j];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        if (b0 + i < B) {
+                            const size_t o = (size_t)(b0 + i) * dim + r0 + j;
+                            const float nv = xv[i] + ys[j * YS + b0 + i];
+                            p.x[o] = nv;
+                            tp.xg[o] = nv * g;
+                            ys[j * YS + b0 + i] = nv;
+                        }
+                }
+            }
+            epi_sync();
+            // this tile's sum of squares of the new x rows, per sequence, in a fixed order
+            const int parts = kRoleThreads / B, rows = min(kTM, dim - r0);  // parts * B <= 128 rows of ys
+            float ss = 0.f;
+            if (et < parts * B) {
+                const int b = et % B;
+                for (int j = et / B; j < rows; j += parts) ss = fmaf(ys[j * YS + b], ys[j * YS + b], ss);
+            }
+            ys[et * YS + BP] = ss;  // the padding column holds the partials
+            epi_sync();
+            if (et < B) {
+                float t = 0.f;
+                for (int i = 0; i < parts; ++i) t += ys[(i * B + et) * YS + BP];
+                p.ss_part[(size_t)tile * B + et] = t;
+            }
+        } else {
+            float *user = p.step->logits_out;
+            const int V = tp.mrows[0];
+            for (int e = et; e < kTM * B; e += kRoleThreads) {
+                const int b = e / kTM, j = e - b * kTM;
+                if (r0 + j >= V) continue;
+                const float y = ys[j * YS + b] * fx.inv[b];
+                p.logits[(size_t)b * V + r0 + j] = y;
+                if (user) user[(size_t)b * V + r0 + j] = y;
+            }
+        }
+        };
+        // partial segments (at most the first and the last): published now, merged after the last one
+        int part0 = -1, part1 = -1;
         long long ni = 0;
-        for (int it = blockIdx.x; it < items && !aborted(fx); it += gridDim.x, ++ni) {
-            int m, r0, wrow, k0t, k1t, tile;
-            item_geom(it, m, r0, wrow, k0t, k1t, tile);
+        bool stop = false;
+        for (long long sq = s_begin; sq < s_end; ++ni) {
+            int tile, k0, k1;
+            segment(sq, tile, k0, k1);
+            const int which = sq == s_begin ? 0 : 1;
+            sq += k1 - k0;
+            const bool whole = k0 == 0 && k1 == KT;
             const int a = (int)(ni & 1);
-            if (!mbar_wait(&fx.acc_full[a], (uint32_t)((ni / 2) & 1), p.err)) set_abort(fx);
-            if (aborted(fx)) break;
+            const bool ok = mbar_wait(&fx.acc_full[a], (uint32_t)((ni / 2) & 1), p.err);
+            if (!ok) set_abort(fx);
+            if ((stop = epi_sync_or(!ok || aborted(fx)))) break;  // the same decision in all four warps
             tc_fence_after();
             // this thread's row of the accumulator: y = W x_hi + W x_lo + W_lo x_hi
-            const uint32_t base = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)a * kAccCols;
-            float *wsrow = (S > 1) ? tp.ws + (size_t)it * kTM * BP : nullptr;  // [BP][128] per item
+            const uint32_t base = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(2 * BP * a);
+            // a partial tile goes to this CTA's workspace slot [BP][128]
+            float *wsrow = tp.ws + ((size_t)blockIdx.x * 2 + which) * kTM * BP;
             for (int c0 = 0; c0 < B; c0 += 8) {
                 float v[8], w[8];
                 tmem_ld8(base + (uint32_t)c0, v);
@@ -386,122 +587,82 @@ __global__ void __launch_bounds__(kTT, 1) gemv_tc_kernel(const __grid_constant__
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     const float y = v[j] + w[j];
-                    if (S > 1) wsrow[(size_t)(c0 + j) * kTM + row] = y;
-                    else ys[row * YS + c0 + j] = y;
+                    if (whole) ys[row * YS + c0 + j] = y;
+                    else wsrow[(size_t)(c0 + j) * kTM + row] = y;
                 }
             }
             tc_fence_before();
             mbar_arrive(&fx.acc_free[a]);
-            if (S > 1) {
-                // publish the partial tile; the last CTA of the tile adds all in range order
-                __threadfence();
-                epi_sync();
-                if (et == 0) fx.last = atomicAdd(&tp.tickets[tile], 1u) == (unsigned)(S - 1) ? 1 : 0;
-                epi_sync();
-                if (!fx.last) continue;
-                __threadfence();
-                // 4 rows of one sequence per float4; all S partials in flight at once, added in range order
-                const float4 *tb = reinterpret_cast<const float4 *>(tp.ws + (size_t)tile * S * kTM * BP);
-                for (int v = et; v < B * (kTM / 4); v += kRoleThreads) {
-                    float4 part[kMaxSplits];
-#pragma unroll
-                    for (int sp = 0; sp < kMaxSplits; ++sp)
-                        if (sp < S) part[sp] = __ldcg(tb + (size_t)sp * (BP * kTM / 4) + v);
-                    float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                    for (int sp = 0; sp < kMaxSplits; ++sp)
-                        if (sp < S) {
-                            y.x += part[sp].x;
-                            y.y += part[sp].y;
-                            y.z += part[sp].z;
-                            y.w += part[sp].w;
-                        }
-                    const int c = v / (kTM / 4), r = (v - c * (kTM / 4)) * 4;
-                    ys[r * YS + c] = y.x;
-                    ys[(r + 1) * YS + c] = y.y;
-                    ys[(r + 2) * YS + c] = y.z;
-                    ys[(r + 3) * YS + c] = y.w;
-                }
-                if (et == 0) tp.tickets[tile] = 0u;
+            if (!whole) {
+                if (which == 0) part0 = tile;
+                else part1 = tile;
+                continue;
             }
             epi_sync();
-
-            // ---- rows r0.. of matrix m, sequences 0..B-1 (row index fastest) ----
-            if (MODE == GEMV_QKV) {
-                const int hs = p.head_size, half = hs >> 1, mr = tp.mrows[m];
-                for (int e = et; e < (kTM / 2) * B; e += kRoleThreads) {
-                    const int b = e / (kTM / 2), j = 2 * (e - b * (kTM / 2)), v = r0 + j;
-                    if (v >= mr) continue;
-                    const float y0 = ys[j * YS + b] * fx.inv[b], y1 = ys[(j + 1) * YS + b] * fx.inv[b];
-                    const int pos = p.step->pos[b];
-                    const float2 *rr = p.rope + (size_t)pos * half;
-                    if (m == 0) {
-                        const float2 cs = rr[(v % hs) >> 1];
-                        float *qv = p.q + (size_t)b * p.dim;
-                        qv[v] = y0 * cs.x - y1 * cs.y;
-                        qv[v + 1] = y0 * cs.y + y1 * cs.x;
-                    } else {
-                        const int g = v / hs, d = v % hs;
-                        const size_t idx =
-                            ((((size_t)p.step->slot[b] * p.n_layers + p.layer) * p.n_kv_heads + g) * p.seq_len + pos) *
-                                hs +
-                            d;
-                        if (m == 1) {
-                            const float2 cs = rr[d >> 1];
-                            p.kcache[idx] = y0 * cs.x - y1 * cs.y;
-                            p.kcache[idx + 1] = y0 * cs.y + y1 * cs.x;
-                        } else {
-                            p.vcache[idx] = y0;
-                            p.vcache[idx + 1] = y1;
-                        }
+            finish(tile);
+            epi_sync();  // ys free for the next tile
+        }
+        if (!stop && (part0 >= 0 || part1 >= 0)) {
+            // Nothing of this CTA's is in flight any more: publish the partial tiles (one
+            // release per CTA) and take the tickets; the last CTA of a tile adds its parts
+            // in K order and finishes it.
+            epi_sync();
+            if (et == 0) {
+                __threadfence();
+                for (int w = 0; w < 2; ++w) {
+                    int last = 0;
+                    const int t = w == 0 ? part0 : part1;
+                    if (t >= 0) {
+                        const int c0 = cta_of((long long)t * KT), c1 = cta_of((long long)(t + 1) * KT - 1);
+                        last = atomicAdd(&tp.tickets[t], 1u) == (unsigned)(c1 - c0) ? 1 : 0;
                     }
+                    fx.last_w[w] = last;
                 }
-            } else if (MODE == GEMV_W13) {
-                const int hidden = tp.mrows[0];
-                for (int e = et; e < (kTM / 2) * B; e += kRoleThreads) {
-                    const int b = e / (kTM / 2), j = e - b * (kTM / 2);
-                    if (r0 + j >= hidden) continue;
-                    const float h1 = ys[j * YS + b] * fx.inv[b], h3 = ys[(j + kTM / 2) * YS + b] * fx.inv[b];
-                    p.hb[(size_t)b * hidden + r0 + j] = silu_t(h1) * h3;
-                }
-            } else if (MODE == GEMV_RESID) {
-                const int dim = tp.mrows[0];
-                for (int e = et; e < kTM * B; e += kRoleThreads) {
-                    const int b = e / kTM, j = e - b * kTM;
-                    if (r0 + j >= dim) continue;
-                    const size_t o = (size_t)b * dim + r0 + j;
-                    const float nv = p.x[o] + ys[j * YS + b];
-                    p.x[o] = nv;
-                    tp.xg[o] = nv * __ldg(tp.next_gain + r0 + j);
-                    ys[j * YS + b] = nv;
-                }
-                epi_sync();
-                // this tile's sum of squares of the new x rows, per sequence, in a fixed order
-                const int parts = kRoleThreads / B, rows = min(kTM, dim - r0);
-                float ss = 0.f;
-                if (et < parts * B) {
-                    const int b = et % B;
-                    for (int j = et / B; j < rows; j += parts) ss = fmaf(ys[j * YS + b], ys[j * YS + b], ss);
-                }
-                fx.red[et] = ss;
-                epi_sync();
-                if (et < B) {
-                    float t = 0.f;
-                    for (int i = 0; i < parts; ++i) t += fx.red[i * B + et];
-                    p.ss_part[(size_t)tile * B + et] = t;
-                }
-            } else {
-                float *user = p.step->logits_out;
-                const int V = tp.mrows[0];
-                for (int e = et; e < kTM * B; e += kRoleThreads) {
-                    const int b = e / kTM, j = e - b * kTM;
-                    if (r0 + j >= V) continue;
-                    const float y = ys[j * YS + b] * fx.inv[b];
-                    p.logits[(size_t)b * V + r0 + j] = y;
-                    if (user) user[(size_t)b * V + r0 + j] = y;
-                }
+                __threadfence();
             }
-            epi_sync();  // ys free for the next item
+            epi_sync();
+            for (int w = 0; w < 2; ++w) {
+                if (!fx.last_w[w]) continue;
+                const int t = w == 0 ? part0 : part1;
+                const int c0 = cta_of((long long)t * KT), c1 = cta_of((long long)(t + 1) * KT - 1);
+                // 4 rows of one sequence per float4, this thread's v = et + 128 i; per part all of
+                // them in flight at once; parts added in K order
+                constexpr int kV = kTN * kTM / 4 / kRoleThreads;  // float4s per thread at most (16)
+                const int nv = B * (kTM / 4);
+                float4 acc[kV];
+#pragma unroll
+                for (int i = 0; i < kV; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int c = c0; c <= c1; ++c) {
+                    const int wh = (long long)c * T / G >= (long long)t * KT ? 0 : 1;
+                    const float4 *src = reinterpret_cast<const float4 *>(tp.ws + ((size_t)c * 2 + wh) * kTM * BP);
+                    float4 part[kV];
+#pragma unroll
+                    for (int i = 0; i < kV; ++i)
+                        if (et + kRoleThreads * i < nv) part[i] = __ldcg(src + et + kRoleThreads * i);
+#pragma unroll
+                    for (int i = 0; i < kV; ++i)
+                        if (et + kRoleThreads * i < nv) {
+                            acc[i].x += part[i].x;
+                            acc[i].y += part[i].y;
+                            acc[i].z += part[i].z;
+                            acc[i].w += part[i].w;
+                        }
+                }
+#pragma unroll
+                for (int i = 0; i < kV; ++i) {
+                    const int v = et + kRoleThreads * i;
+                    if (v >= nv) continue;
+                    const int c = v / (kTM / 4), r = (v - c * (kTM / 4)) * 4;
+                    ys[r * YS + c] = acc[i].x;
+                    ys[(r + 1) * YS + c] = acc[i].y;
+                    ys[(r + 2) * YS + c] = acc[i].z;
+                    ys[(r + 3) * YS + c] = acc[i].w;
+                }
+                if (et == 0) tp.tickets[t] = 0u;
+                epi_sync();
+                finish(t);
+                epi_sync();
+            }
         }
     }
     tc_fence_before();
@@ -515,35 +676,26 @@ __global__ void __launch_bounds__(kTT, 1) gemv_tc_kernel(const __grid_constant__
 
 int gemv_tc_max_batch() { return kTN; }
 
-size_t gemv_tc_smem() { return 1024 + tc_fixed_bytes() + tc_ys_bytes() + (size_t)kTS * kStageBytes; }
+int gemv_tc_stages(int bpad) { return tc_stages(bpad); }
 
-// K ranges per tile: the count that minimises the estimated time in ring
-// stages -- waves of items x K tiles per item, where an item of a split tile
-// costs at least kSplitItemStages (its partial-tile publish), plus the final
-// merge of the last tile's partials.
-constexpr int kSplitItemStages = 6;
-constexpr int kMergeStages = 6;
-int gemv_tc_splits(int ntiles, int n, int ctas) {
-    const int KT = (n + kTK - 1) / kTK;
-    int best = 1;
-    long long best_cost = -1;
-    for (int s = 1; s <= kMaxSplits && s <= KT; ++s) {
-        const long long waves = ((long long)ntiles * s + ctas - 1) / ctas;
-        const long long per = (KT + s - 1) / s;
-        const long long cost = s == 1 ? waves * per : waves * std::max<long long>(per, kSplitItemStages) + kMergeStages;
-        if (best_cost < 0 || cost < best_cost) {
-            best_cost = cost;
-            best = s;
-        }
-    }
-    return best;
+size_t gemv_tc_smem(int bpad) { return 1024 + tc_fixed_bytes() + (size_t)tc_stages(bpad) * stage_bytes(bpad) + ys_bytes(bpad); }
+
+// CTAs for a plan: one per SM, but each with at least kMinCtaStages ring
+// stages of work (fewer, longer ranges: fewer partial tiles to add up).
+constexpr int kMinCtaStages = 4;
+int gemv_tc_grid(int ntiles, int n, int ctas) {
+    const long long T = (long long)ntiles * ((n + kSK - 1) / kSK);
+    return (int)std::max<long long>(1, std::min<long long>(ctas, T / kMinCtaStages));
 }
+
+// Workspace floats for a grid: two partial tiles per CTA.
+size_t gemv_tc_ws_floats(int grid, int bpad) { return (size_t)grid * 2 * kTM * bpad; }
 
 cudaError_t gemv_tc_init() {
     void *fns[] = {reinterpret_cast<void *>(gemv_tc_kernel<GEMV_QKV>), reinterpret_cast<void *>(gemv_tc_kernel<GEMV_RESID>),
                    reinterpret_cast<void *>(gemv_tc_kernel<GEMV_W13>), reinterpret_cast<void *>(gemv_tc_kernel<GEMV_CLS>)};
     for (void *f : fns) {
-        cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gemv_tc_smem());
+        cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemLimit);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
@@ -581,7 +733,7 @@ cudaError_t launch_gemv_tc(int mode, const TcParams &tp, int grid, cudaStream_t 
         default: return cudaErrorInvalidValue;
     }
     cudaLaunchAttribute attr[1];
-    cudaLaunchConfig_t cfg = pdl_config(dim3(grid), dim3(kTT), gemv_tc_smem(), stream, pdl, attr);
+    cudaLaunchConfig_t cfg = pdl_config(dim3(grid), dim3(kTT), gemv_tc_smem(tp.bpad), stream, pdl, attr);
     void *args[] = {const_cast<TcParams *>(&tp)};
     return cudaLaunchKernelExC(&cfg, fn, args);
 }

@@ -399,7 +399,7 @@ bool encode_matrix_sw128(CUtensorMap *m, const void *base, uint64_t cols, uint64
 }
 
 // The tensor-core plans of a batch size (16..64 rows): tiles of 128 output
-// rows (64 of W1 over 64 of W3), K split so that the items fill the SMs.
+// rows (64 of W1 over 64 of W3), the work split evenly over the SMs.
 int build_tc_set(l2_ctx *c, int batch) {
     const L2Config &p = c->cfg;
     BatchSet &set = c->bsets[batch];
@@ -411,6 +411,7 @@ int build_tc_set(l2_ctx *c, int batch) {
         TcParams &tp = set.tcp[k];
         memset(&tp, 0, sizeof(tp));
         tp.bpad = bpad;
+        tp.stages = gemv_tc_stages(bpad);
         bool ok = true;
         int n = 0;
         switch (k) {
@@ -456,10 +457,8 @@ int build_tc_set(l2_ctx *c, int batch) {
         }
         if (!ok) return fail(c, L2_ECUDA, "cuTensorMapEncodeTiled failed for a tensor-core GEMV plan");
         tp.ntiles = tp.tiles[0] + tp.tiles[1] + tp.tiles[2];
-        tp.splits = gemv_tc_splits(tp.ntiles, n, c->num_sms);
-        const int items = tp.ntiles * tp.splits;
-        set.tc_grid[k] = items < c->num_sms ? items : c->num_sms;
-        if (tp.splits > 1) set.tc_ws_floats = std::max(set.tc_ws_floats, (size_t)items * 128 * bpad);
+        set.tc_grid[k] = gemv_tc_grid(tp.ntiles, n, c->num_sms);
+        set.tc_ws_floats = std::max(set.tc_ws_floats, gemv_tc_ws_floats(set.tc_grid[k], bpad));
         set.tc_tiles = std::max(set.tc_tiles, tp.ntiles);
     }
     if (set.tcp[1].ntiles > kMaxParts) return fail(c, L2_EINVAL, "too many residual tiles for the sum-of-squares parts");

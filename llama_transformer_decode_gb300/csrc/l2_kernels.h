@@ -49,8 +49,10 @@ cudaError_t launch_sample(const SampleParams &p, int batch, cudaStream_t stream)
 
 // Tensor-core batched GEMV (gemv_tc.cu), 16..64 sequences.
 int gemv_tc_max_batch();
-size_t gemv_tc_smem();
-int gemv_tc_splits(int ntiles, int n, int ctas);
+int gemv_tc_stages(int bpad);
+size_t gemv_tc_smem(int bpad);
+int gemv_tc_grid(int ntiles, int n, int ctas);
+size_t gemv_tc_ws_floats(int grid, int bpad);
 cudaError_t gemv_tc_init();
 cudaError_t launch_tc_embed(const TcParams &tp, int batch, cudaStream_t stream, bool pdl);
 cudaError_t launch_gemv_tc(int mode, const TcParams &tp, int grid, cudaStream_t stream, bool pdl);

@@ -112,8 +112,9 @@ struct SampleParams {
 };
 
 // Tensor-core batched GEMV (gemv_tc.cu): output tiles of 128 rows (64 rows
-// of W1 over the same 64 rows of W3) x bpad sequences, K split into `splits`
-// ranges; tensor maps with 128-byte swizzle, boxes of 32 columns.
+// of W1 over the same 64 rows of W3) x bpad sequences, the (tile, K stage)
+// work split evenly over the grid; tensor maps with 128-byte swizzle, boxes of
+// 32 columns.
 struct alignas(64) TcParams {
     CUtensorMap wmap[3];  // QKV: Wq, Wk, Wv; W1/W3: W1, W3; otherwise [0]
     CUtensorMap xmap;     // inputs [max rows][n] (x * gain for the RMSNorm modes), box 32 columns x bpad rows
@@ -121,9 +122,9 @@ struct alignas(64) TcParams {
     int tiles[3];         // output tiles per matrix (QKV), or [0]
     int mrows[3];         // rows of each matrix in one layer
     int ntiles;           // all tiles
-    int splits;           // K ranges per tile
     int bpad;             // sequences rounded up to a multiple of 16 (MMA N)
-    float *ws;            // partial tiles [ntiles * splits][128][bpad] when splits > 1
+    int stages;           // ring stages for this width
+    float *ws;            // partial tiles [grid][2][bpad][128]
     unsigned *tickets;    // [ntiles], zero between launches
     float *xg;            // x * gain of the next RMSNorm [max rows][dim], written by the residual kernels
     const float *next_gain;  // residual kernels: the gain vector of the next RMSNorm
