@@ -625,38 +625,53 @@ __global__ void __launch_bounds__(kTT, 1) gemv_tc_kernel(const __grid_constant__
                 if (!fx.last_w[w]) continue;
                 const int t = w == 0 ? part0 : part1;
                 const int c0 = cta_of((long long)t * KT), c1 = cta_of((long long)(t + 1) * KT - 1);
-                // 4 rows of one sequence per float4, this thread's v = et + 128 i; per part all of
-                // them in flight at once; parts added in K order
-                constexpr int kV = kTN * kTM / 4 / kRoleThreads;  // float4s per thread at most (16)
+                // 4 rows of one sequence per float4, this thread's v = et + 128 i (8 at a time);
+                // two parts' loads in flight per round trip; parts added in K order
+                constexpr int kV = 8;
                 const int nv = B * (kTM / 4);
-                float4 acc[kV];
+                for (int i0 = 0; et + kRoleThreads * i0 < nv; i0 += kV) {
+                    float4 acc[kV];
 #pragma unroll
-                for (int i = 0; i < kV; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-                for (int c = c0; c <= c1; ++c) {
-                    const int wh = (long long)c * T / G >= (long long)t * KT ? 0 : 1;
-                    const float4 *src = reinterpret_cast<const float4 *>(tp.ws + ((size_t)c * 2 + wh) * kTM * BP);
-                    float4 part[kV];
+                    for (int i = 0; i < kV; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    for (int c = c0; c <= c1; c += 2) {
+                        const float4 *src[2];
+                        float4 part[2][kV];
 #pragma unroll
-                    for (int i = 0; i < kV; ++i)
-                        if (et + kRoleThreads * i < nv) part[i] = __ldcg(src + et + kRoleThreads * i);
-#pragma unroll
-                    for (int i = 0; i < kV; ++i)
-                        if (et + kRoleThreads * i < nv) {
-                            acc[i].x += part[i].x;
-                            acc[i].y += part[i].y;
-                            acc[i].z += part[i].z;
-                            acc[i].w += part[i].w;
+                        for (int u = 0; u < 2; ++u) {
+                            const int cc = min(c + u, c1);
+                            const int wh = (long long)cc * T / G >= (long long)t * KT ? 0 : 1;
+                            src[u] = reinterpret_cast<const float4 *>(tp.ws + ((size_t)cc * 2 + wh) * kTM * BP);
                         }
-                }
 #pragma unroll
-                for (int i = 0; i < kV; ++i) {
-                    const int v = et + kRoleThreads * i;
-                    if (v >= nv) continue;
-                    const int c = v / (kTM / 4), r = (v - c * (kTM / 4)) * 4;
-                    ys[r * YS + c] = acc[i].x;
-                    ys[(r + 1) * YS + c] = acc[i].y;
-                    ys[(r + 2) * YS + c] = acc[i].z;
-                    ys[(r + 3) * YS + c] = acc[i].w;
+                        for (int u = 0; u < 2; ++u)
+#pragma unroll
+                            for (int i = 0; i < kV; ++i) {
+                                const int v = et + kRoleThreads * (i0 + i);
+                                if (v < nv && c + u <= c1) part[u][i] = __ldcg(src[u] + v);
+                            }
+#pragma unroll
+                        for (int u = 0; u < 2; ++u)
+#pragma unroll
+                            for (int i = 0; i < kV; ++i) {
+                                const int v = et + kRoleThreads * (i0 + i);
+                                if (v < nv && c + u <= c1) {
+                                    acc[i].x += part[u][i].x;
+                                    acc[i].y += part[u][i].y;
+                                    acc[i].z += part[u][i].z;
+                                    acc[i].w += part[u][i].w;
+                                }
+                            }
+                    }
+#pragma unroll
+                    for (int i = 0; i < kV; ++i) {
+                        const int v = et + kRoleThreads * (i0 + i);
+                        if (v >= nv) continue;
+                        const int c = v / (kTM / 4), r = (v - c * (kTM / 4)) * 4;
+                        ys[r * YS + c] = acc[i].x;
+                        ys[(r + 1) * YS + c] = acc[i].y;
+                        ys[(r + 2) * YS + c] = acc[i].z;
+                        ys[(r + 3) * YS + c] = acc[i].w;
+                    }
                 }
                 if (et == 0) tp.tickets[t] = 0u;
                 epi_sync();
@@ -682,7 +697,10 @@ size_t gemv_tc_smem(int bpad) { return 1024 + tc_fixed_bytes() + (size_t)tc_stag
 
 // CTAs for a plan: one per SM, but each with at least kMinCtaStages ring
 // stages of work (fewer, longer ranges: fewer partial tiles to add up).
-constexpr int kMinCtaStages = 4;
+#ifndef L2_TC_MIN_CTA_STAGES
+#define L2_TC_MIN_CTA_STAGES 4
+#endif
+constexpr int kMinCtaStages = L2_TC_MIN_CTA_STAGES;
 int gemv_tc_grid(int ntiles, int n, int ctas) {
     const long long T = (long long)ntiles * ((n + kSK - 1) / kSK);
     return (int)std::max<long long>(1, std::min<long long>(ctas, T / kMinCtaStages));
