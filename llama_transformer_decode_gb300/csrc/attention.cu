@@ -61,7 +61,15 @@ __device__ __forceinline__ void merge_state(float &m, float &l, float4 &acc, flo
 }
 }  // namespace
 
-template <int LP, int GQ>
+// RL = 1: the row-per-lane layout for 4 or 8 query heads per KV head and
+// head size 64 (16 cache rows per ring stage).  Lane (t, half) scores row t
+// for half of the group's heads over the whole head (K chunks read in a
+// lane-rotated order, conflict-free), the online softmax runs over the 16
+// rows with shuffles inside each half-warp (one exponential per row and
+// head), and the probabilities go through shared memory to the PV pass,
+// where lane l accumulates dimensions 2l, 2l+1 of every head.  Each cache row
+// costs a few dozen instructions instead of one shuffle tree per head.
+template <int LP, int GQ, int RL>
 __global__ void __launch_bounds__(kNWA * 32) attn_kernel(const AttnParams p) {
     constexpr int NT = kNWA * 32;
     constexpr int RPI = 32 / LP;  // cache rows a warp handles at once
@@ -74,6 +82,8 @@ __global__ void __launch_bounds__(kNWA * 32) attn_kernel(const AttnParams p) {
     const int hs = p.head_size, hs4 = hs >> 2;
     float4 *ring = reinterpret_cast<float4 *>(smem + hdr);                     // [kNWA][kAttStages][stage]
     float4 *accs = ring + kNWA * kAttStages * (kStageFloats / 4);              // [kNWA][GQ][hs4]
+    float *qs = reinterpret_cast<float *>(accs + kNWA * GQ * hs4);               // RL: [GQ][hs]
+    float *pbuf = qs + GQ * hs;                                                 // RL: [kNWA][16 + 1][GQ]
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int c = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
@@ -139,123 +149,232 @@ __global__ void __launch_bounds__(kNWA * 32) attn_kernel(const AttnParams p) {
 #pragma unroll 1
     for (int s = n_issued; s < kAttStages && ti < wt1; ++s) issue(s);
 
-    // query vectors of the group, one 16-byte word per lane and head
-    const int rg = lane / LP, c4 = lane % LP;
-    const bool lane_on = c4 < hs4;
-    float4 q4[GQ];
-    float m[GQ], l[GQ];
-    float4 acc[GQ];
-#pragma unroll
-    for (int j = 0; j < GQ; ++j) {
-        q4[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (j < nq && lane_on)
-            q4[j] = reinterpret_cast<const float4 *>(p.q + (size_t)b * p.dim + (size_t)(h0 + j) * hs)[c4];
-        m[j] = -CUDART_INF_F;
-        l[j] = 0.f;
-        acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-    float *dbg = p.dbg ? p.dbg + (((size_t)b * p.n_layers + p.layer) * H + h0) * p.seq_len : nullptr;
-
     bool ok = true;
     int k = 0;
-    int tc = wt0;
-#pragma unroll 1
-    for (; tc < wt1; ++k) {
-        const int s = k % kAttStages;
-        const int np = min(TP, wt1 - tc);
-        if (!mbar_wait(&wbars[s], (uint32_t)(k / kAttStages) & 1u, p.err)) {
-            ok = false;
-            break;
+    float *dbg = p.dbg ? p.dbg + (((size_t)b * p.n_layers + p.layer) * H + h0) * p.seq_len : nullptr;
+    if constexpr (RL == 1) {
+        constexpr int TPR = 16;            // cache rows per ring stage (head size 64)
+        constexpr int HS4 = 16;
+        constexpr int HPL = GQ / 2;        // heads per lane
+        // the group's query vectors, shared by all warps
+        for (int i = tid; i < GQ * 64; i += NT) {
+            const int j = i / 64, d = i % 64;
+            qs[i] = j < nq ? p.q[(size_t)b * p.dim + (size_t)(h0 + j) * 64 + d] : 0.f;
         }
-        const float4 *Ks = wring + (size_t)s * (kStageFloats / 4);
-        const float4 *Vs = Ks + (size_t)TP * hs4;
+        __syncthreads();
+        const float4 *qs4 = reinterpret_cast<const float4 *>(qs);
+        float *wp = pbuf + warp * (TPR + 1) * GQ;  // [TPR][GQ] probabilities, then [GQ] rescales
+        const int t = lane & (TPR - 1), jh = lane / TPR;
+        float m[HPL], l[HPL];
+        float acc[GQ][2];
+#pragma unroll
+        for (int jj = 0; jj < HPL; ++jj) {
+            m[jj] = -CUDART_INF_F;
+            l[jj] = 0.f;
+        }
+#pragma unroll
+        for (int j = 0; j < GQ; ++j) acc[j][0] = acc[j][1] = 0.f;
+        int tc = wt0;
 #pragma unroll 1
-        // Up to kPPG positions per lane group at a time: all their scores
-        // first (independent dot products and shuffles), then one online-
-        // softmax update per head (one rescale per group of positions).
-        for (int tt = 0; tt < np; tt += RPI * kPPG) {
-            float sc[kPPG][GQ];
-            float4 vv[kPPG];
+        for (; tc < wt1; ++k) {
+            const int s = k % kAttStages;
+            const int np = min(TP, wt1 - tc);
+            if (!mbar_wait(&wbars[s], (uint32_t)(k / kAttStages) & 1u, p.err)) {
+                ok = false;
+                break;
+            }
+            const float4 *Ks = wring + (size_t)s * (kStageFloats / 4);
+            const float2 *Vs2 = reinterpret_cast<const float2 *>(Ks + (size_t)TP * HS4);
+            // scores of row t for heads jh*HPL.., the row's 16-byte chunks in rotated order
+            const bool row_on = t < np;
+            float sc[HPL];
 #pragma unroll
-            for (int u = 0; u < kPPG; ++u) {
-                const int tl = tt + u * RPI + rg;
-                const bool row_on = tl < np;
-                float4 kv = make_float4(0.f, 0.f, 0.f, 0.f);
-                vv[u] = kv;
-                if (row_on && lane_on) {
-                    kv = Ks[tl * hs4 + c4];
-                    vv[u] = Vs[tl * hs4 + c4];
-                }
+            for (int jj = 0; jj < HPL; ++jj) sc[jj] = 0.f;
+            if (row_on) {
+                const float4 *Kr = Ks + t * HS4;
 #pragma unroll
-                for (int j = 0; j < GQ; ++j) {
-                    float d = dot4(q4[j], kv, 0.f);
+                for (int i = 0; i < HS4; ++i) {
+                    const int ch = (i + t) & (HS4 - 1);
+                    const float4 kv = Kr[ch];
 #pragma unroll
-                    for (int o = LP / 2; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
-                    sc[u][j] = row_on ? d * p.scale : -CUDART_INF_F;
-                    if (dbg && row_on && c4 == 0 && j < nq) dbg[(size_t)j * p.seq_len + tc + tl] = sc[u][j];
+                    for (int jj = 0; jj < HPL; ++jj) sc[jj] = dot4(qs4[(jh * HPL + jj) * HS4 + ch], kv, sc[jj]);
                 }
             }
+#pragma unroll
+            for (int jj = 0; jj < HPL; ++jj) {
+                sc[jj] = row_on ? sc[jj] * p.scale : -CUDART_INF_F;
+                if (dbg && row_on && jh * HPL + jj < nq) dbg[(size_t)(jh * HPL + jj) * p.seq_len + tc + t] = sc[jj];
+                // online softmax over the stage's rows (the 16 lanes of this half)
+                float mx = sc[jj];
+#pragma unroll
+                for (int o = TPR / 2; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+                const float mn = fmaxf(m[jj], mx);  // finite: row 0 of the stage is valid
+                const float corr = expf(m[jj] - mn);
+                const float pe = expf(sc[jj] - mn);
+                float ps = pe;
+#pragma unroll
+                for (int o = TPR / 2; o > 0; o >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
+                l[jj] = l[jj] * corr + ps;
+                m[jj] = mn;
+                wp[t * GQ + jh * HPL + jj] = pe;
+                if (t == 0) wp[TPR * GQ + jh * HPL + jj] = corr;
+            }
+            __syncwarp();
+            // PV: dimensions 2 lane, 2 lane + 1 of every head
 #pragma unroll
             for (int j = 0; j < GQ; ++j) {
-                if (j >= nq) continue;
-                float mx = sc[0][j];
+                const float c = wp[TPR * GQ + j];
+                acc[j][0] *= c;
+                acc[j][1] *= c;
+            }
+#pragma unroll 4
+            for (int tt = 0; tt < np; ++tt) {
+                const float2 v = Vs2[tt * 32 + lane];
 #pragma unroll
-                for (int u = 1; u < kPPG; ++u) mx = fmaxf(mx, sc[u][j]);
-                const float mn = fmaxf(m[j], mx);
-                if (mn == -CUDART_INF_F) continue;  // no position of this group
-                const float corr = expf(m[j] - mn);
-                float ps = 0.f;
-                float4 a = make_float4(acc[j].x * corr, acc[j].y * corr, acc[j].z * corr, acc[j].w * corr);
-#pragma unroll
-                for (int u = 0; u < kPPG; ++u) {
-                    const float pe = expf(sc[u][j] - mn);
-                    ps += pe;
-                    a.x = fmaf(pe, vv[u].x, a.x);
-                    a.y = fmaf(pe, vv[u].y, a.y);
-                    a.z = fmaf(pe, vv[u].z, a.z);
-                    a.w = fmaf(pe, vv[u].w, a.w);
+                for (int j = 0; j < GQ; ++j) {
+                    const float pj = wp[tt * GQ + j];
+                    acc[j][0] = fmaf(pj, v.x, acc[j][0]);
+                    acc[j][1] = fmaf(pj, v.y, acc[j][1]);
                 }
-                l[j] = l[j] * corr + ps;
-                acc[j] = a;
-                m[j] = mn;
+            }
+            __syncwarp();
+            tc += np;
+            if (ti < wt1) {
+                if (lane == 0) fence_proxy_async_smem();
+                issue(s);
             }
         }
-        __syncwarp();
-        tc += np;
-        if (ti < wt1) {
-            if (lane == 0) fence_proxy_async_smem();
-            issue(s);
+        if (!ok) {
+            for (int j = k + 1; j < n_issued; ++j)
+                (void)mbar_wait(&wbars[j % kAttStages], (uint32_t)(j / kAttStages) & 1u, p.err);
+            if (lane == 0) flags[0] = 1;
         }
-    }
-    if (!ok) {
-        for (int j = k + 1; j < n_issued; ++j)
-            (void)mbar_wait(&wbars[j % kAttStages], (uint32_t)(j / kAttStages) & 1u, p.err);
-        if (lane == 0) flags[0] = 1;
-    }
+        if (t == 0) {
+#pragma unroll
+            for (int jj = 0; jj < HPL; ++jj) {
+                mrg[(warp * GQ + jh * HPL + jj) * 2 + 0] = m[jj];
+                mrg[(warp * GQ + jh * HPL + jj) * 2 + 1] = l[jj];
+            }
+        }
+        float *accf = reinterpret_cast<float *>(accs);
+#pragma unroll
+        for (int j = 0; j < GQ; ++j)
+            *reinterpret_cast<float2 *>(accf + (size_t)(warp * GQ + j) * 64 + 2 * lane) = make_float2(acc[j][0], acc[j][1]);
+    } else {
+        // query vectors of the group, one 16-byte word per lane and head
+        const int rg = lane / LP, c4 = lane % LP;
+        const bool lane_on = c4 < hs4;
+        float4 q4[GQ];
+        float m[GQ], l[GQ];
+        float4 acc[GQ];
+    #pragma unroll
+        for (int j = 0; j < GQ; ++j) {
+            q4[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (j < nq && lane_on)
+                q4[j] = reinterpret_cast<const float4 *>(p.q + (size_t)b * p.dim + (size_t)(h0 + j) * hs)[c4];
+            m[j] = -CUDART_INF_F;
+            l[j] = 0.f;
+            acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        int tc = wt0;
+    #pragma unroll 1
+        for (; tc < wt1; ++k) {
+            const int s = k % kAttStages;
+            const int np = min(TP, wt1 - tc);
+            if (!mbar_wait(&wbars[s], (uint32_t)(k / kAttStages) & 1u, p.err)) {
+                ok = false;
+                break;
+            }
+            const float4 *Ks = wring + (size_t)s * (kStageFloats / 4);
+            const float4 *Vs = Ks + (size_t)TP * hs4;
+    #pragma unroll 1
+            // Up to kPPG positions per lane group at a time: all their scores
+            // first (independent dot products and shuffles), then one online-
+            // softmax update per head (one rescale per group of positions).
+            for (int tt = 0; tt < np; tt += RPI * kPPG) {
+                float sc[kPPG][GQ];
+                float4 vv[kPPG];
+    #pragma unroll
+                for (int u = 0; u < kPPG; ++u) {
+                    const int tl = tt + u * RPI + rg;
+                    const bool row_on = tl < np;
+                    float4 kv = make_float4(0.f, 0.f, 0.f, 0.f);
+                    vv[u] = kv;
+                    if (row_on && lane_on) {
+                        kv = Ks[tl * hs4 + c4];
+                        vv[u] = Vs[tl * hs4 + c4];
+                    }
+    #pragma unroll
+                    for (int j = 0; j < GQ; ++j) {
+                        float d = dot4(q4[j], kv, 0.f);
+    #pragma unroll
+                        for (int o = LP / 2; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+                        sc[u][j] = row_on ? d * p.scale : -CUDART_INF_F;
+                        if (dbg && row_on && c4 == 0 && j < nq) dbg[(size_t)j * p.seq_len + tc + tl] = sc[u][j];
+                    }
+                }
+    #pragma unroll
+                for (int j = 0; j < GQ; ++j) {
+                    if (j >= nq) continue;
+                    float mx = sc[0][j];
+    #pragma unroll
+                    for (int u = 1; u < kPPG; ++u) mx = fmaxf(mx, sc[u][j]);
+                    const float mn = fmaxf(m[j], mx);
+                    if (mn == -CUDART_INF_F) continue;  // no position of this group
+                    const float corr = expf(m[j] - mn);
+                    float ps = 0.f;
+                    float4 a = make_float4(acc[j].x * corr, acc[j].y * corr, acc[j].z * corr, acc[j].w * corr);
+    #pragma unroll
+                    for (int u = 0; u < kPPG; ++u) {
+                        const float pe = expf(sc[u][j] - mn);
+                        ps += pe;
+                        a.x = fmaf(pe, vv[u].x, a.x);
+                        a.y = fmaf(pe, vv[u].y, a.y);
+                        a.z = fmaf(pe, vv[u].z, a.z);
+                        a.w = fmaf(pe, vv[u].w, a.w);
+                    }
+                    l[j] = l[j] * corr + ps;
+                    acc[j] = a;
+                    m[j] = mn;
+                }
+            }
+            __syncwarp();
+            tc += np;
+            if (ti < wt1) {
+                if (lane == 0) fence_proxy_async_smem();
+                issue(s);
+            }
+        }
+        if (!ok) {
+            for (int j = k + 1; j < n_issued; ++j)
+                (void)mbar_wait(&wbars[j % kAttStages], (uint32_t)(j / kAttStages) & 1u, p.err);
+            if (lane == 0) flags[0] = 1;
+        }
 
-    // merge the row groups of the warp (lanes LP apart share a column word)
-#pragma unroll
-    for (int o = LP; o < 32; o <<= 1) {
-#pragma unroll
-        for (int j = 0; j < GQ; ++j) {
-            const float m2 = __shfl_xor_sync(0xffffffffu, m[j], o);
-            const float l2v = __shfl_xor_sync(0xffffffffu, l[j], o);
-            float4 a2;
-            a2.x = __shfl_xor_sync(0xffffffffu, acc[j].x, o);
-            a2.y = __shfl_xor_sync(0xffffffffu, acc[j].y, o);
-            a2.z = __shfl_xor_sync(0xffffffffu, acc[j].z, o);
-            a2.w = __shfl_xor_sync(0xffffffffu, acc[j].w, o);
-            merge_state(m[j], l[j], acc[j], m2, l2v, a2);
-        }
-    }
-    if (lane < LP) {
-#pragma unroll
-        for (int j = 0; j < GQ; ++j) {
-            if (lane == 0) {
-                mrg[(warp * GQ + j) * 2 + 0] = m[j];
-                mrg[(warp * GQ + j) * 2 + 1] = l[j];
+        // merge the row groups of the warp (lanes LP apart share a column word)
+    #pragma unroll
+        for (int o = LP; o < 32; o <<= 1) {
+    #pragma unroll
+            for (int j = 0; j < GQ; ++j) {
+                const float m2 = __shfl_xor_sync(0xffffffffu, m[j], o);
+                const float l2v = __shfl_xor_sync(0xffffffffu, l[j], o);
+                float4 a2;
+                a2.x = __shfl_xor_sync(0xffffffffu, acc[j].x, o);
+                a2.y = __shfl_xor_sync(0xffffffffu, acc[j].y, o);
+                a2.z = __shfl_xor_sync(0xffffffffu, acc[j].z, o);
+                a2.w = __shfl_xor_sync(0xffffffffu, acc[j].w, o);
+                merge_state(m[j], l[j], acc[j], m2, l2v, a2);
             }
-            if (lane_on) accs[(size_t)(warp * GQ + j) * hs4 + c4] = acc[j];
+        }
+        if (lane < LP) {
+    #pragma unroll
+            for (int j = 0; j < GQ; ++j) {
+                if (lane == 0) {
+                    mrg[(warp * GQ + j) * 2 + 0] = m[j];
+                    mrg[(warp * GQ + j) * 2 + 1] = l[j];
+                }
+                if (lane_on) accs[(size_t)(warp * GQ + j) * hs4 + c4] = acc[j];
+            }
         }
     }
     __syncthreads();
@@ -364,7 +483,7 @@ typedef void (*AttnFn)(const AttnParams);
 
 template <int LP, int GQ>
 AttnFn pick2() {
-    return attn_kernel<LP, GQ>;
+    return attn_kernel<LP, GQ, 0>;
 }
 
 template <int LP>
@@ -378,7 +497,11 @@ AttnFn pick1(int gq) {
     return nullptr;
 }
 
-AttnFn pick(int lp, int gq) {
+AttnFn pick(int lp, int gq, int rl) {
+    if (rl) {
+        if (lp != 16) return nullptr;
+        return gq == 8 ? attn_kernel<16, 8, 1> : gq == 4 ? attn_kernel<16, 4, 1> : nullptr;
+    }
     switch (lp) {
         case 1: return pick1<1>(gq);
         case 2: return pick1<2>(gq);
@@ -403,16 +526,21 @@ AttnLaunch attn_plan(int head_size, int n_heads, int n_kv_heads) {
     const int max_group = (n_heads + n_kv_heads - 1) / n_kv_heads;
     a.lp = pow2_at_least(hs4);
     a.gq = pow2_at_least(max_group);
+#ifndef L2_ATTN_ROW_LANE
+#define L2_ATTN_ROW_LANE 1
+#endif
+    a.rl = L2_ATTN_ROW_LANE && head_size == 64 && (a.gq == 4 || a.gq == 8) && kStageFloats == 2 * 16 * 64;
     a.threads = kNWA * 32;
     const size_t hdr = (8 * kNWA * kAttStages + 16 + 4 * (kNWA * a.gq * 2 + a.gq * 2) + 127) / 128 * 128;
     a.smem = hdr + (size_t)kNWA * kAttStages * kStageFloats * 4 + (size_t)kNWA * a.gq * hs4 * 16;
+    if (a.rl) a.smem += (size_t)a.gq * head_size * 4 + (size_t)kNWA * 17 * a.gq * 4;  // query vectors, probabilities
     a.ok = a.lp <= 32 && a.gq <= 8 && head_size % 4 == 0 && 2 * head_size <= kStageFloats;
     return a;
 }
 
 int attn_ctas_per_sm(const AttnLaunch &a) {
     int n = 0;
-    AttnFn fn = pick(a.lp, a.gq);
+    AttnFn fn = pick(a.lp, a.gq, a.rl);
     if (!fn || cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, a.threads, a.smem) != cudaSuccess) {
         cudaGetLastError();
         return 1;
@@ -425,14 +553,18 @@ cudaError_t attn_init() {
     static const int gqs[] = {1, 2, 4, 8};
     for (int lp : lps)
         for (int gq : gqs) {
-            cudaError_t e = cudaFuncSetAttribute(pick(lp, gq), cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+            cudaError_t e = cudaFuncSetAttribute(pick(lp, gq, 0), cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
             if (e != cudaSuccess) return e;
         }
+    for (int gq : {4, 8}) {
+        cudaError_t e = cudaFuncSetAttribute(pick(16, gq, 1), cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+        if (e != cudaSuccess) return e;
+    }
     return cudaSuccess;
 }
 
 cudaError_t launch_attn(const AttnLaunch &a, const AttnParams &p, int batch, cudaStream_t stream, bool pdl) {
-    AttnFn fn = pick(a.lp, a.gq);
+    AttnFn fn = pick(a.lp, a.gq, a.rl);
     if (!fn) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.n_chunks, p.n_kv_heads, batch);

@@ -61,6 +61,7 @@ cudaError_t launch_gemv_tc(int mode, const TcParams &tp, int grid, cudaStream_t 
 struct AttnLaunch {
     int lp;       // lanes per cache row (power of two)
     int gq;       // query heads per KV head, rounded up to a power of two
+    int rl;       // 1: row-per-lane layout (head size 64, 4 or 8 heads per KV head)
     int threads;
     size_t smem;
     bool ok;      // this head size / grouping is supported
