@@ -91,9 +91,8 @@ __global__ void __launch_bounds__(kNWA * 32) attn_kernel(const AttnParams p) {
     const int P = pos + 1;
     int chunk = p.min_chunk;
     if (p.capacity > 0) {
-        // spread the positions of every slot over the resident CTAs
-        long long total = 0;
-        for (int b2 = 0; b2 < (int)gridDim.z; ++b2) total += p.step->pos[b2] + 1;
+        // spread the positions of every row over the resident CTAs (the host sums them)
+        const long long total = p.step->attn_total;
         const long long per = (total * p.n_kv_heads + p.capacity - 1) / p.capacity;
         if (per > chunk) chunk = (int)per;
     }

@@ -340,9 +340,11 @@ AttnParams attn_params(const l2_ctx *c, int layer, int batch) {
     int nc = attn_chunks_for(c, batch);
     a.capacity = 0;
     if (batch > 1) {
-        // slots sit at different positions: size the chunks on the device
-        nc = ceil_div(p.seq_len, kMinChunk);
+        // Rows sit at different positions: the chunk size is set on the device from the
+        // step's total (capacity-balanced), so a row never uses more than about
+        // capacity / n_kv_heads + 1 chunks; the grid stops there.
         a.capacity = c->attn_per_sm * c->num_sms;
+        nc = std::min(ceil_div(p.seq_len, kMinChunk), ceil_div(a.capacity, p.n_kv_heads) + 1);
     }
     if (nc > c->attn_chunks) nc = c->attn_chunks;
     a.n_chunks = nc;
@@ -777,12 +779,15 @@ int submit(l2_ctx *c, int B, const int *tokens, const int *pos, float *logits_ou
     c->ring_next = (i + 1) % kRing;
     if (c->ring_used[i]) L2_CUDA(c, cudaEventSynchronize(c->ring_ev[i]));
     StepDev &sh = c->step_host[i];
+    int total = 0;
     for (int b = 0; b < B; ++b) {
         sh.token[b] = tokens_dev ? 0 : tokens[b];
         sh.pos[b] = pos[b];
         sh.slot[b] = prefill_slot >= 0 ? prefill_slot : b;
         sh.stable[b] = prefill_slot >= 0 ? pos[0] : pos[b];
+        total += pos[b] + 1;
     }
+    sh.attn_total = total;
     sh.logits_out = logits_out;
     sh.B = B;
     sh.sync_count = 0;
@@ -1241,6 +1246,7 @@ extern "C" int l2_forward_static(l2_ctx *c, int token, int pos, float *logits_ou
     sh.pos[0] = pos;
     sh.slot[0] = 0;
     sh.stable[0] = pos;
+    sh.attn_total = pos + 1;
     sh.logits_out = logits_out;
     sh.B = 1;
     L2_CUDA(c, cudaMemcpyAsync(c->step_dev, &sh, sizeof(StepDev), cudaMemcpyHostToDevice, c->stream));

@@ -23,7 +23,8 @@ struct StepDev {
     float *logits_out;  // caller's device buffer [B][vocab] or nullptr
     int B;
     unsigned sync_count;  // grid-barrier arrivals of the persistent step kernel (zero at the copy)
-    int pad_[2];
+    int attn_total;       // sum over the step's rows of pos[b] + 1 (attention chunk sizing)
+    int pad_;
 };
 
 // The fused GEMV kernel's modes (prologue / epilogue around y = W v).

@@ -81,6 +81,16 @@ def test_group_of_eight_batched_16():
     run_batched(wl, B, 12, offsets, flags=pkg.L2_FLAG_DEBUG, check_att_every=4)
 
 
+def test_group_of_four_batched():
+    # 4 query heads per KV head, head_size 64: the row-per-lane attention with 2 heads per lane;
+    # positions that end mid-way through a 16-row ring stage
+    wl = WORKLOADS["batched_1b"].replace(name="g4", dim=512, hidden_dim=1376, n_layers=2, n_heads=8,
+                                         n_kv_heads=2, vocab_size=1000, seq_len=256, seed_override=92)
+    B = 6
+    offsets = [0, 1, 15, 16, 33, 200]
+    run_batched(wl, B, 10, offsets, flags=pkg.L2_FLAG_DEBUG, check_att_every=3)
+
+
 def test_ragged_batched_64():
     wl = WORKLOADS["tiny"].replace(name="ragged64", dim=60, hidden_dim=92, n_layers=2, n_heads=5,
                                    n_kv_heads=2, vocab_size=301, seq_len=96, shared_wcls=False,
