@@ -12,7 +12,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libl2decode.so")
-SOURCES = ("gemv.cu", "gemv_batched.cu", "gemv_tc.cu", "attention.cu", "step_kernel.cu", "sample.cu", "l2_api.cu")
+SOURCES = ("gemv.cu", "gemv_batched.cu", "gemv_tc.cu", "attention.cu", "attn_prefill.cu", "step_kernel.cu", "sample.cu",
+           "l2_api.cu")
 HEADERS = ("l2_device.cuh", "l2_params.h", "l2_kernels.h")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-lineinfo", "-O3", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O3"]

@@ -112,6 +112,8 @@ struct l2_ctx {
     int ring_next = 0;
 
     cudaGraphExec_t graph[kMaxBatch + 1] = {};
+    cudaGraphExec_t graph_pf[kMaxBatch + 1] = {};  // prompt chunks (prefill attention)
+    bool attn_pf = false;                           // the prefill attention kernel serves this shape
 
     AttnLaunch attn{};
     int attn_chunks = 1;
@@ -178,6 +180,11 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 void free_all(l2_ctx *c) {
     if (c->stream) cudaStreamSynchronize(c->stream);
     for (auto &g : c->graph)
+        if (g) {
+            cudaGraphExecDestroy(g);
+            g = nullptr;
+        }
+    for (auto &g : c->graph_pf)
         if (g) {
             cudaGraphExecDestroy(g);
             g = nullptr;
@@ -672,7 +679,19 @@ int plan_persistent(l2_ctx *c) {
     return L2_OK;
 }
 
-cudaError_t launch_op(l2_ctx *c, int op, int layer, int batch, cudaStream_t s, bool pdl) {
+// The prompt-chunk attention reads each K/V tile once per 16 query vectors but
+// walks all of a block's positions in one CTA: it beats the per-row kernel
+// (which shares a tile among a group's query heads and splits positions over
+// the SMs) when groups are small and the chunk gives enough CTAs.
+bool attn_prefill_pays(const l2_ctx *c, int batch) {
+    if (!c->attn_pf || batch < 2) return false;
+    const int gq = c->cfg.n_heads / c->cfg.n_kv_heads;
+    const int ctas = ceil_div(batch, 16 / gq) * c->cfg.n_kv_heads;
+    return gq <= 2 && 2 * ctas >= c->num_sms;
+}
+
+// prefill: the step is a prompt chunk (rows of one slot at consecutive positions).
+cudaError_t launch_op(l2_ctx *c, int op, int layer, int batch, cudaStream_t s, bool pdl, bool prefill = false) {
     if (batch > 1 && op != 1) {
         const GemvPlan *pl[] = {&c->plan_qkv, nullptr, &c->plan_wo, &c->plan_w13, &c->plan_w2, &c->plan_cls};
         const int k = op == 0 ? 0 : op - 1;  // index into the batch set's plans
@@ -685,6 +704,7 @@ cudaError_t launch_op(l2_ctx *c, int op, int layer, int batch, cudaStream_t s, b
         }
         case 1: {
             AttnParams a = attn_params(c, layer, batch);
+            if (prefill && attn_prefill_pays(c, batch)) return launch_attn_prefill(a, batch, s, pdl);
             return launch_attn(c->attn, a, batch, s, pdl);
         }
         case 2: {
@@ -707,23 +727,24 @@ cudaError_t launch_op(l2_ctx *c, int op, int layer, int batch, cudaStream_t s, b
     return cudaErrorInvalidValue;
 }
 
-cudaError_t enqueue_step(l2_ctx *c, int batch, cudaStream_t s) {
+cudaError_t enqueue_step(l2_ctx *c, int batch, cudaStream_t s, bool prefill = false) {
     const bool pdl = !(c->flags & L2_FLAG_NO_PDL);
     cudaError_t e;
     for (int l = 0; l < c->cfg.n_layers; ++l)
         for (int op = 0; op < 5; ++op)
-            if ((e = launch_op(c, op, l, batch, s, pdl)) != cudaSuccess) return e;
-    return launch_op(c, 5, 0, batch, s, pdl);
+            if ((e = launch_op(c, op, l, batch, s, pdl, prefill)) != cudaSuccess) return e;
+    return launch_op(c, 5, 0, batch, s, pdl, prefill);
 }
 
-int get_graph(l2_ctx *c, int batch, cudaGraphExec_t *out) {
-    if (c->graph[batch]) {
-        *out = c->graph[batch];
+int get_graph(l2_ctx *c, int batch, bool prefill, cudaGraphExec_t *out) {
+    cudaGraphExec_t *slot = prefill ? &c->graph_pf[batch] : &c->graph[batch];
+    if (*slot) {
+        *out = *slot;
         return L2_OK;
     }
     cudaGraph_t g = nullptr;
     L2_CUDA(c, cudaStreamBeginCapture(c->cap_stream, cudaStreamCaptureModeThreadLocal));
-    cudaError_t e = enqueue_step(c, batch, c->cap_stream);
+    cudaError_t e = enqueue_step(c, batch, c->cap_stream, prefill);
     cudaError_t e2 = cudaStreamEndCapture(c->cap_stream, &g);
     if (e != cudaSuccess) {
         if (g) cudaGraphDestroy(g);
@@ -734,7 +755,7 @@ int get_graph(l2_ctx *c, int batch, cudaGraphExec_t *out) {
     e = cudaGraphInstantiate(&ex, g, 0);
     cudaGraphDestroy(g);
     if (e != cudaSuccess) return cuda_fail(c, e, "cudaGraphInstantiate");
-    c->graph[batch] = ex;
+    *slot = ex;
     *out = ex;
     return L2_OK;
 }
@@ -802,10 +823,10 @@ int submit(l2_ctx *c, int B, const int *tokens, const int *pos, float *logits_ou
     if (B == 1 && c->persist && sh.slot[0] == 0) {
         L2_CUDA(c, launch_step_kernel(c->persist_gq, c->sp, c->num_sms, c->persist_smem, c->stream));
     } else if (c->flags & L2_FLAG_NO_GRAPH) {
-        L2_CUDA(c, enqueue_step(c, B, c->stream));
+        L2_CUDA(c, enqueue_step(c, B, c->stream, prefill_slot >= 0));
     } else {
         cudaGraphExec_t g = nullptr;
-        int rc = get_graph(c, B, &g);
+        int rc = get_graph(c, B, prefill_slot >= 0, &g);
         if (rc != L2_OK) return rc;
         L2_CUDA(c, cudaGraphLaunch(g, c->stream));
     }
@@ -870,6 +891,8 @@ int l2_create(const L2Config *config, const L2Weights *weights, int max_batch, u
     CREATE_CUDA(gemv_init());
     CREATE_CUDA(gemv_batched_init());
     CREATE_CUDA(attn_init());
+    c->attn_pf = !(flags & L2_FLAG_DEBUG) && attn_prefill_supported(c->head_size, p.n_heads, p.n_kv_heads);
+    if (c->attn_pf) CREATE_CUDA(attn_prefill_init());
     c->attn_per_sm = attn_ctas_per_sm(c->attn);
 
     if (cuda_stream) {

@@ -67,6 +67,10 @@ struct AttnLaunch {
     bool ok;      // this head size / grouping is supported
 };
 AttnLaunch attn_plan(int head_size, int n_heads, int n_kv_heads);
+// Attention of a prompt chunk (attn_prefill.cu): rows of one slot at consecutive positions.
+bool attn_prefill_supported(int head_size, int n_heads, int n_kv_heads);
+cudaError_t attn_prefill_init();
+cudaError_t launch_attn_prefill(const AttnParams &p, int rows, cudaStream_t stream, bool pdl);
 cudaError_t attn_init();
 // Attention CTAs that can be resident on one SM (registers, shared memory, threads).
 int attn_ctas_per_sm(const AttnLaunch &a);
