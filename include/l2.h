@@ -194,9 +194,12 @@ int l2_launch_op(l2_ctx *ctx, int op, int layer, int count);
  * at a time with L2_FLAG_DEBUG) as one batched step each: the rows of a
  * chunk share the weights read and read the cache rows the chunk's earlier
  * rows write.  Any handle can prefill in 64-row chunks: the per-row buffers
- * are sized for 64 rows, the KV cache for max_batch slots.  The pages have no counterpart
- * (their loop feeds a prompt one token per step); the R/Keras page's
- * full-sequence causal forward computes the same values.
+ * are sized for 64 rows, the KV cache for max_batch slots.  Chunks of 16 or
+ * more rows run their matrix products on the tensor cores (unless
+ * L2_FLAG_NO_TC), and where it pays their attention reads each cache tile
+ * once per 16 query vectors instead of once per row.  The pages have no
+ * counterpart (their loop feeds a prompt one token per step); the R/Keras
+ * page's full-sequence causal forward computes the same values.
  */
 int l2_prefill(l2_ctx *ctx, int slot, int T, const int *tokens, int pos0, float *logits_out);
 
