@@ -42,14 +42,14 @@ FALLBACK_HBM_GBS = 6800.0
 # the dominant kernel, from the ncu capture summarised in
 # profiles/gemv_w13_llama2_7b.md, valid only for the kernel source whose
 # sha256 prefix is recorded beside it.
-W13_NCU_TRAFFIC = (364191744, "f749e57f10155989")  # (bytes per launch, gemv.cu sha256 prefix)
+W13_NCU_TRAFFIC = (363805696, "0bcb08e0f8b8c52c")  # (bytes per launch, gemv.cu sha256 prefix)
 
 
-def weight_bytes(wl) -> int:
-    """Weight bytes one step streams: every matrix, the RMSNorm gains, the
-    classifier, one embedding row."""
+def weight_bytes(wl, wb: int = 4) -> int:
+    """Weight bytes one step streams: every matrix (wb bytes per weight: 4
+    fp32, 2 bf16), the RMSNorm gains, the classifier, one embedding row (fp32)."""
     d, h, L, kv, V = wl.dim, wl.hidden_dim, wl.n_layers, wl.kv_dim, wl.vocab_size
-    return 4 * (L * (2 * d * d + 2 * kv * d + 3 * d * h + 2 * d) + V * d + 2 * d)
+    return wb * (L * (2 * d * d + 2 * kv * d + 3 * d * h) + V * d) + 4 * (L * 2 * d + 2 * d)
 
 
 def kv_bytes(wl, pos: int) -> int:
@@ -57,10 +57,10 @@ def kv_bytes(wl, pos: int) -> int:
     return 4 * wl.n_layers * 2 * wl.kv_dim * (pos + 1)
 
 
-def w13_bytes(wl) -> int:
-    """Algorithmic bytes of one rmsnorm+W1/W3+SwiGLU launch: both matrices,
-    the gain vector, x in and hb out."""
-    return 4 * (2 * wl.hidden_dim * wl.dim + 2 * wl.dim + wl.hidden_dim)
+def w13_bytes(wl, wb: int = 4) -> int:
+    """Algorithmic bytes of one rmsnorm+W1/W3+SwiGLU launch: both matrices
+    (wb bytes per weight), the gain vector, x in and hb out."""
+    return wb * 2 * wl.hidden_dim * wl.dim + 4 * (2 * wl.dim + wl.hidden_dim)
 
 
 def measured_peaks() -> dict:
@@ -247,11 +247,14 @@ def run_ours(args, wl):
     props = torch.cuda.get_device_properties(local_rank)
     uuid = str(props.uuid)
     B = args.batch
+    bf16 = args.weights == "bf16"
+    wb = 2 if bf16 else 4
 
     cpu_leg = rank == 0 and world == 1 and not args.no_cpu
     w_dev, host_w = load_weights_device(wl, keep_host=cpu_leg)
     stream = torch.cuda.Stream()
-    dec = pkg.Decoder(wl.config_tuple(), w_dev, max_batch=B, stream=stream)
+    dec = pkg.Decoder(wl.config_tuple(), w_dev, max_batch=B, stream=stream,
+                      flags=pkg.L2_FLAG_BF16_WEIGHTS if bf16 else 0)
     S = wl.seq_len
     streams = [synth.token_stream(wl, b, S) for b in range(B)]
     out = torch.empty((B, wl.vocab_size), device="cuda")
@@ -319,7 +322,7 @@ def run_ours(args, wl):
     ms = max_over_ranks(ev0.elapsed_time(ev1))
     value = world * B * args.steps / (ms / 1000.0)
     timed_pos = [positions(s) for s in range(args.warmup, args.warmup + args.steps)]
-    bytes_total = sum(weight_bytes(wl) + sum(kv_bytes(wl, p) for p in pos) for pos in timed_pos)
+    bytes_total = sum(weight_bytes(wl, wb) + sum(kv_bytes(wl, p) for p in pos) for pos in timed_pos)
     step_gbs = bytes_total / (ms / 1000.0) / 1e9
 
     # ---- rate at chosen positions (cache rows before them imported) ----
@@ -338,7 +341,7 @@ def run_ours(args, wl):
             a1.record(stream)
             a1.synchronize()
             t = a0.elapsed_time(a1) / 6
-            gb = sum(weight_bytes(wl) + kv_bytes(wl, p) for p in range(p0 + 2, p0 + 8)) / 6
+            gb = sum(weight_bytes(wl, wb) + kv_bytes(wl, p) for p in range(p0 + 2, p0 + 8)) / 6
             per_pos[str(p0 + 2)] = {"tokens_per_s": 1000.0 / t, "ms_per_step": t, "gbs": gb / t / 1e6}
         dec.sync()
 
@@ -369,15 +372,16 @@ def run_ours(args, wl):
         k1.record(stream)
         k1.synchronize()
         w13_ms = k0.elapsed_time(k1) / (reps * wl.n_layers)
-        achieved = w13_bytes(wl) / (w13_ms / 1000.0) / 1e9
+        achieved = w13_bytes(wl, wb) / (w13_ms / 1000.0) / 1e9
         traffic = None
-        if W13_NCU_TRAFFIC is not None and (wl.dim, wl.hidden_dim) == (4096, 11008):
+        if W13_NCU_TRAFFIC is not None and (wl.dim, wl.hidden_dim) == (4096, 11008) and not bf16:
             src = open(os.path.join(ROOT, "llama_transformer_decode_gb300", "csrc", "gemv.cu"), "rb").read()
             if hashlib.sha256(src).hexdigest().startswith(W13_NCU_TRAFFIC[1]):
                 traffic = W13_NCU_TRAFFIC[0]
         roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                    "traffic": traffic, "kernel": "gemv_kernel<8,3,512,GEMV_W13> (rmsnorm + W1/W3 + SwiGLU)",
-                    "bytes_per_launch": w13_bytes(wl), "us_per_launch": w13_ms * 1000.0,
+                    "traffic": traffic,
+                    "kernel": "gemv_kernel<8,3,512,GEMV_W13> (rmsnorm + W1/W3 + SwiGLU)" + (", bf16 weights" if bf16 else ""),
+                    "bytes_per_launch": w13_bytes(wl, wb), "us_per_launch": w13_ms * 1000.0,
                     "timing": "CUDA events around standalone launches on the decoder's stream, layers cycled",
                     "peak_source": peak_src + " (MEASURED_PEAKS.json hbm_gbs, copy bandwidth)"}
     else:
@@ -412,8 +416,12 @@ def run_ours(args, wl):
     cfg = config_of(wl, B)
     cfg["positions"] = (f"{timed_pos[0][0]}..{timed_pos[-1][0]}" if B == 1 else
                         f"slot b from floor(b*{S}/{B}) + {args.warmup}, {args.steps} steps, wrapping at {S}")
+    metric = METRIC if B == 1 else METRIC.replace("at batch 1", f"at batch {B}")
+    if bf16:
+        metric = metric.replace("at batch 1", "at batch 1 with bf16 weights")
+        cfg["weights"] = "seeded random (synth); matrices streamed as bf16 (rounded once on the device), fp32 arithmetic"
     line = {
-        "metric": METRIC if B == 1 else METRIC.replace("at batch 1", f"at batch {B}"),
+        "metric": metric,
         "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded random weights and tokens)",
@@ -441,6 +449,8 @@ def main(argv=None):
     ap.add_argument("--workload", default="llama2_7b", choices=sorted(WORKLOADS))
     ap.add_argument("--batch", type=int, default=1,
                     help="independent sequences per step at staggered positions (batched_1b: 16 or 64)")
+    ap.add_argument("--weights", choices=("f32", "bf16"), default="f32",
+                    help="bf16: matrices streamed as bf16 (L2_FLAG_BF16_WEIGHTS; batch 1 only)")
     ap.add_argument("--layers", type=int, default=None,
                     help="decode only the first N layers of the workload (a smaller case, e.g. for profiling)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-baseline leg")
@@ -453,6 +463,8 @@ def main(argv=None):
         ap.error("--warmup must be at least 3")
     if not 1 <= args.batch <= 64:
         ap.error("--batch must be in 1..64")
+    if args.weights == "bf16" and (args.batch != 1 or args.impl != "ours"):
+        ap.error("--weights bf16 is a batch-1 option of this implementation")
     wl = WORKLOADS[args.workload]
     if args.layers is not None:
         if not 1 <= args.layers <= wl.n_layers:

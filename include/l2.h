@@ -60,6 +60,16 @@ extern "C" {
  * hi*lo + lo*hi, fp32-level accuracy); with this flag they stay on the CUDA
  * cores. */
 #define L2_FLAG_NO_TC 0x10u
+/* Reduced-precision weight streaming: the handle converts the weight
+ * matrices (Wq, Wk, Wv, Wo, W1, W2, W3, Wcls) once to bf16 (round to nearest
+ * even) in its own device memory, and each step streams those -- half the
+ * bytes of fp32.  Products and sums stay fp32 (each bf16 weight widens
+ * exactly), as do the embedding table, the RMSNorm gains, activations and the
+ * KV cache; the results are those of the model with bf16-rounded matrices.
+ * Batch-1 decode only: max_batch must be 1 (else L2_EINVAL), prompts are fed
+ * one token per step, L2_FLAG_PERSIST is refused, and dim and hidden_dim must
+ * be divisible by 8. */
+#define L2_FLAG_BF16_WEIGHTS 0x20u
 
 /* Model shape: the pages' Config struct ("run.c", Config; walkthrough §2).
  * head_size = dim / n_heads, kv_dim = dim * n_kv_heads / n_heads. */

@@ -25,6 +25,11 @@
 //   - the weight copies for the first stages are issued before
 //     griddepcontrol.wait, so under programmatic dependent launch they overlap
 //     the tail of the previous kernel.
+// Weights are fp32 (WT = 0, 4 per 16-byte word) or bf16 (WT = 1, a handle
+// created with L2_FLAG_BF16_WEIGHTS: 8 per word, each widened exactly to
+// fp32 -- a bf16 value is the top half of an fp32 -- and multiplied into the
+// fp32 input vector with fp32 accumulation); everything else is fp32.
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include "l2_device.cuh"
@@ -101,15 +106,32 @@ __host__ __device__ constexpr size_t fixed_bytes() {
 
 __device__ __forceinline__ float silu(float v) { return v / (1.0f + expf(-v)); }
 
+// 8 bf16 weights (in memory order: low half of w.x first) times 8 fp32
+// inputs: four independent pairs, added as a tree, so the chain a word adds to
+// the running sum is one addition (the word carries twice the fp32 products).
+__device__ __forceinline__ float dot_bf16x8(uint4 w, float4 x0, float4 x1, float acc) {
+    const float p0 = fmaf(__uint_as_float(w.x & 0xffff0000u), x0.y, __uint_as_float(w.x << 16) * x0.x);
+    const float p1 = fmaf(__uint_as_float(w.y & 0xffff0000u), x0.w, __uint_as_float(w.y << 16) * x0.z);
+    const float p2 = fmaf(__uint_as_float(w.z & 0xffff0000u), x1.y, __uint_as_float(w.z << 16) * x1.x);
+    const float p3 = fmaf(__uint_as_float(w.w & 0xffff0000u), x1.w, __uint_as_float(w.w << 16) * x1.z);
+    return acc + ((p0 + p1) + (p2 + p3));
+}
+
 }  // namespace
 
-template <int NW, int STAGES, int CH4, int MODE>
+template <int NW, int STAGES, int CH4, int MODE, int WT>
 __global__ void __launch_bounds__(NW * 32, 1) gemv_kernel(const GemvParams p) {
     constexpr int NT = NW * 32;
     extern __shared__ __align__(128) unsigned char smem[];
     auto &fx = *reinterpret_cast<GemvFixed<NW, STAGES> *>(smem);
     float4 *ring = reinterpret_cast<float4 *>(smem + fixed_bytes<NW, STAGES>());
-    const int n4 = p.n >> 2;
+    const int n4 = p.n >> 2;             // input vector: 16-byte words
+    const int nw = WT ? p.n >> 3 : n4;   // weight row: 16-byte words
+    // the first weight word of row `row` of a matrix
+    auto row_ptr = [&](const float *mat, size_t row) {
+        return WT ? reinterpret_cast<const float4 *>(reinterpret_cast<const unsigned short *>(mat) + row * p.n)
+                  : reinterpret_cast<const float4 *>(mat + row * p.n);
+    };
     float4 *xs = ring + NW * STAGES * CH4;
     float *ys = reinterpret_cast<float *>(xs + n4);
 
@@ -132,20 +154,18 @@ __global__ void __launch_bounds__(NW * 32, 1) gemv_kernel(const GemvParams p) {
                 for (int m = 0; m < 3; ++m) {
                     int lo = max(vr0, b0), hi = min(vr0 + R, b0 + rws[m]);
                     if (lo < hi) {
-                        fx.pieces[np] = {reinterpret_cast<const float4 *>(mats[m] + (size_t)(lo - b0) * p.n), f,
-                                         hi - lo, lo - vr0};
-                        f += (long long)(hi - lo) * n4;
+                        fx.pieces[np] = {row_ptr(mats[m], (size_t)(lo - b0)), f, hi - lo, lo - vr0};
+                        f += (long long)(hi - lo) * nw;
                         ++np;
                     }
                     b0 += rws[m];
                 }
             } else if (MODE == GEMV_W13) {
-                fx.pieces[0] = {reinterpret_cast<const float4 *>(p.mat0 + (size_t)vr0 * p.n), 0, R, 0};
-                fx.pieces[1] = {reinterpret_cast<const float4 *>(p.mat1 + (size_t)vr0 * p.n), (long long)R * n4, R,
-                                R};
+                fx.pieces[0] = {row_ptr(p.mat0, (size_t)vr0), 0, R, 0};
+                fx.pieces[1] = {row_ptr(p.mat1, (size_t)vr0), (long long)R * nw, R, R};
                 np = 2;
             } else {
-                fx.pieces[0] = {reinterpret_cast<const float4 *>(p.mat0 + (size_t)vr0 * p.n), 0, R, 0};
+                fx.pieces[0] = {row_ptr(p.mat0, (size_t)vr0), 0, R, 0};
                 np = 1;
             }
         }
@@ -162,7 +182,7 @@ __global__ void __launch_bounds__(NW * 32, 1) gemv_kernel(const GemvParams p) {
 
     const int np = fx.npieces;
     long long F = 0;
-    for (int i = 0; i < np; ++i) F += (long long)fx.pieces[i].rows * n4;
+    for (int i = 0; i < np; ++i) F += (long long)fx.pieces[i].rows * nw;
     // Warp ranges start on 128-byte boundaries of the stream (whole cache lines
     // whenever the pieces themselves start on one).
     const long long fb = (F * warp / NW) & ~7LL;
@@ -172,7 +192,7 @@ __global__ void __launch_bounds__(NW * 32, 1) gemv_kernel(const GemvParams p) {
     auto chunk_at = [&](long long f, int &pi, int &len) {
         pi = 0;
         while (pi + 1 < np && f >= fx.pieces[pi + 1].f0) ++pi;
-        const long long pend = fx.pieces[pi].f0 + (long long)fx.pieces[pi].rows * n4;
+        const long long pend = fx.pieces[pi].f0 + (long long)fx.pieces[pi].rows * nw;
         long long l = fe - f;
         if (pend - f < l) l = pend - f;
         if (l > CH4) l = CH4;
@@ -273,25 +293,32 @@ __global__ void __launch_bounds__(NW * 32, 1) gemv_kernel(const GemvParams p) {
         const int lf = (int)(fc - pc.f0), lend = lf + len;
         if (pi != cpi) {
             cpi = pi;
-            r = lf / n4;
-            rs = r * n4;
-            re = rs + n4;
+            r = lf / nw;
+            rs = r * nw;
+            re = rs + nw;
         }
         int a = lf;
         while (a < lend) {
             if (a == re) {
                 ++r;
                 rs = re;
-                re += n4;
+                re += nw;
             }
             const int b = lend < re ? lend : re;
             if (a == rs) started = true;
             cur_row = pc.yoff + r;
             const float4 *wr = buf + (a - lf);
-            const float4 *xr = xs + (a - rs);
             const int cnt = b - a;
+            if (WT) {
+                const float4 *xr = xs + 2 * (a - rs);
 #pragma unroll 4
-            for (int i = lane; i < cnt; i += 32) acc = dot4(wr[i], xr[i], acc);
+                for (int i = lane; i < cnt; i += 32)
+                    acc = dot_bf16x8(reinterpret_cast<const uint4 *>(wr)[i], xr[2 * i], xr[2 * i + 1], acc);
+            } else {
+                const float4 *xr = xs + (a - rs);
+#pragma unroll 4
+                for (int i = lane; i < cnt; i += 32) acc = dot4(wr[i], xr[i], acc);
+            }
             pending = true;
             if (b == re) {
                 const float v = warp_sum(acc);
@@ -390,6 +417,19 @@ __global__ void __launch_bounds__(NW * 32, 1) gemv_kernel(const GemvParams p) {
 
 // ---------------------------------------------------------------- host side
 
+__global__ void f32_to_bf16_kernel(const float *src, unsigned short *dst, size_t n) {
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+        const __nv_bfloat16 b = __float2bfloat16_rn(src[i]);
+        dst[i] = *reinterpret_cast<const unsigned short *>(&b);
+    }
+}
+
+cudaError_t convert_to_bf16(const float *src, unsigned short *dst, size_t n, cudaStream_t stream) {
+    if (n == 0) return cudaSuccess;
+    f32_to_bf16_kernel<<<1024, 256, 0, stream>>>(src, dst, n);
+    return cudaGetLastError();
+}
+
 
 namespace {
 struct Shape {
@@ -399,30 +439,33 @@ constexpr Shape kShapes[kGemvShapes] = {{L2_GEMV_WARPS, L2_GEMV_STAGES, L2_GEMV_
                                         {L2_GEMV_WARPS_B, L2_GEMV_STAGES_B, L2_GEMV_CHUNK_WORDS_B},
                                         {8, 2, 512}};
 
-template <int S, int MODE>
+template <int S, int MODE, int WT>
 void *kernel_ptr() {
-    return reinterpret_cast<void *>(gemv_kernel<kShapes[S].nw, kShapes[S].stages, kShapes[S].ch4, MODE>);
+    return reinterpret_cast<void *>(gemv_kernel<kShapes[S].nw, kShapes[S].stages, kShapes[S].ch4, MODE, WT>);
 }
 
-template <int S>
+template <int S, int WT>
 void *kernel_for(int mode) {
     switch (mode) {
-        case GEMV_QKV: return kernel_ptr<S, GEMV_QKV>();
-        case GEMV_RESID: return kernel_ptr<S, GEMV_RESID>();
-        case GEMV_W13: return kernel_ptr<S, GEMV_W13>();
-        case GEMV_CLS: return kernel_ptr<S, GEMV_CLS>();
+        case GEMV_QKV: return kernel_ptr<S, GEMV_QKV, WT>();
+        case GEMV_RESID: return kernel_ptr<S, GEMV_RESID, WT>();
+        case GEMV_W13: return kernel_ptr<S, GEMV_W13, WT>();
+        case GEMV_CLS: return kernel_ptr<S, GEMV_CLS, WT>();
     }
     return nullptr;
 }
 
+template <int WT>
 void *kernel_for(int shape, int mode) {
     switch (shape) {
-        case 0: return kernel_for<0>(mode);
-        case 1: return kernel_for<1>(mode);
-        case 2: return kernel_for<2>(mode);
+        case 0: return kernel_for<0, WT>(mode);
+        case 1: return kernel_for<1, WT>(mode);
+        case 2: return kernel_for<2, WT>(mode);
     }
     return nullptr;
 }
+
+void *kernel_for(int shape, int mode, int wt) { return wt ? kernel_for<1>(shape, mode) : kernel_for<0>(shape, mode); }
 
 template <int S>
 size_t fixed_of() {
@@ -454,19 +497,20 @@ int gemv_pick_shape(int n, int ymax, size_t *smem) {
 }
 
 cudaError_t gemv_init() {
-    for (int sh = 0; sh < kGemvShapes; ++sh)
-        for (int mode = GEMV_QKV; mode <= GEMV_CLS; ++mode) {
-            cudaError_t e =
-                cudaFuncSetAttribute(kernel_for(sh, mode), cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-            if (e != cudaSuccess) return e;
-        }
+    for (int wt = 0; wt < 2; ++wt)
+        for (int sh = 0; sh < kGemvShapes; ++sh)
+            for (int mode = GEMV_QKV; mode <= GEMV_CLS; ++mode) {
+                cudaError_t e = cudaFuncSetAttribute(kernel_for(sh, mode, wt), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                     227 * 1024);
+                if (e != cudaSuccess) return e;
+            }
     return cudaSuccess;
 }
 
 cudaError_t launch_gemv(int mode, int shape, const GemvParams &p, int grid, size_t smem, cudaStream_t stream,
-                        bool pdl) {
+                        bool pdl, int wt) {
     if (shape < 0 || shape >= kGemvShapes) return cudaErrorInvalidValue;
-    void *fn = kernel_for(shape, mode);
+    void *fn = kernel_for(shape, mode, wt);
     if (!fn) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);

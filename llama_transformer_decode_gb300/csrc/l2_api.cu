@@ -86,6 +86,11 @@ struct GemvPlan {
 struct l2_ctx {
     L2Config cfg{};
     L2Weights w{};
+    // L2_FLAG_BF16_WEIGHTS: the matrices as bf16 (the handle's own copies), streamed by the batch-1 kernels
+    int wt = 0;
+    unsigned short *w16 = nullptr;
+    const unsigned short *b16q = nullptr, *b16k = nullptr, *b16v = nullptr, *b16o = nullptr, *b16w1 = nullptr,
+                         *b16w2 = nullptr, *b16w3 = nullptr, *b16cls = nullptr;
     int max_batch = 1;  // sequences, each with its own KV-cache slot
     int max_rows = 1;   // rows of a batched step: max_batch, or 64 for prompt chunks
     unsigned flags = 0;
@@ -285,7 +290,7 @@ void make_plans(l2_ctx *c) {
     c->plan_qkv.base.rows2 = c->kv_dim;
     c->plan_wo.base.in_vec = c->xb;
     c->plan_w2.base.in_vec = c->hb;
-    c->plan_cls.base.mat0 = c->w.wcls;
+    c->plan_cls.base.mat0 = c->wt ? reinterpret_cast<const float *>(c->b16cls) : c->w.wcls;
     c->plan_cls.base.norm_w = c->w.rms_final_weight;
 }
 
@@ -295,6 +300,25 @@ GemvParams layer_params(const l2_ctx *c, const GemvPlan &pl, int layer) {
     g.layer = layer;
     const size_t l = (size_t)layer;
     const size_t dd = (size_t)p.dim * p.dim, kd = (size_t)c->kv_dim * p.dim, hd = (size_t)p.hidden_dim * p.dim;
+    if (c->wt) {
+        // bf16 copies: element offsets in bf16 units
+        auto f = [](const unsigned short *q) { return reinterpret_cast<const float *>(q); };
+        if (&pl == &c->plan_qkv) {
+            g.mat0 = f(c->b16q + l * dd);
+            g.mat1 = f(c->b16k + l * kd);
+            g.mat2 = f(c->b16v + l * kd);
+            g.norm_w = c->w.rms_att_weight + l * p.dim;
+        } else if (&pl == &c->plan_wo) {
+            g.mat0 = f(c->b16o + l * dd);
+        } else if (&pl == &c->plan_w13) {
+            g.mat0 = f(c->b16w1 + l * hd);
+            g.mat1 = f(c->b16w3 + l * hd);
+            g.norm_w = c->w.rms_ffn_weight + l * p.dim;
+        } else if (&pl == &c->plan_w2) {
+            g.mat0 = f(c->b16w2 + l * hd);
+        }
+        return g;
+    }
     if (&pl == &c->plan_qkv) {
         g.mat0 = c->w.wq + l * dd;
         g.mat1 = c->w.wk + l * kd;
@@ -700,7 +724,7 @@ cudaError_t launch_op(l2_ctx *c, int op, int layer, int batch, cudaStream_t s, b
     switch (op) {
         case 0: {
             GemvParams g = layer_params(c, c->plan_qkv, layer);
-            return launch_gemv(GEMV_QKV, c->plan_qkv.shape, g, c->plan_qkv.grid, c->plan_qkv.smem, s, pdl);
+            return launch_gemv(GEMV_QKV, c->plan_qkv.shape, g, c->plan_qkv.grid, c->plan_qkv.smem, s, pdl, c->wt);
         }
         case 1: {
             AttnParams a = attn_params(c, layer, batch);
@@ -709,19 +733,19 @@ cudaError_t launch_op(l2_ctx *c, int op, int layer, int batch, cudaStream_t s, b
         }
         case 2: {
             GemvParams g = layer_params(c, c->plan_wo, layer);
-            return launch_gemv(GEMV_RESID, c->plan_wo.shape, g, c->plan_wo.grid, c->plan_wo.smem, s, pdl);
+            return launch_gemv(GEMV_RESID, c->plan_wo.shape, g, c->plan_wo.grid, c->plan_wo.smem, s, pdl, c->wt);
         }
         case 3: {
             GemvParams g = layer_params(c, c->plan_w13, layer);
-            return launch_gemv(GEMV_W13, c->plan_w13.shape, g, c->plan_w13.grid, c->plan_w13.smem, s, pdl);
+            return launch_gemv(GEMV_W13, c->plan_w13.shape, g, c->plan_w13.grid, c->plan_w13.smem, s, pdl, c->wt);
         }
         case 4: {
             GemvParams g = layer_params(c, c->plan_w2, layer);
-            return launch_gemv(GEMV_RESID, c->plan_w2.shape, g, c->plan_w2.grid, c->plan_w2.smem, s, pdl);
+            return launch_gemv(GEMV_RESID, c->plan_w2.shape, g, c->plan_w2.grid, c->plan_w2.smem, s, pdl, c->wt);
         }
         case 5: {
             GemvParams g = layer_params(c, c->plan_cls, 0);
-            return launch_gemv(GEMV_CLS, c->plan_cls.shape, g, c->plan_cls.grid, c->plan_cls.smem, s, pdl);
+            return launch_gemv(GEMV_CLS, c->plan_cls.shape, g, c->plan_cls.grid, c->plan_cls.smem, s, pdl, c->wt);
         }
     }
     return cudaErrorInvalidValue;
@@ -849,8 +873,15 @@ int l2_create(const L2Config *config, const L2Weights *weights, int max_batch, u
     if (!config || !weights) return fail(nullptr, L2_EINVAL, "config and weights must not be NULL");
     if (max_batch < 1 || max_batch > kMaxBatch)
         return fail(nullptr, L2_EINVAL, "max_batch %d outside 1..%d", max_batch, kMaxBatch);
-    if (flags & ~(L2_FLAG_DEBUG | L2_FLAG_NO_GRAPH | L2_FLAG_NO_PDL | L2_FLAG_PERSIST | L2_FLAG_NO_TC))
+    if (flags & ~(L2_FLAG_DEBUG | L2_FLAG_NO_GRAPH | L2_FLAG_NO_PDL | L2_FLAG_PERSIST | L2_FLAG_NO_TC |
+                  L2_FLAG_BF16_WEIGHTS))
         return fail(nullptr, L2_EINVAL, "unknown flags 0x%x", flags);
+    if (flags & L2_FLAG_BF16_WEIGHTS) {
+        if (max_batch != 1) return fail(nullptr, L2_EINVAL, "L2_FLAG_BF16_WEIGHTS serves one sequence (max_batch 1)");
+        if (flags & L2_FLAG_PERSIST) return fail(nullptr, L2_EINVAL, "L2_FLAG_BF16_WEIGHTS excludes L2_FLAG_PERSIST");
+        if (config->dim % 8 || config->hidden_dim % 8)
+            return fail(nullptr, L2_EINVAL, "L2_FLAG_BF16_WEIGHTS needs dim and hidden_dim divisible by 8");
+    }
     int rc = check_config(*config);
     if (rc) return rc;
     rc = check_weights(*weights);
@@ -864,6 +895,7 @@ int l2_create(const L2Config *config, const L2Weights *weights, int max_batch, u
     // buffers are small); with L2_FLAG_DEBUG the per-row probability export
     // keeps them at max_batch.
     c->max_rows = (flags & L2_FLAG_DEBUG) ? max_batch : kMaxBatch;
+    if (flags & L2_FLAG_BF16_WEIGHTS) c->max_rows = 1;  // batch-1 steps only; a prompt goes one token per step
     c->flags = flags;
     const L2Config &p = c->cfg;
     c->head_size = p.dim / p.n_heads;
@@ -950,6 +982,29 @@ int l2_create(const L2Config *config, const L2Weights *weights, int max_batch, u
     const double wbytes = 4.0 * ((double)L * (2.0 * p.dim * p.dim + 2.0 * c->kv_dim * p.dim + 3.0 * p.dim * p.hidden_dim) +
                                  (double)p.vocab_size * p.dim);
     c->evict_first = wbytes > 0.75 * (double)l2_bytes;
+    if (flags & L2_FLAG_BF16_WEIGHTS) {
+        // the handle's bf16 copies of the matrices (round to nearest even), converted once here
+        const size_t L_ = p.n_layers, dd = L_ * p.dim * p.dim, kd = L_ * c->kv_dim * p.dim,
+                     hd = L_ * p.hidden_dim * p.dim, cls = (size_t)p.vocab_size * p.dim;
+        if ((rc = alloc_n(c, &c->w16, 2 * dd + 2 * kd + 3 * hd + cls, "bf16 weights"))) return bail(rc);
+        unsigned short *at = c->w16;
+        auto take = [&](const float *src, size_t n, const unsigned short *&dst) -> cudaError_t {
+            dst = at;
+            cudaError_t e = convert_to_bf16(src, at, n, c->stream);
+            at += n;
+            return e;
+        };
+        CREATE_CUDA(take(c->w.wq, dd, c->b16q));
+        CREATE_CUDA(take(c->w.wk, kd, c->b16k));
+        CREATE_CUDA(take(c->w.wv, kd, c->b16v));
+        CREATE_CUDA(take(c->w.wo, dd, c->b16o));
+        CREATE_CUDA(take(c->w.w1, hd, c->b16w1));
+        CREATE_CUDA(take(c->w.w2, hd, c->b16w2));
+        CREATE_CUDA(take(c->w.w3, hd, c->b16w3));
+        CREATE_CUDA(take(c->w.wcls, cls, c->b16cls));
+        CREATE_CUDA(cudaStreamSynchronize(c->stream));
+        c->wt = 1;
+    }
     make_plans(c);
     for (const GemvPlan *pl : {&c->plan_qkv, &c->plan_wo, &c->plan_w13, &c->plan_w2, &c->plan_cls})
         if (pl->shape < 0)

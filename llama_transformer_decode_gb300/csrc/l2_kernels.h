@@ -17,7 +17,9 @@ size_t gemv_smem_bytes(int shape, int n, int ymax);
 // (*smem then holds the smallest shape's need).
 int gemv_pick_shape(int n, int ymax, size_t *smem);
 cudaError_t launch_gemv(int mode, int shape, const GemvParams &p, int grid, size_t smem, cudaStream_t stream,
-                        bool pdl);
+                        bool pdl, int wt = 0);
+// Device copy of n fp32 values as bf16 (round to nearest even), on `stream`.
+cudaError_t convert_to_bf16(const float *src, unsigned short *dst, size_t n, cudaStream_t stream);
 
 // Batched fused GEMV, B >= 2 sequences per step (gemv_batched.cu).
 cudaError_t gemv_batched_init();
