@@ -5,7 +5,9 @@
 //
 // Every weight is read from HBM once per step for all B sequences, so the
 // arithmetic intensity is B/2 flop per weight byte: at B = 16 the step is
-// still bandwidth-bound, at B = 64 it is bound by the fp32 CUDA cores.
+// still bandwidth-bound, at B = 64 it is bound by the fp32 CUDA cores.  Steps
+// of 16 or more rows therefore run on the tensor-core kernels (gemv_tc.cu)
+// unless the handle was created with L2_FLAG_NO_TC; this kernel serves 2..15.
 //
 // Design.  CTA c owns a balanced range of rows of one matrix (for W1/W3 the
 // same rows of both), walked in blocks of a few rows; each block walks K in

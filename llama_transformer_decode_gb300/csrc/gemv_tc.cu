@@ -1,7 +1,9 @@
 // Fused matrix-vector kernels for steps of B >= 16 rows (batched decoding or
-// prompt chunks) on the tensor cores: Y[b][r] = sum_k W[r][k] v_b[k] with the
-// fused epilogues of the other kernels (RoPE + KV write, SwiGLU, residual,
-// classifier) and the RMSNorm scale.
+// prompt chunks) on the tensor cores: Y[b][r] = sum_k W[r][k] v_b[k] -- the
+// pages' matmul ("run.c", matmul(): W (d,n) @ x (n,) -> (d,)) for B input
+// vectors at once -- with the fused epilogues of the other kernels (RoPE +
+// KV write, SwiGLU, residual, classifier; the walkthrough §4 forward() steps
+// 2a-2h and 3) and the RMSNorm scale.
 //
 // Precision.  The data are fp32; tcgen05.mma kind::tf32 reads the top 19
 // bits of each operand.  Each product is taken as hi*hi + hi*lo + lo*hi with
@@ -24,19 +26,21 @@
 // the CTAs ("stream-K"): a CTA's range is whole tiles plus at most a partial
 // tile at each end.  Whole tiles are finished at once; partial ones go to a
 // workspace, and after its last tile -- with no copies of its own in flight,
-// so the one release it needs is cheap -- the CTA takes a ticket per partial
-// tile; the last CTA of a tile adds the parts in K order, so results do not
-// depend on timing.  Warp roles, all walking the CTA's range in order:
+// when the one release fence it needs no longer waits behind returning data --
+// the CTA takes a ticket per partial tile; the last CTA of a tile adds the
+// parts in K order, so results do not depend on timing.  Warp roles, all
+// walking the CTA's range (its tile segments) in order:
 //   warp 0      2-D tensor copies (TMA, 128-byte swizzle) of the weight and
 //               input tiles of 64 K columns into a ring of 3 to 5 stages
 //               (as many as shared memory holds for the batch width);
 //   warp 1      the MMAs (M 128, K 8) of each converted stage, committed to
-//               the stage's "empty" barrier, and per item to an accumulator
-//               barrier; two accumulators in tensor memory alternate;
+//               the stage's "empty" barrier, and per segment to an
+//               accumulator barrier; two accumulators in TMEM alternate;
 //   warps 4-7   lo parts of each stage (weights into the stage's TMEM
 //               columns, inputs into shared memory);
-//   warps 8-11  epilogue: accumulator -> shared memory -> outputs, while the
-//               next item's MMAs run in the other accumulator.
+//   warps 8-11  epilogue: accumulator -> shared memory -> outputs (or the
+//               workspace), while the next segment's MMAs run in the other
+//               accumulator; warps 2-3 only join the final barrier.
 #include <algorithm>
 
 #include <cuda.h>
