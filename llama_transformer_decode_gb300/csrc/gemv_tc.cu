@@ -85,6 +85,7 @@ struct TcFixed {
     uint32_t tmem;
     int abort;
     int last_w[2];
+    int part_tile[2];     // the CTA's partial tiles (first, last segment), -1 if none
     float inv[kMaxBatch];
     int pos[kMaxBatch];   // the step's positions and cache slots (QKV)
     int slot[kMaxBatch];
@@ -292,6 +293,7 @@ __global__ void __launch_bounds__(kTT, 1) gemv_tc_kernel(const __grid_constant__
         mbar_init(&fx.fin, 1);
         fence_barrier_init();
         fx.abort = 0;
+        fx.part_tile[0] = fx.part_tile[1] = -1;
     }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&fx.tmem)),
@@ -311,6 +313,107 @@ __global__ void __launch_bounds__(kTT, 1) gemv_tc_kernel(const __grid_constant__
     auto xbox = [&](int s, int h) { return stage_ptr(s) + 2 * kABytes + 2 * h * xbox_bytes(BP); };
     // TMEM: accumulator a at columns [2 bpad a, 2 bpad (a + 1)); stage s's W_lo at 4 bpad + 64 s
     auto wlo_col = [&](int s) { return (uint32_t)(4 * BP + kSK * s); };
+
+    // a finished tile in ys -> the outputs of rows r0.. of matrix m, sequences 0..B-1 (row index fastest)
+    auto finish = [&](int tile, int ti, int nt, auto sync) {
+        int m, r0, wrow;
+        tile_geom(tile, m, r0, wrow);
+        if (MODE == GEMV_QKV) {
+            // pairs (j, j+1) of rows: RoPE on q and k, then the KV cache; the table reads of
+            // 8 pairs go out before their stores
+            const int hs = p.head_size, half = hs >> 1, mr = tp.mrows[m];
+            for (int e0 = ti; e0 < (kTM / 2) * B; e0 += 8 * nt) {
+                float2 cs[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int e = e0 + i * nt, b = e / (kTM / 2), v = r0 + 2 * (e - b * (kTM / 2));
+                    cs[i] = make_float2(1.f, 0.f);
+                    if (m < 2 && e < (kTM / 2) * B && v < mr) cs[i] = p.rope[(size_t)fx.pos[b] * half + ((v % hs) >> 1)];
+                }
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int e = e0 + i * nt, b = e / (kTM / 2), j = 2 * (e - b * (kTM / 2)), v = r0 + j;
+                    if (e >= (kTM / 2) * B || v >= mr) continue;
+                    const float y0 = ys[j * YS + b] * fx.inv[b], y1 = ys[(j + 1) * YS + b] * fx.inv[b];
+                    if (m == 0) {
+                        float *qv = p.q + (size_t)b * p.dim;
+                        qv[v] = y0 * cs[i].x - y1 * cs[i].y;
+                        qv[v + 1] = y0 * cs[i].y + y1 * cs[i].x;
+                    } else {
+                        const int g = v / hs, d = v % hs;
+                        const size_t idx =
+                            ((((size_t)fx.slot[b] * p.n_layers + p.layer) * p.n_kv_heads + g) * p.seq_len + fx.pos[b]) * hs +
+                            d;
+                        if (m == 1) {
+                            p.kcache[idx] = y0 * cs[i].x - y1 * cs[i].y;
+                            p.kcache[idx + 1] = y0 * cs[i].y + y1 * cs[i].x;
+                        } else {
+                            p.vcache[idx] = y0;
+                            p.vcache[idx + 1] = y1;
+                        }
+                    }
+                }
+            }
+        } else if (MODE == GEMV_W13) {
+            const int hidden = tp.mrows[0];
+            for (int e = ti; e < (kTM / 2) * B; e += nt) {
+                const int b = e / (kTM / 2), j = e - b * (kTM / 2);
+                if (r0 + j >= hidden) continue;
+                const float h1 = ys[j * YS + b] * fx.inv[b], h3 = ys[(j + kTM / 2) * YS + b] * fx.inv[b];
+                p.hb[(size_t)b * hidden + r0 + j] = silu_t(h1) * h3;
+            }
+        } else if (MODE == GEMV_RESID) {
+            const int dim = tp.mrows[0];
+            // thread = row j (and a group of sequences); x of 8 sequences loaded before any store
+            const int j = ti % kTM, bg = ti / kTM, nbg = nt / kTM;
+            if (j < dim - r0) {
+                const float g = __ldg(tp.next_gain + r0 + j);
+                for (int b0 = 8 * bg; b0 < B; b0 += 8 * nbg) {
+                    float xv[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        if (b0 + i < B) xv[i] = p.x[(size_t)(b0 + i) * dim + r0 + j];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        if (b0 + i < B) {
+                            const size_t o = (size_t)(b0 + i) * dim + r0 + j;
+                            const float nv = xv[i] + ys[j * YS + b0 + i];
+                            p.x[o] = nv;
+                            tp.xg[o] = nv * g;
+                            ys[j * YS + b0 + i] = nv;
+                        }
+                }
+            }
+            sync();
+            // this tile's sum of squares of the new x rows, per sequence, in a fixed order
+            // (128 partials whatever the thread count: the padding column has 128 rows)
+            const int parts = kTM / B, rows = min(kTM, dim - r0);
+            if (ti < kTM) {
+                float ss = 0.f;
+                if (ti < parts * B) {
+                    const int b = ti % B;
+                    for (int jr = ti / B; jr < rows; jr += parts) ss = fmaf(ys[jr * YS + b], ys[jr * YS + b], ss);
+                }
+                ys[ti * YS + BP] = ss;
+            }
+            sync();
+            if (ti < B) {
+                float t = 0.f;
+                for (int i = 0; i < parts; ++i) t += ys[(i * B + ti) * YS + BP];
+                p.ss_part[(size_t)tile * B + ti] = t;
+            }
+        } else {
+            float *user = p.step->logits_out;
+            const int V = tp.mrows[0];
+            for (int e = ti; e < kTM * B; e += nt) {
+                const int b = e / kTM, j = e - b * kTM;
+                if (r0 + j >= V) continue;
+                const float y = ys[j * YS + b] * fx.inv[b];
+                p.logits[(size_t)b * V + r0 + j] = y;
+                if (user) user[(size_t)b * V + r0 + j] = y;
+            }
+        }
+    };
 
     if (warp == 0) {
         // ---------------- producer: tensor copies into the ring (whole warp, one lane issues) ----------------
@@ -467,103 +570,6 @@ __global__ void __launch_bounds__(kTT, 1) gemv_tc_kernel(const __grid_constant__
             }
         }
         epi_sync();
-        // a finished tile in ys -> the outputs of rows r0.. of matrix m, sequences 0..B-1 (row index fastest)
-        auto finish = [&](int tile) {
-            int m, r0, wrow;
-            tile_geom(tile, m, r0, wrow);
-        if (MODE == GEMV_QKV) {
-            // pairs (j, j+1) of rows: RoPE on q and k, then the KV cache; the table reads of
-            // 8 pairs go out before their stores
-            const int hs = p.head_size, half = hs >> 1, mr = tp.mrows[m];
-            for (int e0 = et; e0 < (kTM / 2) * B; e0 += 8 * kRoleThreads) {
-                float2 cs[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int e = e0 + i * kRoleThreads, b = e / (kTM / 2), v = r0 + 2 * (e - b * (kTM / 2));
-                    cs[i] = make_float2(1.f, 0.f);
-                    if (m < 2 && e < (kTM / 2) * B && v < mr) cs[i] = p.rope[(size_t)fx.pos[b] * half + ((v % hs) >> 1)];
-                }
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int e = e0 + i * kRoleThreads, b = e / (kTM / 2), j = 2 * (e - b * (kTM / 2)), v = r0 + j;
-                    if (e >= (kTM / 2) * B || v >= mr) continue;
-                    const float y0 = ys[j * YS + b] * fx.inv[b], y1 = ys[(j + 1) * YS + b] * fx.inv[b];
-                    if (m == 0) {
-                        float *qv = p.q + (size_t)b * p.dim;
-                        qv[v] = y0 * cs[i].x - y1 * cs[i].y;
-                        qv[v + 1] = y0 * cs[i].y + y1 * cs[i].x;
-                    } else {
-                        const int g = v / hs, d = v % hs;
-                        const size_t idx =
-                            ((((size_t)fx.slot[b] * p.n_layers + p.layer) * p.n_kv_heads + g) * p.seq_len + fx.pos[b]) * hs +
-                            d;
-                        if (m == 1) {
-                            p.kcache[idx] = y0 * cs[i].x - y1 * cs[i].y;
-                            p.kcache[idx + 1] = y0 * cs[i].y + y1 * cs[i].x;
-                        } else {
-                            p.vcache[idx] = y0;
-                            p.vcache[idx + 1] = y1;
-                        }
-                    }
-                }
-            }
-        } else if (MODE == GEMV_W13) {
-            const int hidden = tp.mrows[0];
-            for (int e = et; e < (kTM / 2) * B; e += kRoleThreads) {
-                const int b = e / (kTM / 2), j = e - b * (kTM / 2);
-                if (r0 + j >= hidden) continue;
-                const float h1 = ys[j * YS + b] * fx.inv[b], h3 = ys[(j + kTM / 2) * YS + b] * fx.inv[b];
-                p.hb[(size_t)b * hidden + r0 + j] = silu_t(h1) * h3;
-            }
-        } else if (MODE == GEMV_RESID) {
-            const int dim = tp.mrows[0];
-            // thread = row j; x of 8 sequences loaded before any store
-            if (et < dim - r0) {
-                const int j = et;
-                const float g = __ldg(tp.next_gain + r0 + j);
-                for (int b0 = 0; b0 < B; b0 += 8) {
-                    float xv[8];
-#pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        if (b0 + i < B) xv[i] = p.x[(size_t)(b0 + i) * dim + r0 + j];
-#pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        if (b0 + i < B) {
-                            const size_t o = (size_t)(b0 + i) * dim + r0 + j;
-                            const float nv = xv[i] + ys[j * YS + b0 + i];
-                            p.x[o] = nv;
-                            tp.xg[o] = nv * g;
-                            ys[j * YS + b0 + i] = nv;
-                        }
-                }
-            }
-            epi_sync();
-            // this tile's sum of squares of the new x rows, per sequence, in a fixed order
-            const int parts = kRoleThreads / B, rows = min(kTM, dim - r0);  // parts * B <= 128 rows of ys
-            float ss = 0.f;
-            if (et < parts * B) {
-                const int b = et % B;
-                for (int j = et / B; j < rows; j += parts) ss = fmaf(ys[j * YS + b], ys[j * YS + b], ss);
-            }
-            ys[et * YS + BP] = ss;  // the padding column holds the partials
-            epi_sync();
-            if (et < B) {
-                float t = 0.f;
-                for (int i = 0; i < parts; ++i) t += ys[(i * B + et) * YS + BP];
-                p.ss_part[(size_t)tile * B + et] = t;
-            }
-        } else {
-            float *user = p.step->logits_out;
-            const int V = tp.mrows[0];
-            for (int e = et; e < kTM * B; e += kRoleThreads) {
-                const int b = e / kTM, j = e - b * kTM;
-                if (r0 + j >= V) continue;
-                const float y = ys[j * YS + b] * fx.inv[b];
-                p.logits[(size_t)b * V + r0 + j] = y;
-                if (user) user[(size_t)b * V + r0 + j] = y;
-            }
-        }
-        };
         // partial segments (at most the first and the last): published now, merged after the last one
         int part0 = -1, part1 = -1;
         long long ni = 0;
@@ -603,85 +609,12 @@ __global__ void __launch_bounds__(kTT, 1) gemv_tc_kernel(const __grid_constant__
                 continue;
             }
             epi_sync();
-            finish(tile);
+            finish(tile, et, kRoleThreads, [] { epi_sync(); });
             epi_sync();  // ys free for the next tile
         }
-        if (!stop && (part0 >= 0 || part1 >= 0)) {
-            // Nothing of this CTA's is in flight any more: publish the partial tiles (one
-            // release per CTA) and take the tickets; the last CTA of a tile adds its parts
-            // in K order and finishes it.
-            epi_sync();
-            if (et == 0) {
-                __threadfence();
-                for (int w = 0; w < 2; ++w) {
-                    int last = 0;
-                    const int t = w == 0 ? part0 : part1;
-                    if (t >= 0) {
-                        const int c0 = cta_of((long long)t * KT), c1 = cta_of((long long)(t + 1) * KT - 1);
-                        last = atomicAdd(&tp.tickets[t], 1u) == (unsigned)(c1 - c0) ? 1 : 0;
-                    }
-                    fx.last_w[w] = last;
-                }
-                __threadfence();
-            }
-            epi_sync();
-            for (int w = 0; w < 2; ++w) {
-                if (!fx.last_w[w]) continue;
-                const int t = w == 0 ? part0 : part1;
-                const int c0 = cta_of((long long)t * KT), c1 = cta_of((long long)(t + 1) * KT - 1);
-                // 4 rows of one sequence per float4, this thread's v = et + 128 i (8 at a time);
-                // two parts' loads in flight per round trip; parts added in K order
-                constexpr int kV = 8;
-                const int nv = B * (kTM / 4);
-                for (int i0 = 0; et + kRoleThreads * i0 < nv; i0 += kV) {
-                    float4 acc[kV];
-#pragma unroll
-                    for (int i = 0; i < kV; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-                    for (int c = c0; c <= c1; c += 2) {
-                        const float4 *src[2];
-                        float4 part[2][kV];
-#pragma unroll
-                        for (int u = 0; u < 2; ++u) {
-                            const int cc = min(c + u, c1);
-                            const int wh = (long long)cc * T / G >= (long long)t * KT ? 0 : 1;
-                            src[u] = reinterpret_cast<const float4 *>(tp.ws + ((size_t)cc * 2 + wh) * kTM * BP);
-                        }
-#pragma unroll
-                        for (int u = 0; u < 2; ++u)
-#pragma unroll
-                            for (int i = 0; i < kV; ++i) {
-                                const int v = et + kRoleThreads * (i0 + i);
-                                if (v < nv && c + u <= c1) part[u][i] = __ldcg(src[u] + v);
-                            }
-#pragma unroll
-                        for (int u = 0; u < 2; ++u)
-#pragma unroll
-                            for (int i = 0; i < kV; ++i) {
-                                const int v = et + kRoleThreads * (i0 + i);
-                                if (v < nv && c + u <= c1) {
-                                    acc[i].x += part[u][i].x;
-                                    acc[i].y += part[u][i].y;
-                                    acc[i].z += part[u][i].z;
-                                    acc[i].w += part[u][i].w;
-                                }
-                            }
-                    }
-#pragma unroll
-                    for (int i = 0; i < kV; ++i) {
-                        const int v = et + kRoleThreads * (i0 + i);
-                        if (v >= nv) continue;
-                        const int c = v / (kTM / 4), r = (v - c * (kTM / 4)) * 4;
-                        ys[r * YS + c] = acc[i].x;
-                        ys[(r + 1) * YS + c] = acc[i].y;
-                        ys[(r + 2) * YS + c] = acc[i].z;
-                        ys[(r + 3) * YS + c] = acc[i].w;
-                    }
-                }
-                if (et == 0) tp.tickets[t] = 0u;
-                epi_sync();
-                finish(t);
-                epi_sync();
-            }
+        if (!stop && et == 0) {
+            fx.part_tile[0] = part0;
+            fx.part_tile[1] = part1;
         }
     }
     tc_fence_before();
@@ -689,6 +622,82 @@ __global__ void __launch_bounds__(kTT, 1) gemv_tc_kernel(const __grid_constant__
     tc_fence_after();
     if (warp == 1)
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(kTmemCols) : "memory");
+
+    // Partial tiles, by the whole CTA: nothing of this CTA's is in flight any more, so
+    // the one release fence it needs does not wait behind returning data.  Publish the
+    // partial tiles and take the tickets; the last CTA of a tile adds its parts in K
+    // order and finishes it.  (Every thread reads the same shared values after the
+    // barrier, so the branches below are uniform.)
+    if (aborted(fx) || (fx.part_tile[0] < 0 && fx.part_tile[1] < 0)) return;
+    if (tid == 0) {
+        __threadfence();
+        for (int w = 0; w < 2; ++w) {
+            int last = 0;
+            const int t = fx.part_tile[w];
+            if (t >= 0) {
+                const int c0 = cta_of((long long)t * KT), c1 = cta_of((long long)(t + 1) * KT - 1);
+                last = atomicAdd(&tp.tickets[t], 1u) == (unsigned)(c1 - c0) ? 1 : 0;
+            }
+            fx.last_w[w] = last;
+        }
+        __threadfence();
+    }
+    __syncthreads();
+    auto bar_all = []() { __syncthreads(); };
+    for (int w = 0; w < 2; ++w) {
+        if (!fx.last_w[w]) continue;
+        const int t = fx.part_tile[w];
+        const int c0 = cta_of((long long)t * KT), c1 = cta_of((long long)(t + 1) * KT - 1);
+        // 4 rows of one sequence per float4, this thread's v = tid + 384 i (2 at a time);
+        // up to 8 parts' loads in flight per round trip; parts added in K order
+        constexpr int kV = 2, kPG = 8;
+        const int nv = B * (kTM / 4);
+        for (int i0 = 0; tid + kTT * i0 < nv; i0 += kV) {
+            float4 acc[kV];
+#pragma unroll
+            for (int i = 0; i < kV; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int cb = c0; cb <= c1; cb += kPG) {
+                float4 part[kPG][kV];
+#pragma unroll
+                for (int u = 0; u < kPG; ++u) {
+                    const int cc = min(cb + u, c1);
+                    const int wh = (long long)cc * T / G >= (long long)t * KT ? 0 : 1;
+                    const float4 *src = reinterpret_cast<const float4 *>(tp.ws + ((size_t)cc * 2 + wh) * kTM * BP);
+#pragma unroll
+                    for (int i = 0; i < kV; ++i) {
+                        const int v = tid + kTT * (i0 + i);
+                        if (v < nv && cb + u <= c1) part[u][i] = __ldcg(src + v);
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < kPG; ++u)
+#pragma unroll
+                    for (int i = 0; i < kV; ++i) {
+                        const int v = tid + kTT * (i0 + i);
+                        if (v < nv && cb + u <= c1) {
+                            acc[i].x += part[u][i].x;
+                            acc[i].y += part[u][i].y;
+                            acc[i].z += part[u][i].z;
+                            acc[i].w += part[u][i].w;
+                        }
+                    }
+            }
+#pragma unroll
+            for (int i = 0; i < kV; ++i) {
+                const int v = tid + kTT * (i0 + i);
+                if (v >= nv) continue;
+                const int c = v / (kTM / 4), r = (v - c * (kTM / 4)) * 4;
+                ys[r * YS + c] = acc[i].x;
+                ys[(r + 1) * YS + c] = acc[i].y;
+                ys[(r + 2) * YS + c] = acc[i].z;
+                ys[(r + 3) * YS + c] = acc[i].w;
+            }
+        }
+        if (tid == 0) tp.tickets[t] = 0u;
+        __syncthreads();
+        finish(t, tid, kTT, bar_all);
+        __syncthreads();
+    }
 }
 
 // ---------------------------------------------------------------- host side
