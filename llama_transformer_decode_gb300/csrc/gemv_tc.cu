@@ -629,6 +629,7 @@ __global__ void __launch_bounds__(kTT, 1) gemv_tc_kernel(const __grid_constant__
     // order and finishes it.  (Every thread reads the same shared values after the
     // barrier, so the branches below are uniform.)
     if (aborted(fx) || (fx.part_tile[0] < 0 && fx.part_tile[1] < 0)) return;
+    pdl_wait();  // every warp now reads the previous kernel's outputs (x, the RoPE table's step)
     if (tid == 0) {
         __threadfence();
         for (int w = 0; w < 2; ++w) {
