@@ -173,6 +173,34 @@ def load_weights_device(wl, keep_host: bool):
     return dev, None
 
 
+def host_threads() -> int:
+    """Threads the oracle's parallel loops run on."""
+    import oracle
+    return oracle.num_threads()
+
+
+def metric_of(batch: int, bf16: bool = False) -> str:
+    if batch > 1:
+        return METRIC.replace("at batch 1", f"at batch {batch}")
+    return METRIC.replace("at batch 1", "at batch 1 with bf16 weights") if bf16 else METRIC
+
+
+def max_over_ranks(v: float, world: int, device: str = "cuda") -> float:
+    """The largest of the ranks' values (each rank passes its own)."""
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(units_per_rank: int, world: int, slowest_s: float) -> float:
+    """Whole-job throughput: every rank's units over the slowest rank's time."""
+    return world * units_per_rank / slowest_s
+
+
 def oracle_rate(wl, host_w, tokens, budget_s: float, min_steps: int = 2):
     """Teacher-forced oracle steps from position 0 until the time budget is
     spent; returns (steps, seconds, threads)."""
@@ -184,43 +212,59 @@ def oracle_rate(wl, host_w, tokens, budget_s: float, min_steps: int = 2):
         m.forward(int(tokens[n]), n)
         n += 1
     el = time.perf_counter() - t0
-    threads = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
-    return n, el, threads
+    return n, el, host_threads()
 
 
 def run_reference(args, wl):
+    """The oracle on the host cores, on the same workload, batch and staggered
+    positions as the GPU arm: each step is one forward per slot."""
     rank, _, world = dist_env()
     if rank != 0:
-        return 0
-    host_w = synth.make_weights(wl)
-    toks = synth.token_stream(wl, 0, wl.seq_len)
+        return 0  # one CPU baseline per job, taken on rank 0
     import oracle
-    m = oracle.Model(wl.config_tuple(), host_w)
-    for p in range(args.warmup):
-        m.forward(int(toks[p % wl.seq_len]), p % wl.seq_len)
+    B, S = args.batch, wl.seq_len
+    host_w = synth.make_weights(wl)
+    m = oracle.Model(wl.config_tuple(), host_w, n_slots=B)
+    streams = [synth.token_stream(wl, b, S) for b in range(B)]
+    offsets = [b * S // B for b in range(B)]
+    for b in range(B):
+        if offsets[b]:
+            m.key_cache[b][:, : offsets[b]] = synth.kv_rows(wl, b, offsets[b], "k")
+            m.value_cache[b][:, : offsets[b]] = synth.kv_rows(wl, b, offsets[b], "v")
+
+    def step(s):
+        for b in range(B):
+            p = (offsets[b] + s) % S
+            if p == 0 and s > 0:  # the slot wraps: its cache starts over
+                m.key_cache[b][:] = 0
+                m.value_cache[b][:] = 0
+            m.forward(int(streams[b][p]), p, slot=b)
+
+    for s in range(args.warmup):
+        step(s)
     # size the timed sample from one step's cost so the run stays within the budget
     t0 = time.perf_counter()
-    p = args.warmup % wl.seq_len
-    m.forward(int(toks[p]), p)
+    step(args.warmup)
     one = time.perf_counter() - t0
     k = max(1, min(args.steps, int(args.reference_budget / max(one, 1e-6))))
+    first = args.warmup + 1
     t0 = time.perf_counter()
-    for i in range(k):
-        p = (args.warmup + 1 + i) % wl.seq_len
-        if p == 0:
-            m.key_cache[0][:] = 0
-            m.value_cache[0][:] = 0
-        m.forward(int(toks[p]), p)
+    for s in range(first, first + k):
+        step(s)
     el = time.perf_counter() - t0
-    value = k / el
-    threads = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
-    sample = (f"{k} teacher-forced oracle steps of {wl.name} at positions "
-              f"{args.warmup + 1}..{args.warmup + k} (of {args.steps} requested), after {args.warmup + 1} untimed")
-    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+    value = B * k / el
+    where = (f"positions {first % S}..{(first + k - 1) % S}" if B == 1 else
+             f"slot b from floor(b*{S}/{B}) + {first}, wrapping at {S}")
+    sample = (f"{k} teacher-forced oracle steps of {wl.name} ({B} sequence{'s' if B > 1 else ''}) at {where} "
+              f"(of {args.steps} requested), after {first} untimed")
+    cfg = config_of(wl, B)
+    cfg["gemv"] = "oracle: fp32 storage, double accumulation, OpenMP rows"
+    line = {"impl": "reference", "metric": metric_of(B), "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": k, "warmup": args.warmup, "ms_per_step": 1000.0 * el / k, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64-accumulate/f32-storage", "data": "synthetic",
-            "config": config_of(wl),
-            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle", "sample": sample},
+            "config": cfg,
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": host_threads(), "kind": "oracle",
+                             "sample": sample},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
@@ -297,13 +341,6 @@ def run_ours(args, wl):
         if world > 1:
             dist.barrier()
 
-    def max_over_ranks(v: float) -> float:
-        if world == 1:
-            return v
-        t = torch.tensor([v], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
-
     run_steps(0, args.warmup)
     dec.sync()
 
@@ -319,8 +356,8 @@ def run_ours(args, wl):
     torch.cuda.synchronize()
     barrier()
     dec.sync()
-    ms = max_over_ranks(ev0.elapsed_time(ev1))
-    value = world * B * args.steps / (ms / 1000.0)
+    ms = max_over_ranks(ev0.elapsed_time(ev1), world)
+    value = job_rate(B * args.steps, world, ms / 1000.0)
     timed_pos = [positions(s) for s in range(args.warmup, args.warmup + args.steps)]
     bytes_total = sum(weight_bytes(wl, wb) + sum(kv_bytes(wl, p) for p in pos) for pos in timed_pos)
     step_gbs = bytes_total / (ms / 1000.0) / 1e9
@@ -355,8 +392,8 @@ def run_ours(args, wl):
     barrier()
     t0 = time.perf_counter()
     run_steps(args.warmup, args.steps, host_logits)
-    e2e_s = max_over_ranks(time.perf_counter() - t0)
-    e2e = {"value": world * B * args.steps / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": dec.step_input_bytes(),
+    e2e_s = max_over_ranks(time.perf_counter() - t0, world)
+    e2e = {"value": job_rate(B * args.steps, world, e2e_s), "unit": "tokens/s", "h2d_bytes_per_step": dec.step_input_bytes(),
            "d2h_bytes_per_step": 4 * wl.vocab_size * B}
 
     # ---- roofline ----
@@ -416,9 +453,8 @@ def run_ours(args, wl):
     cfg = config_of(wl, B)
     cfg["positions"] = (f"{timed_pos[0][0]}..{timed_pos[-1][0]}" if B == 1 else
                         f"slot b from floor(b*{S}/{B}) + {args.warmup}, {args.steps} steps, wrapping at {S}")
-    metric = METRIC if B == 1 else METRIC.replace("at batch 1", f"at batch {B}")
+    metric = metric_of(B, bf16)
     if bf16:
-        metric = metric.replace("at batch 1", "at batch 1 with bf16 weights")
         cfg["weights"] = "seeded random (synth); matrices streamed as bf16 (rounded once on the device), fp32 arithmetic"
     line = {
         "metric": metric,

@@ -131,6 +131,8 @@ def _declare(lib):
     lib.oracle_decode.argtypes = [ctypes.POINTER(OracleConfig), ctypes.POINTER(OracleWeights),
                                   vp, vp, vp, i, i, vp]
     lib.oracle_decode.restype = i
+    lib.oracle_num_threads.argtypes = []
+    lib.oracle_num_threads.restype = i
     for f in (lib.oracle_rmsnorm, lib.oracle_softmax, lib.oracle_matmul, lib.oracle_rope,
               lib.oracle_attention_head):
         f.restype = None
@@ -145,6 +147,11 @@ def load(path: str | None = None):
     if _lib is None:
         _lib = _declare(ctypes.CDLL(build()))
     return _lib
+
+
+def num_threads(lib=None) -> int:
+    """Threads the oracle's parallel loops run on (OpenMP's team size)."""
+    return int((lib or load()).oracle_num_threads())
 
 
 def _f32(a) -> np.ndarray:

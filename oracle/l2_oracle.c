@@ -30,6 +30,7 @@
  *   - weights are row-major [out][in]; the KV cache is [layer][pos][kv_dim].
  */
 #include <math.h>
+#include <omp.h>
 #include <stdlib.h>
 #include <string.h>
 
@@ -51,6 +52,9 @@ typedef struct {
     const float *rms_final_weight;      /* (dim,) */
     const float *wcls;                  /* (vocab_size, dim) */
 } OracleWeights;
+
+/* Threads the parallel loops below run on (no arithmetic). */
+int oracle_num_threads(void) { return omp_get_max_threads(); }
 
 /* [RUNC] rmsnorm(): o_j = w_j * (x_j / sqrt(mean(x^2) + 1e-5)). */
 void oracle_rmsnorm(float *o, const float *x, const float *weight, int size) {
