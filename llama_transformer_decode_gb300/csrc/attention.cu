@@ -16,7 +16,9 @@
 // 1-D bulk async copies (TMA).  Lanes are grouped LP to a cache row (LP = the
 // head size in 16-byte words, rounded up to a power of two); each group keeps
 // an online softmax (running max m, sum l, un-normalised accumulator) per
-// query head.  Groups, then warps, then CTAs are merged with the usual
+// query head; with 4 or 8 query heads per KV head at head size 64 the lanes
+// take one cache row each instead (the row-per-lane layout, described at the
+// kernel).  Groups, then warps, then CTAs are merged with the usual
 // log-sum-exp rescaling; the CTA that arrives last on the group's ticket
 // merges the chunks in chunk order and writes the output, so the result does
 // not depend on CTA timing.  With a debug buffer the raw scores are stored and

@@ -38,9 +38,12 @@
 //               accumulator barrier; two accumulators in TMEM alternate;
 //   warps 4-7   lo parts of each stage (weights into the stage's TMEM
 //               columns, inputs into shared memory);
-//   warps 8-11  epilogue: accumulator -> shared memory -> outputs (or the
-//               workspace), while the next segment's MMAs run in the other
-//               accumulator; warps 2-3 only join the final barrier.
+//   warps 8-11  epilogue of whole tiles: accumulator -> shared memory ->
+//               outputs (partial tiles -> the workspace), while the next
+//               segment's MMAs run in the other accumulator;
+//   all 12      after the CTA's last tile: tickets, and the K-order merge and
+//               epilogue of each partial tile this CTA completes (warps 2-3
+//               idle until then).
 #include <algorithm>
 
 #include <cuda.h>
