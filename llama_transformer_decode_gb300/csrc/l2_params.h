@@ -65,7 +65,7 @@ constexpr int kMaxParts = 1024;
 
 // Batched GEMV launch (gemv_batched.cu): tensor maps for 2-D tile copies of
 // the weights (rows x columns boxes) and of the B input rows.
-struct alignas(64) BatchParams {
+struct alignas(128) BatchParams {
     CUtensorMap wmap[3];  // QKV: Wq, Wk, Wv; W1/W3: W1, W3; otherwise [0]
     CUtensorMap xmap;     // input activations [slots][n], box = tk columns x batch rows
     GemvParams g;
@@ -116,7 +116,7 @@ struct SampleParams {
 // of W1 over the same 64 rows of W3) x bpad sequences, the (tile, K stage)
 // work split evenly over the grid; tensor maps with 128-byte swizzle, boxes of
 // 32 columns.
-struct alignas(64) TcParams {
+struct alignas(128) TcParams {
     CUtensorMap wmap[3];  // QKV: Wq, Wk, Wv; W1/W3: W1, W3; otherwise [0]
     CUtensorMap xmap;     // inputs [max rows][n] (x * gain for the RMSNorm modes), box 32 columns x bpad rows
     GemvParams g;
