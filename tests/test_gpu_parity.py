@@ -5,8 +5,6 @@ the debug export, every layer's attention probabilities.  Bounds: per step
 max|d logit| <= 2e-3 and <= 1e-4 * max|oracle logit|; probabilities within
 1e-5.
 """
-import math
-
 import numpy as np
 import pytest
 

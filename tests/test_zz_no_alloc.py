@@ -7,7 +7,6 @@ two calls in a row.  This file is collected last on purpose.
 """
 import ctypes
 
-import numpy as np
 import pytest
 
 import synth
