@@ -63,13 +63,33 @@ def test_create_rejects_bad_arguments_on_the_host(lib):
 
 
 def test_null_handle_calls_fail_cleanly(lib):
+    toks = (ctypes.c_int * 2)(1, 2)
+    pos = (ctypes.c_int * 2)(0, 0)
+    host = (ctypes.c_float * 4)()
+    hp = ctypes.cast(host, ctypes.c_void_p)
     assert lib.l2_forward(None, 0, 0, None) == pkg.L2_EINVAL
+    assert lib.l2_forward_batch(None, 2, toks, pos, None) == pkg.L2_EINVAL
+    assert lib.l2_forward_host(None, 0, 0, hp) == pkg.L2_EINVAL
+    assert lib.l2_forward_static(None, 0, 0, None) == pkg.L2_EINVAL
+    assert lib.l2_forward_dev_tokens(None, 2, None, pos, None) == pkg.L2_EINVAL
+    assert lib.l2_prefill(None, 0, 2, toks, 0, None) == pkg.L2_EINVAL
     assert lib.l2_reset(None, 0) == pkg.L2_EINVAL
     assert lib.l2_sync(None) == pkg.L2_EINVAL
     assert lib.l2_position(None, 0) == pkg.L2_EINVAL
     assert lib.l2_kernels_per_step(None, 1) == pkg.L2_EINVAL
+    assert lib.l2_debug_attention(None, 0, 0, hp) == pkg.L2_EINVAL
+    assert lib.l2_kv_export(None, 0, 0, 1, hp, hp) == pkg.L2_EINVAL
+    assert lib.l2_kv_import(None, 0, 1, hp, hp) == pkg.L2_EINVAL
+    assert lib.l2_launch_op(None, 0, 0, 1) == pkg.L2_EINVAL
     assert lib.l2_logits(None) is None
+    assert lib.l2_last_error(None) is not None  # the last l2_create failure on this thread, never NULL
     lib.l2_destroy(None)
+
+
+def test_step_input_bytes_is_the_step_block(lib):
+    # the bytes one step copies host -> device: its token, position and output-pointer block
+    n = lib.l2_step_input_bytes()
+    assert n > 0 and n % 8 == 0
 
 
 def test_sample_rejects_bad_arguments_on_the_host(lib):
