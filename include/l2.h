@@ -225,7 +225,9 @@ int l2_prefill(l2_ctx *ctx, int slot, int T, const int *tokens, int pos0, float 
  */
 int l2_forward_dev_tokens(l2_ctx *ctx, int B, const int *tokens_dev, const int *pos, float *logits_out);
 
-/* Number of kernel launches one step of batch B enqueues, or L2_EINVAL. */
+/* Number of kernel launches one step of batch B enqueues, or L2_EINVAL:
+ * 5 * n_layers + 1, plus one (the embedding kernel) when the step's matrix
+ * products run on the tensor cores, or 1 for the persistent step kernel. */
 int l2_kernels_per_step(const l2_ctx *ctx, int B);
 
 /* Bytes each step copies from host to device (the step's token, position and
