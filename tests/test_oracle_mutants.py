@@ -39,6 +39,17 @@ MUTANTS = [
     ("softmax_max_not_subtracted", "x[i] = exp(x[i] - max_val);", "x[i] = exp(x[i]);"),
     ("final_norm_skipped", "oracle_rmsnorm(x, x, w->rms_final_weight, dim);", ";"),
     ("ffn_norm_uses_att_weight", "oracle_rmsnorm(xb, x, w->rms_ffn_weight +", "oracle_rmsnorm(xb, x, w->rms_att_weight +"),
+    ("swiglu_gate_on_w3", "double val = hb[i];\n            val *= 1.0 / (1.0 + exp(-val));\n            val *= (double)hb2[i];",
+     "double val = hb2[i];\n            val *= 1.0 / (1.0 + exp(-val));\n            val *= (double)hb[i];"),
+    ("silu_sign_flipped", "val *= 1.0 / (1.0 + exp(-val));", "val *= 1.0 / (1.0 + exp(val));"),
+    ("v_read_from_key_cache", "value_cache + loff + (size_t)g * head_size, kv_dim",
+     "key_cache + loff + (size_t)g * head_size, kv_dim"),
+    ("query_head_offset_uses_kv_head", "q + (size_t)h * head_size,", "q + (size_t)g * head_size,"),
+    ("kv_written_one_row_early", "float *k = key_cache + loff + (size_t)pos * kv_dim;",
+     "float *k = key_cache + loff + (size_t)(pos > 0 ? pos - 1 : 0) * kv_dim;"),
+    ("att_norm_layer_offset_dropped", "w->rms_att_weight + (size_t)l * dim", "w->rms_att_weight"),
+    ("wq_layer_offset_dropped", "w->wq + (size_t)l * dim * dim", "w->wq"),
+    ("classifier_uses_embedding", "oracle_matmul(logits, x, w->wcls, dim", "oracle_matmul(logits, x, w->token_embedding_table, dim"),
 ]
 
 
