@@ -230,8 +230,9 @@ int l2_forward_dev_tokens(l2_ctx *ctx, int B, const int *tokens_dev, const int *
  * products run on the tensor cores, or 1 for the persistent step kernel. */
 int l2_kernels_per_step(const l2_ctx *ctx, int B);
 
-/* Bytes each step copies from host to device (the step's token, position and
- * output-pointer block). */
+/* Bytes each step copies from host to device: the step block (per row its
+ * token, position, cache slot and the slot's rows written before the step;
+ * the output pointer; the row count; the step's total attention rows). */
 int l2_step_input_bytes(void);
 
 /*
