@@ -22,9 +22,10 @@
 // a lane loads 8 weight and 8 input words for 256 FMAs.  A CTA holds at most
 // 8 tiles, so the host sizes the row ranges (and the grid) from the batch.
 // Lane partials are reduced with shuffles in a fixed order.  RMSNorm: the gain
-// scales the input tile in shared memory, 1/rms scales the outputs, and the
-// sums of squares come from the residual kernels' epilogues (per-CTA partials
-// added in CTA order), so no CTA re-reads the whole of x.
+// vector sits in shared memory and scales each weight word as it is read
+// (w g x = w (g x)), 1/rms scales the outputs, and the sums of squares come
+// from the residual kernels' epilogues (per-CTA partials added in CTA order),
+// so no CTA re-reads the whole of x.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
