@@ -63,6 +63,20 @@ def w13_bytes(wl, wb: int = 4) -> int:
     return wb * 2 * wl.hidden_dim * wl.dim + 4 * (2 * wl.dim + wl.hidden_dim)
 
 
+PREFILL_CHUNK = 64  # rows of one prefill step (l2_prefill's chunk without L2_FLAG_DEBUG)
+
+
+def prefill_chunks(T: int) -> list:
+    """(first position, rows) of each chunk of a T-token prompt from position 0."""
+    return [(c0, min(PREFILL_CHUNK, T - c0)) for c0 in range(0, T, PREFILL_CHUNK)]
+
+
+def prefill_bytes(wl, T: int) -> int:
+    """Algorithmic bytes of a T-token prefill: each chunk streams the weights
+    once and reads the cache rows up to its last position once."""
+    return sum(weight_bytes(wl) + kv_bytes(wl, c0 + r - 1) for c0, r in prefill_chunks(T))
+
+
 def measured_peaks() -> dict:
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -179,7 +193,10 @@ def host_threads() -> int:
     return oracle.num_threads()
 
 
-def metric_of(batch: int, bf16: bool = False) -> str:
+def metric_of(batch: int, bf16: bool = False, prefill: int = 0) -> str:
+    if prefill:
+        return (f"prefill tokens/s of a {prefill}-token prompt and % of HBM roofline "
+                "(GB/s vs ~8 TB/s), 1 GB300")
     if batch > 1:
         return METRIC.replace("at batch 1", f"at batch {batch}")
     return METRIC.replace("at batch 1", "at batch 1 with bf16 weights") if bf16 else METRIC
@@ -221,6 +238,8 @@ def run_reference(args, wl):
     rank, _, world = dist_env()
     if rank != 0:
         return 0  # one CPU baseline per job, taken on rank 0
+    if args.prefill:
+        return run_reference_prefill(args, wl, world)
     import oracle
     B, S = args.batch, wl.seq_len
     host_w = synth.make_weights(wl)
@@ -265,6 +284,32 @@ def run_reference(args, wl):
             "config": cfg,
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": host_threads(), "kind": "oracle",
                              "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_reference_prefill(args, wl, world: int):
+    """The oracle on the same prompt, one teacher-forced step per token from
+    position 0, for as many tokens as the time budget allows."""
+    import oracle
+    T = args.prefill
+    host_w = synth.make_weights(wl)
+    toks = synth.token_stream(wl, 0, T)
+    m = oracle.Model(wl.config_tuple(), host_w)
+    for p in range(min(args.warmup, T)):  # untimed
+        m.forward(int(toks[p]), p)
+    n, el, threads = oracle_rate(wl, host_w, toks, args.reference_budget)
+    value = n / el
+    cfg = config_of(wl, 1)
+    cfg.update({"prefill_tokens": T, "chunk_rows": PREFILL_CHUNK, "positions": f"0..{T - 1}",
+                "gemv": "oracle: fp32 storage, double accumulation, OpenMP rows"})
+    sample = f"the first {n} of the prompt's {T} tokens, one oracle step each, after {min(args.warmup, T)} untimed"
+    line = {"impl": "reference", "metric": metric_of(1, prefill=T), "value": value, "unit": "tokens/s",
+            "n_gpus": world, "steps": 1, "warmup": args.warmup, "ms_per_step": 1000.0 * el,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64-accumulate/f32-storage",
+            "data": "synthetic", "config": cfg,
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
@@ -476,6 +521,103 @@ def run_ours(args, wl):
     return 0
 
 
+def run_ours_prefill(args, wl):
+    """A step is one l2_prefill of the T-token prompt from position 0 of slot 0
+    (the slot rewound first): 64-row chunks, each a batched step."""
+    import torch
+    import torch.distributed as dist
+
+    import llama_transformer_decode_gb300 as pkg
+
+    rank, local_rank, world = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local_rank)
+    pkg._native.load()
+    props = torch.cuda.get_device_properties(local_rank)
+    T = args.prefill
+    cpu_leg = rank == 0 and world == 1 and not args.no_cpu
+    w_dev, host_w = load_weights_device(wl, keep_host=cpu_leg)
+    stream = torch.cuda.Stream()
+    dec = pkg.Decoder(wl.config_tuple(), w_dev, max_batch=1, stream=stream)
+    toks = synth.token_stream(wl, 0, T)
+    out = torch.empty((T, wl.vocab_size), device="cuda")
+    peaks = measured_peaks()
+    hbm = peaks.get("hbm_gbs")
+    peak_src = "of measured" if hbm else "of fallback"
+    hbm = hbm or FALLBACK_HBM_GBS
+
+    def step():
+        dec.reset(0)
+        dec.prefill(toks, pos0=0, slot=0, out=out)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        step()
+    dec.sync()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(str(props.uuid)) as clocks:
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
+        ev1.synchronize()
+    torch.cuda.synchronize()
+    barrier()
+    dec.sync()
+    ms = max_over_ranks(ev0.elapsed_time(ev1), world)
+    value = job_rate(T * args.steps, world, ms / 1000.0)
+
+    # end to end: host tokens in (inside the call), the last row's logits back every step
+    host_last = np.empty(wl.vocab_size, np.float32)
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+        stream.synchronize()
+        host_last[:] = out[T - 1].cpu().numpy()
+    e2e_s = max_over_ranks(time.perf_counter() - t0, world)
+    dec.sync()
+    e2e = {"value": job_rate(T * args.steps, world, e2e_s), "unit": "tokens/s",
+           "h2d_bytes_per_step": dec.step_input_bytes() * len(prefill_chunks(T)),  # tokens ride in each chunk's block
+           "d2h_bytes_per_step": 4 * wl.vocab_size}
+
+    gbs = prefill_bytes(wl, T) * args.steps / (ms / 1000.0) / 1e9
+    roofline = {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm, "traffic": None,
+                "kernel": "whole prefill (all kernels of every chunk)",
+                "bytes_per_step": prefill_bytes(wl, T),
+                "peak_source": peak_src + " (MEASURED_PEAKS.json hbm_gbs)"}
+    cpu = None
+    if cpu_leg:
+        n, el, threads = oracle_rate(wl, host_w, toks, args.cpu_budget)
+        cpu = {"value": n / el, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+               "sample": f"the first {n} tokens of the same prompt, teacher-forced one per oracle step"}
+    launches = sum(5 * wl.n_layers + 1 + (1 if r >= TC_MIN_BATCH else 0) for _, r in prefill_chunks(T))
+    cfg = config_of(wl, 1)
+    cfg.update({"prefill_tokens": T, "chunk_rows": PREFILL_CHUNK, "positions": f"0..{T - 1}, slot rewound each step",
+                "gemv": "tensor cores for chunks of 16+ rows (tcgen05 kind::tf32, 3-term hi/lo split), "
+                        "CUDA cores below"})
+    clk = clocks.summary()
+    line = {
+        "metric": metric_of(1, prefill=T), "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded random weights and tokens)",
+        "config": cfg, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": launches * args.steps, "clocks": {k: clk[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
+    }
+    dec.close()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -487,6 +629,8 @@ def main(argv=None):
                     help="independent sequences per step at staggered positions (batched_1b: 16 or 64)")
     ap.add_argument("--weights", choices=("f32", "bf16"), default="f32",
                     help="bf16: matrices streamed as bf16 (L2_FLAG_BF16_WEIGHTS; batch 1 only)")
+    ap.add_argument("--prefill", type=int, default=0, metavar="T",
+                    help="time l2_prefill of a T-token prompt instead of decode steps (one prompt per step)")
     ap.add_argument("--layers", type=int, default=None,
                     help="decode only the first N layers of the workload (a smaller case, e.g. for profiling)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-baseline leg")
@@ -506,11 +650,18 @@ def main(argv=None):
         if not 1 <= args.layers <= wl.n_layers:
             ap.error(f"--layers must be in 1..{wl.n_layers}")
         wl = wl.replace(n_layers=args.layers, name=f"{wl.name} ({args.layers} layers)")
+    if args.prefill:
+        if not 1 <= args.prefill <= wl.seq_len:
+            ap.error(f"--prefill must be in 1..{wl.seq_len}")
+        if args.batch != 1 or args.weights != "f32":
+            ap.error("--prefill times one prompt with fp32 weights")
+        if args.steps is None:
+            args.steps = 5
     if args.steps is None:
         args.steps = max(1, wl.seq_len - args.warmup)
     if args.impl == "reference":
         return run_reference(args, wl)
-    return run_ours(args, wl)
+    return run_ours_prefill(args, wl) if args.prefill else run_ours(args, wl)
 
 
 if __name__ == "__main__":

@@ -83,13 +83,32 @@ def test_reference_arm_line(batch):
                            "d2h_bytes_per_step": 0}
 
 
+def test_reference_arm_prefill_line():
+    r = _run(["--impl", "reference", "--workload", "tiny", "--prefill", "100", "--reference-budget", "5"])
+    assert r.returncode == 0, r.stderr
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["metric"] == bench.metric_of(1, prefill=100)
+    assert line["config"]["prefill_tokens"] == 100 and line["config"]["chunk_rows"] == bench.PREFILL_CHUNK
+    assert line["value"] > 0 and line["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_prefill_chunks_and_bytes():
+    assert bench.prefill_chunks(130) == [(0, 64), (64, 64), (128, 2)]
+    assert bench.prefill_chunks(64) == [(0, 64)]
+    wl = bench.WORKLOADS["tiny"]
+    # each chunk: the weights once, and the cache rows up to its last position once
+    want = 3 * bench.weight_bytes(wl) + sum(bench.kv_bytes(wl, p) for p in (63, 127, 129))
+    assert bench.prefill_bytes(wl, 130) == want
+
+
 def test_reference_arm_other_ranks_exit_quietly():
     r = _run(["--impl", "reference", "--workload", "tiny"], RANK="1", LOCAL_RANK="1", WORLD_SIZE="2")
     assert r.returncode == 0 and r.stdout.strip() == ""
 
 
 @pytest.mark.parametrize("args", [["--warmup", "2"], ["--batch", "65"], ["--weights", "bf16", "--batch", "4"],
-                                  ["--workload", "tiny", "--layers", "6"]])
+                                  ["--workload", "tiny", "--layers", "6"], ["--workload", "tiny", "--prefill", "513"],
+                                  ["--workload", "tiny", "--prefill", "64", "--batch", "2"]])
 def test_bench_rejects_invalid_runs(args):
     r = _run(["--impl", "reference", *args])
     assert r.returncode == 2 and "error" in r.stderr
