@@ -11,12 +11,17 @@
   keeping only the most probable token, topp outside (0, 1) meaning no
   nucleus.
 - temperature 0: argmax of the logits and no draw from the generator.
-- xorshift*: the page prints the recurrence; what is checked here is what
-  follows from its form: each of the three xor-shift steps is linear over
-  GF(2) and invertible, the state never reaches 0 from a non-zero state, and
-  the 32-bit outputs are uniform (chi-square over 256 bins).  No independent
-  reference values exist on the pages, so the exact constants are pinned only
-  through the bit-exact agreement of the two separate implementations.
+- xorshift*: the walkthrough (§6 Sampler, random_u32()) prints the shifts
+  and the multiplier; they are stored with that citation in
+  tests/golden/sampler_constants.txt.  The oracle's state update, observed
+  on the 64 basis states, is a 64 x 64 matrix over GF(2) that must equal the
+  product of the three elementary matrices I + S built from the printed
+  shifts; that matrix must have order exactly 2^64 - 1 (the generator visits
+  every non-zero state), checked against the prime factors of 2^64 - 1; and
+  the output, for states whose successor is 2^k (preimages taken with the
+  printed matrix, not the oracle), must be the top 32 bits of the printed
+  multiplier times 2^k, which fixes all 64 bits of the multiplier.  Linearity,
+  injectivity, a non-zero orbit and chi-square uniformity are checked too.
 """
 import math
 import os
@@ -73,6 +78,111 @@ def test_xorshift_steps_are_linear_invertible_and_never_zero():
     # invertibility: distinct states map to distinct states on a sample
     xs = {int(v) for v in rng.integers(1, 1 << 62, size=5000)}
     assert len({step(x) for x in xs}) == len(xs)
+
+
+# ---- xorshift* pinned to the constants the walkthrough prints ----
+# A linear map of GF(2)^64 is held as its 64 columns (the images of the basis
+# states 1 << j, as Python ints); products use 8-bit lookup tables.
+
+def _gf2_apply(cols, x):
+    r, j = 0, 0
+    while x:
+        if x & 1:
+            r ^= cols[j]
+        x >>= 1
+        j += 1
+    return r
+
+
+def _gf2_tables(cols):
+    tabs = []
+    for k in range(8):
+        t = [0] * 256
+        for v in range(1, 256):
+            low = v & -v
+            t[v] = t[v ^ low] ^ cols[8 * k + low.bit_length() - 1]
+        tabs.append(t)
+    return tabs
+
+
+def _gf2_compose(f, g):
+    """Columns of f o g."""
+    tf = _gf2_tables(f)
+    out = []
+    for x in g:
+        r = 0
+        for k in range(8):
+            r ^= tf[k][(x >> (8 * k)) & 255]
+        out.append(r)
+    return out
+
+
+IDENTITY = [1 << j for j in range(64)]
+
+
+def _gf2_pow(f, n):
+    result, base = IDENTITY, f
+    while n:
+        if n & 1:
+            result = _gf2_compose(base, result)
+        base = _gf2_compose(base, base)
+        n >>= 1
+    return result
+
+
+def _shift_matrix(k):
+    """Columns of I + S where S shifts a state right by k (k > 0) or left by -k, mod 2^64."""
+    cols = []
+    for j in range(64):
+        src = 1 << j
+        shifted = (src >> k) if k > 0 else ((src << -k) & M64)
+        cols.append(src ^ shifted)
+    return cols
+
+
+def golden_xorshift():
+    from tests.golden import read_golden
+    g = read_golden("sampler_constants.txt")
+    r1, l1, r2 = int(g["shift_right_1"]), int(g["shift_left"]), int(g["shift_right_2"])
+    # the page applies right r1, then left l1, then right r2
+    m = _gf2_compose(_shift_matrix(r2), _gf2_compose(_shift_matrix(-l1), _shift_matrix(r1)))
+    return m, int(g["multiplier"], 16), int(g["output_shift"])
+
+
+# prime factors of 2^64 - 1 = (2^32 + 1)(2^16 + 1)(2^8 + 1)(2^4 + 1)(2^2 + 1)(2 + 1)
+ORDER_PRIMES = (3, 5, 17, 257, 641, 65537, 6700417)
+
+
+def _is_prime(n):
+    return n > 1 and all(n % d for d in range(2, int(math.isqrt(n)) + 1))
+
+
+def oracle_step_matrix(lib=None):
+    return [oracle.random_u32(1 << j, lib)[1] for j in range(64)]
+
+
+def test_xorshift_update_is_the_printed_recurrence():
+    m, _, _ = golden_xorshift()
+    assert oracle_step_matrix() == m
+
+
+def test_xorshift_has_full_period():
+    assert math.prod(ORDER_PRIMES) == M64 and all(_is_prime(p) for p in ORDER_PRIMES)
+    m = oracle_step_matrix()
+    assert _gf2_pow(m, M64) == IDENTITY
+    for p in ORDER_PRIMES:
+        assert _gf2_pow(m, M64 // p) != IDENTITY, p
+
+
+def test_xorshift_output_is_the_printed_multiplier():
+    m, mult, out_shift = golden_xorshift()
+    inv = _gf2_pow(m, M64 - 1)  # m has order 2^64 - 1 (checked above), so this is its inverse
+    for k in (0, 1, 7, 31, 32, 33, 63):
+        target = 1 << k
+        pre = _gf2_apply(inv, target)
+        v, s = oracle.random_u32(pre)
+        assert s == target
+        assert v == ((target * mult) & M64) >> out_shift, k
 
 
 def test_coin_is_uniform():
@@ -170,7 +280,27 @@ MUTANTS = [
     ("taylor_term_dropped", "float p = c7;\n    p = fmaf(p, r, c6);", "float p = c6;"),
     ("argmax_last_maximum", "if (v[i] > v[best]) best = i;", "if (v[i] >= v[best]) best = i;"),
     ("exp_reduction_low_part_dropped", "r = fmaf(-k, ln2_lo, r);", ";"),
+    ("xorshift_first_shift_wrong", "*state ^= *state >> 12;", "*state ^= *state >> 13;"),
+    ("xorshift_left_shift_wrong", "*state ^= *state << 25;", "*state ^= *state << 24;"),
+    ("xorshift_last_shift_wrong", "*state ^= *state >> 27;", "*state ^= *state >> 26;"),
+    ("xorshift_shift_direction_flipped", "*state ^= *state << 25;", "*state ^= *state >> 25;"),
+    ("xorshift_steps_reordered", "*state ^= *state >> 12;\n    *state ^= *state << 25;",
+     "*state ^= *state << 25;\n    *state ^= *state >> 12;"),
+    ("xorshift_multiplier_digit_wrong", "0x2545F4914F6CDD1DULL", "0x2545F4914F6CDD1FULL"),
+    ("xorshift_output_low_half", "return (uint32_t)((*state * 0x2545F4914F6CDD1DULL) >> 32);",
+     "return (uint32_t)(*state * 0x2545F4914F6CDD1DULL);"),
 ]
+
+
+_GOLD_INV = []
+
+
+def golden_xorshift_inverse():
+    """((printed update matrix, its inverse), multiplier, output shift), computed once."""
+    if not _GOLD_INV:
+        m, mult, out_shift = golden_xorshift()
+        _GOLD_INV.append(((m, _gf2_pow(m, M64 - 1)), mult, out_shift))
+    return _GOLD_INV[0]
 
 
 def quick_battery(lib) -> list:
@@ -226,8 +356,18 @@ def quick_battery(lib) -> list:
             seen.add(idx)
         return seen == {0, 1, 2}
 
+    def xorshift_ok():
+        m, mult, out_shift = golden_xorshift_inverse()
+        if oracle_step_matrix(lib) != m[0]:
+            return False
+        for k in (0, 32):
+            v, s = oracle.random_u32(_gf2_apply(m[1], 1 << k), lib)
+            if s != 1 << k or v != (((1 << k) * mult) & M64) >> out_shift:
+                return False
+        return True
+
     for name, fn in (("exp", exp_ok), ("argmax", argmax_ok), ("closed_form", closed_form_ok),
-                     ("temperature", temperature_ok), ("topp", topp_ok)):
+                     ("temperature", temperature_ok), ("topp", topp_ok), ("xorshift", xorshift_ok)):
         check(name, fn)
     return failed
 
