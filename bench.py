@@ -39,9 +39,9 @@ NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of
-# the dominant kernel, from the ncu capture summarised in
-# profiles/gemv_w13_llama2_7b.md, valid only for the kernel source whose
-# sha256 prefix is recorded beside it.
+# the dominant kernel (rmsnorm + W1/W3 + SwiGLU at the 7B shape), from one ncu
+# capture of that kernel, valid only for the kernel source whose sha256 prefix
+# is recorded beside it.
 W13_NCU_TRAFFIC = (363805696, "0bcb08e0f8b8c52c")  # (bytes per launch, gemv.cu sha256 prefix)
 
 
@@ -315,6 +315,124 @@ def run_reference_prefill(args, wl, world: int):
     return 0
 
 
+# Every workload's own throughput, reported beside the headline line: the
+# small decoders over their full teacher-forced runs, and the batched workload
+# at one, 16 and 64 sequences.
+DEFAULT_PER_CONFIG = "tiny,gqa_small,mid,batched_1b,batched_1b:16,batched_1b:64"
+BATCHED_PER_CONFIG_STEPS = 256
+L2_BYTES = 129e6  # the GPU's L2 cache: weights below this stay resident between steps
+
+
+def parse_per_config(spec: str) -> list:
+    """[(workload, batch)] from "name[:B],..." ("none": no entries)."""
+    if not spec or spec == "none":
+        return []
+    out = []
+    for item in spec.split(","):
+        name, _, b = item.strip().partition(":")
+        if name not in WORKLOADS:
+            raise ValueError(f"unknown workload {name!r} in --per-config")
+        B = int(b) if b else 1
+        if not 1 <= B <= 64:
+            raise ValueError(f"batch {B} outside 1..64 in --per-config")
+        out.append((name, B))
+    return out
+
+
+def per_config_rates(entries, hbm: float, peak_src: str, runs: int) -> dict:
+    """Tokens/s and HBM bandwidth of each (workload, batch), each on its own
+    decoder and stream, timed with CUDA events after an untimed pass that
+    builds its graphs.  Batch 1: the workload's full teacher-forced run from
+    position 0, `runs` times (the cache rewound each run), median reported.
+    Batches: slot b starts at floor(b * seq_len / B) (earlier rows imported) and
+    steps BATCHED_PER_CONFIG_STEPS times, wrapping at the end of the context;
+    `runs` consecutive segments, median reported."""
+    import torch
+
+    import llama_transformer_decode_gb300 as pkg
+    out = {}
+    loaded = {}
+    for name, B in entries:
+        wl = WORKLOADS[name]
+        if name not in loaded:
+            loaded.clear()
+            loaded[name] = load_weights_device(wl, keep_host=False)[0]
+        w = loaded[name]
+        stream = torch.cuda.Stream()
+        dec = pkg.Decoder(wl.config_tuple(), w, max_batch=B, stream=stream)
+        S = wl.seq_len
+        batched = B > 1 or name == "batched_1b"
+        n = min(BATCHED_PER_CONFIG_STEPS, S) if batched else min(wl.steps or S, S)
+        offsets = [b * S // B for b in range(B)]
+        streams = [synth.token_stream(wl, b, S) for b in range(B)]
+        logits = torch.empty((B, wl.vocab_size), device="cuda")
+
+        def prepare():
+            dec.reset()
+            for b in range(B):
+                if offsets[b]:
+                    dec.kv_import(synth.kv_rows(wl, b, offsets[b], "k"), synth.kv_rows(wl, b, offsets[b], "v"),
+                                  slot=b)
+
+        def steps(first, count):
+            for st in range(first, first + count):
+                pos = [(offsets[b] + st) % S for b in range(B)]
+                for b in range(B):
+                    if pos[b] == 0 and dec.position(b) > 0:
+                        dec.reset(b)
+                if B == 1:
+                    dec.forward(int(streams[0][pos[0]]), pos[0], logits[0])
+                else:
+                    dec.forward_batch([int(streams[b][pos[b]]) for b in range(B)], pos, logits)
+            return [[(offsets[b] + st) % S for b in range(B)] for st in range(first, first + count)]
+
+        prepare()
+        steps(0, min(n, 8))  # untimed: builds the graphs
+        dec.sync()
+        times, byts = [], []
+        if not batched:
+            for _ in range(runs):
+                prepare()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                pos = steps(0, n)
+                e1.record(stream)
+                e1.synchronize()
+                times.append(e0.elapsed_time(e1) / 1000.0)
+                byts.append(sum(weight_bytes(wl) + sum(kv_bytes(wl, p) for p in ps) for ps in pos))
+            where = f"0..{n - 1}, {runs} runs"
+        else:
+            prepare()
+            seg = max(1, n // runs)
+            for r in range(runs):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                pos = steps(r * seg, seg)
+                e1.record(stream)
+                e1.synchronize()
+                times.append(e0.elapsed_time(e1) / 1000.0)
+                byts.append(sum(weight_bytes(wl) + sum(kv_bytes(wl, p) for p in ps) for ps in pos))
+            n = seg
+            where = (f"slot b from floor(b*{S}/{B}), {runs} segments of {seg} steps" if B > 1 else
+                     f"0..{runs * seg - 1} in {runs} segments of {seg} steps")
+        dec.sync()
+        order = sorted(range(len(times)), key=lambda i: times[i])
+        mid = order[len(order) // 2]
+        t, by = times[mid], byts[mid]
+        gbs = by / t / 1e9
+        key = name if B == 1 and name != "batched_1b" else f"{name}_b{B}"
+        out[key] = {
+            "batch": B, "tokens_per_s": B * n / t, "ms_per_step": 1000.0 * t / n, "steps": n, "positions": where,
+            "gbs": gbs, "frac_of_measured": gbs / hbm, "frac_of_8tbs": gbs / NOMINAL_HBM_GBS,
+            "bytes_per_step_avg": by / n, "l2_resident": weight_bytes(wl) < L2_BYTES,
+            "launches_per_step": dec.kernels_per_step(B),
+            "gemv": "tensor cores (3-term tf32)" if B >= TC_MIN_BATCH else "CUDA cores (fp32 FMA)"}
+        dec.close()
+    loaded.clear()
+    out["_peak"] = f"{hbm:.1f} GB/s {peak_src} (MEASURED_PEAKS.json hbm_gbs); timing: CUDA events, median of {runs}"
+    return out
+
+
 def fp32_alu_peak_tflops(props) -> float:
     """fp32 FMA peak: SMs x 128 lanes x 2 flop x the maximum SM clock."""
     peaks = measured_peaks()
@@ -494,6 +612,15 @@ def run_ours(args, wl):
         cpu = {"value": n / el, "unit": "tokens/s", "cores": threads, "kind": "oracle",
                "sample": f"{n} teacher-forced oracle steps of {wl.name} (one sequence) at positions 0..{n - 1}"}
 
+    # ---- every workload's own rate (after the headline decoder is freed) ----
+    per_config = None
+    entries = parse_per_config(args.per_config) if (B == 1 and not bf16 and world == 1) else []
+    if entries:
+        dec.close()
+        del w_dev
+        dec = None
+        per_config = per_config_rates(entries, hbm, peak_src, args.per_config_runs)
+
     clk = clocks.summary()
     cfg = config_of(wl, B)
     cfg["positions"] = (f"{timed_pos[0][0]}..{timed_pos[-1][0]}" if B == 1 else
@@ -511,9 +638,11 @@ def run_ours(args, wl):
                          "frac_of_measured": step_gbs / hbm,
                          "bytes_per_step_avg": bytes_total / max(1, len(timed_pos))},
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "per_position": per_pos or None,
+        "per_config": per_config,
         "gpu_launches": kern * args.steps, "clocks": {k: clk[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
     }
-    dec.close()
+    if dec is not None:
+        dec.close()
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -635,6 +764,10 @@ def main(argv=None):
                     help="decode only the first N layers of the workload (a smaller case, e.g. for profiling)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-baseline leg")
     ap.add_argument("--no-positions", action="store_true", help="skip the per-position rates")
+    ap.add_argument("--per-config", default=None, metavar="LIST",
+                    help="workloads whose own rates the batch-1 decode line reports, as name[:batch],... "
+                         f"(default for llama2_7b: {DEFAULT_PER_CONFIG}; 'none' skips)")
+    ap.add_argument("--per-config-runs", type=int, default=5, help="timed runs per entry of --per-config (median)")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time for the CPU baseline")
     ap.add_argument("--reference-budget", type=float, default=90.0,
                     help="seconds of timed oracle work in --impl reference")
@@ -645,6 +778,14 @@ def main(argv=None):
         ap.error("--batch must be in 1..64")
     if args.weights == "bf16" and (args.batch != 1 or args.impl != "ours"):
         ap.error("--weights bf16 is a batch-1 option of this implementation")
+    if args.per_config is None:
+        args.per_config = DEFAULT_PER_CONFIG if args.workload == "llama2_7b" and args.layers is None else "none"
+    try:
+        parse_per_config(args.per_config)
+    except ValueError as e:
+        ap.error(str(e))
+    if args.per_config_runs < 1:
+        ap.error("--per-config-runs must be at least 1")
     wl = WORKLOADS[args.workload]
     if args.layers is not None:
         if not 1 <= args.layers <= wl.n_layers:

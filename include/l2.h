@@ -117,12 +117,18 @@ int l2_create(const L2Config *config, const L2Weights *weights, int max_batch, u
               void *cuda_stream, l2_ctx **out);
 
 /* Rewinds the KV cache of one slot (-1: all slots) to zero written rows.
- * Host bookkeeping only; no device work.  L2_EINVAL on a bad slot. */
+ * The cache is the pages' key_cache / value_cache of the run state, one per
+ * slot ("run.c 逐行解讀" §3 memory management, malloc_run_state: n_layers x
+ * seq_len x kv_dim floats each; "run.c", RunState and malloc_run_state), which
+ * forward() fills one row per position; rewinding starts a new sequence at
+ * position 0 without clearing memory (rows are always written before they
+ * are read).  Host bookkeeping only; no device work.  L2_EINVAL on a bad slot. */
 int l2_reset(l2_ctx *ctx, int slot);
 
 /*
- * One decode step of slot 0: enqueues forward(token, pos) and writes the
- * vocab_size logits to logits_out (a DEVICE pointer, or NULL to keep them
+ * One decode step of slot 0: enqueues forward(token, pos) ("run.c 逐行解讀"
+ * §4 forward(), steps 1-3; "run.c", transformer(token, pos, ...)) and writes
+ * the vocab_size logits to logits_out (a DEVICE pointer, or NULL to keep them
  * only in the handle's buffer, see l2_logits).  Preconditions checked on
  * the host: 0 <= token < vocab_size, 0 <= pos < seq_len, and pos <= the
  * number of rows already written to the slot's cache (rows 0..pos-1 must
@@ -148,7 +154,9 @@ int l2_forward_host(l2_ctx *ctx, int token, int pos, float *logits_host);
 const float *l2_logits(const l2_ctx *ctx);
 
 /* Number of cache rows written for a slot (the next pos it may step), or
- * L2_EINVAL. */
+ * L2_EINVAL.  forward() at pos reads rows 0..pos of the layer's cache and
+ * writes row pos ("run.c 逐行解讀" §4 forward() step 2e and the K/V write
+ * into key_cache / value_cache), so pos may not exceed this count. */
 int l2_position(const l2_ctx *ctx, int slot);
 
 /*
@@ -171,14 +179,19 @@ int l2_kv_import(l2_ctx *ctx, int slot, int n_pos, const float *k_in, const floa
 
 /* Waits for the handle's stream and reports asynchronous failures:
  * L2_ECUDA for a CUDA error, L2_EDEVICE / L2_ETIMEOUT for a kernel that set
- * the device error word (the word is cleared).  Blocks. */
+ * the device error word (the word is cleared, and so are the attention and
+ * tensor-core tickets, which a kernel that gave up may have left counted).
+ * Blocks.  The pages have no asynchronous work and so no counterpart; their
+ * failures end the process ("run.c", malloc_run_state: exit(1) after a failed
+ * calloc), which this library never does. */
 int l2_sync(l2_ctx *ctx);
 
 /* Text of the last failure on this handle ("" if none).  With a NULL
  * handle, the last failure of l2_create on this thread. */
 const char *l2_last_error(const l2_ctx *ctx);
 
-/* Frees everything the handle owns.  Waits for its stream first. */
+/* Frees everything the handle owns (the pages' free_run_state: "run.c",
+ * the activations, logits and the KV cache).  Waits for its stream first. */
 void l2_destroy(l2_ctx *ctx);
 
 /*
@@ -253,9 +266,11 @@ int l2_step_input_bytes(void);
  * attention CTAs that fit on one SM (at most 4), is refused
  * with L2_EINVAL before anything is enqueued.  (With one attention CTA per
  * SM on 152 SMs: 16.6 k floats at the Llama-2-7B shape; 8 query heads per KV
- * head of size 128 need 158 k and are refused.)  The first call on a device
- * looks up the array's device address; make that first call before any
- * stream capture.  The handle's device must be current.  Every call shares
+ * head of size 128 need 158 k and are refused.)  l2_create looks up the
+ * array's device address (once per device, with that device current), which
+ * loads the module that holds it: the array is resident on a device from the
+ * first handle created there, so this entry point itself never makes the
+ * runtime allocate.  The handle's device must be current.  Every call shares
  * the array and clears its tickets first: calls whose kernels overlap on the
  * GPU (handles on different streams) race and give wrong results.
  */
@@ -297,6 +312,27 @@ int l2_sample(const float *logits, int B, int vocab_size, float temperature, flo
  * (n >= 1) fail as if out of memory; 0 disables.  Process-wide.
  */
 void l2_debug_fail_alloc_at(int n);
+
+/*
+ * Fault injection for tests: makes the n-th CUDA graph instantiation from now
+ * on (n >= 1) fail; the step that needed the graph returns L2_ECUDA with
+ * nothing run and the cache position unchanged, and the next call builds the
+ * graph again.  0 disables.  Process-wide.
+ */
+void l2_debug_fail_graph_at(int n);
+
+/*
+ * Failure-path check for tests: enqueues one kernel on the handle's stream
+ * that waits, with a limit of limit_us microseconds (1..2000000), on an
+ * mbarrier that nothing arrives on, through the same bounded wait the decode
+ * kernels use.  When the wait gives up it sets the device error word, waits
+ * (bounded) for its own bulk copy in flight and returns; it also leaves the
+ * handle's attention tickets counted, as a chunk merge that stopped early
+ * would.  The next l2_sync then returns L2_ETIMEOUT, clears the error word and
+ * the tickets, and the handle steps normally again.  Nothing faults or hangs.
+ * L2_EINVAL for a bad handle or limit.  The pages have no counterpart.
+ */
+int l2_debug_wait_timeout(l2_ctx *ctx, int limit_us);
 
 #ifdef __cplusplus
 }

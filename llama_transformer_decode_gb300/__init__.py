@@ -166,6 +166,10 @@ class Decoder:
     def sync(self):
         self._check(self._lib.l2_sync(self._h))
 
+    def debug_wait_timeout(self, limit_us: int):
+        """Enqueue a kernel whose bounded wait gives up after limit_us (l2_debug_wait_timeout)."""
+        self._check(self._lib.l2_debug_wait_timeout(self._h, int(limit_us)))
+
     def debug_attention(self, layer: int, slot: int = 0) -> np.ndarray:
         n = self.position(slot)
         out = np.empty((self.n_heads, n), np.float32)
@@ -224,6 +228,11 @@ def sample(logits, temperature: float, topp: float, rng_state, out=None, stream=
 def fail_alloc_at(n: int):
     """Fault injection: the n-th device allocation from now on fails (0 disables)."""
     lib().l2_debug_fail_alloc_at(int(n))
+
+
+def fail_graph_at(n: int):
+    """Fault injection: the n-th CUDA graph instantiation from now on fails (0 disables)."""
+    lib().l2_debug_fail_graph_at(int(n))
 
 
 def to_device(weights: dict, device="cuda") -> dict:

@@ -82,7 +82,7 @@ EXPORTS = ("l2_create", "l2_reset", "l2_forward", "l2_forward_batch", "l2_forwar
            "l2_position", "l2_debug_attention", "l2_kv_export", "l2_kv_import", "l2_sync",
            "l2_last_error", "l2_destroy", "l2_launch_op", "l2_kernels_per_step",
            "l2_step_input_bytes", "l2_forward_static", "l2_debug_fail_alloc_at", "l2_sample",
-           "l2_forward_dev_tokens", "l2_prefill")
+           "l2_forward_dev_tokens", "l2_prefill", "l2_debug_fail_graph_at", "l2_debug_wait_timeout")
 
 _lib = None
 
@@ -120,6 +120,10 @@ def declare(lib):
     lib.l2_forward_dev_tokens.restype = i
     lib.l2_prefill.argtypes = [vp, i, i, ip, i, fp]
     lib.l2_prefill.restype = i
+    lib.l2_debug_fail_graph_at.argtypes = [i]
+    lib.l2_debug_fail_graph_at.restype = None
+    lib.l2_debug_wait_timeout.argtypes = [vp, i]
+    lib.l2_debug_wait_timeout.restype = i
     for name in ("l2_create", "l2_reset", "l2_forward", "l2_forward_batch", "l2_forward_host",
                  "l2_position", "l2_debug_attention", "l2_kv_export", "l2_kv_import", "l2_sync",
                  "l2_launch_op", "l2_kernels_per_step", "l2_forward_static"):

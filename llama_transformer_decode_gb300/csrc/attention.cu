@@ -379,11 +379,15 @@ __global__ void __launch_bounds__(kNWA * 32) attn_kernel(const AttnParams p) {
         }
     }
     __syncthreads();
-    if (flags[0]) return;
+    // A CTA whose wait gave up (the error word is already set) publishes
+    // nothing, but with several chunks it still takes its ticket below, so the
+    // group's count completes and the last CTA resets it for the next launch.
+    const bool gave_up = flags[0] != 0;
 
     // merge the warps in warp order and publish this CTA's partial
     const int NC = p.n_chunks;
     if (n_active == 1) {
+        if (gave_up) return;
         // The only chunk: normalise and write the output directly.
         for (int idx = tid; idx < nq * hs4; idx += NT) {
             const int j = idx / hs4, w4 = idx % hs4;
@@ -410,7 +414,7 @@ __global__ void __launch_bounds__(kNWA * 32) attn_kernel(const AttnParams p) {
         }
         return;
     }
-    for (int idx = tid; idx < nq * hs4; idx += NT) {
+    for (int idx = tid; idx < (gave_up ? 0 : nq * hs4); idx += NT) {
         const int j = idx / hs4, w4 = idx % hs4;
         float mm = -CUDART_INF_F, ll = 0.f;
         float4 aa = make_float4(0.f, 0.f, 0.f, 0.f);

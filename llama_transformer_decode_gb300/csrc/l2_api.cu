@@ -17,10 +17,12 @@
 #include <cstddef>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <string>
 #include <vector>
 
 #include "../../include/l2.h"
+#include "l2_device.cuh"
 #include "l2_kernels.h"
 #include "l2_params.h"
 
@@ -55,6 +57,7 @@ constexpr int kMinChunk = L2_ATTN_MIN_CHUNK;
 
 thread_local std::string g_create_error;
 int g_fail_alloc_at = 0;  // fault injection: fail the n-th device allocation
+int g_fail_graph_at = 0;  // fault injection: fail the n-th graph instantiation
 
 struct BatchPlan {
     BatchParams bp;  // tensor maps, partition, tiles (layer fields filled per launch)
@@ -110,6 +113,7 @@ struct l2_ctx {
     float *tc_ws = nullptr;       // tensor-core GEMV split-K partial tiles
     float *xg = nullptr;          // tensor-core path: x * gain of the next RMSNorm [max_rows][dim]
     unsigned *tc_tickets = nullptr;
+    size_t tc_tickets_n = 0;      // entries of tc_tickets
 
     StepDev *step_host = nullptr;  // pinned ring
     cudaEvent_t ring_ev[kRing] = {};
@@ -131,6 +135,7 @@ struct l2_ctx {
     std::vector<BatchSet> bsets;  // batched GEMV plans, indexed by batch size
     bool evict_first = false;
 
+    float *static_scratch = nullptr;  // device address of the l2_forward_static array on this device
     std::vector<int> written;  // cache rows written per slot
     std::string error;
 };
@@ -775,6 +780,10 @@ int get_graph(l2_ctx *c, int batch, bool prefill, cudaGraphExec_t *out) {
         return cuda_fail(c, e, "kernel launch during graph capture");
     }
     if (e2 != cudaSuccess) return cuda_fail(c, e2, "cudaStreamEndCapture");
+    if (g_fail_graph_at > 0 && --g_fail_graph_at == 0) {
+        cudaGraphDestroy(g);
+        return fail(c, L2_ECUDA, "cudaGraphInstantiate failed (injected)");
+    }
     cudaGraphExec_t ex = nullptr;
     e = cudaGraphInstantiate(&ex, g, 0);
     cudaGraphDestroy(g);
@@ -782,6 +791,32 @@ int get_graph(l2_ctx *c, int batch, bool prefill, cudaGraphExec_t *out) {
     *slot = ex;
     *out = ex;
     return L2_OK;
+}
+
+// Failure-path check (l2_debug_wait_timeout): one CTA completes a bulk copy
+// into stage 0 of a two-stage ring, then waits on stage 1, which nothing ever
+// fills, with a short limit.  The wait gives up and sets the error word; the
+// CTA then waits (bounded) for its copy in flight and returns, as the decode
+// kernels do.  It also leaves every attention ticket counted once, as a chunk
+// merge that stopped before resetting its ticket would.
+__global__ void __launch_bounds__(32)
+    debug_wait_kernel(const float *src, uint32_t bytes, int *err, unsigned *tickets, int n_tickets,
+                      unsigned long long limit_ns) {
+    __shared__ __align__(128) float buf[32];
+    __shared__ __align__(8) uint64_t bars[2];
+    if (threadIdx.x == 0) {
+        mbar_init(&bars[0], 1);
+        mbar_init(&bars[1], 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        mbar_arrive_expect_tx(&bars[0], bytes);
+        bulk_g2s_nohint(buf, src, bytes, &bars[0]);
+    }
+    const bool filled = mbar_wait_limit(&bars[1], 0, err, limit_ns);  // nothing arrives: gives up
+    if (!filled) (void)mbar_wait_limit(&bars[0], 0, err, kWaitLimitNs);
+    for (int i = threadIdx.x; i < n_tickets; i += 32) atomicAdd(&tickets[i], 1u);
 }
 
 // Copies B tokens from device memory into the step block, each checked
@@ -863,6 +898,39 @@ int submit(l2_ctx *c, int B, const int *tokens, const int *pos, float *logits_ou
 
 }  // namespace
 
+// Attention scratch of l2_forward_static: accumulators, (max, sum) pairs and
+// tickets, 512 KiB.  Every GPU that loads the library holds it until exit.  In
+// host code this name is only a stand-in: kernels get the address that
+// cudaGetSymbolAddress returns for the current device, looked up by l2_create
+// (so the module that holds the array is loaded, and the array allocated,
+// when the first handle on a device is created, not by a later decode call).
+constexpr size_t kStaticScratchFloats = size_t(1) << 17;
+static __device__ __align__(256) float g_static_scratch[kStaticScratchFloats];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_static_scratch_mu;
+float *g_static_scratch_ptr[kMaxDevices] = {};  // device address, per device
+
+// The array's device address on `device`, which must be current; looked up
+// once per device.
+int static_scratch_address(l2_ctx *c, int device, float **out) {
+    *out = nullptr;
+    if (device < 0 || device >= kMaxDevices) return fail(c, L2_EINVAL, "device index %d too large", device);
+    std::lock_guard<std::mutex> lock(g_static_scratch_mu);
+    if (!g_static_scratch_ptr[device]) {
+        void *p = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
+        if (e != cudaSuccess) return cuda_fail(c, e, "cudaGetSymbolAddress(static attention scratch)");
+        g_static_scratch_ptr[device] = static_cast<float *>(p);
+    }
+    *out = g_static_scratch_ptr[device];
+    return L2_OK;
+}
+
+}  // namespace
+
 extern "C" {
 
 int l2_create(const L2Config *config, const L2Weights *weights, int max_batch, unsigned flags, void *cuda_stream,
@@ -915,6 +983,7 @@ int l2_create(const L2Config *config, const L2Weights *weights, int max_batch, u
     } while (0)
 
     CREATE_CUDA(cudaGetDevice(&c->device));
+    if ((rc = static_scratch_address(c, c->device, &c->static_scratch))) return bail(rc);
     CREATE_CUDA(cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device));
     int l2_bytes = 0;
     CREATE_CUDA(cudaDeviceGetAttribute(&l2_bytes, cudaDevAttrL2CacheSize, c->device));
@@ -1035,6 +1104,7 @@ int l2_create(const L2Config *config, const L2Weights *weights, int max_batch, u
                 (rc = alloc_n(c, &c->tc_tickets, (size_t)tiles, "tensor-core GEMV tickets")))
                 return bail(rc);
             CREATE_CUDA(cudaMemset(c->tc_tickets, 0, (size_t)tiles * sizeof(unsigned)));
+            c->tc_tickets_n = (size_t)tiles;
         }
     }
     if ((rc = plan_persistent(c))) return bail(rc);
@@ -1178,6 +1248,11 @@ int l2_sync(l2_ctx *c) {
     int word = 0;
     L2_CUDA(c, cudaMemcpy(&word, c->err, sizeof(int), cudaMemcpyDeviceToHost));
     if (word) {
+        // A kernel that gave up may have left a ticket counted (the tensor-core
+        // GEMV's CTAs take theirs only after their last tile): start the next
+        // step from zero.
+        L2_CUDA(c, cudaMemset(c->tickets, 0, (size_t)c->max_rows * c->cfg.n_kv_heads * sizeof(unsigned)));
+        if (c->tc_tickets) L2_CUDA(c, cudaMemset(c->tc_tickets, 0, c->tc_tickets_n * sizeof(unsigned)));
         L2_CUDA(c, cudaMemset(c->err, 0, sizeof(int)));
         if (word & L2_DEV_ERR_TIMEOUT) return fail(c, L2_ETIMEOUT, "a device-side wait gave up (error word 0x%x)", word);
         return fail(c, L2_EDEVICE, "a kernel reported an error (error word 0x%x)", word);
@@ -1247,6 +1322,20 @@ int l2_step_input_bytes(void) { return (int)sizeof(StepDev); }
 
 void l2_debug_fail_alloc_at(int n) { g_fail_alloc_at = n > 0 ? n : 0; }
 
+void l2_debug_fail_graph_at(int n) { g_fail_graph_at = n > 0 ? n : 0; }
+
+int l2_debug_wait_timeout(l2_ctx *c, int limit_us) {
+    if (!c) return L2_EINVAL;
+    if (limit_us < 1 || (unsigned long long)limit_us * 1000ull > kWaitLimitNs)
+        return fail(c, L2_EINVAL, "limit_us %d outside 1..%llu", limit_us, kWaitLimitNs / 1000ull);
+    // dim is a multiple of 4, so this is a multiple of 16 bytes, at most the kernel's buffer
+    const uint32_t bytes = (uint32_t)std::min<size_t>(128, (size_t)c->cfg.dim * sizeof(float));
+    debug_wait_kernel<<<1, 32, 0, c->stream>>>(c->x, bytes, c->err, c->tickets, c->max_rows * c->cfg.n_kv_heads,
+                                               (unsigned long long)limit_us * 1000ull);
+    L2_CUDA(c, cudaGetLastError());
+    return L2_OK;
+}
+
 }  // extern "C"
 
 // ---------------------------------------------------------------------------
@@ -1259,33 +1348,6 @@ void l2_debug_fail_alloc_at(int n) { g_fail_alloc_at = n > 0 ? n : 0; }
 // kernels one by one instead, and gives the one kernel that needs scratch
 // memory -- attention, for its cross-CTA partial results and tickets -- a
 // static device array in place of the handle's workspace.
-
-// Attention scratch of l2_forward_static: accumulators, (max, sum) pairs and
-// tickets, 512 KiB.  Every GPU that loads the library holds it until exit.  In
-// host code this name is only a stand-in: kernels get the address that
-// cudaGetSymbolAddress returns for the current device.
-constexpr size_t kStaticScratchFloats = size_t(1) << 17;
-static __device__ __align__(256) float g_static_scratch[kStaticScratchFloats];
-
-namespace {
-
-constexpr int kMaxDevices = 64;
-float *g_static_scratch_ptr[kMaxDevices] = {};  // device address, per device
-
-// Looks up the array's device address on the current device (once per device).
-int static_scratch(l2_ctx *c, float **out) {
-    if (c->device < 0 || c->device >= kMaxDevices) return fail(c, L2_EINVAL, "device index %d too large", c->device);
-    if (!g_static_scratch_ptr[c->device]) {
-        void *p = nullptr;
-        cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
-        if (e != cudaSuccess) return cuda_fail(c, e, "cudaGetSymbolAddress(static attention scratch)");
-        g_static_scratch_ptr[c->device] = static_cast<float *>(p);
-    }
-    *out = g_static_scratch_ptr[c->device];
-    return L2_OK;
-}
-
-}  // namespace
 
 extern "C" int l2_forward_static(l2_ctx *c, int token, int pos, float *logits_out) {
     if (!c) return L2_EINVAL;
@@ -1310,9 +1372,7 @@ extern "C" int l2_forward_static(l2_ctx *c, int token, int pos, float *logits_ou
         return fail(c, L2_EINVAL,
                     "attention needs %zu floats of scratch; l2_forward_static has a static array of %zu floats",
                     need, kStaticScratchFloats);
-    float *scratch = nullptr;
-    int rc = static_scratch(c, &scratch);
-    if (rc) return rc;
+    float *scratch = c->static_scratch;  // looked up by l2_create on this device
     float *ws_acc = scratch, *ws_ml = scratch + acc_f;
     unsigned *tickets = reinterpret_cast<unsigned *>(scratch + acc_f + ml_f);
 

@@ -76,18 +76,23 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 }
 
 // Waits for phase `parity` of `bar` to complete.  Gives up after about
-// kWaitLimitNs of wall time, records L2_DEV_ERR_TIMEOUT in *err and returns
+// limit_ns of wall time, records L2_DEV_ERR_TIMEOUT in *err and returns
 // false; the caller then stops using the barrier's buffer.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *err) {
+__device__ __forceinline__ bool mbar_wait_limit(uint64_t *bar, uint32_t parity, int *err, uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 255u) == 0 && globaltimer_ns() - t0 > kWaitLimitNs) {
+        if ((i & 255u) == 0 && globaltimer_ns() - t0 > limit_ns) {
             atomicOr(err, L2_DEV_ERR_TIMEOUT);
             return false;
         }
     }
+}
+
+// The kernels' wait: gives up after kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *err) {
+    return mbar_wait_limit(bar, parity, err, kWaitLimitNs);
 }
 
 // L2 eviction-priority policies for the bulk copies.

@@ -14,8 +14,7 @@
  *           §4 forward() steps 1, 2a-2h and 3 (GQA, on-the-fly RoPE, KV
  *           written into the cache row, wcls).
  *
- * Readings where the pages leave a step open (each is listed in the design
- * notes with its reasoning):
+ * Readings where the pages leave a step open:
  *   - every stored vector (x, xb, q, k, v, the KV cache, hb, logits) is fp32
  *     as on the pages; dot products, the sum of squares, the softmax sum and
  *     the weighted V sum are accumulated in double and rounded to fp32 once;

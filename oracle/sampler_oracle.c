@@ -19,7 +19,7 @@
  *           with 0 < topp < 1 sampling from the smallest set of most
  *           probable tokens whose probability reaches topp).
  *
- * Readings where the pages are silent (each listed in the design notes):
+ * Readings where the pages are silent:
  *   - the coin: the top 24 bits of one random_u32() draw, k / 2^24;
  *   - the softmax is evaluated as e_i = E(l_i / T - max_j l_j / T), with E
  *     the fp32 exponential specified below, and each e_i is then held as

@@ -69,3 +69,20 @@ def test_prefill_line():
     assert line["config"]["prefill_tokens"] == 130
     assert line["gpu_launches"] == 2 * (2 * (5 * 5 + 2) + (5 * 5 + 1))  # chunks of 64, 64 and 2 rows
     assert line["e2e"]["h2d_bytes_per_step"] == 3 * 1048
+
+
+def test_decode_line_per_config_block():
+    line = run_arm("--workload", "tiny", "--steps", "4", "--warmup", "3", "--cpu-budget", "0.5", "--no-positions",
+                   "--per-config", "tiny,tiny:4", "--per-config-runs", "2")
+    check_common(line, 4, 3)
+    pc = line["per_config"]
+    assert set(pc) == {"tiny", "tiny_b4", "_peak"}
+    for key, B, steps in (("tiny", 1, 128), ("tiny_b4", 4, 128)):
+        e = pc[key]
+        assert e["batch"] == B and e["steps"] == steps
+        assert e["tokens_per_s"] == pytest.approx(B * steps / (e["ms_per_step"] * steps / 1000.0))
+        assert e["frac_of_measured"] == pytest.approx(e["gbs"] / line["roofline"]["peak"])
+        assert e["l2_resident"] is True and e["launches_per_step"] == 5 * 5 + 1
+    # the default run of a small workload reports no per-config block
+    assert run_arm("--workload", "tiny", "--steps", "2", "--warmup", "3", "--cpu-budget", "0.2",
+                   "--no-positions")["per_config"] is None

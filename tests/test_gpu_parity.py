@@ -82,6 +82,37 @@ def test_sharp_attention(name, sharp):
     assert a[:, :, :65].max() > 0.3
 
 
+def attention_sharpness(wl, n_steps, first=8):
+    """Median over steps first.. of the median head's top probability and of its
+    score spread ln(p_max / p_min), from the oracle."""
+    m = oracle.Model(wl.config_tuple(), synth.make_weights(wl))
+    tops, spreads = [], []
+    for t, tok in enumerate(synth.token_stream(wl, 0, n_steps)):
+        _, a = m.forward(int(tok), t, want_att=True)
+        if t >= first:
+            p = a[:, :, : t + 1].astype(np.float64).reshape(-1, t + 1)
+            tops.append(np.median(p.max(axis=1)))
+            spreads.append(np.median(np.log(p.max(axis=1) / np.maximum(p.min(axis=1), 1e-300))))
+    return float(np.median(tops)), float(np.median(spreads))
+
+
+@pytest.mark.parametrize("name,sharp", [("tiny", 25.0), ("gqa_small", 12.0)])
+def test_sharp_attention_one_layer(name, sharp):
+    # One layer with wq and wk scaled so the median head puts more than 0.95 of
+    # its probability on one position and its scores span more than 5 (peaked
+    # attention that exercises the online-softmax rescaling and the chunk
+    # merge's rescaling hard).  With a single layer no rounding difference is
+    # carried into a later layer's queries and keys, so the 1e-5 probability
+    # bound stays well conditioned even this sharp.
+    wl = WORKLOADS[name].replace(name=f"{name}_sharp_1layer", n_layers=1,
+                                 std_scale=(("wq", sharp), ("wk", sharp)))
+    top, spread = attention_sharpness(wl, 64)
+    assert top > 0.95 and spread > 5.0, (top, spread)
+    _, _, rel, att = run_pair(wl, 64, att_every=1)
+    print(f"{wl.name}: median top probability {top:.3f}, score spread {spread:.1f}; "
+          f"worst relative logit error {rel:.2e}, attention {att:.2e}")
+
+
 def test_ragged_shapes():
     # head_size 12 (3 of 4 lanes per row), rows not multiples of any tile, 5 heads on 2 KV heads
     wl = WORKLOADS["tiny"].replace(name="ragged", dim=60, hidden_dim=92, n_layers=3, n_heads=5,
