@@ -580,7 +580,7 @@ def run_ours(args, wl):
                 traffic = W13_NCU_TRAFFIC[0]
         roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                     "traffic": traffic,
-                    "kernel": "gemv_kernel<8,3,512,GEMV_W13> (rmsnorm + W1/W3 + SwiGLU)" + (", bf16 weights" if bf16 else ""),
+                    "kernel": "l2dec_matvec_kernel<8,3,512,GEMV_W13> (rmsnorm + W1/W3 + SwiGLU)" + (", bf16 weights" if bf16 else ""),
                     "bytes_per_launch": w13_bytes(wl, wb), "us_per_launch": w13_ms * 1000.0,
                     "timing": "CUDA events around standalone launches on the decoder's stream, layers cycled",
                     "peak_source": peak_src + " (MEASURED_PEAKS.json hbm_gbs, copy bandwidth)"}

@@ -1,7 +1,7 @@
 // Fused streaming matrix-vector kernels of the decode step (batch 1).
 //
 // Every weight matmul of llama2.c's forward step ("run.c", matmul(): W (d,n)
-// @ x (n,) -> (d,), rows split across threads) is one launch of gemv_kernel,
+// @ x (n,) -> (d,), rows split across threads) is one launch of l2dec_matvec_kernel,
 // with the neighbouring elementwise work fused in:
 //   GEMV_QKV   rmsnorm(x) -> Wq|Wk|Wv -> RoPE -> q, and K/V rows written into
 //              the cache (walkthrough §4 forward() steps 2a-2d)
@@ -120,7 +120,7 @@ __device__ __forceinline__ float dot_bf16x8(uint4 w, float4 x0, float4 x1, float
 }  // namespace
 
 template <int NW, int STAGES, int CH4, int MODE, int WT>
-__global__ void __launch_bounds__(NW * 32, 1) gemv_kernel(const GemvParams p) {
+__global__ void __launch_bounds__(NW * 32, 1) l2dec_matvec_kernel(const GemvParams p) {
     constexpr int NT = NW * 32;
     extern __shared__ __align__(128) unsigned char smem[];
     auto &fx = *reinterpret_cast<GemvFixed<NW, STAGES> *>(smem);
@@ -441,7 +441,7 @@ constexpr Shape kShapes[kGemvShapes] = {{L2_GEMV_WARPS, L2_GEMV_STAGES, L2_GEMV_
 
 template <int S, int MODE, int WT>
 void *kernel_ptr() {
-    return reinterpret_cast<void *>(gemv_kernel<kShapes[S].nw, kShapes[S].stages, kShapes[S].ch4, MODE, WT>);
+    return reinterpret_cast<void *>(l2dec_matvec_kernel<kShapes[S].nw, kShapes[S].stages, kShapes[S].ch4, MODE, WT>);
 }
 
 template <int S, int WT>

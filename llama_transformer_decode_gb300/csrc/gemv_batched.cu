@@ -70,7 +70,7 @@ __device__ __forceinline__ void tensor_g2s(void *dst, const CUtensorMap *map, in
 }  // namespace
 
 template <int MODE>
-__global__ void __launch_bounds__(kBT, 1) gemv_batched_kernel(const __grid_constant__ BatchParams bp) {
+__global__ void __launch_bounds__(kBT, 1) l2dec_matvec_batched_kernel(const __grid_constant__ BatchParams bp) {
     const GemvParams &p = bp.g;
     extern __shared__ __align__(128) unsigned char smem[];
     auto &fx = *reinterpret_cast<BatchFixed *>(smem);
@@ -367,10 +367,10 @@ size_t gemv_batched_smem(int stage_rows, int batch, int n, bool norm, int *stage
 }
 
 cudaError_t gemv_batched_init() {
-    void *fns[] = {reinterpret_cast<void *>(gemv_batched_kernel<GEMV_QKV>),
-                   reinterpret_cast<void *>(gemv_batched_kernel<GEMV_RESID>),
-                   reinterpret_cast<void *>(gemv_batched_kernel<GEMV_W13>),
-                   reinterpret_cast<void *>(gemv_batched_kernel<GEMV_CLS>)};
+    void *fns[] = {reinterpret_cast<void *>(l2dec_matvec_batched_kernel<GEMV_QKV>),
+                   reinterpret_cast<void *>(l2dec_matvec_batched_kernel<GEMV_RESID>),
+                   reinterpret_cast<void *>(l2dec_matvec_batched_kernel<GEMV_W13>),
+                   reinterpret_cast<void *>(l2dec_matvec_batched_kernel<GEMV_CLS>)};
     for (void *f : fns) {
         cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
         if (e != cudaSuccess) return e;
@@ -381,10 +381,10 @@ cudaError_t gemv_batched_init() {
 cudaError_t launch_gemv_batched(int mode, const BatchParams &bp, int grid, size_t smem, cudaStream_t stream, bool pdl) {
     void *fn = nullptr;
     switch (mode) {
-        case GEMV_QKV: fn = reinterpret_cast<void *>(gemv_batched_kernel<GEMV_QKV>); break;
-        case GEMV_RESID: fn = reinterpret_cast<void *>(gemv_batched_kernel<GEMV_RESID>); break;
-        case GEMV_W13: fn = reinterpret_cast<void *>(gemv_batched_kernel<GEMV_W13>); break;
-        case GEMV_CLS: fn = reinterpret_cast<void *>(gemv_batched_kernel<GEMV_CLS>); break;
+        case GEMV_QKV: fn = reinterpret_cast<void *>(l2dec_matvec_batched_kernel<GEMV_QKV>); break;
+        case GEMV_RESID: fn = reinterpret_cast<void *>(l2dec_matvec_batched_kernel<GEMV_RESID>); break;
+        case GEMV_W13: fn = reinterpret_cast<void *>(l2dec_matvec_batched_kernel<GEMV_W13>); break;
+        case GEMV_CLS: fn = reinterpret_cast<void *>(l2dec_matvec_batched_kernel<GEMV_CLS>); break;
         default: return cudaErrorInvalidValue;
     }
     cudaLaunchConfig_t cfg = {};

@@ -218,7 +218,7 @@ __device__ __forceinline__ bool warp_stop(TcFixed &fx, bool ok) {
 // Layer-0 inputs of a step on the tensor-core path: x[b] = emb[token[b]],
 // x[b] * gain for the first RMSNorm, and the sum of squares of each row
 // (ss_part row 0, read with ss_parts = 1).
-__global__ void tc_embed_kernel(const GemvParams p, float *xg) {
+__global__ void l2dec_tc_embed_kernel(const GemvParams p, float *xg) {
     const int b = blockIdx.x, tid = threadIdx.x;
     __shared__ float red[32];
     pdl_launch_dependents();
@@ -248,7 +248,7 @@ __global__ void tc_embed_kernel(const GemvParams p, float *xg) {
 }
 
 template <int MODE>
-__global__ void __launch_bounds__(kTT, 1) gemv_tc_kernel(const __grid_constant__ TcParams tp) {
+__global__ void __launch_bounds__(kTT, 1) l2dec_matvec_tc_kernel(const __grid_constant__ TcParams tp) {
     const GemvParams &p = tp.g;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -727,8 +727,8 @@ int gemv_tc_grid(int ntiles, int n, int ctas) {
 size_t gemv_tc_ws_floats(int grid, int bpad) { return (size_t)grid * 2 * kTM * bpad; }
 
 cudaError_t gemv_tc_init() {
-    void *fns[] = {reinterpret_cast<void *>(gemv_tc_kernel<GEMV_QKV>), reinterpret_cast<void *>(gemv_tc_kernel<GEMV_RESID>),
-                   reinterpret_cast<void *>(gemv_tc_kernel<GEMV_W13>), reinterpret_cast<void *>(gemv_tc_kernel<GEMV_CLS>)};
+    void *fns[] = {reinterpret_cast<void *>(l2dec_matvec_tc_kernel<GEMV_QKV>), reinterpret_cast<void *>(l2dec_matvec_tc_kernel<GEMV_RESID>),
+                   reinterpret_cast<void *>(l2dec_matvec_tc_kernel<GEMV_W13>), reinterpret_cast<void *>(l2dec_matvec_tc_kernel<GEMV_CLS>)};
     for (void *f : fns) {
         cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemLimit);
         if (e != cudaSuccess) return e;
@@ -755,16 +755,16 @@ cudaError_t launch_tc_embed(const TcParams &tp, int batch, cudaStream_t stream, 
     cudaLaunchConfig_t cfg = pdl_config(dim3(batch), dim3(256), 0, stream, pdl, attr);
     float *xg = tp.xg;
     void *args[] = {const_cast<GemvParams *>(&tp.g), &xg};
-    return cudaLaunchKernelExC(&cfg, reinterpret_cast<void *>(tc_embed_kernel), args);
+    return cudaLaunchKernelExC(&cfg, reinterpret_cast<void *>(l2dec_tc_embed_kernel), args);
 }
 
 cudaError_t launch_gemv_tc(int mode, const TcParams &tp, int grid, cudaStream_t stream, bool pdl) {
     void *fn = nullptr;
     switch (mode) {
-        case GEMV_QKV: fn = reinterpret_cast<void *>(gemv_tc_kernel<GEMV_QKV>); break;
-        case GEMV_RESID: fn = reinterpret_cast<void *>(gemv_tc_kernel<GEMV_RESID>); break;
-        case GEMV_W13: fn = reinterpret_cast<void *>(gemv_tc_kernel<GEMV_W13>); break;
-        case GEMV_CLS: fn = reinterpret_cast<void *>(gemv_tc_kernel<GEMV_CLS>); break;
+        case GEMV_QKV: fn = reinterpret_cast<void *>(l2dec_matvec_tc_kernel<GEMV_QKV>); break;
+        case GEMV_RESID: fn = reinterpret_cast<void *>(l2dec_matvec_tc_kernel<GEMV_RESID>); break;
+        case GEMV_W13: fn = reinterpret_cast<void *>(l2dec_matvec_tc_kernel<GEMV_W13>); break;
+        case GEMV_CLS: fn = reinterpret_cast<void *>(l2dec_matvec_tc_kernel<GEMV_CLS>); break;
         default: return cudaErrorInvalidValue;
     }
     cudaLaunchAttribute attr[1];

@@ -55,7 +55,7 @@ struct GemvParams {
     int *err;
     int dim, kv_dim, head_size, seq_len, n_kv_heads, n_layers, vocab;
     int evict_first;  // stream the weights with an L2 evict-first hint
-    // Batched steps (gemv_batched_kernel) only:
+    // Batched steps (l2dec_matvec_batched_kernel) only:
     int batch;        // sequences in the step (slots 0..batch-1)
     float *ss_part;   // [kMaxParts][batch] partial sums of x^2 written by the residual kernels
     int ss_parts;     // rows of ss_part the RMSNorm modes add up (grid of the residual kernels)
