@@ -152,14 +152,26 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def config_of(wl, batch: int = 1) -> dict:
+def config_of(wl, batch: int = 1, bf16: bool = False) -> dict:
     return {"workload": wl.name, "dim": wl.dim, "hidden_dim": wl.hidden_dim, "n_layers": wl.n_layers,
             "n_heads": wl.n_heads, "n_kv_heads": wl.n_kv_heads, "vocab_size": wl.vocab_size,
             "seq_len": wl.seq_len, "batch": batch, "parallelism": "replicas",
             "weights": "seeded random (synth)", "tokens": "seeded uniform, teacher-forced",
             "l2": "inputs larger than L2" if weight_bytes(wl) > 129e6 else "weights fit in L2 (effective bandwidth)",
-            "gemv": ("tensor cores (tcgen05 kind::tf32, 3-term hi/lo split: fp32-level products)" if batch >= TC_MIN_BATCH
-                     else "CUDA cores (fp32 FMA)")}
+            "gemv": gemv_path(batch, bf16)}
+
+
+def on_tensor_cores(batch: int, bf16: bool = False) -> bool:
+    """Steps of this many rows run their matrix products on the tensor cores (all
+    steps of several rows with bf16 weights)."""
+    return batch >= TC_MIN_BATCH or (bf16 and batch > 1)
+
+
+def gemv_path(batch: int, bf16: bool = False) -> str:
+    if on_tensor_cores(batch, bf16):
+        return ("tensor cores (tcgen05 kind::f16: bf16 weights, inputs in three bf16 parts: exact products)" if bf16 else
+                "tensor cores (tcgen05 kind::tf32, 3-term hi/lo split: fp32-level products)")
+    return "CUDA cores (bf16 weights widened to fp32, fp32 FMA)" if bf16 else "CUDA cores (fp32 FMA)"
 
 
 def load_weights_device(wl, keep_host: bool):
@@ -197,9 +209,8 @@ def metric_of(batch: int, bf16: bool = False, prefill: int = 0) -> str:
     if prefill:
         return (f"prefill tokens/s of a {prefill}-token prompt and % of HBM roofline "
                 "(GB/s vs ~8 TB/s), 1 GB300")
-    if batch > 1:
-        return METRIC.replace("at batch 1", f"at batch {batch}")
-    return METRIC.replace("at batch 1", "at batch 1 with bf16 weights") if bf16 else METRIC
+    tail = " with bf16 weights" if bf16 else ""
+    return METRIC.replace("at batch 1", f"at batch {batch}{tail}")
 
 
 def max_over_ranks(v: float, world: int, device: str = "cuda") -> float:
@@ -426,7 +437,7 @@ def per_config_rates(entries, hbm: float, peak_src: str, runs: int) -> dict:
             "gbs": gbs, "frac_of_measured": gbs / hbm, "frac_of_8tbs": gbs / NOMINAL_HBM_GBS,
             "bytes_per_step_avg": by / n, "l2_resident": weight_bytes(wl) < L2_BYTES,
             "launches_per_step": dec.kernels_per_step(B),
-            "gemv": "tensor cores (3-term tf32)" if B >= TC_MIN_BATCH else "CUDA cores (fp32 FMA)"}
+            "gemv": gemv_path(B)}
         dec.close()
     loaded.clear()
     out["_peak"] = f"{hbm:.1f} GB/s {peak_src} (MEASURED_PEAKS.json hbm_gbs); timing: CUDA events, median of {runs}"
@@ -586,10 +597,10 @@ def run_ours(args, wl):
                     "peak_source": peak_src + " (MEASURED_PEAKS.json hbm_gbs, copy bandwidth)"}
     else:
         # whole batched step: B/2 flop per weight byte
-        flops = 2.0 * B * (weight_bytes(wl) / 4.0) * args.steps
+        flops = 2.0 * B * (weight_bytes(wl) / 4.0) * args.steps  # 2 flops per weight (fp32 byte count / 4) per row
         tflops = flops / (ms / 1000.0) / 1e12
         alu = fp32_alu_peak_tflops(props)
-        if B >= TC_MIN_BATCH:
+        if on_tensor_cores(B, bf16):
             # tensor-core GEMV: 3 tf32 products per multiply-add are far below the tensor
             # peak, so the weights and the KV cache streamed from HBM bound the step
             roofline = {"bound": "hbm", "achieved": step_gbs, "peak": hbm, "unit": "GB/s", "frac": step_gbs / hbm,
@@ -622,7 +633,7 @@ def run_ours(args, wl):
         per_config = per_config_rates(entries, hbm, peak_src, args.per_config_runs)
 
     clk = clocks.summary()
-    cfg = config_of(wl, B)
+    cfg = config_of(wl, B, bf16)
     cfg["positions"] = (f"{timed_pos[0][0]}..{timed_pos[-1][0]}" if B == 1 else
                         f"slot b from floor(b*{S}/{B}) + {args.warmup}, {args.steps} steps, wrapping at {S}")
     metric = metric_of(B, bf16)
@@ -757,7 +768,7 @@ def main(argv=None):
     ap.add_argument("--batch", type=int, default=1,
                     help="independent sequences per step at staggered positions (batched_1b: 16 or 64)")
     ap.add_argument("--weights", choices=("f32", "bf16"), default="f32",
-                    help="bf16: matrices streamed as bf16 (L2_FLAG_BF16_WEIGHTS; batch 1 only)")
+                    help="bf16: matrices streamed as bf16 (L2_FLAG_BF16_WEIGHTS)")
     ap.add_argument("--prefill", type=int, default=0, metavar="T",
                     help="time l2_prefill of a T-token prompt instead of decode steps (one prompt per step)")
     ap.add_argument("--layers", type=int, default=None,
@@ -776,8 +787,8 @@ def main(argv=None):
         ap.error("--warmup must be at least 3")
     if not 1 <= args.batch <= 64:
         ap.error("--batch must be in 1..64")
-    if args.weights == "bf16" and (args.batch != 1 or args.impl != "ours"):
-        ap.error("--weights bf16 is a batch-1 option of this implementation")
+    if args.weights == "bf16" and args.impl != "ours":
+        ap.error("--weights bf16 is an option of this implementation, not of the reference arm")
     if args.per_config is None:
         args.per_config = DEFAULT_PER_CONFIG if args.workload == "llama2_7b" and args.layers is None else "none"
     try:

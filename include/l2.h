@@ -196,7 +196,9 @@ void l2_destroy(l2_ctx *ctx);
 
 /*
  * Profiling hook: enqueues `count` launches of one kernel of the step,
- * exactly as the step launches it, for timing it alone.  op: 0 = fused
+ * exactly as the step launches it (consecutive launches linked by
+ * programmatic dependent launch, as the step's kernels are, unless the handle
+ * has L2_FLAG_NO_PDL), for timing it alone.  op: 0 = fused
  * rmsnorm+QKV+RoPE+KV write, 1 = attention, 2 = Wo+residual, 3 = rmsnorm +
  * W1/W3 + SwiGLU, 4 = W2+residual, 5 = final rmsnorm + classifier.  Uses
  * slot 0's last token and position.  It overwrites activations and the

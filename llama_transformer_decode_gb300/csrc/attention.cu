@@ -48,7 +48,42 @@ namespace {
 constexpr int kNWA = L2_ATTN_WARPS;
 constexpr int kAttStages = L2_ATTN_STAGES;
 constexpr int kStageFloats = L2_ATTN_STAGE_FLOATS;
-constexpr int kPPG = 4;              // positions a lane group scores before one softmax update
+
+// The WPR * 32 threads of one ring: named barrier 1 + ring (ids taken from
+// constants, so the kernel reserves only the barriers it uses).  ring_sync_or
+// gives every thread the OR of their flags; ring_sync is a plain barrier.
+template <int ID, int NTH>
+__device__ __forceinline__ bool bar_or_id(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v), "n"(ID), "n"(NTH)
+        : "memory");
+    return r != 0;
+}
+template <int ID, int NTH>
+__device__ __forceinline__ void bar_id(void) {
+    asm volatile("bar.sync %0, %1;" ::"n"(ID), "n"(NTH) : "memory");
+}
+template <int NTH>
+__device__ __forceinline__ bool ring_sync_or(bool v, int ring) {
+    switch (ring) {
+        case 0: return bar_or_id<1, NTH>(v);
+        case 1: return bar_or_id<2, NTH>(v);
+        case 2: return bar_or_id<3, NTH>(v);
+        default: return bar_or_id<4, NTH>(v);
+    }
+}
+template <int NTH>
+__device__ __forceinline__ void ring_sync(int ring) {
+    switch (ring) {
+        case 0: bar_id<1, NTH>(); break;
+        case 1: bar_id<2, NTH>(); break;
+        case 2: bar_id<3, NTH>(); break;
+        default: bar_id<4, NTH>(); break;
+    }
+}
 
 __device__ __forceinline__ void merge_state(float &m, float &l, float4 &acc, float m2, float l2v, float4 acc2) {
     const float M = fmaxf(m, m2);
@@ -64,42 +99,46 @@ __device__ __forceinline__ void merge_state(float &m, float &l, float4 &acc, flo
 }  // namespace
 
 // RL = 1: the row-per-lane layout for 4 or 8 query heads per KV head and
-// head size 64 (16 cache rows per ring stage).  Lane (t, half) scores row t
-// for half of the group's heads over the whole head (K chunks read in a
-// lane-rotated order, conflict-free), the online softmax runs over the 16
-// rows with shuffles inside each half-warp (one exponential per row and
-// head), and the probabilities go through shared memory to the PV pass,
-// where lane l accumulates dimensions 2l, 2l+1 of every head.  Each cache row
+// head size 64 (16 cache rows per ring stage).  Two warps share each ring and
+// split the group's query heads between them (so a CTA needs half the ring
+// memory per warp and two CTAs fit on an SM).  Lane (t, half) of a warp
+// scores row t for half of that warp's heads over the whole head (K chunks
+// read in a lane-rotated order, conflict-free), the online softmax runs over
+// the 16 rows with shuffles inside each half-warp (one exponential per row and
+// head), and the probabilities go through shared memory to the PV pass, where
+// lane l accumulates dimensions 2l, 2l+1 of the warp's heads.  Each cache row
 // costs a few dozen instructions instead of one shuffle tree per head.
 template <int LP, int GQ, int RL>
 __global__ void __launch_bounds__(kNWA * 32) attn_kernel(const AttnParams p) {
     constexpr int NT = kNWA * 32;
-    constexpr int RPI = 32 / LP;  // cache rows a warp handles at once
+    constexpr int RPI = 32 / LP;        // cache rows a warp handles at once
+    constexpr int WPR = RL ? 2 : 1;     // warps sharing one ring
+    constexpr int NRG = kNWA / WPR;     // rings per CTA (one softmax state per ring and head)
+    static_assert(!RL || NRG <= 4, "ring barriers are ids 1..4");
     extern __shared__ __align__(128) unsigned char smem[];
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem);                      // [kNWA][kAttStages]
-    int *flags = reinterpret_cast<int *>(smem + 8 * kNWA * kAttStages);        // [4]
-    float *mrg = reinterpret_cast<float *>(smem + 8 * kNWA * kAttStages + 16); // [kNWA][GQ][2]
-    float *fin = mrg + kNWA * GQ * 2;                                          // [GQ][2]
-    const size_t hdr = (8 * kNWA * kAttStages + 16 + 4 * (kNWA * GQ * 2 + GQ * 2) + 127) / 128 * 128;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem);                      // [NRG][kAttStages]
+    int *flags = reinterpret_cast<int *>(smem + 8 * NRG * kAttStages);        // [4]
+    float *mrg = reinterpret_cast<float *>(smem + 8 * NRG * kAttStages + 16); // [NRG][GQ][2]
+    float *fin = mrg + NRG * GQ * 2;                                          // [GQ][2]
+    const size_t hdr = (8 * NRG * kAttStages + 16 + 4 * (NRG * GQ * 2 + GQ * 2) + 127) / 128 * 128;
     const int hs = p.head_size, hs4 = hs >> 2;
-    float4 *ring = reinterpret_cast<float4 *>(smem + hdr);                     // [kNWA][kAttStages][stage]
-    float4 *accs = ring + kNWA * kAttStages * (kStageFloats / 4);              // [kNWA][GQ][hs4]
-    float *qs = reinterpret_cast<float *>(accs + kNWA * GQ * hs4);               // RL: [GQ][hs]
-    float *pbuf = qs + GQ * hs;                                                 // RL: [kNWA][16 + 1][GQ]
+    float4 *ring = reinterpret_cast<float4 *>(smem + hdr);                     // [NRG][kAttStages][stage]
+    float4 *accs = ring + NRG * kAttStages * (kStageFloats / 4);              // [NRG][GQ][hs4]
+    float *qs = reinterpret_cast<float *>(accs + NRG * GQ * hs4);               // RL: [GQ][hs]
+    float *pbuf = qs + GQ * hs;                                                 // RL: [kNWA][16 + 1][GQ / WPR]
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int c = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+    // several rows: the host orders them, longest CTAs first
+    const int c = blockIdx.x, g = blockIdx.y, b = p.capacity > 0 ? (int)p.step->row_order[blockIdx.z] : blockIdx.z;
     const int pos = p.step->pos[b];
     const int P = pos + 1;
-    int chunk = p.min_chunk;
-    if (p.capacity > 0) {
-        // spread the positions of every row over the resident CTAs (the host sums them)
-        const long long total = p.step->attn_total;
-        const long long per = (total * p.n_kv_heads + p.capacity - 1) / p.capacity;
-        if (per > chunk) chunk = (int)per;
-    }
-    int n_active = (P + chunk - 1) / chunk;
+    // CTAs of this (row, KV head): at least min_chunk positions each for a step of
+    // one row; for several rows, the host's plan, which fits every row's CTAs
+    // into the kernel's resident capacity at once
+    int n_active = p.capacity > 0 ? (int)p.step->nchunk[b] : (P + p.min_chunk - 1) / p.min_chunk;
     if (n_active > p.n_chunks) n_active = p.n_chunks;
+    if (n_active > P) n_active = P;
+    if (n_active < 1) n_active = 1;
     if (c >= n_active) return;  // too few positions for this CTA to join
 
     const int H = p.n_heads, KV = p.n_kv_heads;
@@ -107,8 +146,9 @@ __global__ void __launch_bounds__(kNWA * 32) attn_kernel(const AttnParams p) {
     const int nq = h1 - h0;
 
     const int t0 = (int)((long long)c * P / n_active), t1 = (int)((long long)(c + 1) * P / n_active);
-    const int wt0 = t0 + (int)((long long)(t1 - t0) * warp / kNWA);
-    const int wt1 = t0 + (int)((long long)(t1 - t0) * (warp + 1) / kNWA);
+    const int rgi = warp / WPR, wsub = warp % WPR;  // this warp's ring, and its place in it
+    const int wt0 = t0 + (int)((long long)(t1 - t0) * rgi / NRG);
+    const int wt1 = t0 + (int)((long long)(t1 - t0) * (rgi + 1) / NRG);
     const int TP = kStageFloats / (2 * hs);  // positions per stage
 
     const size_t head_base = (((size_t)p.step->slot[b] * p.n_layers + p.layer) * KV + g) * (size_t)p.seq_len * hs;
@@ -116,20 +156,21 @@ __global__ void __launch_bounds__(kNWA * 32) attn_kernel(const AttnParams p) {
     const float *vbase = p.vcache + head_base;
 
     if (tid == 0) {
-        for (int i = 0; i < kNWA * kAttStages; ++i) mbar_init(&bars[i], 1);
+        for (int i = 0; i < NRG * kAttStages; ++i) mbar_init(&bars[i], 1);
         fence_barrier_init();
         flags[0] = 0;  // a warp gave up waiting
         flags[1] = 0;  // this CTA merges the chunks
     }
     __syncthreads();
 
-    uint64_t *wbars = bars + warp * kAttStages;
-    float4 *wring = ring + (size_t)warp * kAttStages * (kStageFloats / 4);
+    uint64_t *wbars = bars + rgi * kAttStages;
+    float4 *wring = ring + (size_t)rgi * kAttStages * (kStageFloats / 4);
+    const bool producer = wsub == 0 && lane == 0;  // issues the ring's copies; every warp tracks them
     int ti = wt0;  // next position to request
     int n_issued = 0;
     auto issue = [&](int stage) {
         const int np = min(TP, wt1 - ti);
-        if (lane == 0) {
+        if (producer) {
             const uint32_t bytes = (uint32_t)np * hs * 4u;
             float4 *dst = wring + (size_t)stage * (kStageFloats / 4);
             mbar_arrive_expect_tx(&wbars[stage], 2u * bytes);
@@ -156,7 +197,9 @@ __global__ void __launch_bounds__(kNWA * 32) attn_kernel(const AttnParams p) {
     if constexpr (RL == 1) {
         constexpr int TPR = 16;            // cache rows per ring stage (head size 64)
         constexpr int HS4 = 16;
-        constexpr int HPL = GQ / 2;        // heads per lane
+        constexpr int HPW = GQ / WPR;      // heads per warp
+        constexpr int HPL = HPW / 2;       // heads per lane (one half-warp each)
+        constexpr int RTH = WPR * 32;      // threads of one ring
         // the group's query vectors, shared by all warps
         for (int i = tid; i < GQ * 64; i += NT) {
             const int j = i / 64, d = i % 64;
@@ -164,29 +207,32 @@ __global__ void __launch_bounds__(kNWA * 32) attn_kernel(const AttnParams p) {
         }
         __syncthreads();
         const float4 *qs4 = reinterpret_cast<const float4 *>(qs);
-        float *wp = pbuf + warp * (TPR + 1) * GQ;  // [TPR][GQ] probabilities, then [GQ] rescales
+        float *wp = pbuf + warp * (TPR + 1) * HPW;  // [TPR][HPW] probabilities, then [HPW] rescales
         const int t = lane & (TPR - 1), jh = lane / TPR;
+        const int jw0 = wsub * HPW;                 // the warp's first head of the group
         float m[HPL], l[HPL];
-        float acc[GQ][2];
+        float acc[HPW][2];
 #pragma unroll
         for (int jj = 0; jj < HPL; ++jj) {
             m[jj] = -CUDART_INF_F;
             l[jj] = 0.f;
         }
 #pragma unroll
-        for (int j = 0; j < GQ; ++j) acc[j][0] = acc[j][1] = 0.f;
+        for (int j = 0; j < HPW; ++j) acc[j][0] = acc[j][1] = 0.f;
         int tc = wt0;
 #pragma unroll 1
         for (; tc < wt1; ++k) {
             const int s = k % kAttStages;
             const int np = min(TP, wt1 - tc);
-            if (!mbar_wait(&wbars[s], (uint32_t)(k / kAttStages) & 1u, p.err)) {
+            const bool got = mbar_wait(&wbars[s], (uint32_t)(k / kAttStages) & 1u, p.err);
+            // the ring's warps take one decision (the loop bounds are the ring's, so both get here)
+            if (ring_sync_or<RTH>(!got, rgi)) {
                 ok = false;
                 break;
             }
             const float4 *Ks = wring + (size_t)s * (kStageFloats / 4);
             const float2 *Vs2 = reinterpret_cast<const float2 *>(Ks + (size_t)TP * HS4);
-            // scores of row t for heads jh*HPL.., the row's 16-byte chunks in rotated order
+            // scores of row t for heads jw0 + jh*HPL.., the row's 16-byte chunks in rotated order
             const bool row_on = t < np;
             float sc[HPL];
 #pragma unroll
@@ -198,13 +244,14 @@ __global__ void __launch_bounds__(kNWA * 32) attn_kernel(const AttnParams p) {
                     const int ch = (i + t) & (HS4 - 1);
                     const float4 kv = Kr[ch];
 #pragma unroll
-                    for (int jj = 0; jj < HPL; ++jj) sc[jj] = dot4(qs4[(jh * HPL + jj) * HS4 + ch], kv, sc[jj]);
+                    for (int jj = 0; jj < HPL; ++jj) sc[jj] = dot4(qs4[(jw0 + jh * HPL + jj) * HS4 + ch], kv, sc[jj]);
                 }
             }
 #pragma unroll
             for (int jj = 0; jj < HPL; ++jj) {
+                const int hj = jw0 + jh * HPL + jj;
                 sc[jj] = row_on ? sc[jj] * p.scale : -CUDART_INF_F;
-                if (dbg && row_on && jh * HPL + jj < nq) dbg[(size_t)(jh * HPL + jj) * p.seq_len + tc + t] = sc[jj];
+                if (dbg && row_on && hj < nq) dbg[(size_t)hj * p.seq_len + tc + t] = sc[jj];
                 // online softmax over the stage's rows (the 16 lanes of this half)
                 float mx = sc[jj];
 #pragma unroll
@@ -217,31 +264,32 @@ __global__ void __launch_bounds__(kNWA * 32) attn_kernel(const AttnParams p) {
                 for (int o = TPR / 2; o > 0; o >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
                 l[jj] = l[jj] * corr + ps;
                 m[jj] = mn;
-                wp[t * GQ + jh * HPL + jj] = pe;
-                if (t == 0) wp[TPR * GQ + jh * HPL + jj] = corr;
+                wp[t * HPW + jh * HPL + jj] = pe;
+                if (t == 0) wp[TPR * HPW + jh * HPL + jj] = corr;
             }
             __syncwarp();
-            // PV: dimensions 2 lane, 2 lane + 1 of every head
+            // PV: dimensions 2 lane, 2 lane + 1 of the warp's heads
 #pragma unroll
-            for (int j = 0; j < GQ; ++j) {
-                const float c = wp[TPR * GQ + j];
-                acc[j][0] *= c;
-                acc[j][1] *= c;
+            for (int j = 0; j < HPW; ++j) {
+                const float cr = wp[TPR * HPW + j];
+                acc[j][0] *= cr;
+                acc[j][1] *= cr;
             }
 #pragma unroll 4
             for (int tt = 0; tt < np; ++tt) {
                 const float2 v = Vs2[tt * 32 + lane];
 #pragma unroll
-                for (int j = 0; j < GQ; ++j) {
-                    const float pj = wp[tt * GQ + j];
+                for (int j = 0; j < HPW; ++j) {
+                    const float pj = wp[tt * HPW + j];
                     acc[j][0] = fmaf(pj, v.x, acc[j][0]);
                     acc[j][1] = fmaf(pj, v.y, acc[j][1]);
                 }
             }
             __syncwarp();
             tc += np;
+            ring_sync<RTH>(rgi);  // both warps are done with this stage's buffer
             if (ti < wt1) {
-                if (lane == 0) fence_proxy_async_smem();
+                if (producer) fence_proxy_async_smem();
                 issue(s);
             }
         }
@@ -253,32 +301,40 @@ __global__ void __launch_bounds__(kNWA * 32) attn_kernel(const AttnParams p) {
         if (t == 0) {
 #pragma unroll
             for (int jj = 0; jj < HPL; ++jj) {
-                mrg[(warp * GQ + jh * HPL + jj) * 2 + 0] = m[jj];
-                mrg[(warp * GQ + jh * HPL + jj) * 2 + 1] = l[jj];
+                mrg[(rgi * GQ + jw0 + jh * HPL + jj) * 2 + 0] = m[jj];
+                mrg[(rgi * GQ + jw0 + jh * HPL + jj) * 2 + 1] = l[jj];
             }
         }
         float *accf = reinterpret_cast<float *>(accs);
 #pragma unroll
-        for (int j = 0; j < GQ; ++j)
-            *reinterpret_cast<float2 *>(accf + (size_t)(warp * GQ + j) * 64 + 2 * lane) = make_float2(acc[j][0], acc[j][1]);
+        for (int j = 0; j < HPW; ++j)
+            *reinterpret_cast<float2 *>(accf + (size_t)(rgi * GQ + jw0 + j) * 64 + 2 * lane) =
+                make_float2(acc[j][0], acc[j][1]);
     } else {
-        // query vectors of the group, one 16-byte word per lane and head
+        // A row's 16-byte words c4, c4 + LP, .. (WPL of them) go to the LP lanes of its
+        // lane group: with one or two query heads per KV head a lane keeps several
+        // words of q per head in registers, so a row's dot product ends in a short
+        // shuffle tree (log2 LP levels) instead of one level per halving of 32 lanes.
+        constexpr int WPL = GQ == 1 ? 4 : GQ == 2 ? 2 : 1;
+        constexpr int PPG = WPL >= 4 ? 2 : 4;  // rows a lane group scores before one softmax update
         const int rg = lane / LP, c4 = lane % LP;
-        const bool lane_on = c4 < hs4;
-        float4 q4[GQ];
+        float4 q4[GQ][WPL];
         float m[GQ], l[GQ];
-        float4 acc[GQ];
-    #pragma unroll
+        float4 acc[GQ][WPL];
+#pragma unroll
         for (int j = 0; j < GQ; ++j) {
-            q4[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (j < nq && lane_on)
-                q4[j] = reinterpret_cast<const float4 *>(p.q + (size_t)b * p.dim + (size_t)(h0 + j) * hs)[c4];
+#pragma unroll
+            for (int w = 0; w < WPL; ++w) {
+                q4[j][w] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (j < nq && c4 + w * LP < hs4)
+                    q4[j][w] = reinterpret_cast<const float4 *>(p.q + (size_t)b * p.dim + (size_t)(h0 + j) * hs)[c4 + w * LP];
+                acc[j][w] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
             m[j] = -CUDART_INF_F;
             l[j] = 0.f;
-            acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
         int tc = wt0;
-    #pragma unroll 1
+#pragma unroll 1
         for (; tc < wt1; ++k) {
             const int s = k % kAttStages;
             const int np = min(TP, wt1 - tc);
@@ -288,54 +344,68 @@ __global__ void __launch_bounds__(kNWA * 32) attn_kernel(const AttnParams p) {
             }
             const float4 *Ks = wring + (size_t)s * (kStageFloats / 4);
             const float4 *Vs = Ks + (size_t)TP * hs4;
-    #pragma unroll 1
-            // Up to kPPG positions per lane group at a time: all their scores
-            // first (independent dot products and shuffles), then one online-
-            // softmax update per head (one rescale per group of positions).
-            for (int tt = 0; tt < np; tt += RPI * kPPG) {
-                float sc[kPPG][GQ];
-                float4 vv[kPPG];
-    #pragma unroll
-                for (int u = 0; u < kPPG; ++u) {
+            // Up to PPG rows per lane group at a time: all their scores first
+            // (independent dot products and shuffles), then one online-softmax
+            // update per head (one rescale per group of rows).
+#pragma unroll 1
+            for (int tt = 0; tt < np; tt += RPI * PPG) {
+                float sc[PPG][GQ];
+                float4 vv[PPG][WPL];
+#pragma unroll
+                for (int u = 0; u < PPG; ++u) {
                     const int tl = tt + u * RPI + rg;
                     const bool row_on = tl < np;
-                    float4 kv = make_float4(0.f, 0.f, 0.f, 0.f);
-                    vv[u] = kv;
-                    if (row_on && lane_on) {
-                        kv = Ks[tl * hs4 + c4];
-                        vv[u] = Vs[tl * hs4 + c4];
+                    float4 kv[WPL];
+#pragma unroll
+                    for (int w = 0; w < WPL; ++w) {
+                        kv[w] = make_float4(0.f, 0.f, 0.f, 0.f);
+                        vv[u][w] = kv[w];
+                        if (row_on && c4 + w * LP < hs4) {
+                            kv[w] = Ks[tl * hs4 + c4 + w * LP];
+                            vv[u][w] = Vs[tl * hs4 + c4 + w * LP];
+                        }
                     }
-    #pragma unroll
+#pragma unroll
                     for (int j = 0; j < GQ; ++j) {
-                        float d = dot4(q4[j], kv, 0.f);
-    #pragma unroll
+                        float d = 0.f;
+#pragma unroll
+                        for (int w = 0; w < WPL; ++w) d = dot4(q4[j][w], kv[w], d);
+#pragma unroll
                         for (int o = LP / 2; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
                         sc[u][j] = row_on ? d * p.scale : -CUDART_INF_F;
                         if (dbg && row_on && c4 == 0 && j < nq) dbg[(size_t)j * p.seq_len + tc + tl] = sc[u][j];
                     }
                 }
-    #pragma unroll
+#pragma unroll
                 for (int j = 0; j < GQ; ++j) {
                     if (j >= nq) continue;
                     float mx = sc[0][j];
-    #pragma unroll
-                    for (int u = 1; u < kPPG; ++u) mx = fmaxf(mx, sc[u][j]);
+#pragma unroll
+                    for (int u = 1; u < PPG; ++u) mx = fmaxf(mx, sc[u][j]);
                     const float mn = fmaxf(m[j], mx);
                     if (mn == -CUDART_INF_F) continue;  // no position of this group
                     const float corr = expf(m[j] - mn);
+                    float pe[PPG];
                     float ps = 0.f;
-                    float4 a = make_float4(acc[j].x * corr, acc[j].y * corr, acc[j].z * corr, acc[j].w * corr);
-    #pragma unroll
-                    for (int u = 0; u < kPPG; ++u) {
-                        const float pe = expf(sc[u][j] - mn);
-                        ps += pe;
-                        a.x = fmaf(pe, vv[u].x, a.x);
-                        a.y = fmaf(pe, vv[u].y, a.y);
-                        a.z = fmaf(pe, vv[u].z, a.z);
-                        a.w = fmaf(pe, vv[u].w, a.w);
+#pragma unroll
+                    for (int u = 0; u < PPG; ++u) {
+                        pe[u] = expf(sc[u][j] - mn);
+                        ps += pe[u];
+                    }
+#pragma unroll
+                    for (int w = 0; w < WPL; ++w) {
+                        float4 a = make_float4(acc[j][w].x * corr, acc[j][w].y * corr, acc[j][w].z * corr,
+                                               acc[j][w].w * corr);
+#pragma unroll
+                        for (int u = 0; u < PPG; ++u) {
+                            a.x = fmaf(pe[u], vv[u][w].x, a.x);
+                            a.y = fmaf(pe[u], vv[u][w].y, a.y);
+                            a.z = fmaf(pe[u], vv[u][w].z, a.z);
+                            a.w = fmaf(pe[u], vv[u][w].w, a.w);
+                        }
+                        acc[j][w] = a;
                     }
                     l[j] = l[j] * corr + ps;
-                    acc[j] = a;
                     m[j] = mn;
                 }
             }
@@ -352,29 +422,43 @@ __global__ void __launch_bounds__(kNWA * 32) attn_kernel(const AttnParams p) {
             if (lane == 0) flags[0] = 1;
         }
 
-        // merge the row groups of the warp (lanes LP apart share a column word)
-    #pragma unroll
+        // merge the row groups of the warp (lanes LP apart hold the same words)
+#pragma unroll
         for (int o = LP; o < 32; o <<= 1) {
-    #pragma unroll
+#pragma unroll
             for (int j = 0; j < GQ; ++j) {
                 const float m2 = __shfl_xor_sync(0xffffffffu, m[j], o);
                 const float l2v = __shfl_xor_sync(0xffffffffu, l[j], o);
-                float4 a2;
-                a2.x = __shfl_xor_sync(0xffffffffu, acc[j].x, o);
-                a2.y = __shfl_xor_sync(0xffffffffu, acc[j].y, o);
-                a2.z = __shfl_xor_sync(0xffffffffu, acc[j].z, o);
-                a2.w = __shfl_xor_sync(0xffffffffu, acc[j].w, o);
-                merge_state(m[j], l[j], acc[j], m2, l2v, a2);
+                const float M = fmaxf(m[j], m2);
+                const float fa = M == -CUDART_INF_F ? 0.f : expf(m[j] - M);
+                const float fb = M == -CUDART_INF_F ? 0.f : expf(m2 - M);
+#pragma unroll
+                for (int w = 0; w < WPL; ++w) {
+                    float4 a2;
+                    a2.x = __shfl_xor_sync(0xffffffffu, acc[j][w].x, o);
+                    a2.y = __shfl_xor_sync(0xffffffffu, acc[j][w].y, o);
+                    a2.z = __shfl_xor_sync(0xffffffffu, acc[j][w].z, o);
+                    a2.w = __shfl_xor_sync(0xffffffffu, acc[j][w].w, o);
+                    if (M != -CUDART_INF_F)
+                        acc[j][w] = make_float4(acc[j][w].x * fa + a2.x * fb, acc[j][w].y * fa + a2.y * fb,
+                                                acc[j][w].z * fa + a2.z * fb, acc[j][w].w * fa + a2.w * fb);
+                }
+                if (M != -CUDART_INF_F) {
+                    l[j] = l[j] * fa + l2v * fb;
+                    m[j] = M;
+                }
             }
         }
         if (lane < LP) {
-    #pragma unroll
+#pragma unroll
             for (int j = 0; j < GQ; ++j) {
                 if (lane == 0) {
-                    mrg[(warp * GQ + j) * 2 + 0] = m[j];
-                    mrg[(warp * GQ + j) * 2 + 1] = l[j];
+                    mrg[(rgi * GQ + j) * 2 + 0] = m[j];
+                    mrg[(rgi * GQ + j) * 2 + 1] = l[j];
                 }
-                if (lane_on) accs[(size_t)(warp * GQ + j) * hs4 + c4] = acc[j];
+#pragma unroll
+                for (int w = 0; w < WPL; ++w)
+                    if (c4 + w * LP < hs4) accs[(size_t)(rgi * GQ + j) * hs4 + c4 + w * LP] = acc[j][w];
             }
         }
     }
@@ -393,7 +477,7 @@ __global__ void __launch_bounds__(kNWA * 32) attn_kernel(const AttnParams p) {
             const int j = idx / hs4, w4 = idx % hs4;
             float mm = -CUDART_INF_F, ll = 0.f;
             float4 aa = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int w = 0; w < kNWA; ++w)
+            for (int w = 0; w < NRG; ++w)
                 merge_state(mm, ll, aa, mrg[(w * GQ + j) * 2], mrg[(w * GQ + j) * 2 + 1],
                             accs[(size_t)(w * GQ + j) * hs4 + w4]);
             const float inv = 1.0f / ll;
@@ -418,7 +502,7 @@ __global__ void __launch_bounds__(kNWA * 32) attn_kernel(const AttnParams p) {
         const int j = idx / hs4, w4 = idx % hs4;
         float mm = -CUDART_INF_F, ll = 0.f;
         float4 aa = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int w = 0; w < kNWA; ++w)
+        for (int w = 0; w < NRG; ++w)
             merge_state(mm, ll, aa, mrg[(w * GQ + j) * 2], mrg[(w * GQ + j) * 2 + 1], accs[(size_t)(w * GQ + j) * hs4 + w4]);
         const size_t slot = ((size_t)b * H + h0 + j) * NC + c;
         reinterpret_cast<float4 *>(p.ws_acc + slot * hs)[w4] = aa;
@@ -529,16 +613,19 @@ AttnLaunch attn_plan(int head_size, int n_heads, int n_kv_heads) {
     AttnLaunch a{};
     const int hs4 = head_size / 4;
     const int max_group = (n_heads + n_kv_heads - 1) / n_kv_heads;
-    a.lp = pow2_at_least(hs4);
     a.gq = pow2_at_least(max_group);
+    // lanes per cache row: the row's 16-byte words over WPL words per lane (WPL as in the kernel)
+    const int wpl = a.gq == 1 ? 4 : a.gq == 2 ? 2 : 1;
+    a.lp = pow2_at_least((hs4 + wpl - 1) / wpl);
 #ifndef L2_ATTN_ROW_LANE
 #define L2_ATTN_ROW_LANE 1
 #endif
     a.rl = L2_ATTN_ROW_LANE && head_size == 64 && (a.gq == 4 || a.gq == 8) && kStageFloats == 2 * 16 * 64;
     a.threads = kNWA * 32;
-    const size_t hdr = (8 * kNWA * kAttStages + 16 + 4 * (kNWA * a.gq * 2 + a.gq * 2) + 127) / 128 * 128;
-    a.smem = hdr + (size_t)kNWA * kAttStages * kStageFloats * 4 + (size_t)kNWA * a.gq * hs4 * 16;
-    if (a.rl) a.smem += (size_t)a.gq * head_size * 4 + (size_t)kNWA * 17 * a.gq * 4;  // query vectors, probabilities
+    const int wpr = a.rl ? 2 : 1, nrg = kNWA / wpr;  // warps per ring, rings per CTA (as in the kernel)
+    const size_t hdr = (8 * nrg * kAttStages + 16 + 4 * (nrg * a.gq * 2 + a.gq * 2) + 127) / 128 * 128;
+    a.smem = hdr + (size_t)nrg * kAttStages * kStageFloats * 4 + (size_t)nrg * a.gq * hs4 * 16;
+    if (a.rl) a.smem += (size_t)a.gq * head_size * 4 + (size_t)kNWA * 17 * (a.gq / wpr) * 4;  // query vectors, probabilities
     a.ok = a.lp <= 32 && a.gq <= 8 && head_size % 4 == 0 && 2 * head_size <= kStageFloats;
     return a;
 }

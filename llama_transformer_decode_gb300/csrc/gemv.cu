@@ -71,6 +71,13 @@
 #ifndef L2_GEMV_FENCE
 #define L2_GEMV_FENCE 0
 #endif
+// With issue-ahead, request every ring buffer before griddepcontrol.wait (all
+// STAGES chunks, not STAGES - 1): the buffer the steady state keeps free for
+// the next refill is free at the start too, so one more chunk of this
+// kernel's weights streams while the previous kernel drains.
+#ifndef L2_GEMV_PREISSUE_ALL
+#define L2_GEMV_PREISSUE_ALL 0
+#endif
 
 namespace l2 {
 
@@ -222,8 +229,9 @@ __global__ void __launch_bounds__(NW * 32, 1) l2dec_matvec_kernel(const GemvPara
 
     // Weights do not depend on the previous kernel: start streaming them now.
     constexpr bool AHEAD = L2_GEMV_ISSUE_AHEAD && STAGES >= 3;
+    constexpr int PRE = AHEAD && !L2_GEMV_PREISSUE_ALL ? STAGES - 1 : STAGES;
 #pragma unroll 1
-    for (int s = 0; s < (AHEAD ? STAGES - 1 : STAGES) && fi < fe; ++s) issue(s);
+    for (int s = 0; s < PRE && fi < fe; ++s) issue(s);
 
     pdl_launch_dependents();
     pdl_wait();
@@ -287,7 +295,8 @@ __global__ void __launch_bounds__(NW * 32, 1) l2dec_matvec_kernel(const GemvPara
             break;
         }
         // chunk k + STAGES - 1 goes into the buffer finished in iteration k - 1
-        if (AHEAD && fi < fe) issue((k + STAGES - 1) % STAGES);
+        // (at k = 0 it may already be in flight: every buffer was requested up front)
+        if (AHEAD && fi < fe && n_issued == k + STAGES - 1) issue((k + STAGES - 1) % STAGES);
         const Piece &pc = fx.pieces[pi];
         const float4 *buf = wring + (size_t)s * CH4;
         const int lf = (int)(fc - pc.f0), lend = lf + len;

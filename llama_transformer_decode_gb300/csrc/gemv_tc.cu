@@ -6,15 +6,21 @@
 // 2a-2h and 3) and the RMSNorm scale.
 //
 // Precision.  The data are fp32; tcgen05.mma kind::tf32 reads the top 19
-// bits of each operand.  Each product is taken as hi*hi + hi*lo + lo*hi with
-// hi the truncated tf32 part and lo = x - hi (the "3xTF32" split of Ootomo
-// and Yokota), accumulating in fp32 in tensor memory: the dropped lo*lo term
-// and the truncation of lo leave a relative error near 2^-21 per product,
-// fp32-level for these sums.  The raw fp32 tiles serve as hi (the hardware
-// truncates).  Converter warps write the inputs' lo rows beside the inputs
-// in shared memory, and the weights' lo parts into tensor memory (one row
-// per TMEM lane), where the MMA reads its A operand directly.  Per K step:
-// one MMA of N = 2*bpad, W * [x_hi; x_lo], and one of N = bpad, W_lo * x_hi.
+// bits of each operand.  Each product is taken as hi*hi + hi*lo + lo*hi (the
+// "3xTF32" split of Ootomo and Yokota), accumulating in fp32 in tensor
+// memory.  For the weights, hi is the copied tile as the MMA truncates it and
+// lo = w - hi (truncated in turn: under 2^-20 relative); for the inputs, hi is
+// the tf32 value nearest to x (written back over the input tile) and lo the
+// tf32 value nearest to x - hi.  Converter warps write the inputs' lo rows
+// beside the inputs in shared memory and the weights' lo parts into tensor
+// memory (one row per TMEM lane), where the MMA reads its A operand directly.
+// Per K step: one MMA of N = 2*bpad, W * [x_hi; x_lo], and one of N = bpad,
+// W_lo * x_hi.  The tensor core's fp32 accumulation loses more than an fp32
+// FMA chain as a chain of MMAs into one accumulator grows (measured on GB300:
+// attention probabilities 20 layers on were 10x further from the oracle than
+// on the CUDA cores with whole K ranges in one accumulator), so the MMAs of at
+// most kDrain ring stages share an accumulator and the epilogue warps add the
+// groups up in fp32, in K order.
 //
 // Inputs.  The RMSNorm modes read x * gain, written by the previous residual
 // kernel (or the embedding kernel) beside x, and scale the outputs by 1/rms
@@ -47,6 +53,7 @@
 #include <algorithm>
 
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include "l2_device.cuh"
@@ -66,15 +73,33 @@ constexpr int kConvWarp0 = 4;   // converter warps 4..7
 constexpr int kEpiWarp0 = 8;    // epilogue warps 8..11
 constexpr int kRoleThreads = 128;
 constexpr uint32_t kABytes = kTM * kBK * 4;          // 16 KB: one box of weights (128 rows x 32)
-constexpr uint32_t kTmemCols = 512;                   // accumulators [0, 4 bpad), W_lo ring above
+constexpr uint32_t kTmemCols = 512;                   // accumulators [0, 2 bpad naccs), W_lo ring above
+constexpr int kMaxAccs = 4;                           // accumulators in tensor memory (2..4, as TMEM allows)
+// Ring stages the MMAs add into one accumulator before the epilogue takes it and
+// adds it to the tile's running sum in fp32: the tensor core's accumulation
+// error grows faster than linearly with the length of a chain of MMAs into one
+// accumulator, so the chains are kept short.
+#ifndef L2_TC_DRAIN
+#define L2_TC_DRAIN 4
+#endif
+constexpr int kDrain = L2_TC_DRAIN;
 constexpr size_t kSmemLimit = 227 * 1024;
 
-// A stage covers 64 K columns as two 32-column halves h: weights W_h (16 KB
-// each), then per half the bpad input rows X_h followed by their bpad lo
-// rows.  Whole stages move with one barrier phase: fewer, larger phases
-// stream from HBM markedly faster than twice as many 16 KB ones.
+// A stage covers 64 K columns.  fp32 weights (WT 0): two 32-column halves h,
+// weights W_h (16 KB each), then per half the bpad input rows X_h followed by
+// their bpad lo rows.  bf16 weights (WT 1): one 16 KB tile of weights (128 rows
+// of 64), the two fp32 input boxes X_0, X_1, then the inputs split into three
+// bf16 parts (hi, mid, lo), 3 bpad rows of 64 -- the MMA's B operand.  Whole
+// stages move with one barrier phase: fewer, larger phases stream from HBM
+// markedly faster than twice as many 16 KB ones.
 __host__ __device__ constexpr uint32_t xbox_bytes(int bpad) { return (uint32_t)bpad * kBK * 4; }
-__host__ __device__ constexpr uint32_t stage_bytes(int bpad) { return 2 * kABytes + 4 * xbox_bytes(bpad); }
+__host__ __device__ constexpr uint32_t wstage_bytes(int wt) { return wt ? (uint32_t)kTM * kSK * 2 : 2 * kABytes; }
+__host__ __device__ constexpr uint32_t xparts_bytes(int bpad) { return 3u * (uint32_t)bpad * kSK * 2; }
+__host__ __device__ constexpr uint32_t stage_bytes(int bpad, int wt) {
+    return wt ? wstage_bytes(1) + 2 * xbox_bytes(bpad) + xparts_bytes(bpad) : 2 * kABytes + 4 * xbox_bytes(bpad);
+}
+// accumulator columns: W [x_hi; x_lo] (WT 0) or W [x_hi; x_mid; x_lo] (WT 1)
+__host__ __device__ constexpr int acc_cols(int bpad, int wt) { return (wt ? 3 : 2) * bpad; }
 // ys: the finished tile [128][bpad + 1] (odd stride: conflict-free columns)
 __host__ __device__ constexpr size_t ys_bytes(int bpad) { return (size_t)kTM * (bpad + 1) * 4; }
 
@@ -82,8 +107,8 @@ struct TcFixed {
     uint64_t full[kMaxStages];   // copies landed
     uint64_t conv[kMaxStages];   // lo parts written
     uint64_t empty[kMaxStages];  // MMAs done with the stage
-    uint64_t acc_full[2];   // accumulator complete
-    uint64_t acc_free[2];   // accumulator read out
+    uint64_t acc_full[kMaxAccs];   // accumulator complete
+    uint64_t acc_free[kMaxAccs];   // accumulator read out
     uint64_t fin;
     uint32_t tmem;
     int abort;
@@ -96,20 +121,39 @@ struct TcFixed {
 
 __host__ __device__ constexpr size_t tc_fixed_bytes() { return (sizeof(TcFixed) + 1023) / 1024 * 1024; }
 
-// Ring stages for a batch width: what shared memory and the TMEM columns left
-// beside the two accumulators hold.
-__host__ __device__ constexpr int tc_stages(int bpad) {
-    const int by_smem = (int)((kSmemLimit - 1024 - tc_fixed_bytes() - ys_bytes(bpad)) / stage_bytes(bpad));
-    const int by_tmem = (int)((kTmemCols - 4u * (uint32_t)bpad) / kSK);
+// Ring stages for a batch width: what shared memory holds and, with fp32
+// weights, the TMEM columns left beside two accumulators (the W_lo ring).
+__host__ __device__ constexpr int tc_stages(int bpad, int wt) {
+    const int by_smem = (int)((kSmemLimit - 1024 - tc_fixed_bytes() - ys_bytes(bpad)) / stage_bytes(bpad, wt));
+    const int by_tmem = wt ? kMaxStages : (int)((kTmemCols - 4u * (uint32_t)bpad) / kSK);
     const int n = by_smem < by_tmem ? by_smem : by_tmem;
     return n < kMaxStages ? n : kMaxStages;
 }
+// Accumulators: as many as fit beside the W_lo ring (fp32 weights), 2 to 4.
+__host__ __device__ constexpr int tc_naccs(int bpad, int stages, int wt) {
+    const int n = (int)((kTmemCols - (wt ? 0u : (uint32_t)(kSK * stages))) / (uint32_t)acc_cols(bpad, wt));
+    return n < 2 ? 2 : n > kMaxAccs ? kMaxAccs : n;
+}
 
 __device__ __forceinline__ float silu_t(float v) { return v / (1.0f + expf(-v)); }
-__device__ __forceinline__ float tf32_lo(float x) { return x - __uint_as_float(__float_as_uint(x) & 0xFFFFE000u); }
-__device__ __forceinline__ float4 tf32_lo4(float4 v) {
-    return make_float4(tf32_lo(v.x), tf32_lo(v.y), tf32_lo(v.z), tf32_lo(v.w));
+// x = hi + lo with hi the tf32 value nearest to x and lo the tf32 value nearest to
+// x - hi (both exact in fp32, so the MMA reads them without further rounding):
+// |x - hi - lo| <= 2^-22 |x|.
+__device__ __forceinline__ float tf32_rna(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return __uint_as_float(r);
 }
+__device__ __forceinline__ void tf32_split4(float4 v, float4 &hi, float4 &lo) {
+    hi = make_float4(tf32_rna(v.x), tf32_rna(v.y), tf32_rna(v.z), tf32_rna(v.w));
+    lo = make_float4(tf32_rna(v.x - hi.x), tf32_rna(v.y - hi.y), tf32_rna(v.z - hi.z), tf32_rna(v.w - hi.w));
+}
+// The weights' lo part against the tile as copied, whose hi part the MMA takes
+// by truncating each operand to tf32: lo = w - trunc(w), itself truncated by the
+// MMA, |w - trunc(w) - trunc(lo)| < 2^-20 |w| (rounding the weight tile to
+// nearest in place would halve that, but writing 32 KB per stage back into
+// shared memory measurably slowed the converter warps).
+__device__ __forceinline__ float tf32_lo_trunc(float x) { return x - __uint_as_float(__float_as_uint(x) & 0xFFFFE000u); }
 
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
@@ -130,9 +174,36 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t addr) {
            ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
 
-// Instruction descriptor: D fp32, A and B tf32, both K-major, M x N.
+// Instruction descriptor: D fp32, A and B tf32 (kind::tf32) or bf16 (kind::f16),
+// both K-major, M x N.
 __device__ __forceinline__ uint32_t idesc_tf32(int M, int N) {
     return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+__device__ __forceinline__ uint32_t idesc_bf16(int M, int N) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t tmem, uint64_t da, uint64_t db, uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem),
+        "l"(da), "l"(db), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// x = hi + mid + lo in bf16, each part the bf16 value nearest to what the parts
+// before it leave: fp32's 24-bit significand in three 8-bit pieces, so the sum
+// is exact for every fp32 that is not far below 2^-100.  Returns the three
+// parts' bits.
+__device__ __forceinline__ void bf16_split3(float x, uint32_t &h, uint32_t &m, uint32_t &l) {
+    const __nv_bfloat16 bh = __float2bfloat16_rn(x);
+    const float r1 = x - __bfloat162float(bh);
+    const __nv_bfloat16 bm = __float2bfloat16_rn(r1);
+    const float r2 = r1 - __bfloat162float(bm);
+    const __nv_bfloat16 bl = __float2bfloat16_rn(r2);
+    h = __bfloat16_as_ushort(bh);
+    m = __bfloat16_as_ushort(bm);
+    l = __bfloat16_as_ushort(bl);
 }
 
 __device__ __forceinline__ void mma_tf32(uint32_t tmem, uint64_t da, uint64_t db, uint32_t idesc, uint32_t accumulate) {
@@ -187,6 +258,16 @@ __device__ __forceinline__ void tmem_ld8(uint32_t addr, float *v) {
 #pragma unroll
     for (int j = 0; j < 8; ++j) v[j] = __uint_as_float(r[j]);
 }
+__device__ __forceinline__ void tmem_ld16(uint32_t addr, float *v) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(addr));
+#pragma unroll
+    for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
+}
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
@@ -203,6 +284,29 @@ __device__ __forceinline__ bool epi_sync_or(bool v) {
         : "r"((uint32_t)v)
         : "memory");
     return r != 0;
+}
+
+// Thread-block clusters: this CTA's rank, the address of a shared-memory word
+// in another CTA of the cluster, a load through it, and a barrier of every
+// thread of the cluster (release / acquire: shared-memory writes before it are
+// visible to the other CTAs' reads after it).
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t dsmem_addr(const void *p, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ float ld_dsmem(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ bool aborted(const TcFixed &fx) { return *reinterpret_cast<const volatile int *>(&fx.abort) != 0; }
@@ -247,7 +351,9 @@ __global__ void l2dec_tc_embed_kernel(const GemvParams p, float *xg) {
     }
 }
 
-template <int MODE>
+// WT: 0 fp32 weights (3xTF32 products), 1 bf16 weights (kind::f16, exact products
+// of the bf16 weights and the three bf16 parts of each input).
+template <int MODE, int WT>
 __global__ void __launch_bounds__(kTT, 1) l2dec_matvec_tc_kernel(const __grid_constant__ TcParams tp) {
     const GemvParams &p = tp.g;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -255,16 +361,21 @@ __global__ void __launch_bounds__(kTT, 1) l2dec_matvec_tc_kernel(const __grid_co
     TcFixed &fx = *reinterpret_cast<TcFixed *>(smem);
     const int B = p.batch, BP = tp.bpad, n = p.n;
     const int NS = tp.stages;
-    const uint32_t SB = stage_bytes(BP);
+    const uint32_t SB = stage_bytes(BP, WT);
     unsigned char *ring = smem + tc_fixed_bytes();  // 1024-aligned stages, then ys
     float *ys = reinterpret_cast<float *>(ring + (size_t)NS * SB);  // [128][bpad + 1]
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int YS = BP + 1;
     const int KT = (n + kSK - 1) / kSK;  // ring stages of 64 columns per tile
     // Stream-K: the (tile, stage) pairs in tile-major order, split evenly over the CTAs.
+    // Cluster split (CS > 1): CTA rank r of cluster t takes stages [KT r / CS, KT (r + 1) / CS)
+    // of tile t (the host keeps CS <= KT).
     const long long T = (long long)tp.ntiles * KT;
-    const int G = gridDim.x;
-    const long long s_begin = (long long)blockIdx.x * T / G, s_end = (long long)(blockIdx.x + 1) * T / G;
+    const int G = gridDim.x, CS = tp.csplit;
+    const long long s_begin = CS > 1 ? (long long)(blockIdx.x / CS) * KT + (long long)KT * (blockIdx.x % CS) / CS
+                                     : (long long)blockIdx.x * T / G;
+    const long long s_end = CS > 1 ? (long long)(blockIdx.x / CS) * KT + (long long)KT * (blockIdx.x % CS + 1) / CS
+                                   : (long long)(blockIdx.x + 1) * T / G;
     // the CTA holding stage x of the sequence
     auto cta_of = [&](long long x) { return (int)(((x + 1) * G + T - 1) / T - 1); };
     // the next segment (one tile's part of the CTA's range) at sequence position sq
@@ -289,7 +400,7 @@ __global__ void __launch_bounds__(kTT, 1) l2dec_matvec_tc_kernel(const __grid_co
             mbar_init(&fx.conv[i], kRoleThreads);
             mbar_init(&fx.empty[i], 1);
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kMaxAccs; ++i) {
             mbar_init(&fx.acc_full[i], 1);
             mbar_init(&fx.acc_free[i], kRoleThreads);
         }
@@ -311,33 +422,43 @@ __global__ void __launch_bounds__(kTT, 1) l2dec_matvec_tc_kernel(const __grid_co
     pdl_launch_dependents();
 
     auto stage_ptr = [&](int s) { return ring + (size_t)s * SB; };
-    // stage s: W_0 | W_1 | X_0 | X_0 lo | X_1 | X_1 lo
+    // stage s, fp32 weights: W_0 | W_1 | X_0 | X_0 lo | X_1 | X_1 lo;
+    //          bf16 weights: W | X_0 | X_1 | X parts (hi, mid, lo rows)
     auto wbox = [&](int s, int h) { return stage_ptr(s) + h * kABytes; };
-    auto xbox = [&](int s, int h) { return stage_ptr(s) + 2 * kABytes + 2 * h * xbox_bytes(BP); };
-    // TMEM: accumulator a at columns [2 bpad a, 2 bpad (a + 1)); stage s's W_lo at 4 bpad + 64 s
-    auto wlo_col = [&](int s) { return (uint32_t)(4 * BP + kSK * s); };
+    auto xbox = [&](int s, int h) {
+        return WT ? stage_ptr(s) + wstage_bytes(1) + h * xbox_bytes(BP) : stage_ptr(s) + 2 * kABytes + 2 * h * xbox_bytes(BP);
+    };
+    auto xparts = [&](int s) { return stage_ptr(s) + wstage_bytes(1) + 2 * xbox_bytes(BP); };
+    // TMEM: accumulator a at columns [AC a, AC (a + 1)); with fp32 weights stage s's W_lo
+    // at AC NA + 64 s
+    const int AC = acc_cols(BP, WT), NA = tc_naccs(BP, NS, WT);
+    auto wlo_col = [&](int s) { return (uint32_t)(AC * NA + kSK * s); };
 
-    // a finished tile in ys -> the outputs of rows r0.. of matrix m, sequences 0..B-1 (row index fastest)
-    auto finish = [&](int tile, int ti, int nt, auto sync) {
+    // A finished tile in src ([128][bpad + 1]) -> the outputs of its rows jlo..jhi-1
+    // (for W1/W3: the SwiGLU pairs jlo..jhi-1 of rows j and j + 64; for QKV jlo and
+    // jhi are even, keeping RoPE pairs together), sequences 0..B-1.  The residual
+    // mode writes its rows' sums of squares to ss_part row `part`.
+    auto finish = [&](int tile, int ti, int nt, auto sync, float *src, int jlo, int jhi, int part) {
         int m, r0, wrow;
         tile_geom(tile, m, r0, wrow);
+        const int nj = jhi - jlo;
         if (MODE == GEMV_QKV) {
             // pairs (j, j+1) of rows: RoPE on q and k, then the KV cache; the table reads of
             // 8 pairs go out before their stores
-            const int hs = p.head_size, half = hs >> 1, mr = tp.mrows[m];
-            for (int e0 = ti; e0 < (kTM / 2) * B; e0 += 8 * nt) {
+            const int hs = p.head_size, half = hs >> 1, mr = tp.mrows[m], npr = nj >> 1;
+            for (int e0 = ti; e0 < npr * B; e0 += 8 * nt) {
                 float2 cs[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
-                    const int e = e0 + i * nt, b = e / (kTM / 2), v = r0 + 2 * (e - b * (kTM / 2));
+                    const int e = e0 + i * nt, b = e / npr, v = r0 + jlo + 2 * (e - b * npr);
                     cs[i] = make_float2(1.f, 0.f);
-                    if (m < 2 && e < (kTM / 2) * B && v < mr) cs[i] = p.rope[(size_t)fx.pos[b] * half + ((v % hs) >> 1)];
+                    if (m < 2 && e < npr * B && v < mr) cs[i] = p.rope[(size_t)fx.pos[b] * half + ((v % hs) >> 1)];
                 }
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
-                    const int e = e0 + i * nt, b = e / (kTM / 2), j = 2 * (e - b * (kTM / 2)), v = r0 + j;
-                    if (e >= (kTM / 2) * B || v >= mr) continue;
-                    const float y0 = ys[j * YS + b] * fx.inv[b], y1 = ys[(j + 1) * YS + b] * fx.inv[b];
+                    const int e = e0 + i * nt, b = e / npr, j = jlo + 2 * (e - b * npr), v = r0 + j;
+                    if (e >= npr * B || v >= mr) continue;
+                    const float y0 = src[j * YS + b] * fx.inv[b], y1 = src[(j + 1) * YS + b] * fx.inv[b];
                     if (m == 0) {
                         float *qv = p.q + (size_t)b * p.dim;
                         qv[v] = y0 * cs[i].x - y1 * cs[i].y;
@@ -359,72 +480,87 @@ __global__ void __launch_bounds__(kTT, 1) l2dec_matvec_tc_kernel(const __grid_co
             }
         } else if (MODE == GEMV_W13) {
             const int hidden = tp.mrows[0];
-            for (int e = ti; e < (kTM / 2) * B; e += nt) {
-                const int b = e / (kTM / 2), j = e - b * (kTM / 2);
+            for (int e = ti; e < nj * B; e += nt) {
+                const int b = e / nj, j = jlo + (e - b * nj);
                 if (r0 + j >= hidden) continue;
-                const float h1 = ys[j * YS + b] * fx.inv[b], h3 = ys[(j + kTM / 2) * YS + b] * fx.inv[b];
+                const float h1 = src[j * YS + b] * fx.inv[b], h3 = src[(j + kTM / 2) * YS + b] * fx.inv[b];
                 p.hb[(size_t)b * hidden + r0 + j] = silu_t(h1) * h3;
             }
         } else if (MODE == GEMV_RESID) {
             const int dim = tp.mrows[0];
-            // thread = row j (and a group of sequences); x of 8 sequences loaded before any store
-            const int j = ti % kTM, bg = ti / kTM, nbg = nt / kTM;
-            if (j < dim - r0) {
+            const int jend = min(jhi, dim - r0);
+            // item = a row and a group of 8 sequences; x of the 8 loaded before any store
+            const int ng = (B + 7) / 8;
+            for (int e = ti; e < nj * ng; e += nt) {
+                const int j = jlo + e % nj, b0 = 8 * (e / nj);
+                if (j >= jend) continue;
                 const float g = __ldg(tp.next_gain + r0 + j);
-                for (int b0 = 8 * bg; b0 < B; b0 += 8 * nbg) {
-                    float xv[8];
+                float xv[8];
 #pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        if (b0 + i < B) xv[i] = p.x[(size_t)(b0 + i) * dim + r0 + j];
+                for (int i = 0; i < 8; ++i)
+                    if (b0 + i < B) xv[i] = p.x[(size_t)(b0 + i) * dim + r0 + j];
 #pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        if (b0 + i < B) {
-                            const size_t o = (size_t)(b0 + i) * dim + r0 + j;
-                            const float nv = xv[i] + ys[j * YS + b0 + i];
-                            p.x[o] = nv;
-                            tp.xg[o] = nv * g;
-                            ys[j * YS + b0 + i] = nv;
-                        }
-                }
+                for (int i = 0; i < 8; ++i)
+                    if (b0 + i < B) {
+                        const size_t o = (size_t)(b0 + i) * dim + r0 + j;
+                        const float nv = xv[i] + src[j * YS + b0 + i];
+                        p.x[o] = nv;
+                        tp.xg[o] = nv * g;
+                        src[j * YS + b0 + i] = nv;
+                    }
             }
             sync();
-            // this tile's sum of squares of the new x rows, per sequence, in a fixed order
+            // these rows' sum of squares of the new x, per sequence, in a fixed order
             // (128 partials whatever the thread count: the padding column has 128 rows)
-            const int parts = kTM / B, rows = min(kTM, dim - r0);
+            const int parts = kTM / B;
             if (ti < kTM) {
                 float ss = 0.f;
                 if (ti < parts * B) {
                     const int b = ti % B;
-                    for (int jr = ti / B; jr < rows; jr += parts) ss = fmaf(ys[jr * YS + b], ys[jr * YS + b], ss);
+                    for (int jr = jlo + ti / B; jr < jend; jr += parts) ss = fmaf(src[jr * YS + b], src[jr * YS + b], ss);
                 }
-                ys[ti * YS + BP] = ss;
+                src[ti * YS + BP] = ss;
             }
             sync();
             if (ti < B) {
                 float t = 0.f;
-                for (int i = 0; i < parts; ++i) t += ys[(i * B + ti) * YS + BP];
-                p.ss_part[(size_t)tile * B + ti] = t;
+                for (int i = 0; i < parts; ++i) t += src[(i * B + ti) * YS + BP];
+                p.ss_part[(size_t)part * B + ti] = t;
             }
         } else {
             float *user = p.step->logits_out;
             const int V = tp.mrows[0];
-            for (int e = ti; e < kTM * B; e += nt) {
-                const int b = e / kTM, j = e - b * kTM;
+            for (int e = ti; e < nj * B; e += nt) {
+                const int b = e / nj, j = jlo + (e - b * nj);
                 if (r0 + j >= V) continue;
-                const float y = ys[j * YS + b] * fx.inv[b];
+                const float y = src[j * YS + b] * fx.inv[b];
                 p.logits[(size_t)b * V + r0 + j] = y;
                 if (user) user[(size_t)b * V + r0 + j] = y;
             }
         }
     };
+    constexpr int kUnit = MODE == GEMV_W13 ? kTM / 2 : kTM;  // rows (W1/W3: row pairs) of a tile
 
     if (warp == 0) {
         // ---------------- producer: tensor copies into the ring (whole warp, one lane issues) ----------------
-        const uint32_t stage_tx = 2 * kABytes + 2 * xbox_bytes(BP);  // the lo rows are written here
+        // the copies of a stage: its weights and the two fp32 input boxes (the lo rows or
+        // the bf16 parts are written here)
+        const uint32_t stage_tx = wstage_bytes(WT) + 2 * xbox_bytes(BP);
         long long nl = 0;
         bool stop = false;
         auto issue_weights = [&](int s, int m, int wrow, int kt) {
             mbar_arrive_expect_tx(&fx.full[s], stage_tx);
+            if (WT) {
+                // one box of 64 bf16 columns (128-byte rows): 128 rows, or 64 of W1 over 64 of W3
+                const int x = kt * kSK;
+                if (MODE == GEMV_W13) {
+                    tensor2d(wbox(s, 0), &tp.wmap[0], x, wrow, &fx.full[s]);
+                    tensor2d(wbox(s, 0) + wstage_bytes(1) / 2, &tp.wmap[1], x, wrow, &fx.full[s]);
+                } else {
+                    tensor2d(wbox(s, 0), &tp.wmap[MODE == GEMV_QKV ? m : 0], x, wrow, &fx.full[s]);
+                }
+                return;
+            }
             for (int h = 0; h < 2; ++h) {
                 const int x = kt * kSK + h * kBK;
                 if (MODE == GEMV_W13) {
@@ -470,29 +606,48 @@ __global__ void __launch_bounds__(kTT, 1) l2dec_matvec_tc_kernel(const __grid_co
                 (void)mbar_wait(&fx.full[j % NS], (uint32_t)((j / NS) & 1), p.err);
     } else if (warp == 1) {
         // ---------------- MMA issuer (whole warp, one lane issues) ----------------
-        const uint32_t idesc2 = idesc_tf32(kTM, 2 * BP), idesc1 = idesc_tf32(kTM, BP);
+        const uint32_t idesc2 = idesc_tf32(kTM, 2 * BP), idesc1 = idesc_tf32(kTM, BP), idesc3 = idesc_bf16(kTM, 3 * BP);
         const uint64_t dring = desc_sw128(smem_u32(ring));  // stage 0's weight tile
-        long long nc = 0, ni = 0;
+        long long nc = 0, ng = 0;  // stages, accumulator groups
         bool stop = false;
-        for (long long sq = s_begin; sq < s_end && !stop; ++ni) {
+        for (long long sq = s_begin; sq < s_end && !stop;) {
             int tile, k0, k1;
             segment(sq, tile, k0, k1);
             sq += k1 - k0;
-            const int a = (int)(ni & 1);
-            const bool ok = ni < 2 || mbar_wait(&fx.acc_free[a], (uint32_t)(((ni / 2) - 1) & 1), p.err);
-            if ((stop = warp_stop(fx, ok))) break;
-            tc_fence_after();
-            const uint32_t dacc = tmem + (uint32_t)(2 * BP * a);
             for (int kt = k0; kt < k1; ++kt, ++nc) {
                 const int s = (int)(nc % NS);
+                // every kDrain stages of a segment start a fresh accumulator (NA of them
+                // rotate): the epilogue adds the groups up in fp32, so no MMA accumulation
+                // chain is longer than kDrain stages
+                const bool g_first = (kt - k0) % kDrain == 0, g_last = (kt - k0) % kDrain == kDrain - 1 || kt == k1 - 1;
+                const int a = (int)(ng % NA);
+                if (g_first) {
+                    const bool okf = ng < NA || mbar_wait(&fx.acc_free[a], (uint32_t)(((ng / NA) - 1) & 1), p.err);
+                    if ((stop = warp_stop(fx, okf))) break;
+                }
                 const bool okc = mbar_wait(&fx.conv[s], (uint32_t)((nc / NS) & 1), p.err);
                 if ((stop = warp_stop(fx, okc))) break;
                 tc_fence_after();
-                // descriptor start addresses are in 16-byte units; a K step of 8 is 32 bytes
+                const uint32_t dacc = tmem + (uint32_t)(AC * a);
+                // descriptor start addresses are in 16-byte units; a K step of 8 tf32 or of 16
+                // bf16 is 32 bytes
                 const uint64_t dw = dring + (uint64_t)((uint32_t)s * (SB >> 4));
+                if (WT) {
+                    // columns [0, BP): W x_hi; [BP, 2 BP): W x_mid; [2 BP, 3 BP): W x_lo
+                    const uint64_t dxp = dw + ((wstage_bytes(1) + 2 * xbox_bytes(BP)) >> 4);
+                    if (elect_one()) {
+#pragma unroll
+                        for (int ks = 0; ks < kSK / 16; ++ks)
+                            mma_bf16(dacc, dw + 2 * ks, dxp + 2 * ks, idesc3, (g_first && ks == 0) ? 0u : 1u);
+                        mma_commit(&fx.empty[s]);
+                        if (g_last) mma_commit(&fx.acc_full[a]);
+                    }
+                    __syncwarp();
+                    if (g_last) ++ng;
+                    continue;
+                }
                 const uint64_t dx = dw + ((2 * kABytes) >> 4), dxh = (2 * xbox_bytes(BP)) >> 4;
                 const uint32_t twl = tmem + wlo_col(s);
-                const uint32_t first = kt == k0 ? 0u : 1u;
                 if (elect_one()) {
 #pragma unroll
                     for (int h = 0; h < 2; ++h)
@@ -500,16 +655,15 @@ __global__ void __launch_bounds__(kTT, 1) l2dec_matvec_tc_kernel(const __grid_co
                         for (int ks = 0; ks < kBK / 8; ++ks) {
                             // columns [0, BP): W x_hi; [BP, 2 BP): W x_lo; then W_lo x_hi into [0, BP)
                             const uint64_t a = dw + h * (kABytes >> 4) + 2 * ks, b = dx + h * dxh + 2 * ks;
-                            mma_tf32(dacc, a, b, idesc2, (h == 0 && ks == 0) ? first : 1u);
+                            mma_tf32(dacc, a, b, idesc2, (g_first && h == 0 && ks == 0) ? 0u : 1u);
                             mma_tf32_ta(dacc, twl + (uint32_t)(kBK * h + 8 * ks), b, idesc1, 1u);
                         }
                     mma_commit(&fx.empty[s]);
+                    if (g_last) mma_commit(&fx.acc_full[a]);
                 }
                 __syncwarp();
+                if (g_last) ++ng;
             }
-            if (stop) break;
-            if (elect_one()) mma_commit(&fx.acc_full[a]);
-            __syncwarp();
         }
         // nothing of this CTA's may still run on the tensor core when its memory goes
         if (elect_one()) mma_commit(&fx.fin);
@@ -528,6 +682,37 @@ __global__ void __launch_bounds__(kTT, 1) l2dec_matvec_tc_kernel(const __grid_co
             for (int kt = k0; kt < k1; ++kt, ++nc) {
                 const int s = (int)(nc % NS);
                 if ((stop = warp_stop(fx, mbar_wait(&fx.full[s], (uint32_t)((nc / NS) & 1), p.err)))) break;
+                if (WT) {
+                    // bf16 weights: the inputs' three bf16 parts, rows [part][bpad] of 64 columns in
+                    // the 128-byte swizzled layout of the fp32 boxes (16-byte chunk g of row r at
+                    // g ^ (r % 8); bpad is a multiple of 16, so row part * bpad + r swizzles as r)
+                    uint4 *XP = reinterpret_cast<uint4 *>(xparts(s));
+                    for (int i = ct; i < BP * 8; i += kRoleThreads) {
+                        const int r = i >> 3, g = i & 7;                   // row, group of 8 columns
+                        const int j0 = (g & 3) * 2;                         // its first fp32 chunk in box g / 4
+                        const float4 *Xr = reinterpret_cast<const float4 *>(xbox(s, g >> 2)) + r * (kBK / 4);
+                        const float4 u0 = Xr[j0 ^ (r & 7)], u1 = Xr[(j0 + 1) ^ (r & 7)];
+                        const float v[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+                        uint32_t ph[4], pm[4], pl[4];
+#pragma unroll
+                        for (int k2 = 0; k2 < 4; ++k2) {
+                            uint32_t h0, m0, l0, h1, m1, l1;
+                            bf16_split3(v[2 * k2], h0, m0, l0);
+                            bf16_split3(v[2 * k2 + 1], h1, m1, l1);
+                            ph[k2] = h0 | (h1 << 16);  // the lower column at the lower address
+                            pm[k2] = m0 | (m1 << 16);
+                            pl[k2] = l0 | (l1 << 16);
+                        }
+                        const int pc = g ^ (r & 7);
+                        XP[(size_t)r * 8 + pc] = make_uint4(ph[0], ph[1], ph[2], ph[3]);
+                        XP[(size_t)(BP + r) * 8 + pc] = make_uint4(pm[0], pm[1], pm[2], pm[3]);
+                        XP[(size_t)(2 * BP + r) * 8 + pc] = make_uint4(pl[0], pl[1], pl[2], pl[3]);
+                    }
+                    fence_proxy_async_smem();
+                    tc_fence_before();
+                    mbar_arrive(&fx.conv[s]);
+                    continue;
+                }
                 tc_fence_after();  // after the MMAs that last read this stage's TMEM columns
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
@@ -536,7 +721,9 @@ __global__ void __launch_bounds__(kTT, 1) l2dec_matvec_tc_kernel(const __grid_co
                     uint32_t v[kBK];
 #pragma unroll
                     for (int j = 0; j < kBK / 4; ++j) {
-                        const float4 a = tf32_lo4(A4[j ^ (row & 7)]);
+                        const float4 w4 = A4[j ^ (row & 7)];
+                        const float4 a =
+                            make_float4(tf32_lo_trunc(w4.x), tf32_lo_trunc(w4.y), tf32_lo_trunc(w4.z), tf32_lo_trunc(w4.w));
                         v[4 * j] = __float_as_uint(a.x);
                         v[4 * j + 1] = __float_as_uint(a.y);
                         v[4 * j + 2] = __float_as_uint(a.z);
@@ -547,7 +734,12 @@ __global__ void __launch_bounds__(kTT, 1) l2dec_matvec_tc_kernel(const __grid_co
                 for (int h = 0; h < 2; ++h) {
                     float4 *X4 = reinterpret_cast<float4 *>(xbox(s, h));
                     float4 *Xlo4 = X4 + BP * kBK / 4;  // right after the BP input rows
-                    for (int i = ct; i < BP * kBK / 4; i += kRoleThreads) Xlo4[i] = tf32_lo4(X4[i]);
+                    for (int i = ct; i < BP * kBK / 4; i += kRoleThreads) {
+                        float4 hi, lo;
+                        tf32_split4(X4[i], hi, lo);
+                        X4[i] = hi;
+                        Xlo4[i] = lo;
+                    }
                 }
                 tmem_wait_st();
                 fence_proxy_async_smem();
@@ -575,44 +767,52 @@ __global__ void __launch_bounds__(kTT, 1) l2dec_matvec_tc_kernel(const __grid_co
         epi_sync();
         // partial segments (at most the first and the last): published now, merged after the last one
         int part0 = -1, part1 = -1;
-        long long ni = 0;
+        long long ng = 0;  // accumulator groups, in the MMA warp's order
         bool stop = false;
-        for (long long sq = s_begin; sq < s_end; ++ni) {
+        for (long long sq = s_begin; sq < s_end && !stop;) {
             int tile, k0, k1;
             segment(sq, tile, k0, k1);
             const int which = sq == s_begin ? 0 : 1;
             sq += k1 - k0;
             const bool whole = k0 == 0 && k1 == KT;
-            const int a = (int)(ni & 1);
-            const bool ok = mbar_wait(&fx.acc_full[a], (uint32_t)((ni / 2) & 1), p.err);
-            if (!ok) set_abort(fx);
-            if ((stop = epi_sync_or(!ok || aborted(fx)))) break;  // the same decision in all four warps
-            tc_fence_after();
-            // this thread's row of the accumulator: y = W x_hi + W x_lo + W_lo x_hi
-            const uint32_t base = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(2 * BP * a);
-            // a partial tile goes to this CTA's workspace slot [BP][128]
-            float *wsrow = tp.ws + ((size_t)blockIdx.x * 2 + which) * kTM * BP;
-            for (int c0 = 0; c0 < B; c0 += 8) {
-                float v[8], w[8];
-                tmem_ld8(base + (uint32_t)c0, v);
-                tmem_ld8(base + (uint32_t)(BP + c0), w);
-                tmem_wait_ld();
+            // this thread's row of each group's accumulator, y = W x_hi + W x_lo + W_lo x_hi,
+            // added up over the segment's groups in ys (fp32, in K order)
+            for (int kg = k0; kg < k1; kg += kDrain, ++ng) {
+                const int a = (int)(ng % NA);
+                const bool ok = mbar_wait(&fx.acc_full[a], (uint32_t)((ng / NA) & 1), p.err);
+                if (!ok) set_abort(fx);
+                if ((stop = epi_sync_or(!ok || aborted(fx)))) break;  // the same decision in all four warps
+                tc_fence_after();
+                const uint32_t base = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(AC * a);
+                float *yr = ys + row * YS;
+                for (int c0 = 0; c0 < B; c0 += 16) {
+                    float v[16], w[16], u[16];
+                    tmem_ld16(base + (uint32_t)c0, v);
+                    tmem_ld16(base + (uint32_t)(BP + c0), w);
+                    if (WT) tmem_ld16(base + (uint32_t)(2 * BP + c0), u);
+                    tmem_wait_ld();
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const float y = v[j] + w[j];
-                    if (whole) ys[row * YS + c0 + j] = y;
-                    else wsrow[(size_t)(c0 + j) * kTM + row] = y;
+                    for (int j = 0; j < 16; ++j) {
+                        if (c0 + j >= B) break;
+                        const float y = WT ? (v[j] + w[j]) + u[j] : v[j] + w[j];
+                        yr[c0 + j] = kg == k0 ? y : yr[c0 + j] + y;
+                    }
                 }
+                tc_fence_before();
+                mbar_arrive(&fx.acc_free[a]);
             }
-            tc_fence_before();
-            mbar_arrive(&fx.acc_free[a]);
+            if (stop) break;
             if (!whole) {
+                if (CS > 1) continue;  // the CTA's only segment: added up across the cluster below
+                // a stream-K partial tile goes to this CTA's workspace slot [BP][128]
+                float *wsrow = tp.ws + ((size_t)blockIdx.x * 2 + which) * kTM * BP;
+                for (int c = 0; c < B; ++c) wsrow[(size_t)c * kTM + row] = ys[row * YS + c];
                 if (which == 0) part0 = tile;
                 else part1 = tile;
                 continue;
             }
             epi_sync();
-            finish(tile, et, kRoleThreads, [] { epi_sync(); });
+            finish(tile, et, kRoleThreads, [] { epi_sync(); }, ys, 0, kUnit, tile);
             epi_sync();  // ys free for the next tile
         }
         if (!stop && et == 0) {
@@ -625,6 +825,40 @@ __global__ void __launch_bounds__(kTT, 1) l2dec_matvec_tc_kernel(const __grid_co
     tc_fence_after();
     if (warp == 1)
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(kTmemCols) : "memory");
+
+    auto bar_all = []() { __syncthreads(); };
+    if (CS > 1) {
+        // Cluster split: every CTA of the cluster holds its K range's part of tile t in
+        // ys.  After a cluster barrier, rank r adds the parts of its rows jlo..jhi-1 in
+        // rank order (K order), reading the other CTAs' ys through distributed shared
+        // memory, into the ring (free now); a second barrier keeps every ys alive until
+        // all of those reads are done; then rank r finishes its rows.  Every CTA reaches
+        // both barriers (the waits before them are bounded), aborted or not.
+        const int tile = blockIdx.x / CS;
+        const uint32_t rk = cluster_rank();
+        const int jlo = (int)(((long long)kUnit * rk / CS) & ~1LL);
+        const int jhi = rk + 1 == (uint32_t)CS ? kUnit : (int)(((long long)kUnit * (rk + 1) / CS) & ~1LL);
+        const bool ab = aborted(fx);
+        float *red = reinterpret_cast<float *>(ring);  // [kTM][bpad + 1], as ys
+        cluster_sync_all();
+        if (!ab) {
+            const int half = MODE == GEMV_W13 ? 2 : 1;  // W1/W3: rows j and j + 64
+            const int nj = jhi - jlo;
+            for (int e = tid; e < nj * half * B; e += kTT) {
+                const int b = e % B, jj = e / B;
+                const int j = jlo + jj % nj + (jj / nj) * (kTM / 2);
+                const int o = j * YS + b;
+                float acc = 0.f;
+                for (int q = 0; q < CS; ++q) acc += ld_dsmem(dsmem_addr(ys + o, (uint32_t)q));
+                red[o] = acc;
+            }
+        }
+        cluster_sync_all();
+        if (ab) return;
+        pdl_wait();  // the previous kernel's outputs (x, the step's positions) are read below
+        finish(tile, tid, kTT, bar_all, red, jlo, jhi, tile * CS + (int)rk);
+        return;
+    }
 
     // Partial tiles, by the whole CTA: nothing of this CTA's is in flight any more, so
     // the one release fence it needs does not wait behind returning data.  Publish the
@@ -647,7 +881,6 @@ __global__ void __launch_bounds__(kTT, 1) l2dec_matvec_tc_kernel(const __grid_co
         __threadfence();
     }
     __syncthreads();
-    auto bar_all = []() { __syncthreads(); };
     for (int w = 0; w < 2; ++w) {
         if (!fx.last_w[w]) continue;
         const int t = fx.part_tile[w];
@@ -699,7 +932,7 @@ __global__ void __launch_bounds__(kTT, 1) l2dec_matvec_tc_kernel(const __grid_co
         }
         if (tid == 0) tp.tickets[t] = 0u;
         __syncthreads();
-        finish(t, tid, kTT, bar_all);
+        finish(t, tid, kTT, bar_all, ys, 0, kUnit, t);
         __syncthreads();
     }
 }
@@ -708,9 +941,11 @@ __global__ void __launch_bounds__(kTT, 1) l2dec_matvec_tc_kernel(const __grid_co
 
 int gemv_tc_max_batch() { return kTN; }
 
-int gemv_tc_stages(int bpad) { return tc_stages(bpad); }
+int gemv_tc_stages(int bpad, int wt) { return tc_stages(bpad, wt); }
 
-size_t gemv_tc_smem(int bpad) { return 1024 + tc_fixed_bytes() + (size_t)tc_stages(bpad) * stage_bytes(bpad) + ys_bytes(bpad); }
+size_t gemv_tc_smem(int bpad, int wt) {
+    return 1024 + tc_fixed_bytes() + (size_t)tc_stages(bpad, wt) * stage_bytes(bpad, wt) + ys_bytes(bpad);
+}
 
 // CTAs for a plan: one per SM, but each with at least kMinCtaStages ring
 // stages of work (fewer, longer ranges: fewer partial tiles to add up).
@@ -723,16 +958,60 @@ int gemv_tc_grid(int ntiles, int n, int ctas) {
     return (int)std::max<long long>(1, std::min<long long>(ctas, T / kMinCtaStages));
 }
 
+template <int WT>
+static void *tc_fn_wt(int mode) {
+    switch (mode) {
+        case GEMV_QKV: return reinterpret_cast<void *>(l2dec_matvec_tc_kernel<GEMV_QKV, WT>);
+        case GEMV_RESID: return reinterpret_cast<void *>(l2dec_matvec_tc_kernel<GEMV_RESID, WT>);
+        case GEMV_W13: return reinterpret_cast<void *>(l2dec_matvec_tc_kernel<GEMV_W13, WT>);
+        case GEMV_CLS: return reinterpret_cast<void *>(l2dec_matvec_tc_kernel<GEMV_CLS, WT>);
+    }
+    return nullptr;
+}
+static void *tc_fn(int mode, int wt) { return wt ? tc_fn_wt<1>(mode) : tc_fn_wt<0>(mode); }
+
+// Cluster split for plans with few tiles (fewer than half the SMs): the largest
+// cluster of 2..8 CTAs (at most one per K stage) of which all `ntiles` clusters
+// are resident at once on this device (one CTA per SM, so a cluster takes that
+// many SMs of one GPC).  0: no cluster size fits, use stream-K.
+#ifndef L2_TC_CLUSTER
+#define L2_TC_CLUSTER 1
+#endif
+int gemv_tc_cluster_split(int mode, int wt, int ntiles, int n, int bpad, int num_sms) {
+    const int KT = (n + kSK - 1) / kSK;
+    if (!L2_TC_CLUSTER || 2 * ntiles > num_sms) return 0;
+    void *fn = tc_fn(mode, wt);
+    for (int c = std::min(8, KT); c >= 2; --c) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(ntiles * c);
+        cfg.blockDim = dim3(kTT);
+        cfg.dynamicSmemBytes = gemv_tc_smem(bpad, wt);
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = (unsigned)c;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int clusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&clusters, fn, &cfg) != cudaSuccess) {
+            cudaGetLastError();
+            continue;
+        }
+        if (clusters >= ntiles) return c;
+    }
+    return 0;
+}
+
 // Workspace floats for a grid: two partial tiles per CTA.
 size_t gemv_tc_ws_floats(int grid, int bpad) { return (size_t)grid * 2 * kTM * bpad; }
 
 cudaError_t gemv_tc_init() {
-    void *fns[] = {reinterpret_cast<void *>(l2dec_matvec_tc_kernel<GEMV_QKV>), reinterpret_cast<void *>(l2dec_matvec_tc_kernel<GEMV_RESID>),
-                   reinterpret_cast<void *>(l2dec_matvec_tc_kernel<GEMV_W13>), reinterpret_cast<void *>(l2dec_matvec_tc_kernel<GEMV_CLS>)};
-    for (void *f : fns) {
-        cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemLimit);
-        if (e != cudaSuccess) return e;
-    }
+    for (int wt = 0; wt < 2; ++wt)
+        for (int mode : {GEMV_QKV, GEMV_RESID, GEMV_W13, GEMV_CLS}) {
+            cudaError_t e = cudaFuncSetAttribute(tc_fn(mode, wt), cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemLimit);
+            if (e != cudaSuccess) return e;
+        }
     return cudaSuccess;
 }
 
@@ -759,16 +1038,17 @@ cudaError_t launch_tc_embed(const TcParams &tp, int batch, cudaStream_t stream, 
 }
 
 cudaError_t launch_gemv_tc(int mode, const TcParams &tp, int grid, cudaStream_t stream, bool pdl) {
-    void *fn = nullptr;
-    switch (mode) {
-        case GEMV_QKV: fn = reinterpret_cast<void *>(l2dec_matvec_tc_kernel<GEMV_QKV>); break;
-        case GEMV_RESID: fn = reinterpret_cast<void *>(l2dec_matvec_tc_kernel<GEMV_RESID>); break;
-        case GEMV_W13: fn = reinterpret_cast<void *>(l2dec_matvec_tc_kernel<GEMV_W13>); break;
-        case GEMV_CLS: fn = reinterpret_cast<void *>(l2dec_matvec_tc_kernel<GEMV_CLS>); break;
-        default: return cudaErrorInvalidValue;
+    void *fn = tc_fn(mode, tp.wt);
+    if (!fn) return cudaErrorInvalidValue;
+    cudaLaunchAttribute attr[2];
+    cudaLaunchConfig_t cfg = pdl_config(dim3(grid), dim3(kTT), gemv_tc_smem(tp.bpad, tp.wt), stream, pdl, attr);
+    if (tp.csplit > 1) {
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = (unsigned)tp.csplit;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.numAttrs = 2;
     }
-    cudaLaunchAttribute attr[1];
-    cudaLaunchConfig_t cfg = pdl_config(dim3(grid), dim3(kTT), gemv_tc_smem(tp.bpad), stream, pdl, attr);
     void *args[] = {const_cast<TcParams *>(&tp)};
     return cudaLaunchKernelExC(&cfg, fn, args);
 }

@@ -376,9 +376,10 @@ AttnParams attn_params(const l2_ctx *c, int layer, int batch) {
     int nc = attn_chunks_for(c, batch);
     a.capacity = 0;
     if (batch > 1) {
-        // Rows sit at different positions: the chunk size is set on the device from the
-        // step's total (capacity-balanced), so a row never uses more than about
-        // capacity / n_kv_heads + 1 chunks; the grid stops there.
+        // Rows sit at different positions: each row's CTAs per KV head are planned on
+        // the host (attn_chunk_plan) so that the step's CTAs fit `capacity` at once;
+        // a row never gets more than capacity / n_kv_heads of them, and the grid
+        // stops one above that.
         a.capacity = c->attn_per_sm * c->num_sms;
         nc = std::min(ceil_div(p.seq_len, kMinChunk), ceil_div(a.capacity, p.n_kv_heads) + 1);
     }
@@ -387,6 +388,63 @@ AttnParams attn_params(const l2_ctx *c, int layer, int batch) {
     a.min_chunk = kMinChunk;
     a.scale = (float)(1.0 / std::sqrt((double)c->head_size));
     return a;
+}
+
+// Attention CTAs per KV head for each row of a step of several rows, written
+// into the step block with the order the grid takes the rows in.  Row b
+// (P_b = pos[b] + 1 positions) gets n_b = ceil(P_b / X) CTAs, at least one and
+// at most the grid's chunk dimension or one per kMinChunk positions.  X is
+// chosen from a simple model of the launch: it lasts about
+// max(X, all positions / capacity) -- the longest CTA, or the resident CTAs
+// working through everything -- plus a fixed cost per CTA (kAttnCtaCost
+// positions' worth: its ring fill and share of the merge) times the CTAs per
+// resident slot.  Rows are taken longest CTA first, so the long CTAs start in
+// the first wave and shorter ones fill in behind them.  (Sizing every row
+// from the step's mean instead overflowed the capacity into an unbalanced
+// second wave of CTAs with staggered positions.)
+#ifndef L2_ATTN_CTA_COST
+#define L2_ATTN_CTA_COST 96
+#endif
+constexpr int kAttnCtaCost = L2_ATTN_CTA_COST;
+
+void attn_chunk_plan(const l2_ctx *c, int B, const int *pos, unsigned short *out, unsigned char *order) {
+    const AttnParams a = attn_params(c, 0, B);
+    const long long slots = std::max(1, a.capacity / c->cfg.n_kv_heads);  // resident CTAs per KV head
+    int cap[kMaxBatch];
+    long long work = 0;
+    int pmax = 1;
+    for (int b = 0; b < B; ++b) {
+        cap[b] = std::max(1, std::min(a.n_chunks, ceil_div(pos[b] + 1, kMinChunk)));
+        work += pos[b] + 1;
+        pmax = std::max(pmax, pos[b] + 1);
+    }
+    auto count = [&](int X, int b) { return std::max(1, std::min(cap[b], ceil_div(pos[b] + 1, X))); };
+    auto cost = [&](int X, int &longest) {
+        long long ctas = 0;
+        longest = 0;
+        for (int b = 0; b < B; ++b) {
+            const int n = count(X, b);
+            ctas += n;
+            longest = std::max(longest, ceil_div(pos[b] + 1, n));
+        }
+        return std::max<long long>(longest, (work + slots - 1) / slots) + kAttnCtaCost * ((ctas + slots - 1) / slots);
+    };
+    int bestX = pmax, longest = 0;
+    long long best = cost(pmax, longest);
+    for (int X = kMinChunk; X < pmax; X += std::max(kMinChunk / 4, X / 8)) {
+        const long long v = cost(X, longest);
+        if (v < best) {
+            best = v;
+            bestX = X;
+        }
+    }
+    int len[kMaxBatch];
+    for (int b = 0; b < B; ++b) {
+        out[b] = (unsigned short)count(bestX, b);
+        len[b] = ceil_div(pos[b] + 1, out[b]);
+        order[b] = (unsigned char)b;
+    }
+    std::stable_sort(order, order + B, [&](unsigned char x, unsigned char y) { return len[x] > len[y]; });
 }
 
 // ---- batched GEMV plans: grid, tensor maps and tiles per batch size ----
@@ -436,6 +494,29 @@ bool encode_matrix_sw128(CUtensorMap *m, const void *base, uint64_t cols, uint64
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Rows of ss_part a residual plan (Wo: 1, W2: 3) writes: one per tile, or per
+// tile and cluster rank with the cluster split.
+int tc_ss_parts(const BatchSet &set, int k) {
+    const TcParams &tp = set.tcp[k];
+    return tp.ntiles * (tp.csplit > 1 ? tp.csplit : 1);
+}
+
+// A weight matrix [rows][cols] for the tensor-core GEMV: fp32 in boxes of
+// box_rows x 32 columns, or (the handle's bf16 copies) bf16 in boxes of
+// box_rows x 64 columns -- 128-byte lines with the 128-byte swizzle either way.
+bool encode_weights_sw128(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows, uint32_t box_rows, int wt) {
+    if (!wt) return encode_matrix_sw128(m, base, cols, rows, box_rows);
+    EncodeTiledFn fn = encode_tiled();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols * 2};
+    const cuuint32_t box[2] = {64, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // The tensor-core plans of a batch size (16..64 rows): tiles of 128 output
 // rows (64 of W1 over 64 of W3), the work split evenly over the SMs.
 int build_tc_set(l2_ctx *c, int batch) {
@@ -443,13 +524,17 @@ int build_tc_set(l2_ctx *c, int batch) {
     BatchSet &set = c->bsets[batch];
     const uint64_t L = p.n_layers, D = p.dim, H = p.hidden_dim, KVD = c->kv_dim, V = p.vocab_size;
     const int bpad = (batch + 15) / 16 * 16;
+    const int wt = c->wt;
+    // the weights a plan streams: the caller's fp32 matrices, or the handle's bf16 copies
+    auto W = [&](const float *f32, const unsigned short *b16) { return wt ? (const void *)b16 : (const void *)f32; };
     set.tc_ws_floats = 0;
     set.tc_tiles = 0;
     for (int k = 0; k < 5; ++k) {
         TcParams &tp = set.tcp[k];
         memset(&tp, 0, sizeof(tp));
         tp.bpad = bpad;
-        tp.stages = gemv_tc_stages(bpad);
+        tp.wt = c->wt;
+        tp.stages = gemv_tc_stages(bpad, c->wt);
         bool ok = true;
         int n = 0;
         switch (k) {
@@ -457,49 +542,52 @@ int build_tc_set(l2_ctx *c, int batch) {
                 tp.mrows[0] = p.dim;
                 tp.mrows[1] = tp.mrows[2] = c->kv_dim;
                 for (int m = 0; m < 3; ++m) tp.tiles[m] = ceil_div(tp.mrows[m], 128);
-                ok = encode_matrix_sw128(&tp.wmap[0], c->w.wq, D, L * D, 128) &&
-                     encode_matrix_sw128(&tp.wmap[1], c->w.wk, D, L * KVD, 128) &&
-                     encode_matrix_sw128(&tp.wmap[2], c->w.wv, D, L * KVD, 128) &&
+                ok = encode_weights_sw128(&tp.wmap[0], W(c->w.wq, c->b16q), D, L * D, 128, wt) &&
+                     encode_weights_sw128(&tp.wmap[1], W(c->w.wk, c->b16k), D, L * KVD, 128, wt) &&
+                     encode_weights_sw128(&tp.wmap[2], W(c->w.wv, c->b16v), D, L * KVD, 128, wt) &&
                      encode_matrix_sw128(&tp.xmap, c->xg, D, c->max_rows, bpad);
                 n = p.dim;
                 break;
             case 1:
                 tp.mrows[0] = p.dim;
                 tp.tiles[0] = ceil_div(p.dim, 128);
-                ok = encode_matrix_sw128(&tp.wmap[0], c->w.wo, D, L * D, 128) &&
+                ok = encode_weights_sw128(&tp.wmap[0], W(c->w.wo, c->b16o), D, L * D, 128, wt) &&
                      encode_matrix_sw128(&tp.xmap, c->xb, D, c->max_rows, bpad);
                 n = p.dim;
                 break;
             case 2:
                 tp.mrows[0] = p.hidden_dim;
                 tp.tiles[0] = ceil_div(p.hidden_dim, 64);
-                ok = encode_matrix_sw128(&tp.wmap[0], c->w.w1, D, L * H, 64) &&
-                     encode_matrix_sw128(&tp.wmap[1], c->w.w3, D, L * H, 64) &&
+                ok = encode_weights_sw128(&tp.wmap[0], W(c->w.w1, c->b16w1), D, L * H, 64, wt) &&
+                     encode_weights_sw128(&tp.wmap[1], W(c->w.w3, c->b16w3), D, L * H, 64, wt) &&
                      encode_matrix_sw128(&tp.xmap, c->xg, D, c->max_rows, bpad);
                 n = p.dim;
                 break;
             case 3:
                 tp.mrows[0] = p.dim;
                 tp.tiles[0] = ceil_div(p.dim, 128);
-                ok = encode_matrix_sw128(&tp.wmap[0], c->w.w2, H, L * D, 128) &&
+                ok = encode_weights_sw128(&tp.wmap[0], W(c->w.w2, c->b16w2), H, L * D, 128, wt) &&
                      encode_matrix_sw128(&tp.xmap, c->hb, H, c->max_rows, bpad);
                 n = p.hidden_dim;
                 break;
             case 4:
                 tp.mrows[0] = p.vocab_size;
                 tp.tiles[0] = ceil_div(p.vocab_size, 128);
-                ok = encode_matrix_sw128(&tp.wmap[0], c->w.wcls, D, V, 128) &&
+                ok = encode_weights_sw128(&tp.wmap[0], W(c->w.wcls, c->b16cls), D, V, 128, wt) &&
                      encode_matrix_sw128(&tp.xmap, c->xg, D, c->max_rows, bpad);
                 n = p.dim;
                 break;
         }
         if (!ok) return fail(c, L2_ECUDA, "cuTensorMapEncodeTiled failed for a tensor-core GEMV plan");
         tp.ntiles = tp.tiles[0] + tp.tiles[1] + tp.tiles[2];
-        set.tc_grid[k] = gemv_tc_grid(tp.ntiles, n, c->num_sms);
+        static const int modes[5] = {GEMV_QKV, GEMV_RESID, GEMV_W13, GEMV_RESID, GEMV_CLS};
+        tp.csplit = gemv_tc_cluster_split(modes[k], c->wt, tp.ntiles, n, bpad, c->num_sms);
+        set.tc_grid[k] = tp.csplit > 1 ? tp.ntiles * tp.csplit : gemv_tc_grid(tp.ntiles, n, c->num_sms);
         set.tc_ws_floats = std::max(set.tc_ws_floats, gemv_tc_ws_floats(set.tc_grid[k], bpad));
         set.tc_tiles = std::max(set.tc_tiles, tp.ntiles);
     }
-    if (set.tcp[1].ntiles > kMaxParts) return fail(c, L2_EINVAL, "too many residual tiles for the sum-of-squares parts");
+    if (tc_ss_parts(set, 1) > kMaxParts || tc_ss_parts(set, 3) > kMaxParts)
+        return fail(c, L2_EINVAL, "too many residual tiles for the sum-of-squares parts");
     set.tc = true;
     return L2_OK;
 }
@@ -594,7 +682,8 @@ cudaError_t launch_batched(l2_ctx *c, int k, const GemvPlan &pl, int layer, int 
         tp.g = layer_params(c, pl, layer);
         tp.g.batch = batch;
         tp.g.ss_part = c->ss_part;
-        tp.g.ss_parts = (k == 0 && layer == 0) ? 1 : set.tcp[1].ntiles;  // the embedding, else the residual tiles
+        // the sums of squares come from the embedding kernel (layer 0), Wo (for W1/W3) or W2
+        tp.g.ss_parts = (k == 0 && layer == 0) ? 1 : tc_ss_parts(set, k == 2 ? 1 : 3);
         tp.ws = c->tc_ws;
         tp.tickets = c->tc_tickets;
         tp.xg = c->xg;
@@ -695,7 +784,10 @@ int plan_persistent(l2_ctx *c) {
     k.seq_len = p.seq_len;
     k.n_chunks = nc;
     k.min_chunk = kMinChunk;
-    k.lp = c->attn.lp;
+    // one 16-byte word of a cache row per lane (the decode attention kernel may
+    // give a lane several; this kernel's attention phase does not)
+    k.lp = 1;
+    while (k.lp < c->head_size / 4) k.lp <<= 1;
     k.xs_floats = xs;
     k.ys_floats = ys;
     k.evict_first = c->evict_first ? 1 : 0;
@@ -859,15 +951,13 @@ int submit(l2_ctx *c, int B, const int *tokens, const int *pos, float *logits_ou
     c->ring_next = (i + 1) % kRing;
     if (c->ring_used[i]) L2_CUDA(c, cudaEventSynchronize(c->ring_ev[i]));
     StepDev &sh = c->step_host[i];
-    int total = 0;
     for (int b = 0; b < B; ++b) {
         sh.token[b] = tokens_dev ? 0 : tokens[b];
         sh.pos[b] = pos[b];
         sh.slot[b] = prefill_slot >= 0 ? prefill_slot : b;
         sh.stable[b] = prefill_slot >= 0 ? pos[0] : pos[b];
-        total += pos[b] + 1;
     }
-    sh.attn_total = total;
+    if (B > 1) attn_chunk_plan(c, B, pos, sh.nchunk, sh.row_order);
     sh.logits_out = logits_out;
     sh.B = B;
     sh.sync_count = 0;
@@ -945,7 +1035,10 @@ int l2_create(const L2Config *config, const L2Weights *weights, int max_batch, u
                   L2_FLAG_BF16_WEIGHTS))
         return fail(nullptr, L2_EINVAL, "unknown flags 0x%x", flags);
     if (flags & L2_FLAG_BF16_WEIGHTS) {
-        if (max_batch != 1) return fail(nullptr, L2_EINVAL, "L2_FLAG_BF16_WEIGHTS serves one sequence (max_batch 1)");
+        if ((flags & L2_FLAG_NO_TC) && max_batch != 1)
+            return fail(nullptr, L2_EINVAL,
+                        "L2_FLAG_BF16_WEIGHTS streams steps of several rows through the tensor cores: with "
+                        "L2_FLAG_NO_TC it serves one sequence (max_batch 1)");
         if (flags & L2_FLAG_PERSIST) return fail(nullptr, L2_EINVAL, "L2_FLAG_BF16_WEIGHTS excludes L2_FLAG_PERSIST");
         if (config->dim % 8 || config->hidden_dim % 8)
             return fail(nullptr, L2_EINVAL, "L2_FLAG_BF16_WEIGHTS needs dim and hidden_dim divisible by 8");
@@ -963,7 +1056,8 @@ int l2_create(const L2Config *config, const L2Weights *weights, int max_batch, u
     // buffers are small); with L2_FLAG_DEBUG the per-row probability export
     // keeps them at max_batch.
     c->max_rows = (flags & L2_FLAG_DEBUG) ? max_batch : kMaxBatch;
-    if (flags & L2_FLAG_BF16_WEIGHTS) c->max_rows = 1;  // batch-1 steps only; a prompt goes one token per step
+    // bf16 weights without the tensor cores: batch-1 steps only, a prompt one token per step
+    if ((flags & L2_FLAG_BF16_WEIGHTS) && (flags & L2_FLAG_NO_TC)) c->max_rows = 1;
     c->flags = flags;
     const L2Config &p = c->cfg;
     c->head_size = p.dim / p.n_heads;
@@ -1081,20 +1175,24 @@ int l2_create(const L2Config *config, const L2Weights *weights, int max_batch, u
                              pl->smem));
     if (c->attn.smem > 227 * 1024) return bail(fail(c, L2_EINVAL, "attention needs too much shared memory"));
     c->bsets.resize(c->max_rows + 1);
-    for (int b = 2; b <= c->max_rows; ++b)
+    // CUDA-core plans for steps of several rows (fp32 weights only: a bf16 handle's
+    // steps of several rows all run on the tensor cores)
+    for (int b = 2; b <= c->max_rows && !c->wt; ++b)
         if ((rc = build_batch_set(c, b))) {
             if (b <= max_batch) return bail(rc);
             c->max_rows = b - 1;  // prompt chunks stop at the widest step that could be planned
             c->error.clear();
             break;
         }
-    // tensor-core plans for 16..64 rows, with one workspace and ticket array for all
-    if (!(flags & L2_FLAG_NO_TC) && c->max_rows >= L2_TC_MIN_BATCH) {
+    // tensor-core plans for 16..64 rows (2..64 with bf16 weights), with one workspace and
+    // ticket array for all
+    const int tc_min = c->wt ? 2 : L2_TC_MIN_BATCH;
+    if (!(flags & L2_FLAG_NO_TC) && c->max_rows >= tc_min) {
         CREATE_CUDA(gemv_tc_init());
         if ((rc = alloc_n(c, &c->xg, (size_t)c->max_rows * p.dim, "x * gain"))) return bail(rc);
         size_t ws = 0;
         int tiles = 0;
-        for (int b = L2_TC_MIN_BATCH; b <= c->max_rows && b <= gemv_tc_max_batch(); ++b) {
+        for (int b = tc_min; b <= c->max_rows && b <= gemv_tc_max_batch(); ++b) {
             if ((rc = build_tc_set(c, b))) return bail(rc);
             ws = std::max(ws, c->bsets[b].tc_ws_floats);
             tiles = std::max(tiles, c->bsets[b].tc_tiles);
@@ -1276,7 +1374,10 @@ int l2_launch_op(l2_ctx *c, int op, int layer, int count) {
     // Standalone launches write the classifier's output only to the handle's buffer.
     L2_CUDA(c, cudaMemsetAsync(reinterpret_cast<char *>(c->step_dev) + offsetof(StepDev, logits_out), 0,
                                sizeof(float *), c->stream));
-    for (int i = 0; i < count; ++i) L2_CUDA(c, launch_op(c, op, layer, 1, c->stream, false));
+    // as in the step: consecutive launches linked by programmatic dependent launch
+    // unless the handle was created with L2_FLAG_NO_PDL
+    const bool pdl = !(c->flags & L2_FLAG_NO_PDL);
+    for (int i = 0; i < count; ++i) L2_CUDA(c, launch_op(c, op, layer, 1, c->stream, pdl));
     return L2_OK;
 }
 
@@ -1384,7 +1485,6 @@ extern "C" int l2_forward_static(l2_ctx *c, int token, int pos, float *logits_ou
     sh.pos[0] = pos;
     sh.slot[0] = 0;
     sh.stable[0] = pos;
-    sh.attn_total = pos + 1;
     sh.logits_out = logits_out;
     sh.B = 1;
     L2_CUDA(c, cudaMemcpyAsync(c->step_dev, &sh, sizeof(StepDev), cudaMemcpyHostToDevice, c->stream));

@@ -51,9 +51,12 @@ cudaError_t launch_sample(const SampleParams &p, int batch, cudaStream_t stream)
 
 // Tensor-core batched GEMV (gemv_tc.cu), 16..64 sequences.
 int gemv_tc_max_batch();
-int gemv_tc_stages(int bpad);
-size_t gemv_tc_smem(int bpad);
+int gemv_tc_stages(int bpad, int wt);
+size_t gemv_tc_smem(int bpad, int wt);
 int gemv_tc_grid(int ntiles, int n, int ctas);
+// Cluster size for the cluster split of a plan (0: stream-K), see gemv_tc.cu.
+// wt: 0 fp32 weights, 1 bf16 weights.
+int gemv_tc_cluster_split(int mode, int wt, int ntiles, int n, int bpad, int num_sms);
 size_t gemv_tc_ws_floats(int grid, int bpad);
 cudaError_t gemv_tc_init();
 cudaError_t launch_tc_embed(const TcParams &tp, int batch, cudaStream_t stream, bool pdl);
@@ -61,7 +64,8 @@ cudaError_t launch_gemv_tc(int mode, const TcParams &tp, int grid, cudaStream_t 
 
 // Flash-decoding attention (attention.cu).
 struct AttnLaunch {
-    int lp;       // lanes per cache row (power of two)
+    int lp;       // lanes per cache row (power of two; a lane takes 4 / 2 / 1 of its 16-byte words
+                  // with 1 / 2 / more query heads per KV head)
     int gq;       // query heads per KV head, rounded up to a power of two
     int rl;       // 1: row-per-lane layout (head size 64, 4 or 8 heads per KV head)
     int threads;

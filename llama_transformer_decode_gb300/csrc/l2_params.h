@@ -23,8 +23,11 @@ struct StepDev {
     float *logits_out;  // caller's device buffer [B][vocab] or nullptr
     int B;
     unsigned sync_count;  // grid-barrier arrivals of the persistent step kernel (zero at the copy)
-    int attn_total;       // sum over the step's rows of pos[b] + 1 (attention chunk sizing)
-    int pad_;
+    // Steps of several rows (attn_chunk_plan, on the host): attention CTAs per KV head
+    // for row b, and the order in which the attention grid takes the rows (most
+    // positions per CTA first, so the longest CTAs start in the first wave).
+    unsigned short nchunk[kMaxBatch];
+    unsigned char row_order[kMaxBatch];
 };
 
 // The fused GEMV kernel's modes (prologue / epilogue around y = W v).
@@ -124,7 +127,12 @@ struct alignas(128) TcParams {
     int mrows[3];         // rows of each matrix in one layer
     int ntiles;           // all tiles
     int bpad;             // sequences rounded up to a multiple of 16 (MMA N)
+    int wt;               // weights: 0 fp32 (3xTF32 products), 1 bf16 (kind::f16, inputs in three bf16 parts)
     int stages;           // ring stages for this width
+    // > 1: each tile's K range is split over a thread-block cluster of csplit CTAs
+    // (grid ntiles * csplit) whose parts are added through distributed shared
+    // memory; 0: the stream-K split with the workspace and tickets below.
+    int csplit;
     float *ws;            // partial tiles [grid][2][bpad][128]
     unsigned *tickets;    // [ntiles], zero between launches
     float *xg;            // x * gain of the next RMSNorm [max rows][dim], written by the residual kernels

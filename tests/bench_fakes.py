@@ -79,7 +79,7 @@ class FakeDecoder:
         return 5 * self.n_layers + 1 + (1 if batch >= bench.TC_MIN_BATCH else 0)
 
     def step_input_bytes(self):
-        return 1048
+        return 1232  # sizeof the step block (tokens, positions, slots, rows written, output, count, chunk plan)
 
     def sync(self):
         pass

@@ -33,13 +33,16 @@ def attn():
     h0, h1 = (eval("lambda g, H, KV: " + _c_to_py(e)) for e in m.groups())
     m = re.search(r"const int max_group = (.+?);", src)
     max_group = eval("lambda n_heads, n_kv_heads: " + _c_to_py(m.group(1)))
-    m = re.search(r"int n_active = (.+?);\n\s*if \(n_active > p.n_chunks\) n_active = p.n_chunks;", src)
+    m = re.search(r"int n_active = p.capacity > 0 \? \(int\)p.step->nchunk\[b\] : (.+?);\n"
+                  r"\s*if \(n_active > p.n_chunks\) n_active = p.n_chunks;\n"
+                  r"\s*if \(n_active > P\) n_active = P;\n\s*if \(n_active < 1\) n_active = 1;", src)
     assert m, "chunk count not found in the decode attention kernel"
-    n_active = eval("lambda P, chunk: " + _c_to_py(m.group(1)))
+    # a step of one row: at least min_chunk positions per CTA (several rows: the host's plan)
+    n_active = eval("lambda P, chunk: " + _c_to_py(m.group(1).replace("p.min_chunk", "chunk")))
     m = re.search(r"const int t0 = (.+?), t1 = (.+?);", src)
     t0, t1 = (eval("lambda c, P, n_active: " + _c_to_py(e)) for e in m.groups())
     m = re.search(r"const int wt0 = (.+?);\n\s*const int wt1 = (.+?);", src)
-    wt0, wt1 = (eval("lambda t0, t1, warp, kNWA: " + _c_to_py(e)) for e in m.groups())
+    wt0, wt1 = (eval("lambda t0, t1, rgi, NRG: " + _c_to_py(e)) for e in m.groups())
     return dict(h0=h0, h1=h1, max_group=max_group, n_active=n_active, t0=t0, t1=t1, wt0=wt0, wt1=wt1)
 
 
@@ -76,21 +79,33 @@ def test_prompt_chunk_kernel_head_groups(oracle_lib):
 
 
 @pytest.mark.parametrize("n_chunks", [1, 2, 7, 16, 64, 152])
-def test_positions_split_over_chunks_and_warps(attn, n_chunks):
-    kNWA = 8
-    for chunk in (1, 3, 32, 64, 100):
-        for P in list(range(1, 300)) + [1024, 2047, 2048, 4095, 4096]:
-            n = min(attn["n_active"](P, chunk), n_chunks)
-            assert 1 <= n <= P
-            prev = 0
-            for c in range(n):
-                a, b = attn["t0"](c, P, n), attn["t1"](c, P, n)
-                assert a == prev and b > a  # every joining CTA has positions
-                wprev = a
-                for w in range(kNWA):
-                    wa, wb = attn["wt0"](a, b, w, kNWA), attn["wt1"](a, b, w, kNWA)
-                    assert wa == wprev and wb >= wa
-                    wprev = wb
-                assert wprev == b
-                prev = b
-            assert prev == P
+def test_positions_split_over_chunks_and_rings(attn, n_chunks):
+    # rings per CTA: 8 (one warp per ring) or 4 (two warps sharing a ring)
+    for NRG in (8, 4):
+        for chunk in (1, 3, 32, 64, 100, 128):
+            for P in list(range(1, 300)) + [1024, 2047, 2048, 4095, 4096]:
+                n = max(1, min(attn["n_active"](P, chunk), n_chunks, P))
+                assert 1 <= n <= P
+                prev = 0
+                for c in range(n):
+                    a, b = attn["t0"](c, P, n), attn["t1"](c, P, n)
+                    assert a == prev and b > a  # every joining CTA has positions
+                    wprev = a
+                    for r in range(NRG):
+                        wa, wb = attn["wt0"](a, b, r, NRG), attn["wt1"](a, b, r, NRG)
+                        assert wa == wprev and wb >= wa
+                        wprev = wb
+                    assert wprev == b
+                    prev = b
+                assert prev == P
+
+
+def test_any_host_planned_chunk_count_splits_every_row(attn):
+    # several rows: n_active comes from the host's plan (clamped to 1..min(n_chunks, P));
+    # every count in that range must split the row's positions into non-empty chunks
+    for P in list(range(1, 200)) + [1023, 2048]:
+        for n in range(1, min(P, 40) + 1):
+            ends = [attn["t1"](c, P, n) for c in range(n)]
+            starts = [attn["t0"](c, P, n) for c in range(n)]
+            assert starts[0] == 0 and ends[-1] == P
+            assert all(b > a for a, b in zip(starts, ends)) and starts[1:] == ends[:-1]

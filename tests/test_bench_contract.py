@@ -50,7 +50,7 @@ def test_decode_batch_one_line():
     assert line["roofline"]["bound"] == "hbm" and line["roofline"]["unit"] == "GB/s"
     assert "GEMV_W13" in line["roofline"]["kernel"]
     assert line["gpu_launches"] == 12 * (5 * 5 + 1)  # tiny: 5 layers
-    assert line["e2e"]["d2h_bytes_per_step"] == 4 * 512 and line["e2e"]["h2d_bytes_per_step"] == 1048
+    assert line["e2e"]["d2h_bytes_per_step"] == 4 * 512 and line["e2e"]["h2d_bytes_per_step"] == 1232
     assert set(line["per_position"]) == {"2", "129", "505"}
 
 
@@ -68,7 +68,7 @@ def test_prefill_line():
     assert line["metric"].startswith("prefill tokens/s of a 130-token prompt")
     assert line["config"]["prefill_tokens"] == 130
     assert line["gpu_launches"] == 2 * (2 * (5 * 5 + 2) + (5 * 5 + 1))  # chunks of 64, 64 and 2 rows
-    assert line["e2e"]["h2d_bytes_per_step"] == 3 * 1048
+    assert line["e2e"]["h2d_bytes_per_step"] == 3 * 1232
 
 
 def test_decode_line_per_config_block():

@@ -1,4 +1,6 @@
-"""The tensor-core GEMV's stream-K work split, checked exhaustively on the CPU.
+"""The tensor-core GEMV's work splits, checked exhaustively on the CPU.
+
+Stream-K (plans with many tiles):
 
 The kernel lays the (output tile, K stage) pairs of a launch out tile-major,
 T = tiles * KT of them, and gives CTA c the range [c*T/G, (c+1)*T/G).  A
@@ -11,6 +13,13 @@ kernel) and checked for every shape class the host plans: every pair is
 covered exactly once, cta_of inverts the ranges, the slot the merge reads is
 the one the CTA wrote, the ticket count equals the contributing CTAs, and
 the parts cover K once, in K order.
+
+Cluster split (plans with fewer tiles than half the SMs): tile t's K stages
+are split over the CS CTAs of cluster t as [KT r / CS, KT (r + 1) / CS), and
+after the distributed-shared-memory reduction rank r finishes the tile's
+rows (W1/W3: row pairs) [jlo, jhi); both are read from the source and must
+cover their ranges exactly once, in rank order, with no empty part and even
+row bounds (RoPE pairs stay in one CTA).
 """
 import os
 import re
@@ -31,9 +40,15 @@ def _c_to_py(expr: str) -> str:
 @pytest.fixture(scope="module")
 def formulas():
     src = open(SRC).read()
-    m = re.search(r"const long long s_begin = (.+?), s_end = (.+?);", src)
-    assert m, "range formulas not found in the kernel"
-    s_begin, s_end = (eval("lambda c, T, G: " + _c_to_py(g)) for g in m.groups())
+    mb = re.search(r"const long long s_begin = CS > 1 \? (.+?)\n\s*: (.+?);", src)
+    me = re.search(r"const long long s_end = CS > 1 \? (.+?)\n\s*: (.+?);", src)
+    assert mb and me, "range formulas not found in the kernel"
+    s_begin, s_end = (eval("lambda c, T, G: " + _c_to_py(m.group(2))) for m in (mb, me))
+    # the cluster split: CTA c of a grid of ntiles * CS, K stages per tile KT
+    cs_begin, cs_end = (eval("lambda c, KT, CS: " + _c_to_py(m.group(1))) for m in (mb, me))
+    m = re.search(r"const int jlo = (.+?);\n\s*const int jhi = rk \+ 1 == \(uint32_t\)CS \? kUnit : (.+?);", src)
+    assert m, "row split of the cluster reduction not found in the kernel"
+    row_lo, row_hi = (eval("lambda rk, CS, kUnit: " + _c_to_py(g).replace("~1LL", "~1")) for g in m.groups())
     m = re.search(r"auto cta_of = \[&\]\(long long x\) \{ return (.+?); \};", src)
     assert m, "cta_of not found in the kernel"
     cta_of = eval("lambda x, T, G: " + _c_to_py(m.group(1)))
@@ -48,7 +63,8 @@ def formulas():
     m = re.search(r"#define L2_TC_MIN_CTA_STAGES (\d+)", src)
     min_stages = int(m.group(1))
     assert re.search(r"std::min<long long>\(ctas, T / kMinCtaStages\)", src), "grid rule changed in the kernel"
-    return dict(s_begin=s_begin, s_end=s_end, cta_of=cta_of, k1_rest=k1_rest, wh=wh, min_stages=min_stages)
+    return dict(s_begin=s_begin, s_end=s_end, cta_of=cta_of, k1_rest=k1_rest, wh=wh, min_stages=min_stages,
+                cs_begin=cs_begin, cs_end=cs_end, row_lo=row_lo, row_hi=row_hi)
 
 
 def check_plan(f, ntiles: int, KT: int, ctas: int):
@@ -128,3 +144,43 @@ def test_checker_rejects_plausible_mistakes(formulas, name):
         for ntiles in (3, 7, 40):
             for KT in (4, 9, 32):
                 check_plan(bad, ntiles, KT, 152)
+
+
+def check_cluster_plan(f, ntiles: int, KT: int, CS: int):
+    """Cluster split: CTA c = tile * CS + rank covers stages [cs_begin, cs_end) of its
+    tile; every tile's K stages exactly once, in rank order, none empty; and the
+    ranks' output rows (rows of a tile, or W1/W3 row pairs) split [0, kUnit) into
+    non-empty even-aligned slices in rank order."""
+    for t in range(ntiles):
+        prev = t * KT
+        for rk in range(CS):
+            c = t * CS + rk
+            b, e = f["cs_begin"](c, KT, CS), f["cs_end"](c, KT, CS)
+            assert b == prev and e > b, (ntiles, KT, CS, c)
+            # the kernel's segment walk gives this CTA one segment, of tile t
+            tile, k0 = divmod(b, KT)
+            assert tile == t and min(KT, f["k1_rest"](k0, e, b)) == k0 + (e - b)
+            prev = e
+        assert prev == (t + 1) * KT
+    for unit in (128, 64):
+        prev = 0
+        for rk in range(CS):
+            lo = f["row_lo"](rk, CS, unit)
+            hi = unit if rk + 1 == CS else f["row_hi"](rk, CS, unit)
+            assert lo == prev and hi > lo and lo % 2 == 0 and hi % 2 == 0
+            prev = hi
+        assert prev == unit
+
+
+@pytest.mark.parametrize("CS", [2, 3, 4, 5, 6, 7, 8])
+def test_cluster_partition(formulas, CS):
+    for ntiles in (1, 2, 16, 20, 32, 76):
+        for KT in [k for k in SHAPES_KT if k >= CS]:  # the host keeps CS <= KT
+            check_cluster_plan(formulas, ntiles, KT, CS)
+
+
+def test_cluster_checker_rejects_a_rounding_mistake(formulas):
+    bad = dict(formulas)
+    bad["cs_end"] = lambda c, KT, CS: (c // CS) * KT + -(-KT * (c % CS + 1) // CS) + 1
+    with pytest.raises(AssertionError):
+        check_cluster_plan(bad, 3, 32, 6)
