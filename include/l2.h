@@ -336,6 +336,23 @@ void l2_debug_fail_graph_at(int n);
  */
 int l2_debug_wait_timeout(l2_ctx *ctx, int limit_us);
 
+/*
+ * The bounds-checked build of this library (compiled with L2_DEBUG_BOUNDS=1;
+ * the Python binding loads it when L2DECODE_BOUNDS_CHECKED=1): every index the
+ * kernels compute into the handle's buffers, and every bulk copy's source
+ * range, is checked against the buffer's size; a violation sets the device
+ * error word (l2_sync then returns L2_EDEVICE) and the access is skipped, so
+ * nothing is read or written out of range.  The persistent step kernel
+ * (L2_FLAG_PERSIST) is not instrumented.  l2_debug_bounds_checked returns 1
+ * in that build and 0 in the release build.  l2_debug_limit_cache lowers the
+ * size the checks assume for each KV cache to `floats` (never above the
+ * real size; blocks): steps that then read or write cache rows past it are
+ * flagged, which lets a test see the checks fire without any access out of
+ * range.  It has no effect in the release build.  L2_EINVAL on a NULL handle.
+ */
+int l2_debug_bounds_checked(void);
+int l2_debug_limit_cache(l2_ctx *ctx, unsigned long long floats);
+
 #ifdef __cplusplus
 }
 #endif

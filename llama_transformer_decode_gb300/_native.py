@@ -12,6 +12,9 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libl2decode.so")
+# the bounds-checked build (every kernel index checked; see l2_debug_bounds_checked)
+BUILD_CHECKED = os.path.join(BUILD, "checked")
+LIB_CHECKED = os.path.join(BUILD, "libl2decode_checked.so")
 SOURCES = ("gemv.cu", "gemv_batched.cu", "gemv_tc.cu", "attention.cu", "attn_prefill.cu", "step_kernel.cu", "sample.cu",
            "l2_api.cu")
 HEADERS = ("l2_device.cuh", "l2_params.h", "l2_kernels.h")
@@ -26,24 +29,29 @@ def _nvcc() -> str:
     return "nvcc"
 
 
-def _stale() -> bool:
-    if not os.path.exists(LIB):
+def _stale(lib: str | None = None) -> bool:
+    lib = lib or LIB
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     deps = [os.path.join(CSRC, f) for f in SOURCES + HEADERS] + [os.path.join(ROOT, "include", "l2.h")]
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile every CUDA source for sm_103a (in parallel) and link the shared library."""
-    if not force and not _stale():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, checked: bool = False) -> str:
+    """Compile every CUDA source for sm_103a (in parallel) and link the shared
+    library; checked=True builds the bounds-checked variant instead."""
+    lib = LIB_CHECKED if checked else LIB
+    if not force and not _stale(lib):
+        return lib
+    objdir = BUILD_CHECKED if checked else BUILD
+    os.makedirs(objdir, exist_ok=True)
     nvcc = _nvcc()
+    extra = ["-DL2_DEBUG_BOUNDS=1"] if checked else []
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(BUILD, src + ".o")
-        cmd = [nvcc, *NVCC_FLAGS, "-c", os.path.join(CSRC, src), "-o", obj]
+        obj = os.path.join(objdir, src + ".o")
+        cmd = [nvcc, *NVCC_FLAGS, *extra, "-c", os.path.join(CSRC, src), "-o", obj]
         if verbose:
             cmd.insert(1, "-Xptxas=-v")
         r = subprocess.run(cmd, capture_output=True, text=True)
@@ -55,14 +63,14 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
     with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [nvcc, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs,
            "-Xlinker", "-rpath=/usr/local/cuda/lib64"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 class L2Config(ctypes.Structure):
@@ -82,7 +90,8 @@ EXPORTS = ("l2_create", "l2_reset", "l2_forward", "l2_forward_batch", "l2_forwar
            "l2_position", "l2_debug_attention", "l2_kv_export", "l2_kv_import", "l2_sync",
            "l2_last_error", "l2_destroy", "l2_launch_op", "l2_kernels_per_step",
            "l2_step_input_bytes", "l2_forward_static", "l2_debug_fail_alloc_at", "l2_sample",
-           "l2_forward_dev_tokens", "l2_prefill", "l2_debug_fail_graph_at", "l2_debug_wait_timeout")
+           "l2_forward_dev_tokens", "l2_prefill", "l2_debug_fail_graph_at", "l2_debug_wait_timeout",
+           "l2_debug_bounds_checked", "l2_debug_limit_cache")
 
 _lib = None
 
@@ -124,6 +133,10 @@ def declare(lib):
     lib.l2_debug_fail_graph_at.restype = None
     lib.l2_debug_wait_timeout.argtypes = [vp, i]
     lib.l2_debug_wait_timeout.restype = i
+    lib.l2_debug_bounds_checked.argtypes = []
+    lib.l2_debug_bounds_checked.restype = i
+    lib.l2_debug_limit_cache.argtypes = [vp, ctypes.c_ulonglong]
+    lib.l2_debug_limit_cache.restype = i
     for name in ("l2_create", "l2_reset", "l2_forward", "l2_forward_batch", "l2_forward_host",
                  "l2_position", "l2_debug_attention", "l2_kv_export", "l2_kv_import", "l2_sync",
                  "l2_launch_op", "l2_kernels_per_step", "l2_forward_static"):
@@ -132,12 +145,15 @@ def declare(lib):
 
 
 def load(build_if_missing: bool = True):
-    """The loaded CUDA library.  Raises if it is not built (and cannot be)."""
+    """The loaded CUDA library (the bounds-checked build when the environment
+    sets L2DECODE_BOUNDS_CHECKED=1).  Raises if it is not built (and cannot be)."""
     global _lib
     if _lib is None:
-        if build_if_missing and _stale():
-            build()
-        if not os.path.exists(LIB):
-            raise RuntimeError(f"CUDA library {LIB} is missing; run build()")
-        _lib = declare(ctypes.CDLL(LIB))
+        checked = os.environ.get("L2DECODE_BOUNDS_CHECKED") == "1"
+        lib = LIB_CHECKED if checked else LIB
+        if build_if_missing and _stale(lib):
+            build(checked=checked)
+        if not os.path.exists(lib):
+            raise RuntimeError(f"CUDA library {lib} is missing; run build()")
+        _lib = declare(ctypes.CDLL(lib))
     return _lib

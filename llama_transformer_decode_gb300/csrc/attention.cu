@@ -48,6 +48,9 @@ namespace {
 constexpr int kNWA = L2_ATTN_WARPS;
 constexpr int kAttStages = L2_ATTN_STAGES;
 constexpr int kStageFloats = L2_ATTN_STAGE_FLOATS;
+// Row-per-lane layout: two to four warps share a ring, so a CTA has fewer rings;
+// deeper rings keep as many bytes in flight per SM.
+constexpr int kAttStagesRL = 4;
 
 // The WPR * 32 threads of one ring: named barrier 1 + ring (ids taken from
 // constants, so the kernel reserves only the barriers it uses).  ring_sync_or
@@ -112,18 +115,19 @@ template <int LP, int GQ, int RL>
 __global__ void __launch_bounds__(kNWA * 32) attn_kernel(const AttnParams p) {
     constexpr int NT = kNWA * 32;
     constexpr int RPI = 32 / LP;        // cache rows a warp handles at once
-    constexpr int WPR = RL ? 2 : 1;     // warps sharing one ring
+    constexpr int WPR = RL ? GQ / 2 : 1;  // warps sharing one ring (row-per-lane: two heads per warp)
     constexpr int NRG = kNWA / WPR;     // rings per CTA (one softmax state per ring and head)
+    constexpr int STG = RL ? kAttStagesRL : kAttStages;  // ring buffers per ring
     static_assert(!RL || NRG <= 4, "ring barriers are ids 1..4");
     extern __shared__ __align__(128) unsigned char smem[];
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem);                      // [NRG][kAttStages]
-    int *flags = reinterpret_cast<int *>(smem + 8 * NRG * kAttStages);        // [4]
-    float *mrg = reinterpret_cast<float *>(smem + 8 * NRG * kAttStages + 16); // [NRG][GQ][2]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem);                      // [NRG][STG]
+    int *flags = reinterpret_cast<int *>(smem + 8 * NRG * STG);        // [4]
+    float *mrg = reinterpret_cast<float *>(smem + 8 * NRG * STG + 16); // [NRG][GQ][2]
     float *fin = mrg + NRG * GQ * 2;                                          // [GQ][2]
-    const size_t hdr = (8 * NRG * kAttStages + 16 + 4 * (NRG * GQ * 2 + GQ * 2) + 127) / 128 * 128;
+    const size_t hdr = (8 * NRG * STG + 16 + 4 * (NRG * GQ * 2 + GQ * 2) + 127) / 128 * 128;
     const int hs = p.head_size, hs4 = hs >> 2;
-    float4 *ring = reinterpret_cast<float4 *>(smem + hdr);                     // [NRG][kAttStages][stage]
-    float4 *accs = ring + NRG * kAttStages * (kStageFloats / 4);              // [NRG][GQ][hs4]
+    float4 *ring = reinterpret_cast<float4 *>(smem + hdr);                     // [NRG][STG][stage]
+    float4 *accs = ring + NRG * STG * (kStageFloats / 4);              // [NRG][GQ][hs4]
     float *qs = reinterpret_cast<float *>(accs + NRG * GQ * hs4);               // RL: [GQ][hs]
     float *pbuf = qs + GQ * hs;                                                 // RL: [kNWA][16 + 1][GQ / WPR]
 
@@ -156,15 +160,15 @@ __global__ void __launch_bounds__(kNWA * 32) attn_kernel(const AttnParams p) {
     const float *vbase = p.vcache + head_base;
 
     if (tid == 0) {
-        for (int i = 0; i < NRG * kAttStages; ++i) mbar_init(&bars[i], 1);
+        for (int i = 0; i < NRG * STG; ++i) mbar_init(&bars[i], 1);
         fence_barrier_init();
         flags[0] = 0;  // a warp gave up waiting
         flags[1] = 0;  // this CTA merges the chunks
     }
     __syncthreads();
 
-    uint64_t *wbars = bars + rgi * kAttStages;
-    float4 *wring = ring + (size_t)rgi * kAttStages * (kStageFloats / 4);
+    uint64_t *wbars = bars + rgi * STG;
+    float4 *wring = ring + (size_t)rgi * STG * (kStageFloats / 4);
     const bool producer = wsub == 0 && lane == 0;  // issues the ring's copies; every warp tracks them
     int ti = wt0;  // next position to request
     int n_issued = 0;
@@ -173,9 +177,13 @@ __global__ void __launch_bounds__(kNWA * 32) attn_kernel(const AttnParams p) {
         if (producer) {
             const uint32_t bytes = (uint32_t)np * hs * 4u;
             float4 *dst = wring + (size_t)stage * (kStageFloats / 4);
-            mbar_arrive_expect_tx(&wbars[stage], 2u * bytes);
-            bulk_g2s_nohint(dst, kbase + (size_t)ti * hs, bytes, &wbars[stage]);
-            bulk_g2s_nohint(dst + (size_t)TP * hs4, vbase + (size_t)ti * hs, bytes, &wbars[stage]);
+            // rows outside the cache (bounds-checked build) are skipped; the barrier expects nothing
+            const bool ok = in_bounds(head_base + (size_t)ti * hs, (size_t)np * hs, p.ext->cache, p.err);
+            mbar_arrive_expect_tx(&wbars[stage], ok ? 2u * bytes : 0u);
+            if (ok) {
+                bulk_g2s_nohint(dst, kbase + (size_t)ti * hs, bytes, &wbars[stage]);
+                bulk_g2s_nohint(dst + (size_t)TP * hs4, vbase + (size_t)ti * hs, bytes, &wbars[stage]);
+            }
         }
         ti += np;
         ++n_issued;
@@ -185,31 +193,42 @@ __global__ void __launch_bounds__(kNWA * 32) attn_kernel(const AttnParams p) {
     // before the previous kernel (which writes the newer rows) has finished.
     const int stable = p.step->stable[b];
 #pragma unroll 1
-    for (int s = 0; s < kAttStages && ti < wt1 && ti + min(TP, wt1 - ti) <= stable; ++s) issue(s);
+    for (int s = 0; s < STG && ti < wt1 && ti + min(TP, wt1 - ti) <= stable; ++s) issue(s);
     pdl_launch_dependents();
     pdl_wait();
 #pragma unroll 1
-    for (int s = n_issued; s < kAttStages && ti < wt1; ++s) issue(s);
+    for (int s = n_issued; s < STG && ti < wt1; ++s) issue(s);
 
     bool ok = true;
     int k = 0;
     float *dbg = p.dbg ? p.dbg + (((size_t)b * p.n_layers + p.layer) * H + h0) * p.seq_len : nullptr;
+    // the export's rows of this CTA's heads lie inside it (bounds-checked build), or it is not written
+    if (dbg && !in_bounds((((size_t)b * p.n_layers + p.layer) * H + h0) * p.seq_len, (size_t)nq * p.seq_len,
+                          p.ext->dbg, p.err))
+        dbg = nullptr;
     if constexpr (RL == 1) {
         constexpr int TPR = 16;            // cache rows per ring stage (head size 64)
         constexpr int HS4 = 16;
-        constexpr int HPW = GQ / WPR;      // heads per warp
-        constexpr int HPL = HPW / 2;       // heads per lane (one half-warp each)
+        constexpr int HPW = GQ / WPR;      // heads per warp: 2
+        constexpr int HPL = HPW / 2;       // heads per lane: 1 (one half-warp each)
         constexpr int RTH = WPR * 32;      // threads of one ring
+        static_assert(HPL == 1, "row-per-lane attention: one head per half-warp");
         // the group's query vectors, shared by all warps
         for (int i = tid; i < GQ * 64; i += NT) {
             const int j = i / 64, d = i % 64;
-            qs[i] = j < nq ? p.q[(size_t)b * p.dim + (size_t)(h0 + j) * 64 + d] : 0.f;
+            const size_t qi = (size_t)b * p.dim + (size_t)(h0 + j) * 64 + d;
+            qs[i] = j < nq && in_bounds(qi, 1, p.ext->q, p.err) ? p.q[qi] : 0.f;
         }
         __syncthreads();
         const float4 *qs4 = reinterpret_cast<const float4 *>(qs);
         float *wp = pbuf + warp * (TPR + 1) * HPW;  // [TPR][HPW] probabilities, then [HPW] rescales
         const int t = lane & (TPR - 1), jh = lane / TPR;
         const int jw0 = wsub * HPW;                 // the warp's first head of the group
+        // this lane's head's query vector in registers, its 16-byte chunks in the lane's
+        // rotated order (chunk i of the loop below is chunk (i + t) % 16 of the head)
+        float4 qr[HS4];
+#pragma unroll
+        for (int i = 0; i < HS4; ++i) qr[i] = qs4[(jw0 + jh) * HS4 + ((i + t) & (HS4 - 1))];
         float m[HPL], l[HPL];
         float acc[HPW][2];
 #pragma unroll
@@ -222,9 +241,9 @@ __global__ void __launch_bounds__(kNWA * 32) attn_kernel(const AttnParams p) {
         int tc = wt0;
 #pragma unroll 1
         for (; tc < wt1; ++k) {
-            const int s = k % kAttStages;
+            const int s = k % STG;
             const int np = min(TP, wt1 - tc);
-            const bool got = mbar_wait(&wbars[s], (uint32_t)(k / kAttStages) & 1u, p.err);
+            const bool got = mbar_wait(&wbars[s], (uint32_t)(k / STG) & 1u, p.err);
             // the ring's warps take one decision (the loop bounds are the ring's, so both get here)
             if (ring_sync_or<RTH>(!got, rgi)) {
                 ok = false;
@@ -240,12 +259,7 @@ __global__ void __launch_bounds__(kNWA * 32) attn_kernel(const AttnParams p) {
             if (row_on) {
                 const float4 *Kr = Ks + t * HS4;
 #pragma unroll
-                for (int i = 0; i < HS4; ++i) {
-                    const int ch = (i + t) & (HS4 - 1);
-                    const float4 kv = Kr[ch];
-#pragma unroll
-                    for (int jj = 0; jj < HPL; ++jj) sc[jj] = dot4(qs4[(jw0 + jh * HPL + jj) * HS4 + ch], kv, sc[jj]);
-                }
+                for (int i = 0; i < HS4; ++i) sc[0] = dot4(qr[i], Kr[(i + t) & (HS4 - 1)], sc[0]);
             }
 #pragma unroll
             for (int jj = 0; jj < HPL; ++jj) {
@@ -278,12 +292,11 @@ __global__ void __launch_bounds__(kNWA * 32) attn_kernel(const AttnParams p) {
 #pragma unroll 4
             for (int tt = 0; tt < np; ++tt) {
                 const float2 v = Vs2[tt * 32 + lane];
-#pragma unroll
-                for (int j = 0; j < HPW; ++j) {
-                    const float pj = wp[tt * HPW + j];
-                    acc[j][0] = fmaf(pj, v.x, acc[j][0]);
-                    acc[j][1] = fmaf(pj, v.y, acc[j][1]);
-                }
+                const float2 pp = *reinterpret_cast<const float2 *>(wp + tt * HPW);  // the warp's two heads
+                acc[0][0] = fmaf(pp.x, v.x, acc[0][0]);
+                acc[0][1] = fmaf(pp.x, v.y, acc[0][1]);
+                acc[1][0] = fmaf(pp.y, v.x, acc[1][0]);
+                acc[1][1] = fmaf(pp.y, v.y, acc[1][1]);
             }
             __syncwarp();
             tc += np;
@@ -295,7 +308,7 @@ __global__ void __launch_bounds__(kNWA * 32) attn_kernel(const AttnParams p) {
         }
         if (!ok) {
             for (int j = k + 1; j < n_issued; ++j)
-                (void)mbar_wait(&wbars[j % kAttStages], (uint32_t)(j / kAttStages) & 1u, p.err);
+                (void)mbar_wait(&wbars[j % STG], (uint32_t)(j / STG) & 1u, p.err);
             if (lane == 0) flags[0] = 1;
         }
         if (t == 0) {
@@ -326,7 +339,8 @@ __global__ void __launch_bounds__(kNWA * 32) attn_kernel(const AttnParams p) {
 #pragma unroll
             for (int w = 0; w < WPL; ++w) {
                 q4[j][w] = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (j < nq && c4 + w * LP < hs4)
+                if (j < nq && c4 + w * LP < hs4 &&
+                    in_bounds((size_t)b * p.dim + (size_t)(h0 + j) * hs + 4 * (c4 + w * LP), 4, p.ext->q, p.err))
                     q4[j][w] = reinterpret_cast<const float4 *>(p.q + (size_t)b * p.dim + (size_t)(h0 + j) * hs)[c4 + w * LP];
                 acc[j][w] = make_float4(0.f, 0.f, 0.f, 0.f);
             }
@@ -336,9 +350,9 @@ __global__ void __launch_bounds__(kNWA * 32) attn_kernel(const AttnParams p) {
         int tc = wt0;
 #pragma unroll 1
         for (; tc < wt1; ++k) {
-            const int s = k % kAttStages;
+            const int s = k % STG;
             const int np = min(TP, wt1 - tc);
-            if (!mbar_wait(&wbars[s], (uint32_t)(k / kAttStages) & 1u, p.err)) {
+            if (!mbar_wait(&wbars[s], (uint32_t)(k / STG) & 1u, p.err)) {
                 ok = false;
                 break;
             }
@@ -418,7 +432,7 @@ __global__ void __launch_bounds__(kNWA * 32) attn_kernel(const AttnParams p) {
         }
         if (!ok) {
             for (int j = k + 1; j < n_issued; ++j)
-                (void)mbar_wait(&wbars[j % kAttStages], (uint32_t)(j / kAttStages) & 1u, p.err);
+                (void)mbar_wait(&wbars[j % STG], (uint32_t)(j / STG) & 1u, p.err);
             if (lane == 0) flags[0] = 1;
         }
 
@@ -481,8 +495,9 @@ __global__ void __launch_bounds__(kNWA * 32) attn_kernel(const AttnParams p) {
                 merge_state(mm, ll, aa, mrg[(w * GQ + j) * 2], mrg[(w * GQ + j) * 2 + 1],
                             accs[(size_t)(w * GQ + j) * hs4 + w4]);
             const float inv = 1.0f / ll;
-            reinterpret_cast<float4 *>(p.out + (size_t)b * p.dim + (size_t)(h0 + j) * hs)[w4] =
-                make_float4(aa.x * inv, aa.y * inv, aa.z * inv, aa.w * inv);
+            if (in_bounds((size_t)b * p.dim + (size_t)(h0 + j) * hs + 4 * w4, 4, p.ext->xb, p.err))
+                reinterpret_cast<float4 *>(p.out + (size_t)b * p.dim + (size_t)(h0 + j) * hs)[w4] =
+                    make_float4(aa.x * inv, aa.y * inv, aa.z * inv, aa.w * inv);
             if (w4 == 0) {
                 fin[j * 2] = mm;
                 fin[j * 2 + 1] = ll;
@@ -505,6 +520,7 @@ __global__ void __launch_bounds__(kNWA * 32) attn_kernel(const AttnParams p) {
         for (int w = 0; w < NRG; ++w)
             merge_state(mm, ll, aa, mrg[(w * GQ + j) * 2], mrg[(w * GQ + j) * 2 + 1], accs[(size_t)(w * GQ + j) * hs4 + w4]);
         const size_t slot = ((size_t)b * H + h0 + j) * NC + c;
+        if (!in_bounds(slot, 1, p.ext->ws_rows, p.err)) continue;
         reinterpret_cast<float4 *>(p.ws_acc + slot * hs)[w4] = aa;
         if (w4 == 0) {
             p.ws_ml[slot * 2 + 0] = mm;
@@ -514,7 +530,8 @@ __global__ void __launch_bounds__(kNWA * 32) attn_kernel(const AttnParams p) {
     __threadfence();
     __syncthreads();
     if (tid == 0) {
-        const unsigned t = atomicAdd(&p.tickets[b * KV + g], 1u);
+        unsigned t = 0;
+        if (in_bounds((size_t)b * KV + g, 1, p.ext->tickets, p.err)) t = atomicAdd(&p.tickets[b * KV + g], 1u);
         flags[1] = (t == (unsigned)(n_active - 1)) ? 1 : 0;
     }
     __syncthreads();
@@ -522,6 +539,7 @@ __global__ void __launch_bounds__(kNWA * 32) attn_kernel(const AttnParams p) {
     __threadfence();
 
     // last CTA of the group: merge the chunks in chunk order
+    if (!in_bounds(((size_t)b * H + h0 + nq - 1) * NC + n_active - 1, 1, p.ext->ws_rows, p.err)) return;
     if (tid < nq) {
         const int j = tid;
         float M = -CUDART_INF_F;
@@ -553,7 +571,8 @@ __global__ void __launch_bounds__(kNWA * 32) attn_kernel(const AttnParams p) {
         o.y *= inv;
         o.z *= inv;
         o.w *= inv;
-        reinterpret_cast<float4 *>(p.out + (size_t)b * p.dim + (size_t)(h0 + j) * hs)[w4] = o;
+        if (in_bounds((size_t)b * p.dim + (size_t)(h0 + j) * hs + 4 * w4, 4, p.ext->xb, p.err))
+            reinterpret_cast<float4 *>(p.out + (size_t)b * p.dim + (size_t)(h0 + j) * hs)[w4] = o;
     }
     if (dbg) {
         for (int idx = tid; idx < nq * P; idx += NT) {
@@ -562,7 +581,7 @@ __global__ void __launch_bounds__(kNWA * 32) attn_kernel(const AttnParams p) {
             *cell = expf(__ldcg(cell) - fin[j * 2]) / fin[j * 2 + 1];
         }
     }
-    if (tid == 0) p.tickets[b * KV + g] = 0u;
+    if (tid == 0 && in_bounds((size_t)b * KV + g, 1, p.ext->tickets, p.err)) p.tickets[b * KV + g] = 0u;
 }
 
 // ---------------------------------------------------------------- host side
@@ -622,9 +641,10 @@ AttnLaunch attn_plan(int head_size, int n_heads, int n_kv_heads) {
 #endif
     a.rl = L2_ATTN_ROW_LANE && head_size == 64 && (a.gq == 4 || a.gq == 8) && kStageFloats == 2 * 16 * 64;
     a.threads = kNWA * 32;
-    const int wpr = a.rl ? 2 : 1, nrg = kNWA / wpr;  // warps per ring, rings per CTA (as in the kernel)
-    const size_t hdr = (8 * nrg * kAttStages + 16 + 4 * (nrg * a.gq * 2 + a.gq * 2) + 127) / 128 * 128;
-    a.smem = hdr + (size_t)nrg * kAttStages * kStageFloats * 4 + (size_t)nrg * a.gq * hs4 * 16;
+    const int wpr = a.rl ? a.gq / 2 : 1, nrg = kNWA / wpr;  // warps per ring, rings per CTA (as in the kernel)
+    const int stg = a.rl ? kAttStagesRL : kAttStages;
+    const size_t hdr = (8 * nrg * stg + 16 + 4 * (nrg * a.gq * 2 + a.gq * 2) + 127) / 128 * 128;
+    a.smem = hdr + (size_t)nrg * stg * kStageFloats * 4 + (size_t)nrg * a.gq * hs4 * 16;
     if (a.rl) a.smem += (size_t)a.gq * head_size * 4 + (size_t)kNWA * 17 * (a.gq / wpr) * 4;  // query vectors, probabilities
     a.ok = a.lp <= 32 && a.gq <= 8 && head_size % 4 == 0 && 2 * head_size <= kStageFloats;
     return a;

@@ -79,7 +79,8 @@ __global__ void __launch_bounds__(kPfThreads) attn_prefill_kernel(const AttnPara
     for (int i = tid; i < kPfNQ * HS4; i += kPfThreads) {
         const int qi = i / HS4, c4 = i - qi * HS4, r = qi / GQ, j = qi - r * GQ;
         float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (r < nr) v = reinterpret_cast<const float4 *>(p.q + (size_t)(r0 + r) * p.dim + (size_t)(h0 + j) * HS)[c4];
+        if (r < nr && in_bounds((size_t)(r0 + r) * p.dim + (size_t)(h0 + j) * HS + 4 * c4, 4, p.ext->q, p.err))
+            v = reinterpret_cast<const float4 *>(p.q + (size_t)(r0 + r) * p.dim + (size_t)(h0 + j) * HS)[c4];
         reinterpret_cast<float4 *>(qs + qi * KP)[c4] = v;
     }
     __syncthreads();  // barriers initialised, query vectors in place
@@ -88,9 +89,11 @@ __global__ void __launch_bounds__(kPfThreads) attn_prefill_kernel(const AttnPara
     // warp 0: tile `tile` into ring stage `st`, one copy per K row and per V row
     auto issue = [&](int tile, int st) {
         const int t0 = tile * kPfTK, n = min(kPfTK, P - t0);
-        if (lane == 0) mbar_arrive_expect_tx(&bars[st], 2u * (uint32_t)n * HS * 4u);
+        // rows outside the cache (bounds-checked build) are skipped; the barrier expects nothing
+        const bool ok = in_bounds(head_base + (size_t)t0 * HS, (size_t)n * HS, p.ext->cache, p.err);
+        if (lane == 0) mbar_arrive_expect_tx(&bars[st], ok ? 2u * (uint32_t)n * HS * 4u : 0u);
         __syncwarp();
-        if (lane < n) {
+        if (ok && lane < n) {
             bulk_g2s_nohint(ks + ((size_t)st * kPfTK + lane) * KP, kb + (size_t)(t0 + lane) * HS, HS * 4, &bars[st]);
             bulk_g2s_nohint(vs + ((size_t)st * kPfTK + lane) * HS, vb + (size_t)(t0 + lane) * HS, HS * 4, &bars[st]);
         }
@@ -188,7 +191,8 @@ __global__ void __launch_bounds__(kPfThreads) attn_prefill_kernel(const AttnPara
         float4 *out = reinterpret_cast<float4 *>(p.out + (size_t)(r0 + qrow) * p.dim + (size_t)(h0 + j) * HS) + pj;
 #pragma unroll
         for (int d4 = 0; d4 < DPT / 4; ++d4)
-            out[8 * d4] = make_float4(o[4 * d4] * inv, o[4 * d4 + 1] * inv, o[4 * d4 + 2] * inv, o[4 * d4 + 3] * inv);
+            if (in_bounds((size_t)(r0 + qrow) * p.dim + (size_t)(h0 + j) * HS + 4 * (pj + 8 * d4), 4, p.ext->xb, p.err))
+                out[8 * d4] = make_float4(o[4 * d4] * inv, o[4 * d4 + 1] * inv, o[4 * d4 + 2] * inv, o[4 * d4 + 3] * inv);
     }
 }
 

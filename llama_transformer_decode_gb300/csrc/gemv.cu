@@ -88,6 +88,8 @@ struct Piece {
     long long f0;       // offset of the piece in the CTA's word stream
     int rows;           // whole rows of n floats
     int yoff;           // local output index of the piece's first row
+    long long off;      // its first word's offset in the layer's matrix (bounds checks)
+    long long words;    // that matrix's words (bounds checks)
 };
 
 template <int NW, int STAGES>
@@ -161,18 +163,21 @@ __global__ void __launch_bounds__(NW * 32, 1) l2dec_matvec_kernel(const GemvPara
                 for (int m = 0; m < 3; ++m) {
                     int lo = max(vr0, b0), hi = min(vr0 + R, b0 + rws[m]);
                     if (lo < hi) {
-                        fx.pieces[np] = {row_ptr(mats[m], (size_t)(lo - b0)), f, hi - lo, lo - vr0};
+                        fx.pieces[np] = {row_ptr(mats[m], (size_t)(lo - b0)), f, hi - lo, lo - vr0,
+                                         (long long)(lo - b0) * nw, (long long)rws[m] * nw};
                         f += (long long)(hi - lo) * nw;
                         ++np;
                     }
                     b0 += rws[m];
                 }
             } else if (MODE == GEMV_W13) {
-                fx.pieces[0] = {row_ptr(p.mat0, (size_t)vr0), 0, R, 0};
-                fx.pieces[1] = {row_ptr(p.mat1, (size_t)vr0), (long long)R * nw, R, R};
+                const long long mw = (long long)p.total_units * p.unit_rows * nw;
+                fx.pieces[0] = {row_ptr(p.mat0, (size_t)vr0), 0, R, 0, (long long)vr0 * nw, mw};
+                fx.pieces[1] = {row_ptr(p.mat1, (size_t)vr0), (long long)R * nw, R, R, (long long)vr0 * nw, mw};
                 np = 2;
             } else {
-                fx.pieces[0] = {row_ptr(p.mat0, (size_t)vr0), 0, R, 0};
+                fx.pieces[0] = {row_ptr(p.mat0, (size_t)vr0), 0, R, 0, (long long)vr0 * nw,
+                                (long long)p.total_units * p.unit_rows * nw};
                 np = 1;
             }
         }
@@ -217,10 +222,13 @@ __global__ void __launch_bounds__(NW * 32, 1) l2dec_matvec_kernel(const GemvPara
         chunk_at(fi, pi, len);
         if (lane == 0) {
             const Piece &pc = fx.pieces[pi];
-            mbar_arrive_expect_tx(&bars[stage], (uint32_t)len * 16u);
-            if (hint)
+            // a copy outside its matrix (bounds-checked build) is skipped; the barrier expects nothing
+            const bool ok = in_bounds((size_t)(pc.off + (fi - pc.f0)), (size_t)len, (size_t)pc.words, p.err) &&
+                            len <= CH4;
+            mbar_arrive_expect_tx(&bars[stage], ok ? (uint32_t)len * 16u : 0u);
+            if (ok && hint)
                 bulk_g2s(wring + (size_t)stage * CH4, pc.src + (fi - pc.f0), (uint32_t)len * 16u, &bars[stage], pol);
-            else
+            else if (ok)
                 bulk_g2s_nohint(wring + (size_t)stage * CH4, pc.src + (fi - pc.f0), (uint32_t)len * 16u, &bars[stage]);
         }
         fi += len;
@@ -242,7 +250,10 @@ __global__ void __launch_bounds__(NW * 32, 1) l2dec_matvec_kernel(const GemvPara
         for (int i = tid; i < n4; i += NT) xs[i] = in4[i];
     } else {
         const float *src = p.x;
-        if (MODE == GEMV_QKV && p.layer == 0) src = p.emb + (size_t)p.step->token[0] * p.dim;
+        if (MODE == GEMV_QKV && p.layer == 0) {
+            const size_t row = (size_t)p.step->token[0] * p.dim;
+            src = in_bounds(row, (size_t)p.dim, p.ext->emb, p.err) ? p.emb + row : p.emb;
+        }
         const float4 *s4 = reinterpret_cast<const float4 *>(src);
         float ss = 0.f;
         for (int i = tid; i < n4; i += NT) {
@@ -392,6 +403,9 @@ __global__ void __launch_bounds__(NW * 32, 1) l2dec_matvec_kernel(const GemvPara
             const int j = 2 * i, v = vr0 + j;
             const float y0 = ys[j], y1 = ys[j + 1];
             if (v < p.dim) {
+                if (!in_bounds((size_t)pos * half + ((v % hs) >> 1), 1, p.ext->rope, p.err) ||
+                    !in_bounds((size_t)v, 2, p.ext->q, p.err))
+                    continue;
                 const float2 cs = rr[(v % hs) >> 1];
                 p.q[v] = y0 * cs.x - y1 * cs.y;
                 p.q[v + 1] = y0 * cs.y + y1 * cs.x;
@@ -401,6 +415,9 @@ __global__ void __launch_bounds__(NW * 32, 1) l2dec_matvec_kernel(const GemvPara
                 const int g = c / hs, d = c % hs;
                 const size_t idx =
                     ((((size_t)p.step->slot[0] * p.n_layers + p.layer) * p.n_kv_heads + g) * p.seq_len + pos) * hs + d;
+                if (!in_bounds(idx, 2, p.ext->cache, p.err) ||
+                    !in_bounds((size_t)pos * half + (d >> 1), 1, p.ext->rope, p.err))
+                    continue;
                 if (is_k) {
                     const float2 cs = rr[d >> 1];
                     p.kcache[idx] = y0 * cs.x - y1 * cs.y;
@@ -412,12 +429,15 @@ __global__ void __launch_bounds__(NW * 32, 1) l2dec_matvec_kernel(const GemvPara
             }
         }
     } else if (MODE == GEMV_RESID) {
-        for (int j = tid; j < R; j += NT) p.x[vr0 + j] += ys[j];
+        for (int j = tid; j < R; j += NT)
+            if (in_bounds((size_t)vr0 + j, 1, p.ext->x, p.err)) p.x[vr0 + j] += ys[j];
     } else if (MODE == GEMV_W13) {
-        for (int j = tid; j < R; j += NT) p.hb[vr0 + j] = silu(ys[j]) * ys[R + j];
+        for (int j = tid; j < R; j += NT)
+            if (in_bounds((size_t)vr0 + j, 1, p.ext->hb, p.err)) p.hb[vr0 + j] = silu(ys[j]) * ys[R + j];
     } else {
         float *user = p.step->logits_out;
         for (int j = tid; j < R; j += NT) {
+            if (!in_bounds((size_t)vr0 + j, 1, p.ext->logits, p.err)) continue;
             p.logits[vr0 + j] = ys[j];
             if (user) user[vr0 + j] = ys[j];
         }

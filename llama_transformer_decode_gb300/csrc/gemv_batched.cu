@@ -128,9 +128,12 @@ __global__ void __launch_bounds__(kBT, 1) l2dec_matvec_batched_kernel(const __gr
             // one embedding row per sequence; columns past n stay unused
             if (lane == 0) mbar_arrive_expect_tx(&fx.bars[s], (uint32_t)(B * len * 4));
             __syncwarp();
-            for (int b = lane; b < B; b += 32)
-                bulk_g2s_nohint(X + (size_t)b * tk, p.emb + (size_t)p.step->token[b] * p.dim + k0, (uint32_t)len * 4u,
-                                &fx.bars[s]);
+            for (int b = lane; b < B; b += 32) {
+                // a row outside the table (bounds-checked build) is read from row 0 instead
+                const size_t row = in_bounds((size_t)p.step->token[b] * p.dim + k0, (size_t)len, p.ext->emb, p.err)
+                                       ? (size_t)p.step->token[b] * p.dim : 0;
+                bulk_g2s_nohint(X + (size_t)b * tk, p.emb + row + k0, (uint32_t)len * 4u, &fx.bars[s]);
+            }
         } else if (lane == 0) {
             mbar_arrive_expect_tx(&fx.bars[s], (uint32_t)(B * tk * 4));
             tensor_g2s(X, &bp.xmap, k0, 0, &fx.bars[s]);
@@ -290,7 +293,9 @@ __global__ void __launch_bounds__(kBT, 1) l2dec_matvec_batched_kernel(const __gr
                 const int pos = p.step->pos[b];
                 const float2 *rr = p.rope + (size_t)pos * half;
                 const int v = rr0 + j;  // row within matrix m
+                if (!in_bounds((size_t)pos * half + half - 1, 1, p.ext->rope, p.err)) continue;
                 if (m == 0) {
+                    if (!in_bounds((size_t)b * p.dim + v, 2, p.ext->q, p.err)) continue;
                     const float2 cs = rr[(v % hs) >> 1];
                     float *qv = p.q + (size_t)b * p.dim;
                     qv[v] = y0 * cs.x - y1 * cs.y;
@@ -300,6 +305,7 @@ __global__ void __launch_bounds__(kBT, 1) l2dec_matvec_batched_kernel(const __gr
                     const size_t idx =
                         ((((size_t)p.step->slot[b] * p.n_layers + p.layer) * p.n_kv_heads + g) * p.seq_len + pos) * hs +
                         d;
+                    if (!in_bounds(idx, 2, p.ext->cache, p.err)) continue;
                     if (m == 1) {
                         const float2 cs = rr[d >> 1];
                         p.kcache[idx] = y0 * cs.x - y1 * cs.y;
@@ -314,12 +320,14 @@ __global__ void __launch_bounds__(kBT, 1) l2dec_matvec_batched_kernel(const __gr
             const int hidden = p.total_units;
             for (int e = tid; e < RR * B; e += kBT) {
                 const int r = e / B, b = e - r * B;
+                if (!in_bounds((size_t)b * hidden + rr0 + r, 1, p.ext->hb, p.err)) continue;
                 p.hb[(size_t)b * hidden + rr0 + r] = silu_b(ys[e]) * ys[(size_t)(RB + r) * B + b];
             }
         } else if (MODE == GEMV_RESID) {
             const int dim = p.total_units;
             for (int e = tid; e < RR * B; e += kBT) {
                 const int r = e / B, b = e - r * B;
+                if (!in_bounds((size_t)b * dim + rr0 + r, 1, p.ext->x, p.err)) continue;
                 float *xp = p.x + (size_t)b * dim + rr0 + r;
                 const float nv = *xp + ys[e];
                 *xp = nv;
@@ -336,6 +344,7 @@ __global__ void __launch_bounds__(kBT, 1) l2dec_matvec_batched_kernel(const __gr
             const int V = p.total_units;
             for (int e = tid; e < RR * B; e += kBT) {
                 const int r = e / B, b = e - r * B;
+                if (!in_bounds((size_t)b * V + rr0 + r, 1, p.ext->logits, p.err)) continue;
                 p.logits[(size_t)b * V + rr0 + r] = ys[e];
                 if (user) user[(size_t)b * V + rr0 + r] = ys[e];
             }
@@ -343,7 +352,8 @@ __global__ void __launch_bounds__(kBT, 1) l2dec_matvec_batched_kernel(const __gr
         __syncthreads();
     }
     if (MODE == GEMV_RESID)
-        for (int b = tid; b < B; b += kBT) p.ss_part[(size_t)blockIdx.x * B + b] = fx.inv[b];
+        for (int b = tid; b < B; b += kBT)
+            if (in_bounds((size_t)blockIdx.x * B + b, 1, p.ext->ss_part, p.err)) p.ss_part[(size_t)blockIdx.x * B + b] = fx.inv[b];
 }
 
 // ---------------------------------------------------------------- host side

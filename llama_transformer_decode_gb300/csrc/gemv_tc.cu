@@ -116,8 +116,11 @@ struct TcFixed {
     int part_tile[2];     // the CTA's partial tiles (first, last segment), -1 if none
     float inv[kMaxBatch];
     int pos[kMaxBatch];   // the step's positions and cache slots (QKV)
-    int slot[kMaxBatch];
+    unsigned char slot[kMaxBatch];
 };
+// The ring stages start 1024-aligned after this block: keeping it within 1 KB keeps
+// a whole ring stage (64 KB at 64 rows) that a second KB of header would cost.
+static_assert(sizeof(TcFixed) <= 1024, "the tensor-core GEMV's fixed shared-memory block must fit 1 KB");
 
 __host__ __device__ constexpr size_t tc_fixed_bytes() { return (sizeof(TcFixed) + 1023) / 1024 * 1024; }
 
@@ -452,7 +455,9 @@ __global__ void __launch_bounds__(kTT, 1) l2dec_matvec_tc_kernel(const __grid_co
                 for (int i = 0; i < 8; ++i) {
                     const int e = e0 + i * nt, b = e / npr, v = r0 + jlo + 2 * (e - b * npr);
                     cs[i] = make_float2(1.f, 0.f);
-                    if (m < 2 && e < npr * B && v < mr) cs[i] = p.rope[(size_t)fx.pos[b] * half + ((v % hs) >> 1)];
+                    if (m < 2 && e < npr * B && v < mr &&
+                        in_bounds((size_t)fx.pos[b] * half + ((v % hs) >> 1), 1, p.ext->rope, p.err))
+                        cs[i] = p.rope[(size_t)fx.pos[b] * half + ((v % hs) >> 1)];
                 }
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
@@ -460,6 +465,7 @@ __global__ void __launch_bounds__(kTT, 1) l2dec_matvec_tc_kernel(const __grid_co
                     if (e >= npr * B || v >= mr) continue;
                     const float y0 = src[j * YS + b] * fx.inv[b], y1 = src[(j + 1) * YS + b] * fx.inv[b];
                     if (m == 0) {
+                        if (!in_bounds((size_t)b * p.dim + v, 2, p.ext->q, p.err)) continue;
                         float *qv = p.q + (size_t)b * p.dim;
                         qv[v] = y0 * cs[i].x - y1 * cs[i].y;
                         qv[v + 1] = y0 * cs[i].y + y1 * cs[i].x;
@@ -468,6 +474,7 @@ __global__ void __launch_bounds__(kTT, 1) l2dec_matvec_tc_kernel(const __grid_co
                         const size_t idx =
                             ((((size_t)fx.slot[b] * p.n_layers + p.layer) * p.n_kv_heads + g) * p.seq_len + fx.pos[b]) * hs +
                             d;
+                        if (!in_bounds(idx, 2, p.ext->cache, p.err)) continue;
                         if (m == 1) {
                             p.kcache[idx] = y0 * cs[i].x - y1 * cs[i].y;
                             p.kcache[idx + 1] = y0 * cs[i].y + y1 * cs[i].x;
@@ -482,7 +489,7 @@ __global__ void __launch_bounds__(kTT, 1) l2dec_matvec_tc_kernel(const __grid_co
             const int hidden = tp.mrows[0];
             for (int e = ti; e < nj * B; e += nt) {
                 const int b = e / nj, j = jlo + (e - b * nj);
-                if (r0 + j >= hidden) continue;
+                if (r0 + j >= hidden || !in_bounds((size_t)b * hidden + r0 + j, 1, p.ext->hb, p.err)) continue;
                 const float h1 = src[j * YS + b] * fx.inv[b], h3 = src[(j + kTM / 2) * YS + b] * fx.inv[b];
                 p.hb[(size_t)b * hidden + r0 + j] = silu_t(h1) * h3;
             }
@@ -493,7 +500,9 @@ __global__ void __launch_bounds__(kTT, 1) l2dec_matvec_tc_kernel(const __grid_co
             const int ng = (B + 7) / 8;
             for (int e = ti; e < nj * ng; e += nt) {
                 const int j = jlo + e % nj, b0 = 8 * (e / nj);
-                if (j >= jend) continue;
+                if (j >= jend || !in_bounds((size_t)(B - 1) * dim + r0 + j, 1, p.ext->x, p.err) ||
+                    !in_bounds((size_t)(B - 1) * dim + r0 + j, 1, p.ext->xg, p.err))
+                    continue;
                 const float g = __ldg(tp.next_gain + r0 + j);
                 float xv[8];
 #pragma unroll
@@ -522,7 +531,7 @@ __global__ void __launch_bounds__(kTT, 1) l2dec_matvec_tc_kernel(const __grid_co
                 src[ti * YS + BP] = ss;
             }
             sync();
-            if (ti < B) {
+            if (ti < B && in_bounds((size_t)part * B + ti, 1, p.ext->ss_part, p.err)) {
                 float t = 0.f;
                 for (int i = 0; i < parts; ++i) t += src[(i * B + ti) * YS + BP];
                 p.ss_part[(size_t)part * B + ti] = t;
@@ -532,7 +541,7 @@ __global__ void __launch_bounds__(kTT, 1) l2dec_matvec_tc_kernel(const __grid_co
             const int V = tp.mrows[0];
             for (int e = ti; e < nj * B; e += nt) {
                 const int b = e / nj, j = jlo + (e - b * nj);
-                if (r0 + j >= V) continue;
+                if (r0 + j >= V || !in_bounds((size_t)b * V + r0 + j, 1, p.ext->logits, p.err)) continue;
                 const float y = src[j * YS + b] * fx.inv[b];
                 p.logits[(size_t)b * V + r0 + j] = y;
                 if (user) user[(size_t)b * V + r0 + j] = y;
@@ -754,7 +763,7 @@ __global__ void __launch_bounds__(kTT, 1) l2dec_matvec_tc_kernel(const __grid_co
         if (MODE == GEMV_QKV)
             for (int b = et; b < B; b += kRoleThreads) {
                 fx.pos[b] = p.step->pos[b];
-                fx.slot[b] = p.step->slot[b];
+                fx.slot[b] = (unsigned char)p.step->slot[b];  // slots < kMaxBatch
             }
         if (MODE != GEMV_RESID) {
             for (int b = et >> 5; b < B; b += kRoleThreads / 32) {
@@ -806,7 +815,8 @@ __global__ void __launch_bounds__(kTT, 1) l2dec_matvec_tc_kernel(const __grid_co
                 if (CS > 1) continue;  // the CTA's only segment: added up across the cluster below
                 // a stream-K partial tile goes to this CTA's workspace slot [BP][128]
                 float *wsrow = tp.ws + ((size_t)blockIdx.x * 2 + which) * kTM * BP;
-                for (int c = 0; c < B; ++c) wsrow[(size_t)c * kTM + row] = ys[row * YS + c];
+                if (in_bounds(((size_t)blockIdx.x * 2 + which) * kTM * BP, (size_t)kTM * BP, p.ext->tc_ws, p.err))
+                    for (int c = 0; c < B; ++c) wsrow[(size_t)c * kTM + row] = ys[row * YS + c];
                 if (which == 0) part0 = tile;
                 else part1 = tile;
                 continue;
@@ -872,7 +882,7 @@ __global__ void __launch_bounds__(kTT, 1) l2dec_matvec_tc_kernel(const __grid_co
         for (int w = 0; w < 2; ++w) {
             int last = 0;
             const int t = fx.part_tile[w];
-            if (t >= 0) {
+            if (t >= 0 && in_bounds((size_t)t, 1, p.ext->tc_tickets, p.err)) {
                 const int c0 = cta_of((long long)t * KT), c1 = cta_of((long long)(t + 1) * KT - 1);
                 last = atomicAdd(&tp.tickets[t], 1u) == (unsigned)(c1 - c0) ? 1 : 0;
             }
@@ -899,7 +909,8 @@ __global__ void __launch_bounds__(kTT, 1) l2dec_matvec_tc_kernel(const __grid_co
                 for (int u = 0; u < kPG; ++u) {
                     const int cc = min(cb + u, c1);
                     const int wh = (long long)cc * T / G >= (long long)t * KT ? 0 : 1;
-                    const float4 *src = reinterpret_cast<const float4 *>(tp.ws + ((size_t)cc * 2 + wh) * kTM * BP);
+                    const bool cc_ok = in_bounds(((size_t)cc * 2 + wh) * kTM * BP, (size_t)kTM * BP, p.ext->tc_ws, p.err);
+                    const float4 *src = reinterpret_cast<const float4 *>(tp.ws + (cc_ok ? ((size_t)cc * 2 + wh) * kTM * BP : 0));
 #pragma unroll
                     for (int i = 0; i < kV; ++i) {
                         const int v = tid + kTT * (i0 + i);

@@ -114,6 +114,7 @@ struct l2_ctx {
     float *xg = nullptr;          // tensor-core path: x * gain of the next RMSNorm [max_rows][dim]
     unsigned *tc_tickets = nullptr;
     size_t tc_tickets_n = 0;      // entries of tc_tickets
+    size_t tc_ws_n = 0;           // floats of tc_ws
 
     StepDev *step_host = nullptr;  // pinned ring
     cudaEvent_t ring_ev[kRing] = {};
@@ -136,6 +137,8 @@ struct l2_ctx {
     bool evict_first = false;
 
     float *static_scratch = nullptr;  // device address of the l2_forward_static array on this device
+    Extents ext{}, ext_static{};      // buffer sizes for the bounds-checked build, and their device copies
+    Extents *ext_dev = nullptr, *ext_static_dev = nullptr;
     std::vector<int> written;  // cache rows written per slot
     std::string error;
 };
@@ -284,6 +287,7 @@ void make_plans(l2_ctx *c) {
         b.n_layers = p.n_layers;
         b.vocab = p.vocab_size;
         b.evict_first = c->evict_first ? 1 : 0;
+        b.ext = c->ext_dev;
     };
     plan(c->plan_qkv, GEMV_QKV, p.dim, 2, (p.dim + 2 * c->kv_dim) / 2, 1);
     plan(c->plan_wo, GEMV_RESID, p.dim, 1, p.dim, 1);
@@ -387,6 +391,7 @@ AttnParams attn_params(const l2_ctx *c, int layer, int batch) {
     a.n_chunks = nc;
     a.min_chunk = kMinChunk;
     a.scale = (float)(1.0 / std::sqrt((double)c->head_size));
+    a.ext = c->ext_dev;
     return a;
 }
 
@@ -1111,7 +1116,8 @@ int l2_create(const L2Config *config, const L2Weights *weights, int max_batch, u
         (rc = alloc_n(c, &c->tickets, B * p.n_kv_heads, "attention tickets")) ||
         (rc = alloc_n(c, &c->rope, S * (hs / 2), "RoPE table")) || (rc = alloc_n(c, &c->step_dev, 1, "step inputs")) ||
         (rc = alloc_n(c, &c->err, 1, "error word")) ||
-        (rc = alloc_n(c, &c->ss_part, (size_t)kMaxParts * B, "sum-of-squares partials")))
+        (rc = alloc_n(c, &c->ss_part, (size_t)kMaxParts * B, "sum-of-squares partials")) ||
+        (rc = alloc_n(c, &c->ext_dev, 1, "buffer extents")) || (rc = alloc_n(c, &c->ext_static_dev, 1, "buffer extents")))
         return bail(rc);
     if (flags & L2_FLAG_DEBUG) {
         if ((rc = alloc_n(c, &c->dbg, B * L * p.n_heads * S, "attention probabilities"))) return bail(rc);
@@ -1198,7 +1204,8 @@ int l2_create(const L2Config *config, const L2Weights *weights, int max_batch, u
             tiles = std::max(tiles, c->bsets[b].tc_tiles);
         }
         if (tiles > 0) {
-            if ((rc = alloc_n(c, &c->tc_ws, ws ? ws : 1, "tensor-core GEMV workspace")) ||
+            c->tc_ws_n = ws ? ws : 1;
+            if ((rc = alloc_n(c, &c->tc_ws, c->tc_ws_n, "tensor-core GEMV workspace")) ||
                 (rc = alloc_n(c, &c->tc_tickets, (size_t)tiles, "tensor-core GEMV tickets")))
                 return bail(rc);
             CREATE_CUDA(cudaMemset(c->tc_tickets, 0, (size_t)tiles * sizeof(unsigned)));
@@ -1206,6 +1213,31 @@ int l2_create(const L2Config *config, const L2Weights *weights, int max_batch, u
         }
     }
     if ((rc = plan_persistent(c))) return bail(rc);
+    // buffer sizes, read by the bounds-checked build only
+    {
+        Extents &e = c->ext;
+        const size_t R = (size_t)c->max_rows;
+        e.emb = (size_t)p.vocab_size * p.dim;
+        e.x = e.xb = e.q = R * p.dim;
+        e.hb = R * p.hidden_dim;
+        e.logits = R * p.vocab_size;
+        e.cache = cache;
+        e.rope = S * (hs / 2);
+        e.ws_rows = ws;
+        e.tickets = R * p.n_kv_heads;
+        e.dbg = c->dbg ? R * L * p.n_heads * S : 0;
+        e.ss_part = (size_t)kMaxParts * R;
+        e.xg = c->xg ? R * p.dim : 0;
+        e.tc_ws = c->tc_ws_n;
+        e.tc_tickets = c->tc_tickets_n;
+        // l2_forward_static: its attention partials and tickets live in the static array
+        c->ext_static = e;
+        const AttnParams probe = attn_params(c, 0, 1);
+        c->ext_static.ws_rows = (size_t)p.n_heads * probe.n_chunks;
+        c->ext_static.tickets = (size_t)p.n_kv_heads;
+        CREATE_CUDA(cudaMemcpy(c->ext_dev, &c->ext, sizeof(Extents), cudaMemcpyHostToDevice));
+        CREATE_CUDA(cudaMemcpy(c->ext_static_dev, &c->ext_static, sizeof(Extents), cudaMemcpyHostToDevice));
+    }
     CREATE_CUDA(cudaDeviceSynchronize());
 #undef CREATE_CUDA
     *out = c;
@@ -1425,6 +1457,18 @@ void l2_debug_fail_alloc_at(int n) { g_fail_alloc_at = n > 0 ? n : 0; }
 
 void l2_debug_fail_graph_at(int n) { g_fail_graph_at = n > 0 ? n : 0; }
 
+int l2_debug_bounds_checked(void) { return L2_DEBUG_BOUNDS ? 1 : 0; }
+
+int l2_debug_limit_cache(l2_ctx *c, unsigned long long floats) {
+    if (!c) return L2_EINVAL;
+    L2_CUDA(c, cudaStreamSynchronize(c->stream));
+    c->ext.cache = std::min<size_t>(c->ext.cache, (size_t)floats);
+    c->ext_static.cache = c->ext.cache;
+    L2_CUDA(c, cudaMemcpy(c->ext_dev, &c->ext, sizeof(Extents), cudaMemcpyHostToDevice));
+    L2_CUDA(c, cudaMemcpy(c->ext_static_dev, &c->ext_static, sizeof(Extents), cudaMemcpyHostToDevice));
+    return L2_OK;
+}
+
 int l2_debug_wait_timeout(l2_ctx *c, int limit_us) {
     if (!c) return L2_EINVAL;
     if (limit_us < 1 || (unsigned long long)limit_us * 1000ull > kWaitLimitNs)
@@ -1500,6 +1544,7 @@ extern "C" int l2_forward_static(l2_ctx *c, int token, int pos, float *logits_ou
         a.ws_acc = ws_acc;
         a.ws_ml = ws_ml;
         a.tickets = tickets;
+        a.ext = c->ext_static_dev;
         L2_CUDA(c, launch_attn(c->attn, a, 1, c->stream, pdl));
         for (int op = 2; op < 5; ++op) L2_CUDA(c, launch_op(c, op, l, 1, c->stream, pdl));
     }

@@ -95,6 +95,26 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *e
     return mbar_wait_limit(bar, parity, err, kWaitLimitNs);
 }
 
+// Bounds checks of the bounds-checked build (compiled with L2_DEBUG_BOUNDS=1):
+// true when elements [i, i + n) lie inside a buffer of len elements; otherwise
+// L2_DEV_ERR_BOUNDS goes into the error word and the caller skips the access.
+// In the release build it is always true and costs nothing.
+// In the release build the macro is the constant true and evaluates none of its
+// arguments (the extents are never read).
+#ifndef L2_DEBUG_BOUNDS
+#define L2_DEBUG_BOUNDS 0
+#endif
+__device__ __forceinline__ bool in_bounds_check(size_t i, size_t n, size_t len, int *err) {
+    if (i + n <= len) return true;
+    atomicOr(err, L2_DEV_ERR_BOUNDS);
+    return false;
+}
+#if L2_DEBUG_BOUNDS
+#define in_bounds(i, n, len, err) ::l2::in_bounds_check((size_t)(i), (size_t)(n), (size_t)(len), (err))
+#else
+#define in_bounds(i, n, len, err) true
+#endif
+
 // L2 eviction-priority policies for the bulk copies.
 __device__ __forceinline__ uint64_t policy_evict_first() {
     uint64_t p;

@@ -13,6 +13,24 @@ constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 // Bits of the device error word.
 enum : int { L2_DEV_ERR_TIMEOUT = 1, L2_DEV_ERR_BOUNDS = 2 };
 
+// Element counts of the buffers the kernels index, for the bounds-checked build
+// (compiled with L2_DEBUG_BOUNDS=1): there every computed index into these buffers
+// and every bulk-copy source range is checked, a violation sets
+// L2_DEV_ERR_BOUNDS in the error word and the access is skipped.  A device copy
+// lives with the handle; the release build never reads it.
+struct Extents {
+    size_t emb;              // token embedding table
+    size_t x, xb, q, hb;     // activations (rows x width)
+    size_t logits;           // the handle's logits buffer
+    size_t cache;            // each of the K and V caches
+    size_t rope;             // RoPE table entries (cos, sin pairs)
+    size_t ws_rows;          // attention partials: (m, l) pairs and head_size-wide accumulators
+    size_t tickets;          // attention tickets
+    size_t dbg;              // probability export (0: none)
+    size_t ss_part, xg;      // batched steps: sums-of-squares partials, x * gain
+    size_t tc_ws, tc_tickets;  // tensor-core GEMV: partial tiles, tickets
+};
+
 // Per-step inputs, filled by one host->device copy before each step.
 struct StepDev {
     int token[kMaxBatch];
@@ -58,6 +76,7 @@ struct GemvParams {
     int *err;
     int dim, kv_dim, head_size, seq_len, n_kv_heads, n_layers, vocab;
     int evict_first;  // stream the weights with an L2 evict-first hint
+    const Extents *ext;  // buffer sizes (read only by the bounds-checked build)
     // Batched steps (l2dec_matvec_batched_kernel) only:
     int batch;        // sequences in the step (slots 0..batch-1)
     float *ss_part;   // [kMaxParts][batch] partial sums of x^2 written by the residual kernels
@@ -155,6 +174,7 @@ struct AttnParams {
     int capacity;   // batches: CTAs resident at once; the chunk grows so the
                     // positions of all slots fill about that many (0: fixed chunk)
     float scale;    // 1 / sqrt(head_size)
+    const Extents *ext;  // buffer sizes (read only by the bounds-checked build)
 };
 
 }  // namespace l2

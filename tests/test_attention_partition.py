@@ -80,8 +80,8 @@ def test_prompt_chunk_kernel_head_groups(oracle_lib):
 
 @pytest.mark.parametrize("n_chunks", [1, 2, 7, 16, 64, 152])
 def test_positions_split_over_chunks_and_rings(attn, n_chunks):
-    # rings per CTA: 8 (one warp per ring) or 4 (two warps sharing a ring)
-    for NRG in (8, 4):
+    # rings per CTA: 8 (one warp per ring), 4 or 2 (two or four warps sharing a ring)
+    for NRG in (8, 4, 2):
         for chunk in (1, 3, 32, 64, 100, 128):
             for P in list(range(1, 300)) + [1024, 2047, 2048, 4095, 4096]:
                 n = max(1, min(attn["n_active"](P, chunk), n_chunks, P))
