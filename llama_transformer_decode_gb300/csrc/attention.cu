@@ -48,6 +48,11 @@ namespace {
 constexpr int kNWA = L2_ATTN_WARPS;
 constexpr int kAttStages = L2_ATTN_STAGES;
 constexpr int kStageFloats = L2_ATTN_STAGE_FLOATS;
+// Row-per-lane layout: packed fp32 FMAs (two per instruction) for the scores and
+// the weighted V sums.
+#ifndef L2_ATTN_FFMA2
+#define L2_ATTN_FFMA2 1
+#endif
 // Row-per-lane layout: two to four warps share a ring, so a CTA has fewer rings;
 // deeper rings keep as many bytes in flight per SM.
 constexpr int kAttStagesRL = 4;
@@ -258,8 +263,20 @@ __global__ void __launch_bounds__(kNWA * 32) attn_kernel(const AttnParams p) {
             for (int jj = 0; jj < HPL; ++jj) sc[jj] = 0.f;
             if (row_on) {
                 const float4 *Kr = Ks + t * HS4;
+#if L2_ATTN_FFMA2
+                // even and odd dimensions in the two halves of packed fp32 FMAs
+                float2 s2 = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int i = 0; i < HS4; ++i) {
+                    const float4 kv = Kr[(i + t) & (HS4 - 1)];
+                    s2 = ffma2(make_float2(qr[i].x, qr[i].y), make_float2(kv.x, kv.y), s2);
+                    s2 = ffma2(make_float2(qr[i].z, qr[i].w), make_float2(kv.z, kv.w), s2);
+                }
+                sc[0] = s2.x + s2.y;
+#else
 #pragma unroll
                 for (int i = 0; i < HS4; ++i) sc[0] = dot4(qr[i], Kr[(i + t) & (HS4 - 1)], sc[0]);
+#endif
             }
 #pragma unroll
             for (int jj = 0; jj < HPL; ++jj) {
@@ -293,10 +310,19 @@ __global__ void __launch_bounds__(kNWA * 32) attn_kernel(const AttnParams p) {
             for (int tt = 0; tt < np; ++tt) {
                 const float2 v = Vs2[tt * 32 + lane];
                 const float2 pp = *reinterpret_cast<const float2 *>(wp + tt * HPW);  // the warp's two heads
+#if L2_ATTN_FFMA2
+                const float2 a0 = ffma2(make_float2(pp.x, pp.x), v, make_float2(acc[0][0], acc[0][1]));
+                const float2 a1 = ffma2(make_float2(pp.y, pp.y), v, make_float2(acc[1][0], acc[1][1]));
+                acc[0][0] = a0.x;
+                acc[0][1] = a0.y;
+                acc[1][0] = a1.x;
+                acc[1][1] = a1.y;
+#else
                 acc[0][0] = fmaf(pp.x, v.x, acc[0][0]);
                 acc[0][1] = fmaf(pp.x, v.y, acc[0][1]);
                 acc[1][0] = fmaf(pp.y, v.x, acc[1][0]);
                 acc[1][1] = fmaf(pp.y, v.y, acc[1][1]);
+#endif
             }
             __syncwarp();
             tc += np;

@@ -159,6 +159,17 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
+// Two fp32 fused multiply-adds in one instruction (a.x*b.x + c.x, a.y*b.y + c.y),
+// each rounded to nearest as fmaf would be.
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+    unsigned long long d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;"
+        : "=l"(d)
+        : "l"(*reinterpret_cast<const unsigned long long *>(&a)), "l"(*reinterpret_cast<const unsigned long long *>(&b)),
+          "l"(*reinterpret_cast<const unsigned long long *>(&c)));
+    return *reinterpret_cast<float2 *>(&d);
+}
+
 __device__ __forceinline__ float dot4(float4 a, float4 b, float acc) {
     acc = fmaf(a.x, b.x, acc);
     acc = fmaf(a.y, b.y, acc);
