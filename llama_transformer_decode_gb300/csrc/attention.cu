@@ -12,13 +12,13 @@
 // slice of positions 0..pos of slot b and serves every query head of group g,
 // so each K/V row is read from HBM once.  The cache layout is
 // [slot][layer][kv_head][pos][head_size], so a slice is one contiguous range
-// of K and one of V; each warp streams a sub-slice through a private ring of
-// 1-D bulk async copies (TMA).  Lanes are grouped LP to a cache row (LP = the
+// of K and one of V; each warp (with 8 query heads per KV head, each pair of
+// warps) streams a sub-slice through its own ring of 1-D bulk async copies (TMA).  Lanes are grouped LP to a cache row (LP = the
 // head size in 16-byte words, rounded up to a power of two); each group keeps
 // an online softmax (running max m, sum l, un-normalised accumulator) per
-// query head; with 4 or 8 query heads per KV head at head size 64 the lanes
-// take one cache row each instead (the row-per-lane layout, described at the
-// kernel).  Groups, then warps, then CTAs are merged with the usual
+// query head; with 4 or 8 query heads per KV head at head size 64 the
+// row-per-lane layout (described at the kernel) splits rows, heads and
+// dimensions over the lanes instead.  Groups, then warps, then CTAs are merged with the usual
 // log-sum-exp rescaling; the CTA that arrives last on the group's ticket
 // merges the chunks in chunk order and writes the output, so the result does
 // not depend on CTA timing.  With a debug buffer the raw scores are stored and
@@ -48,14 +48,11 @@ namespace {
 constexpr int kNWA = L2_ATTN_WARPS;
 constexpr int kAttStages = L2_ATTN_STAGES;
 constexpr int kStageFloats = L2_ATTN_STAGE_FLOATS;
-// Row-per-lane layout: packed fp32 FMAs (two per instruction) for the scores and
-// the weighted V sums.
-#ifndef L2_ATTN_FFMA2
-#define L2_ATTN_FFMA2 1
+// Row-per-lane layout: ring buffers per ring (shared by the warps of a ring).
+#ifndef L2_ATTN_STAGES_RL
+#define L2_ATTN_STAGES_RL 3
 #endif
-// Row-per-lane layout: two to four warps share a ring, so a CTA has fewer rings;
-// deeper rings keep as many bytes in flight per SM.
-constexpr int kAttStagesRL = 4;
+constexpr int kAttStagesRL = L2_ATTN_STAGES_RL;
 
 // The WPR * 32 threads of one ring: named barrier 1 + ring (ids taken from
 // constants, so the kernel reserves only the barriers it uses).  ring_sync_or
@@ -106,24 +103,28 @@ __device__ __forceinline__ void merge_state(float &m, float &l, float4 &acc, flo
 }
 }  // namespace
 
-// RL = 1: the row-per-lane layout for 4 or 8 query heads per KV head and
-// head size 64 (16 cache rows per ring stage).  Two warps share each ring and
-// split the group's query heads between them (so a CTA needs half the ring
-// memory per warp and two CTAs fit on an SM).  Lane (t, half) of a warp
-// scores row t for half of that warp's heads over the whole head (K chunks
-// read in a lane-rotated order, conflict-free), the online softmax runs over
-// the 16 rows with shuffles inside each half-warp (one exponential per row and
-// head), and the probabilities go through shared memory to the PV pass, where
-// lane l accumulates dimensions 2l, 2l+1 of the warp's heads.  Each cache row
-// costs a few dozen instructions instead of one shuffle tree per head.
+// RL = 1: the row-per-lane layout for 4 or 8 query heads per KV head at
+// head size 64 (16 cache rows per ring stage).  Each warp serves 4 of the
+// group's heads and keeps their query words in registers; with 8 heads two
+// warps share a ring (two CTAs fit on an SM).  For the scores, lane (rg, dq)
+// multiplies rows 4 rg .. 4 rg + 3 of the stage with the 4 heads over 8 of
+// the 64 dimensions, and the 8 lanes of a row group add their partial sums up
+// by exchanging halves (three shuffle rounds), leaving each (head, row) score
+// in one lane.  The online softmax runs over the stage's 16 rows per head;
+// the probabilities go through shared memory to the PV pass, where lane
+// (hg, dg) accumulates two heads over 4 dimensions.  A cache row is read from
+// shared memory twice per warp (scores, weighted sum), and no 16-byte load is
+// a broadcast of one word to the whole warp: at 8 warps per SM the loop was
+// bound by instruction latency, so the layout that halves the registers per
+// thread (two CTAs per SM) is the one that pays.
 template <int LP, int GQ, int RL>
 __global__ void __launch_bounds__(kNWA * 32) attn_kernel(const AttnParams p) {
     constexpr int NT = kNWA * 32;
     constexpr int RPI = 32 / LP;        // cache rows a warp handles at once
-    constexpr int WPR = RL ? GQ / 2 : 1;  // warps sharing one ring (row-per-lane: two heads per warp)
+    constexpr int WPR = RL ? GQ / 4 : 1;  // warps sharing one ring (row-per-lane: four heads per warp)
     constexpr int NRG = kNWA / WPR;     // rings per CTA (one softmax state per ring and head)
     constexpr int STG = RL ? kAttStagesRL : kAttStages;  // ring buffers per ring
-    static_assert(!RL || NRG <= 4, "ring barriers are ids 1..4");
+    static_assert(WPR == 1 || NRG <= 4, "ring barriers are ids 1..4");
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem);                      // [NRG][STG]
     int *flags = reinterpret_cast<int *>(smem + 8 * NRG * STG);        // [4]
@@ -133,8 +134,7 @@ __global__ void __launch_bounds__(kNWA * 32) attn_kernel(const AttnParams p) {
     const int hs = p.head_size, hs4 = hs >> 2;
     float4 *ring = reinterpret_cast<float4 *>(smem + hdr);                     // [NRG][STG][stage]
     float4 *accs = ring + NRG * STG * (kStageFloats / 4);              // [NRG][GQ][hs4]
-    float *qs = reinterpret_cast<float *>(accs + NRG * GQ * hs4);               // RL: [GQ][hs]
-    float *pbuf = qs + GQ * hs;                                                 // RL: [kNWA][16 + 1][GQ / WPR]
+    float *pbuf = reinterpret_cast<float *>(accs + NRG * GQ * hs4);            // RL: [kNWA][4 heads][16 + 1]
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // several rows: the host orders them, longest CTAs first
@@ -212,121 +212,130 @@ __global__ void __launch_bounds__(kNWA * 32) attn_kernel(const AttnParams p) {
                           p.ext->dbg, p.err))
         dbg = nullptr;
     if constexpr (RL == 1) {
-        constexpr int TPR = 16;            // cache rows per ring stage (head size 64)
-        constexpr int HS4 = 16;
-        constexpr int HPW = GQ / WPR;      // heads per warp: 2
-        constexpr int HPL = HPW / 2;       // heads per lane: 1 (one half-warp each)
-        constexpr int RTH = WPR * 32;      // threads of one ring
-        static_assert(HPL == 1, "row-per-lane attention: one head per half-warp");
-        // the group's query vectors, shared by all warps
-        for (int i = tid; i < GQ * 64; i += NT) {
-            const int j = i / 64, d = i % 64;
-            const size_t qi = (size_t)b * p.dim + (size_t)(h0 + j) * 64 + d;
-            qs[i] = j < nq && in_bounds(qi, 1, p.ext->q, p.err) ? p.q[qi] : 0.f;
+        constexpr int TPR = 16;   // cache rows per ring stage (head size 64)
+        constexpr int NHW = 4;    // query heads per warp (GQ / WPR)
+        constexpr int RTH = WPR * 32;
+        static_assert(GQ == NHW * WPR, "row-per-lane attention: 4 or 8 query heads per KV head");
+        // Scores: lane (rg, dq) takes rows 4 rg .. 4 rg + 3 of the stage over dimensions
+        // 4 dq .. 4 dq + 3 and 32 + 4 dq .. 32 + 4 dq + 3, for the warp's 4 heads (their
+        // query words stay in registers), then the 8 lanes of the row group add up by
+        // exchanging halves.  The lane's heads are numbered i ^ (dq >> 1) and its rows
+        // r ^ 2 (dq & 1), so at every exchange a lane keeps the low half of its values and
+        // sends the high half: it ends with head jw0 + (dq >> 1), rows r0, r0 + 1.
+        const int rg = lane >> 3, dq = lane & 7, qh = dq >> 1, rb = 2 * (dq & 1);
+        const int jw0 = wsub * NHW;          // the warp's first head of the group
+        const int r0 = 4 * rg + rb;
+        // PV: lane (hg, dg) accumulates heads jw0 + 2 hg, + 1 over dimensions 4 dg .. 4 dg + 3
+        const int hg = lane >> 4, dg = lane & 15;
+        float4 qa[NHW], qb[NHW];
+#pragma unroll
+        for (int i = 0; i < NHW; ++i) {
+            const int j = jw0 + (i ^ qh);
+            qa[i] = qb[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            const size_t qi = (size_t)b * p.dim + (size_t)(h0 + j) * 64 + 4 * dq;
+            if (j < nq && in_bounds(qi, 36, p.ext->q, p.err)) {
+                qa[i] = *reinterpret_cast<const float4 *>(p.q + qi);
+                qb[i] = *reinterpret_cast<const float4 *>(p.q + qi + 32);
+            }
         }
-        __syncthreads();
-        const float4 *qs4 = reinterpret_cast<const float4 *>(qs);
-        float *wp = pbuf + warp * (TPR + 1) * HPW;  // [TPR][HPW] probabilities, then [HPW] rescales
-        const int t = lane & (TPR - 1), jh = lane / TPR;
-        const int jw0 = wsub * HPW;                 // the warp's first head of the group
-        // this lane's head's query vector in registers, its 16-byte chunks in the lane's
-        // rotated order (chunk i of the loop below is chunk (i + t) % 16 of the head)
-        float4 qr[HS4];
-#pragma unroll
-        for (int i = 0; i < HS4; ++i) qr[i] = qs4[(jw0 + jh) * HS4 + ((i + t) & (HS4 - 1))];
-        float m[HPL], l[HPL];
-        float acc[HPW][2];
-#pragma unroll
-        for (int jj = 0; jj < HPL; ++jj) {
-            m[jj] = -CUDART_INF_F;
-            l[jj] = 0.f;
-        }
-#pragma unroll
-        for (int j = 0; j < HPW; ++j) acc[j][0] = acc[j][1] = 0.f;
+        float *pT = pbuf + warp * (NHW * TPR + NHW);  // [head][row] probabilities of the stage, then [head] rescales
+        float m = -CUDART_INF_F, l = 0.f;              // head jw0 + qh: running max and sum
+        float4 acc[2];
+        acc[0] = acc[1] = make_float4(0.f, 0.f, 0.f, 0.f);
         int tc = wt0;
 #pragma unroll 1
         for (; tc < wt1; ++k) {
             const int s = k % STG;
             const int np = min(TP, wt1 - tc);
             const bool got = mbar_wait(&wbars[s], (uint32_t)(k / STG) & 1u, p.err);
-            // the ring's warps take one decision (the loop bounds are the ring's, so both get here)
-            if (ring_sync_or<RTH>(!got, rgi)) {
+            // the ring's warps take one decision (the loop bounds are the ring's, so all get here)
+            if (WPR > 1 ? ring_sync_or<RTH>(!got, rgi) : !got) {
                 ok = false;
                 break;
             }
-            const float4 *Ks = wring + (size_t)s * (kStageFloats / 4);
-            const float2 *Vs2 = reinterpret_cast<const float2 *>(Ks + (size_t)TP * HS4);
-            // scores of row t for heads jw0 + jh*HPL.., the row's 16-byte chunks in rotated order
-            const bool row_on = t < np;
-            float sc[HPL];
+            const float4 *K4 = wring + (size_t)s * (kStageFloats / 4);
+            const float4 *V4 = K4 + TPR * 16;
+            // partial scores w[i][r] over the lane's 8 dimensions (even and odd ones in the
+            // two halves of packed fp32 FMAs)
+            float w[NHW][4];
 #pragma unroll
-            for (int jj = 0; jj < HPL; ++jj) sc[jj] = 0.f;
-            if (row_on) {
-                const float4 *Kr = Ks + t * HS4;
-#if L2_ATTN_FFMA2
-                // even and odd dimensions in the two halves of packed fp32 FMAs
-                float2 s2 = make_float2(0.f, 0.f);
+            for (int r = 0; r < 4; ++r) {
+                const int t = 4 * rg + (r ^ rb);
+                const float4 ka = K4[t * 16 + dq], kb = K4[t * 16 + 8 + dq];
 #pragma unroll
-                for (int i = 0; i < HS4; ++i) {
-                    const float4 kv = Kr[(i + t) & (HS4 - 1)];
-                    s2 = ffma2(make_float2(qr[i].x, qr[i].y), make_float2(kv.x, kv.y), s2);
-                    s2 = ffma2(make_float2(qr[i].z, qr[i].w), make_float2(kv.z, kv.w), s2);
+                for (int i = 0; i < NHW; ++i) {
+                    float2 s2 = ffma2(make_float2(qa[i].x, qa[i].y), make_float2(ka.x, ka.y), make_float2(0.f, 0.f));
+                    s2 = ffma2(make_float2(qa[i].z, qa[i].w), make_float2(ka.z, ka.w), s2);
+                    s2 = ffma2(make_float2(qb[i].x, qb[i].y), make_float2(kb.x, kb.y), s2);
+                    s2 = ffma2(make_float2(qb[i].z, qb[i].w), make_float2(kb.z, kb.w), s2);
+                    w[i][r] = s2.x + s2.y;
                 }
-                sc[0] = s2.x + s2.y;
-#else
-#pragma unroll
-                for (int i = 0; i < HS4; ++i) sc[0] = dot4(qr[i], Kr[(i + t) & (HS4 - 1)], sc[0]);
-#endif
             }
 #pragma unroll
-            for (int jj = 0; jj < HPL; ++jj) {
-                const int hj = jw0 + jh * HPL + jj;
-                sc[jj] = row_on ? sc[jj] * p.scale : -CUDART_INF_F;
-                if (dbg && row_on && hj < nq) dbg[(size_t)hj * p.seq_len + tc + t] = sc[jj];
-                // online softmax over the stage's rows (the 16 lanes of this half)
-                float mx = sc[jj];
-#pragma unroll
-                for (int o = TPR / 2; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-                const float mn = fmaxf(m[jj], mx);  // finite: row 0 of the stage is valid
-                const float corr = expf(m[jj] - mn);
-                const float pe = expf(sc[jj] - mn);
-                float ps = pe;
-#pragma unroll
-                for (int o = TPR / 2; o > 0; o >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
-                l[jj] = l[jj] * corr + ps;
-                m[jj] = mn;
-                wp[t * HPW + jh * HPL + jj] = pe;
-                if (t == 0) wp[TPR * HPW + jh * HPL + jj] = corr;
+            for (int r = 0; r < 4; ++r) {
+                w[0][r] += __shfl_xor_sync(0xffffffffu, w[2][r], 4);
+                w[1][r] += __shfl_xor_sync(0xffffffffu, w[3][r], 4);
             }
+#pragma unroll
+            for (int r = 0; r < 4; ++r) w[0][r] += __shfl_xor_sync(0xffffffffu, w[1][r], 2);
+            float sc[2];
+#pragma unroll
+            for (int r = 0; r < 2; ++r) sc[r] = w[0][r] + __shfl_xor_sync(0xffffffffu, w[0][r + 2], 1);
+            // head jw0 + qh, rows r0, r0 + 1: scale, mask, export
+            const int hj = jw0 + qh;
+            float mx = -CUDART_INF_F;
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const int t = r0 + r;
+                sc[r] = t < np ? sc[r] * p.scale : -CUDART_INF_F;
+                if (dbg && t < np && hj < nq) dbg[(size_t)hj * p.seq_len + tc + t] = sc[r];
+                mx = fmaxf(mx, sc[r]);
+            }
+            // online softmax over the stage's rows: the 8 lanes of the head
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+            const float mn = fmaxf(m, mx);  // finite: row 0 of the stage is valid
+            const float corr = expf(m - mn);
+            const float pe0 = expf(sc[0] - mn), pe1 = expf(sc[1] - mn);
+            float ps = pe0 + pe1;
+            ps += __shfl_xor_sync(0xffffffffu, ps, 1);
+            ps += __shfl_xor_sync(0xffffffffu, ps, 8);
+            ps += __shfl_xor_sync(0xffffffffu, ps, 16);
+            l = l * corr + ps;
+            m = mn;
+            *reinterpret_cast<float2 *>(pT + qh * TPR + r0) = make_float2(pe0, pe1);
+            if (r0 == 0) pT[NHW * TPR + qh] = corr;
             __syncwarp();
-            // PV: dimensions 2 lane, 2 lane + 1 of the warp's heads
+            // PV: heads jw0 + 2 hg + j, dimensions 4 dg .. 4 dg + 3
 #pragma unroll
-            for (int j = 0; j < HPW; ++j) {
-                const float cr = wp[TPR * HPW + j];
-                acc[j][0] *= cr;
-                acc[j][1] *= cr;
+            for (int j = 0; j < 2; ++j) {
+                const float cr = pT[NHW * TPR + 2 * hg + j];
+                acc[j] = make_float4(acc[j].x * cr, acc[j].y * cr, acc[j].z * cr, acc[j].w * cr);
             }
-#pragma unroll 4
-            for (int tt = 0; tt < np; ++tt) {
-                const float2 v = Vs2[tt * 32 + lane];
-                const float2 pp = *reinterpret_cast<const float2 *>(wp + tt * HPW);  // the warp's two heads
-#if L2_ATTN_FFMA2
-                const float2 a0 = ffma2(make_float2(pp.x, pp.x), v, make_float2(acc[0][0], acc[0][1]));
-                const float2 a1 = ffma2(make_float2(pp.y, pp.y), v, make_float2(acc[1][0], acc[1][1]));
-                acc[0][0] = a0.x;
-                acc[0][1] = a0.y;
-                acc[1][0] = a1.x;
-                acc[1][1] = a1.y;
-#else
-                acc[0][0] = fmaf(pp.x, v.x, acc[0][0]);
-                acc[0][1] = fmaf(pp.x, v.y, acc[0][1]);
-                acc[1][0] = fmaf(pp.y, v.x, acc[1][0]);
-                acc[1][1] = fmaf(pp.y, v.y, acc[1][1]);
-#endif
+#pragma unroll
+            for (int tq = 0; tq < TPR / 4; ++tq) {
+                if (4 * tq >= np) break;
+                const float4 p0 = *reinterpret_cast<const float4 *>(pT + (2 * hg) * TPR + 4 * tq);
+                const float4 p1 = *reinterpret_cast<const float4 *>(pT + (2 * hg + 1) * TPR + 4 * tq);
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const int t = 4 * tq + r;
+                    if (t >= np) break;  // rows past the slice hold stale data
+                    const float4 v = V4[t * 16 + dg];
+                    const float a = r == 0 ? p0.x : r == 1 ? p0.y : r == 2 ? p0.z : p0.w;
+                    const float c = r == 0 ? p1.x : r == 1 ? p1.y : r == 2 ? p1.z : p1.w;
+                    float2 lo = ffma2(make_float2(a, a), make_float2(v.x, v.y), make_float2(acc[0].x, acc[0].y));
+                    float2 hi = ffma2(make_float2(a, a), make_float2(v.z, v.w), make_float2(acc[0].z, acc[0].w));
+                    acc[0] = make_float4(lo.x, lo.y, hi.x, hi.y);
+                    lo = ffma2(make_float2(c, c), make_float2(v.x, v.y), make_float2(acc[1].x, acc[1].y));
+                    hi = ffma2(make_float2(c, c), make_float2(v.z, v.w), make_float2(acc[1].z, acc[1].w));
+                    acc[1] = make_float4(lo.x, lo.y, hi.x, hi.y);
+                }
             }
             __syncwarp();
             tc += np;
-            ring_sync<RTH>(rgi);  // both warps are done with this stage's buffer
+            if (WPR > 1) ring_sync<RTH>(rgi);  // the ring's warps are done with this buffer
             if (ti < wt1) {
                 if (producer) fence_proxy_async_smem();
                 issue(s);
@@ -337,18 +346,12 @@ __global__ void __launch_bounds__(kNWA * 32) attn_kernel(const AttnParams p) {
                 (void)mbar_wait(&wbars[j % STG], (uint32_t)(j / STG) & 1u, p.err);
             if (lane == 0) flags[0] = 1;
         }
-        if (t == 0) {
-#pragma unroll
-            for (int jj = 0; jj < HPL; ++jj) {
-                mrg[(rgi * GQ + jw0 + jh * HPL + jj) * 2 + 0] = m[jj];
-                mrg[(rgi * GQ + jw0 + jh * HPL + jj) * 2 + 1] = l[jj];
-            }
+        if (r0 == 0) {
+            mrg[(rgi * GQ + jw0 + qh) * 2 + 0] = m;
+            mrg[(rgi * GQ + jw0 + qh) * 2 + 1] = l;
         }
-        float *accf = reinterpret_cast<float *>(accs);
 #pragma unroll
-        for (int j = 0; j < HPW; ++j)
-            *reinterpret_cast<float2 *>(accf + (size_t)(rgi * GQ + jw0 + j) * 64 + 2 * lane) =
-                make_float2(acc[j][0], acc[j][1]);
+        for (int j = 0; j < 2; ++j) accs[(size_t)(rgi * GQ + jw0 + 2 * hg + j) * 16 + dg] = acc[j];
     } else {
         // A row's 16-byte words c4, c4 + LP, .. (WPL of them) go to the LP lanes of its
         // lane group: with one or two query heads per KV head a lane keeps several
@@ -564,41 +567,97 @@ __global__ void __launch_bounds__(kNWA * 32) attn_kernel(const AttnParams p) {
     if (!flags[1]) return;
     __threadfence();
 
-    // last CTA of the group: merge the chunks in chunk order
+    // last CTA of the group: merge the chunks in chunk order.  With up to kMrgRegs
+    // chunks a thread loads every chunk's (max, sum) and accumulator words at once
+    // (one round trip); with more, the (max, sum) pairs are staged in shared
+    // memory first (the ring is free now: every copy has completed).
     if (!in_bounds(((size_t)b * H + h0 + nq - 1) * NC + n_active - 1, 1, p.ext->ws_rows, p.err)) return;
-    if (tid < nq) {
-        const int j = tid;
-        float M = -CUDART_INF_F;
-        for (int cc = 0; cc < n_active; ++cc)
-            M = fmaxf(M, __ldcg(p.ws_ml + (((size_t)b * H + h0 + j) * NC + cc) * 2));
-        float L = 0.f;
-        for (int cc = 0; cc < n_active; ++cc) {
-            const size_t sl = ((size_t)b * H + h0 + j) * NC + cc;
-            L += __ldcg(p.ws_ml + sl * 2 + 1) * expf(__ldcg(p.ws_ml + sl * 2) - M);
+    constexpr int kMrgRegs = 8;
+    if (n_active <= kMrgRegs) {
+        for (int idx = tid; idx < nq * hs4; idx += NT) {
+            const int j = idx / hs4, w4 = idx % hs4;
+            const size_t sl0 = ((size_t)b * H + h0 + j) * NC;
+            float2 ml[kMrgRegs];
+            float4 a[kMrgRegs];
+#pragma unroll
+            for (int cc = 0; cc < kMrgRegs; ++cc) {
+                if (cc < n_active) {
+                    ml[cc] = __ldcg(reinterpret_cast<const float2 *>(p.ws_ml) + sl0 + cc);
+                    a[cc] = __ldcg(reinterpret_cast<const float4 *>(p.ws_acc + (sl0 + cc) * hs) + w4);
+                }
+            }
+            float M = -CUDART_INF_F;
+#pragma unroll
+            for (int cc = 0; cc < kMrgRegs; ++cc)
+                if (cc < n_active) M = fmaxf(M, ml[cc].x);
+            float L = 0.f;
+            float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int cc = 0; cc < kMrgRegs; ++cc) {
+                if (cc < n_active) {
+                    const float e = expf(ml[cc].x - M);
+                    L += ml[cc].y * e;
+                    o.x += a[cc].x * e;
+                    o.y += a[cc].y * e;
+                    o.z += a[cc].z * e;
+                    o.w += a[cc].w * e;
+                }
+            }
+            const float inv = 1.0f / L;
+            o.x *= inv;
+            o.y *= inv;
+            o.z *= inv;
+            o.w *= inv;
+            if (in_bounds((size_t)b * p.dim + (size_t)(h0 + j) * hs + 4 * w4, 4, p.ext->xb, p.err))
+                reinterpret_cast<float4 *>(p.out + (size_t)b * p.dim + (size_t)(h0 + j) * hs)[w4] = o;
+            if (w4 == 0) {
+                fin[j * 2] = M;
+                fin[j * 2 + 1] = L;
+            }
         }
-        fin[j * 2] = M;
-        fin[j * 2 + 1] = L;
-    }
-    __syncthreads();
-    for (int idx = tid; idx < nq * hs4; idx += NT) {
-        const int j = idx / hs4, w4 = idx % hs4;
-        const float M = fin[j * 2], inv = 1.0f / fin[j * 2 + 1];
-        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int cc = 0; cc < n_active; ++cc) {
-            const size_t sl = ((size_t)b * H + h0 + j) * NC + cc;
-            const float e = expf(__ldcg(p.ws_ml + sl * 2) - M);
-            const float4 a = __ldcg(reinterpret_cast<const float4 *>(p.ws_acc + sl * hs) + w4);
-            o.x += a.x * e;
-            o.y += a.y * e;
-            o.z += a.z * e;
-            o.w += a.w * e;
+        if (dbg) __syncthreads();
+    } else {
+        float *cml = reinterpret_cast<float *>(ring);  // [nq][n_active][2]
+        for (int i = tid; i < nq * n_active; i += NT) {
+            const size_t sl = ((size_t)b * H + h0 + i / n_active) * NC + i % n_active;
+            const float2 ml = __ldcg(reinterpret_cast<const float2 *>(p.ws_ml + sl * 2));
+            cml[2 * i] = ml.x;
+            cml[2 * i + 1] = ml.y;
         }
-        o.x *= inv;
-        o.y *= inv;
-        o.z *= inv;
-        o.w *= inv;
-        if (in_bounds((size_t)b * p.dim + (size_t)(h0 + j) * hs + 4 * w4, 4, p.ext->xb, p.err))
-            reinterpret_cast<float4 *>(p.out + (size_t)b * p.dim + (size_t)(h0 + j) * hs)[w4] = o;
+        __syncthreads();
+        if (tid < nq) {
+            const float *c = cml + (size_t)tid * n_active * 2;
+            float M = -CUDART_INF_F;
+            for (int cc = 0; cc < n_active; ++cc) M = fmaxf(M, c[2 * cc]);
+            float L = 0.f;
+            for (int cc = 0; cc < n_active; ++cc) L += c[2 * cc + 1] * expf(c[2 * cc] - M);
+            fin[tid * 2] = M;
+            fin[tid * 2 + 1] = L;
+        }
+        __syncthreads();
+        for (int i = tid; i < nq * n_active; i += NT) cml[2 * i] = expf(cml[2 * i] - fin[(i / n_active) * 2]);
+        __syncthreads();
+        for (int idx = tid; idx < nq * hs4; idx += NT) {
+            const int j = idx / hs4, w4 = idx % hs4;
+            const float inv = 1.0f / fin[j * 2 + 1];
+            const float *e = cml + (size_t)j * n_active * 2;
+            const float4 *src = reinterpret_cast<const float4 *>(p.ws_acc + ((size_t)b * H + h0 + j) * NC * hs) + w4;
+            float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+            for (int cc = 0; cc < n_active; ++cc) {
+                const float4 a = __ldcg(src + (size_t)cc * hs4);
+                o.x += a.x * e[2 * cc];
+                o.y += a.y * e[2 * cc];
+                o.z += a.z * e[2 * cc];
+                o.w += a.w * e[2 * cc];
+            }
+            o.x *= inv;
+            o.y *= inv;
+            o.z *= inv;
+            o.w *= inv;
+            if (in_bounds((size_t)b * p.dim + (size_t)(h0 + j) * hs + 4 * w4, 4, p.ext->xb, p.err))
+                reinterpret_cast<float4 *>(p.out + (size_t)b * p.dim + (size_t)(h0 + j) * hs)[w4] = o;
+        }
     }
     if (dbg) {
         for (int idx = tid; idx < nq * P; idx += NT) {
@@ -613,7 +672,7 @@ __global__ void __launch_bounds__(kNWA * 32) attn_kernel(const AttnParams p) {
 // ---------------------------------------------------------------- host side
 
 namespace {
-typedef void (*AttnFn)(const AttnParams);
+typedef void (*AttnFn)(const AttnParams);  // (the kernels take it as a grid constant)
 
 template <int LP, int GQ>
 AttnFn pick2() {
@@ -667,11 +726,13 @@ AttnLaunch attn_plan(int head_size, int n_heads, int n_kv_heads) {
 #endif
     a.rl = L2_ATTN_ROW_LANE && head_size == 64 && (a.gq == 4 || a.gq == 8) && kStageFloats == 2 * 16 * 64;
     a.threads = kNWA * 32;
-    const int wpr = a.rl ? a.gq / 2 : 1, nrg = kNWA / wpr;  // warps per ring, rings per CTA (as in the kernel)
+    const int wpr = a.rl ? a.gq / 4 : 1, nrg = kNWA / wpr;  // warps per ring, rings per CTA (as in the kernel)
     const int stg = a.rl ? kAttStagesRL : kAttStages;
     const size_t hdr = (8 * nrg * stg + 16 + 4 * (nrg * a.gq * 2 + a.gq * 2) + 127) / 128 * 128;
     a.smem = hdr + (size_t)nrg * stg * kStageFloats * 4 + (size_t)nrg * a.gq * hs4 * 16;
-    if (a.rl) a.smem += (size_t)a.gq * head_size * 4 + (size_t)kNWA * 17 * (a.gq / wpr) * 4;  // query vectors, probabilities
+    if (a.rl) a.smem += (size_t)kNWA * (16 + 1) * 4 * 4;  // probabilities [head][row] and rescales per warp
+    // the last CTA stages (max, sum) of every chunk and head in its ring
+    a.max_chunks = nrg * stg * kStageFloats / (2 * a.gq);
     a.ok = a.lp <= 32 && a.gq <= 8 && head_size % 4 == 0 && 2 * head_size <= kStageFloats;
     return a;
 }

@@ -1107,6 +1107,7 @@ int l2_create(const L2Config *config, const L2Weights *weights, int max_batch, u
     const size_t cache = (size_t)max_batch * L * p.n_kv_heads * S * hs;
     c->attn_chunks = attn_chunks_for(c, 1);
     if (c->max_rows > 1 && ceil_div(p.seq_len, kMinChunk) > c->attn_chunks) c->attn_chunks = ceil_div(p.seq_len, kMinChunk);
+    c->attn_chunks = std::min(c->attn_chunks, c->attn.max_chunks);
     const size_t ws = B * p.n_heads * (size_t)c->attn_chunks;
     if ((rc = alloc_n(c, &c->x, B * p.dim, "x")) || (rc = alloc_n(c, &c->xb, B * p.dim, "xb")) ||
         (rc = alloc_n(c, &c->q, B * p.dim, "q")) || (rc = alloc_n(c, &c->hb, B * p.hidden_dim, "hb")) ||

@@ -70,6 +70,7 @@ struct AttnLaunch {
     int rl;       // 1: row-per-lane layout (head size 64, 4 or 8 heads per KV head)
     int threads;
     size_t smem;
+    int max_chunks;  // CTAs per KV head the last CTA's merge can stage in its ring
     bool ok;      // this head size / grouping is supported
 };
 AttnLaunch attn_plan(int head_size, int n_heads, int n_kv_heads);
