@@ -83,6 +83,11 @@ constexpr int kMaxAccs = 4;                           // accumulators in tensor 
 #define L2_TC_DRAIN 4
 #endif
 constexpr int kDrain = L2_TC_DRAIN;
+// RMSNorm modes: from this many sequences on, the partial sums of squares arrive by one
+// bulk copy; below it each epilogue warp loads its few sequences' sums directly.
+#ifndef L2_TC_SS_COPY_MIN_ROWS
+#define L2_TC_SS_COPY_MIN_ROWS 32
+#endif
 constexpr size_t kSmemLimit = 227 * 1024;
 
 // A stage covers 64 K columns.  fp32 weights (WT 0): two 32-column halves h,
@@ -110,6 +115,7 @@ struct TcFixed {
     uint64_t acc_full[kMaxAccs];   // accumulator complete
     uint64_t acc_free[kMaxAccs];   // accumulator read out
     uint64_t fin;
+    uint64_t ssbar;  // the partial sums of squares copied into ys (RMSNorm modes)
     uint32_t tmem;
     int abort;
     int last_w[2];
@@ -379,6 +385,12 @@ __global__ void __launch_bounds__(kTT, 1) l2dec_matvec_tc_kernel(const __grid_co
                                      : (long long)blockIdx.x * T / G;
     const long long s_end = CS > 1 ? (long long)(blockIdx.x / CS) * KT + (long long)KT * (blockIdx.x % CS + 1) / CS
                                    : (long long)(blockIdx.x + 1) * T / G;
+    // RMSNorm modes: the residual kernels' partial sums of squares ss_part[parts][B] come
+    // in one bulk copy into ys, which the epilogue needs only from its first drain on.
+    // Loaded one sequence per round trip per warp, they queued behind the ring's copies
+    // for tens of microseconds at 64 sequences while the accumulators waited to be drained.
+    const uint32_t ss_bytes = (uint32_t)(((size_t)p.ss_parts * B * 4 + 15) & ~(size_t)15);
+    const bool ss_copy = B >= L2_TC_SS_COPY_MIN_ROWS && MODE != GEMV_RESID && ss_bytes <= (uint32_t)ys_bytes(BP) && (size_t)p.ss_parts * B + 3 <= (size_t)kMaxParts * B;
     // the CTA holding stage x of the sequence
     auto cta_of = [&](long long x) { return (int)(((x + 1) * G + T - 1) / T - 1); };
     // the next segment (one tile's part of the CTA's range) at sequence position sq
@@ -408,6 +420,7 @@ __global__ void __launch_bounds__(kTT, 1) l2dec_matvec_tc_kernel(const __grid_co
             mbar_init(&fx.acc_free[i], kRoleThreads);
         }
         mbar_init(&fx.fin, 1);
+        mbar_init(&fx.ssbar, 1);
         fence_barrier_init();
         fx.abort = 0;
         fx.part_tile[0] = fx.part_tile[1] = -1;
@@ -592,6 +605,12 @@ __global__ void __launch_bounds__(kTT, 1) l2dec_matvec_tc_kernel(const __grid_co
             __syncwarp();
         }
         pdl_wait();  // the inputs come from the previous kernel
+        const bool ss_ok = ss_copy && in_bounds(0, ss_bytes / 4, p.ext->ss_part, p.err);
+        if (ss_copy && elect_one()) {
+            mbar_arrive_expect_tx(&fx.ssbar, ss_ok ? ss_bytes : 0u);
+            if (ss_ok) bulk_g2s_nohint(ys, p.ss_part, ss_bytes, &fx.ssbar);
+        }
+        __syncwarp();
         for (long long sq = s_begin; sq < s_end && !stop;) {
             int tile, k0, k1, m, r0, wrow;
             segment(sq, tile, k0, k1);
@@ -613,6 +632,7 @@ __global__ void __launch_bounds__(kTT, 1) l2dec_matvec_tc_kernel(const __grid_co
         if (stop)  // the copies still in flight land before the CTA's memory goes
             for (long long j = nl > NS ? nl - NS : 0; j < nl; ++j)
                 (void)mbar_wait(&fx.full[j % NS], (uint32_t)((j / NS) & 1), p.err);
+        if (ss_copy) (void)mbar_wait(&fx.ssbar, 0u, p.err);
     } else if (warp == 1) {
         // ---------------- MMA issuer (whole warp, one lane issues) ----------------
         const uint32_t idesc2 = idesc_tf32(kTM, 2 * BP), idesc1 = idesc_tf32(kTM, BP), idesc3 = idesc_bf16(kTM, 3 * BP);
@@ -765,7 +785,15 @@ __global__ void __launch_bounds__(kTT, 1) l2dec_matvec_tc_kernel(const __grid_co
                 fx.pos[b] = p.step->pos[b];
                 fx.slot[b] = (unsigned char)p.step->slot[b];  // slots < kMaxBatch
             }
-        if (MODE != GEMV_RESID) {
+        if (ss_copy) {
+            // the copy in ys: thread b adds sequence b's parts in order (conflict-free columns)
+            if (!mbar_wait(&fx.ssbar, 0u, p.err)) set_abort(fx);
+            for (int b = et; b < B; b += kRoleThreads) {
+                float ss = 0.f;
+                for (int i = 0; i < p.ss_parts; ++i) ss += ys[(size_t)i * B + b];
+                fx.inv[b] = 1.0f / sqrtf(ss / (float)n + 1e-5f);
+            }
+        } else if (MODE != GEMV_RESID) {
             for (int b = et >> 5; b < B; b += kRoleThreads / 32) {
                 float ss = 0.f;
                 for (int i = lane; i < p.ss_parts; i += 32) ss += __ldcg(p.ss_part + (size_t)i * B + b);
