@@ -85,6 +85,10 @@ constexpr int kMaxAccs = 4;                           // accumulators in tensor 
 constexpr int kDrain = L2_TC_DRAIN;
 // RMSNorm modes: from this many sequences on, the partial sums of squares arrive by one
 // bulk copy; below it each epilogue warp loads its few sequences' sums directly.
+// Partial tiles: the last CTA of a tile fetches the parts by bulk copies (1) or loads (0).
+#ifndef L2_TC_MERGE_COPY
+#define L2_TC_MERGE_COPY 1
+#endif
 #ifndef L2_TC_SS_COPY_MIN_ROWS
 #define L2_TC_SS_COPY_MIN_ROWS 32
 #endif
@@ -116,6 +120,7 @@ struct TcFixed {
     uint64_t acc_free[kMaxAccs];   // accumulator read out
     uint64_t fin;
     uint64_t ssbar;  // the partial sums of squares copied into ys (RMSNorm modes)
+    uint64_t mrg;    // the parts of a partial tile copied into the ring (its last CTA)
     uint32_t tmem;
     int abort;
     int last_w[2];
@@ -421,6 +426,7 @@ __global__ void __launch_bounds__(kTT, 1) l2dec_matvec_tc_kernel(const __grid_co
         }
         mbar_init(&fx.fin, 1);
         mbar_init(&fx.ssbar, 1);
+        mbar_init(&fx.mrg, 1);
         fence_barrier_init();
         fx.abort = 0;
         fx.part_tile[0] = fx.part_tile[1] = -1;
@@ -919,54 +925,98 @@ __global__ void __launch_bounds__(kTT, 1) l2dec_matvec_tc_kernel(const __grid_co
         __threadfence();
     }
     __syncthreads();
+    int mphase = 0;  // phases of fx.mrg used so far
     for (int w = 0; w < 2; ++w) {
         if (!fx.last_w[w]) continue;
         const int t = fx.part_tile[w];
         const int c0 = cta_of((long long)t * KT), c1 = cta_of((long long)(t + 1) * KT - 1);
-        // 4 rows of one sequence per float4, this thread's v = tid + 384 i (2 at a time);
-        // up to 8 parts' loads in flight per round trip; parts added in K order
-        constexpr int kV = 2, kPG = 8;
-        const int nv = B * (kTM / 4);
-        for (int i0 = 0; tid + kTT * i0 < nv; i0 += kV) {
-            float4 acc[kV];
-#pragma unroll
-            for (int i = 0; i < kV; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int cb = c0; cb <= c1; cb += kPG) {
-                float4 part[kPG][kV];
-#pragma unroll
-                for (int u = 0; u < kPG; ++u) {
-                    const int cc = min(cb + u, c1);
+        const int nparts = c1 - c0 + 1;
+        const uint32_t pbytes = (uint32_t)B * kTM * 4;  // a part: [B][128] floats
+        if (L2_TC_MERGE_COPY && (size_t)nparts * pbytes <= (size_t)NS * SB) {
+            // Every part with one bulk copy into the ring (free now): one round trip
+            // instead of a few rounds of loads per part; added in K order below.
+            if (tid == 0) {
+                bool okp = true;
+                for (int cc = c0; cc <= c1; ++cc) {
                     const int wh = (long long)cc * T / G >= (long long)t * KT ? 0 : 1;
-                    const bool cc_ok = in_bounds(((size_t)cc * 2 + wh) * kTM * BP, (size_t)kTM * BP, p.ext->tc_ws, p.err);
-                    const float4 *src = reinterpret_cast<const float4 *>(tp.ws + (cc_ok ? ((size_t)cc * 2 + wh) * kTM * BP : 0));
-#pragma unroll
-                    for (int i = 0; i < kV; ++i) {
-                        const int v = tid + kTT * (i0 + i);
-                        if (v < nv && cb + u <= c1) part[u][i] = __ldcg(src + v);
-                    }
+                    okp = okp && in_bounds(((size_t)cc * 2 + wh) * kTM * BP, (size_t)B * kTM, p.ext->tc_ws, p.err);
                 }
-#pragma unroll
-                for (int u = 0; u < kPG; ++u)
-#pragma unroll
-                    for (int i = 0; i < kV; ++i) {
-                        const int v = tid + kTT * (i0 + i);
-                        if (v < nv && cb + u <= c1) {
-                            acc[i].x += part[u][i].x;
-                            acc[i].y += part[u][i].y;
-                            acc[i].z += part[u][i].z;
-                            acc[i].w += part[u][i].w;
-                        }
+                fence_proxy_async_all();  // the parts are other CTAs' ordinary stores; the ring was read by this CTA
+                mbar_arrive_expect_tx(&fx.mrg, okp ? (uint32_t)nparts * pbytes : 0u);
+                if (okp)
+                    for (int cc = c0; cc <= c1; ++cc) {
+                        const int wh = (long long)cc * T / G >= (long long)t * KT ? 0 : 1;
+                        bulk_g2s_nohint(ring + (size_t)(cc - c0) * pbytes, tp.ws + ((size_t)cc * 2 + wh) * kTM * BP, pbytes,
+                                        &fx.mrg);
                     }
             }
+            const bool okw = mbar_wait(&fx.mrg, (uint32_t)(mphase & 1), p.err);
+            ++mphase;
+            if (okw) {
+                const float4 *P4 = reinterpret_cast<const float4 *>(ring);
+                const int nv = B * (kTM / 4);
+                for (int v = tid; v < nv; v += kTT) {
+                    float4 a = P4[v];
+                    for (int k = 1; k < nparts; ++k) {
+                        const float4 b = P4[(size_t)k * nv + v];
+                        a.x += b.x;
+                        a.y += b.y;
+                        a.z += b.z;
+                        a.w += b.w;
+                    }
+                    const int c = v / (kTM / 4), r = (v - c * (kTM / 4)) * 4;
+                    ys[r * YS + c] = a.x;
+                    ys[(r + 1) * YS + c] = a.y;
+                    ys[(r + 2) * YS + c] = a.z;
+                    ys[(r + 3) * YS + c] = a.w;
+                }
+            }
+        } else {
+            // 4 rows of one sequence per float4, this thread's v = tid + 384 i (2 at a time);
+            // up to 8 parts' loads in flight per round trip; parts added in K order
+            constexpr int kV = 2, kPG = 8;
+            const int nv = B * (kTM / 4);
+            for (int i0 = 0; tid + kTT * i0 < nv; i0 += kV) {
+                float4 acc[kV];
 #pragma unroll
-            for (int i = 0; i < kV; ++i) {
-                const int v = tid + kTT * (i0 + i);
-                if (v >= nv) continue;
-                const int c = v / (kTM / 4), r = (v - c * (kTM / 4)) * 4;
-                ys[r * YS + c] = acc[i].x;
-                ys[(r + 1) * YS + c] = acc[i].y;
-                ys[(r + 2) * YS + c] = acc[i].z;
-                ys[(r + 3) * YS + c] = acc[i].w;
+                for (int i = 0; i < kV; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int cb = c0; cb <= c1; cb += kPG) {
+                    float4 part[kPG][kV];
+#pragma unroll
+                    for (int u = 0; u < kPG; ++u) {
+                        const int cc = min(cb + u, c1);
+                        const int wh = (long long)cc * T / G >= (long long)t * KT ? 0 : 1;
+                        const bool cc_ok = in_bounds(((size_t)cc * 2 + wh) * kTM * BP, (size_t)kTM * BP, p.ext->tc_ws, p.err);
+                        const float4 *src = reinterpret_cast<const float4 *>(tp.ws + (cc_ok ? ((size_t)cc * 2 + wh) * kTM * BP : 0));
+#pragma unroll
+                        for (int i = 0; i < kV; ++i) {
+                            const int v = tid + kTT * (i0 + i);
+                            if (v < nv && cb + u <= c1) part[u][i] = __ldcg(src + v);
+                        }
+                    }
+#pragma unroll
+                    for (int u = 0; u < kPG; ++u)
+#pragma unroll
+                        for (int i = 0; i < kV; ++i) {
+                            const int v = tid + kTT * (i0 + i);
+                            if (v < nv && cb + u <= c1) {
+                                acc[i].x += part[u][i].x;
+                                acc[i].y += part[u][i].y;
+                                acc[i].z += part[u][i].z;
+                                acc[i].w += part[u][i].w;
+                            }
+                        }
+                }
+#pragma unroll
+                for (int i = 0; i < kV; ++i) {
+                    const int v = tid + kTT * (i0 + i);
+                    if (v >= nv) continue;
+                    const int c = v / (kTM / 4), r = (v - c * (kTM / 4)) * 4;
+                    ys[r * YS + c] = acc[i].x;
+                    ys[(r + 1) * YS + c] = acc[i].y;
+                    ys[(r + 2) * YS + c] = acc[i].z;
+                    ys[(r + 3) * YS + c] = acc[i].w;
+                }
             }
         }
         if (tid == 0) tp.tickets[t] = 0u;
