@@ -148,13 +148,17 @@ __global__ void __launch_bounds__(kNWA * 32) attn_kernel(const AttnParams p) {
     if (n_active > p.n_chunks) n_active = p.n_chunks;
     if (n_active > P) n_active = P;
     if (n_active < 1) n_active = 1;
-    if (c >= n_active) return;  // too few positions for this CTA to join
+    // With a cluster and several chunks every CTA of the cluster takes part in the
+    // merge (those past n_active with no positions); otherwise they have nothing to do.
+    const bool in_cluster = p.cluster > 1 && n_active > 1;
+    if (c >= n_active && !in_cluster) return;  // too few positions for this CTA to join
 
     const int H = p.n_heads, KV = p.n_kv_heads;
     const int h0 = (g * H + KV - 1) / KV, h1 = ((g + 1) * H + KV - 1) / KV;
     const int nq = h1 - h0;
 
-    const int t0 = (int)((long long)c * P / n_active), t1 = (int)((long long)(c + 1) * P / n_active);
+    // (an idle cluster member, c >= n_active, gets the empty range [P, P))
+    const int t0 = (int)((long long)min(c, n_active) * P / n_active), t1 = (int)((long long)min(c + 1, n_active) * P / n_active);
     const int rgi = warp / WPR, wsub = warp % WPR;  // this warp's ring, and its place in it
     const int wt0 = t0 + (int)((long long)(t1 - t0) * rgi / NRG);
     const int wt1 = t0 + (int)((long long)(t1 - t0) * (rgi + 1) / NRG);
@@ -513,6 +517,81 @@ __global__ void __launch_bounds__(kNWA * 32) attn_kernel(const AttnParams p) {
 
     // merge the warps in warp order and publish this CTA's partial
     const int NC = p.n_chunks;
+    if (in_cluster) {
+        // Thread-block cluster of the (row, KV head)'s n_chunks CTAs, rank = chunk: each
+        // CTA leaves its partial (max, sum and accumulator per head, merged over its
+        // rings) in its ring buffer (free now); after a cluster barrier rank 0 reads them
+        // through distributed shared memory in chunk order and writes the output; a
+        // second barrier keeps every partial alive until then.  No global workspace,
+        // fence or ticket: those round trips took several microseconds per launch.
+        float *cp = reinterpret_cast<float *>(ring);  // [GQ][2] (max, sum) in the first 64 bytes,
+        float4 *ca = reinterpret_cast<float4 *>(cp + 16);  // then [GQ][hs] accumulators (16-byte aligned)
+        static_assert(2 * GQ <= 16, "(max, sum) pairs fit 64 bytes");
+        for (int idx = tid; idx < nq * hs4; idx += NT) {
+            const int j = idx / hs4, w4 = idx % hs4;
+            float mm = -CUDART_INF_F, ll = 0.f;
+            float4 aa = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (!gave_up)
+                for (int w = 0; w < NRG; ++w)
+                    merge_state(mm, ll, aa, mrg[(w * GQ + j) * 2], mrg[(w * GQ + j) * 2 + 1],
+                                accs[(size_t)(w * GQ + j) * hs4 + w4]);
+            ca[(size_t)j * hs4 + w4] = aa;
+            if (w4 == 0) {
+                cp[2 * j] = mm;
+                cp[2 * j + 1] = ll;
+            }
+        }
+        cluster_sync_all();
+        if (c == 0) {
+            constexpr int kMaxCl = 8;
+            for (int idx = tid; idx < nq * hs4; idx += NT) {
+                const int j = idx / hs4, w4 = idx % hs4;
+                float2 ml[kMaxCl];
+                float4 a[kMaxCl];
+#pragma unroll
+                for (int r = 0; r < kMaxCl; ++r)
+                    if (r < n_active) {
+                        ml[r] = ld_dsmem2(dsmem_addr(cp + 2 * j, (uint32_t)r));
+                        a[r] = ld_dsmem4(dsmem_addr(ca + (size_t)j * hs4 + w4, (uint32_t)r));
+                    }
+                float M = -CUDART_INF_F;
+#pragma unroll
+                for (int r = 0; r < kMaxCl; ++r)
+                    if (r < n_active) M = fmaxf(M, ml[r].x);
+                float L = 0.f;
+                float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int r = 0; r < kMaxCl; ++r)
+                    if (r < n_active) {
+                        const float e = expf(ml[r].x - M);
+                        L += ml[r].y * e;
+                        o.x += a[r].x * e;
+                        o.y += a[r].y * e;
+                        o.z += a[r].z * e;
+                        o.w += a[r].w * e;
+                    }
+                const float inv = 1.0f / L;
+                if (in_bounds((size_t)b * p.dim + (size_t)(h0 + j) * hs + 4 * w4, 4, p.ext->xb, p.err))
+                    reinterpret_cast<float4 *>(p.out + (size_t)b * p.dim + (size_t)(h0 + j) * hs)[w4] =
+                        make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
+                if (w4 == 0) {
+                    fin[j * 2] = M;
+                    fin[j * 2 + 1] = L;
+                }
+            }
+            if (dbg) {
+                __syncthreads();
+                // the scores of every chunk (global, ordered before by the cluster barrier)
+                for (int idx = tid; idx < nq * P; idx += NT) {
+                    const int j = idx / P, t = idx % P;
+                    float *cell = dbg + (size_t)j * p.seq_len + t;
+                    *cell = expf(__ldcg(cell) - fin[j * 2]) / fin[j * 2 + 1];
+                }
+            }
+        }
+        cluster_sync_all();
+        return;
+    }
     if (n_active == 1) {
         if (gave_up) return;
         // The only chunk: normalise and write the output directly.
@@ -747,6 +826,28 @@ int attn_ctas_per_sm(const AttnLaunch &a) {
     return n < 1 ? 1 : n;
 }
 
+bool attn_cluster_fits(const AttnLaunch &a, int n_chunks, int clusters) {
+    AttnFn fn = pick(a.lp, a.gq, a.rl);
+    if (!fn || n_chunks < 2 || n_chunks > 8) return false;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(n_chunks, clusters, 1);
+    cfg.blockDim = dim3(a.threads);
+    cfg.dynamicSmemBytes = a.smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)n_chunks;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return n >= clusters;
+}
+
 cudaError_t attn_init() {
     static const int lps[] = {1, 2, 4, 8, 16, 32};
     static const int gqs[] = {1, 2, 4, 8};
@@ -770,11 +871,15 @@ cudaError_t launch_attn(const AttnLaunch &a, const AttnParams &p, int batch, cud
     cfg.blockDim = dim3(a.threads);
     cfg.dynamicSmemBytes = a.smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = (unsigned)(p.cluster > 1 ? p.cluster : 1);
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = p.cluster > 1 ? 2 : 1;
     void *args[] = {const_cast<AttnParams *>(&p)};
     return cudaLaunchKernelExC(&cfg, reinterpret_cast<void *>(fn), args);
 }

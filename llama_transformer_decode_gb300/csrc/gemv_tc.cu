@@ -304,24 +304,6 @@ __device__ __forceinline__ bool epi_sync_or(bool v) {
 // in another CTA of the cluster, a load through it, and a barrier of every
 // thread of the cluster (release / acquire: shared-memory writes before it are
 // visible to the other CTAs' reads after it).
-__device__ __forceinline__ uint32_t cluster_rank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-__device__ __forceinline__ uint32_t dsmem_addr(const void *p, uint32_t rank) {
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
-    return r;
-}
-__device__ __forceinline__ float ld_dsmem(uint32_t addr) {
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-    return v;
-}
-__device__ __forceinline__ void cluster_sync_all() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
 
 __device__ __forceinline__ bool aborted(const TcFixed &fx) { return *reinterpret_cast<const volatile int *>(&fx.abort) != 0; }
 __device__ __forceinline__ void set_abort(TcFixed &fx) { *reinterpret_cast<volatile int *>(&fx.abort) = 1; }

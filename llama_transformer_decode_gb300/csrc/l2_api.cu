@@ -128,6 +128,7 @@ struct l2_ctx {
     AttnLaunch attn{};
     int attn_chunks = 1;
     int attn_per_sm = 1;  // attention CTAs resident per SM
+    int attn_cluster = 0;  // steps of one row: chunks per KV head merged in a cluster (0: tickets)
     GemvPlan plan_qkv{}, plan_wo{}, plan_w13{}, plan_w2{}, plan_cls{};
     bool persist = false;  // batch-1 steps run as the persistent step kernel
     int persist_gq = 1;
@@ -389,6 +390,7 @@ AttnParams attn_params(const l2_ctx *c, int layer, int batch) {
     }
     if (nc > c->attn_chunks) nc = c->attn_chunks;
     a.n_chunks = nc;
+    a.cluster = batch == 1 && c->attn_cluster == nc ? nc : 0;
     a.min_chunk = kMinChunk;
     a.scale = (float)(1.0 / std::sqrt((double)c->head_size));
     a.ext = c->ext_dev;
@@ -1108,6 +1110,15 @@ int l2_create(const L2Config *config, const L2Weights *weights, int max_batch, u
     c->attn_chunks = attn_chunks_for(c, 1);
     if (c->max_rows > 1 && ceil_div(p.seq_len, kMinChunk) > c->attn_chunks) c->attn_chunks = ceil_div(p.seq_len, kMinChunk);
     c->attn_chunks = std::min(c->attn_chunks, c->attn.max_chunks);
+    // Steps of one row merge their attention chunks through distributed shared memory
+    // when the chunks of every KV head fit one cluster and all clusters are resident.
+#ifndef L2_ATTN_CLUSTER
+#define L2_ATTN_CLUSTER 1
+#endif
+    {
+        const int nc1 = std::min(attn_chunks_for(c, 1), c->attn_chunks);
+        c->attn_cluster = L2_ATTN_CLUSTER && attn_cluster_fits(c->attn, nc1, p.n_kv_heads) ? nc1 : 0;
+    }
     const size_t ws = B * p.n_heads * (size_t)c->attn_chunks;
     if ((rc = alloc_n(c, &c->x, B * p.dim, "x")) || (rc = alloc_n(c, &c->xb, B * p.dim, "xb")) ||
         (rc = alloc_n(c, &c->q, B * p.dim, "q")) || (rc = alloc_n(c, &c->hb, B * p.hidden_dim, "hb")) ||

@@ -81,6 +81,9 @@ cudaError_t launch_attn_prefill(const AttnParams &p, int rows, cudaStream_t stre
 cudaError_t attn_init();
 // Attention CTAs that can be resident on one SM (registers, shared memory, threads).
 int attn_ctas_per_sm(const AttnLaunch &a);
+// Whether `clusters` thread-block clusters of n_chunks attention CTAs (2..8) can all
+// be resident at once.
+bool attn_cluster_fits(const AttnLaunch &a, int n_chunks, int clusters);
 cudaError_t launch_attn(const AttnLaunch &a, const AttnParams &p, int batch, cudaStream_t stream, bool pdl);
 
 }  // namespace l2

@@ -173,6 +173,8 @@ struct AttnParams {
     int min_chunk;  // fewest positions a CTA takes before more CTAs join
     int capacity;   // batches: CTAs resident at once; the chunk grows so the
                     // positions of all slots fill about that many (0: fixed chunk)
+    int cluster;    // > 1: the n_chunks CTAs of a (row, KV head) form one thread-block
+                    // cluster and merge their chunks through distributed shared memory
     float scale;    // 1 / sqrt(head_size)
     const Extents *ext;  // buffer sizes (read only by the bounds-checked build)
 };
