@@ -66,10 +66,21 @@ extern "C" {
  * bytes of fp32.  Products and sums stay fp32 (each bf16 weight widens
  * exactly), as do the embedding table, the RMSNorm gains, activations and the
  * KV cache; the results are those of the model with bf16-rounded matrices.
- * Batch-1 decode only: max_batch must be 1 (else L2_EINVAL), prompts are fed
- * one token per step, L2_FLAG_PERSIST is refused, and dim and hidden_dim must
- * be divisible by 8. */
+ * Steps of one row read the bf16 words on the CUDA cores; batched steps and
+ * prompt chunks of 16 or more rows multiply them on the tensor cores
+ * (kind::f16, each fp32 input split exactly into three bf16 parts).  With
+ * L2_FLAG_NO_TC max_batch must be 1 (else L2_EINVAL) and prompts are fed one
+ * token per step; L2_FLAG_PERSIST is refused; dim and hidden_dim must be
+ * divisible by 8. */
 #define L2_FLAG_BF16_WEIGHTS 0x20u
+/* Batch-1 steps of a model whose weights take at most 4 MiB (they stay in L2,
+ * so a step of one kernel per matrix product costs its kernel boundaries, not
+ * its bytes) normally run as ONE kernel of one thread block that does every
+ * phase of the step with block-wide barriers between them (l2_kernels_per_step
+ * then reports 1; with L2_FLAG_DEBUG it exports the probabilities too).  This
+ * flag keeps such models on the graph of per-matrix kernels.  Larger models,
+ * L2_FLAG_PERSIST and L2_FLAG_BF16_WEIGHTS always use the other paths. */
+#define L2_FLAG_NO_ONE_CTA 0x40u
 
 /* Model shape: the pages' Config struct ("run.c", Config; walkthrough §2).
  * head_size = dim / n_heads, kv_dim = dim * n_kv_heads / n_heads. */

@@ -17,6 +17,7 @@ from ._native import EXPORTS, WEIGHT_FIELDS, L2Config, L2Weights, build  # noqa:
 L2_OK, L2_EINVAL, L2_ESTATE, L2_ENOMEM, L2_ECUDA, L2_EDEVICE, L2_ETIMEOUT = 0, -1, -2, -3, -4, -5, -6
 L2_FLAG_DEBUG, L2_FLAG_NO_GRAPH, L2_FLAG_NO_PDL, L2_FLAG_PERSIST, L2_FLAG_NO_TC = 0x1, 0x2, 0x4, 0x8, 0x10
 L2_FLAG_BF16_WEIGHTS = 0x20
+L2_FLAG_NO_ONE_CTA = 0x40
 
 OPS = {"qkv": 0, "attention": 1, "wo": 2, "w13": 3, "w2": 4, "cls": 5}
 

@@ -15,8 +15,8 @@ LIB = os.path.join(BUILD, "libl2decode.so")
 # the bounds-checked build (every kernel index checked; see l2_debug_bounds_checked)
 BUILD_CHECKED = os.path.join(BUILD, "checked")
 LIB_CHECKED = os.path.join(BUILD, "libl2decode_checked.so")
-SOURCES = ("gemv.cu", "gemv_batched.cu", "gemv_tc.cu", "attention.cu", "attn_prefill.cu", "step_kernel.cu", "sample.cu",
-           "l2_api.cu")
+SOURCES = ("gemv.cu", "gemv_batched.cu", "gemv_tc.cu", "attention.cu", "attn_prefill.cu", "step_kernel.cu", "step_cta.cu",
+           "sample.cu", "l2_api.cu")
 HEADERS = ("l2_device.cuh", "l2_params.h", "l2_kernels.h")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-lineinfo", "-O3", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O3"]

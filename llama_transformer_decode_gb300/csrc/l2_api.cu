@@ -130,6 +130,9 @@ struct l2_ctx {
     int attn_per_sm = 1;  // attention CTAs resident per SM
     int attn_cluster = 0;  // steps of one row: chunks per KV head merged in a cluster (0: tickets)
     GemvPlan plan_qkv{}, plan_wo{}, plan_w13{}, plan_w2{}, plan_cls{};
+    bool cta = false;      // batch-1 steps run as the one-block step kernel (small models)
+    size_t cta_smem = 0;
+    CtaStepParams ctap{};
     bool persist = false;  // batch-1 steps run as the persistent step kernel
     int persist_gq = 1;
     size_t persist_smem = 0;
@@ -807,6 +810,62 @@ int plan_persistent(l2_ctx *c) {
     return L2_OK;
 }
 
+// The one-block step kernel (step_cta.cu) for batch-1 steps of a model whose
+// weights fit a few MB (L2-resident: a step of per-matrix launches costs its
+// kernel boundaries, not its bytes): the default unless L2_FLAG_NO_ONE_CTA,
+// L2_FLAG_PERSIST or L2_FLAG_BF16_WEIGHTS is set, when its shared memory fits.
+// With L2_FLAG_DEBUG it exports the probabilities as the attention kernel does.
+constexpr double kCtaMaxWeightBytes = 4.0 * 1024 * 1024;
+
+int plan_cta(l2_ctx *c) {
+    c->cta = false;
+    if (c->flags & (L2_FLAG_NO_ONE_CTA | L2_FLAG_PERSIST | L2_FLAG_BF16_WEIGHTS)) return L2_OK;
+    const L2Config &p = c->cfg;
+    const double d = p.dim, h = p.hidden_dim, kv = c->kv_dim, L = p.n_layers, V = p.vocab_size;
+    const double bytes = 4.0 * (L * (2 * d * d + 2 * kv * d + 3 * d * h + 2 * d) + V * d + d);
+    if (bytes > kCtaMaxWeightBytes) return L2_OK;
+    const size_t smem = step_cta_smem(p.dim, p.hidden_dim, c->kv_dim, p.n_heads, p.seq_len);
+    if (smem > 227 * 1024) return L2_OK;
+    cudaError_t e = step_cta_init();
+    if (e != cudaSuccess) return cuda_fail(c, e, "step_cta_init()");
+    CtaStepParams &k = c->ctap;
+    k = CtaStepParams{};
+    k.emb = c->w.token_embedding_table;
+    k.rms_att = c->w.rms_att_weight;
+    k.rms_ffn = c->w.rms_ffn_weight;
+    k.rms_final = c->w.rms_final_weight;
+    k.wq = c->w.wq;
+    k.wk = c->w.wk;
+    k.wv = c->w.wv;
+    k.wo = c->w.wo;
+    k.w1 = c->w.w1;
+    k.w2 = c->w.w2;
+    k.w3 = c->w.w3;
+    k.wcls = c->w.wcls;
+    k.x = c->x;
+    k.logits = c->logits;
+    k.kcache = c->kcache;
+    k.vcache = c->vcache;
+    k.rope = c->rope;
+    k.dbg = c->dbg;
+    k.step = c->step_dev;
+    k.err = c->err;
+    k.ext = c->ext_dev;
+    k.dim = p.dim;
+    k.hidden_dim = p.hidden_dim;
+    k.n_layers = p.n_layers;
+    k.n_heads = p.n_heads;
+    k.n_kv_heads = p.n_kv_heads;
+    k.head_size = c->head_size;
+    k.kv_dim = c->kv_dim;
+    k.vocab = p.vocab_size;
+    k.seq_len = p.seq_len;
+    k.scale = (float)(1.0 / std::sqrt((double)c->head_size));
+    c->cta_smem = smem;
+    c->cta = true;
+    return L2_OK;
+}
+
 // The prompt-chunk attention reads each K/V tile once per 16 query vectors but
 // walks all of a block's positions in one CTA: it beats the per-row kernel
 // (which shares a tile among a group's query heads and splits positions over
@@ -976,7 +1035,9 @@ int submit(l2_ctx *c, int B, const int *tokens, const int *pos, float *logits_ou
         L2_CUDA(c, cudaGetLastError());
     }
 
-    if (B == 1 && c->persist && sh.slot[0] == 0) {
+    if (B == 1 && c->cta && prefill_slot < 0) {
+        L2_CUDA(c, launch_step_cta(c->ctap, c->cta_smem, c->stream));
+    } else if (B == 1 && c->persist && sh.slot[0] == 0) {
         L2_CUDA(c, launch_step_kernel(c->persist_gq, c->sp, c->num_sms, c->persist_smem, c->stream));
     } else if (c->flags & L2_FLAG_NO_GRAPH) {
         L2_CUDA(c, enqueue_step(c, B, c->stream, prefill_slot >= 0));
@@ -1039,7 +1100,7 @@ int l2_create(const L2Config *config, const L2Weights *weights, int max_batch, u
     if (max_batch < 1 || max_batch > kMaxBatch)
         return fail(nullptr, L2_EINVAL, "max_batch %d outside 1..%d", max_batch, kMaxBatch);
     if (flags & ~(L2_FLAG_DEBUG | L2_FLAG_NO_GRAPH | L2_FLAG_NO_PDL | L2_FLAG_PERSIST | L2_FLAG_NO_TC |
-                  L2_FLAG_BF16_WEIGHTS))
+                  L2_FLAG_BF16_WEIGHTS | L2_FLAG_NO_ONE_CTA))
         return fail(nullptr, L2_EINVAL, "unknown flags 0x%x", flags);
     if (flags & L2_FLAG_BF16_WEIGHTS) {
         if ((flags & L2_FLAG_NO_TC) && max_batch != 1)
@@ -1225,6 +1286,7 @@ int l2_create(const L2Config *config, const L2Weights *weights, int max_batch, u
         }
     }
     if ((rc = plan_persistent(c))) return bail(rc);
+    if ((rc = plan_cta(c))) return bail(rc);
     // buffer sizes, read by the bounds-checked build only
     {
         Extents &e = c->ext;
@@ -1459,7 +1521,7 @@ int l2_sample(const float *logits, int B, int vocab_size, float temperature, flo
 
 int l2_kernels_per_step(const l2_ctx *c, int B) {
     if (!c || B < 1 || B > c->max_batch) return L2_EINVAL;
-    if (B == 1 && c->persist) return 1;
+    if (B == 1 && (c->cta || c->persist)) return 1;
     return 5 * c->cfg.n_layers + 1 + (B > 1 && c->bsets[B].tc ? 1 : 0);
 }
 

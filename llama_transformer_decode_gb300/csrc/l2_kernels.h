@@ -43,6 +43,12 @@ cudaError_t step_kernel_init();
 int step_kernel_ctas_per_sm(int gq, size_t smem);
 cudaError_t launch_step_kernel(int gq, const StepKParams &p, int grid, size_t smem, cudaStream_t stream);
 
+// Whole batch-1 step of a small model in one thread block (step_cta.cu): its
+// dynamic shared memory, the one-time attribute set-up, and the launch.
+size_t step_cta_smem(int dim, int hidden, int kv_dim, int n_heads, int seq_len);
+cudaError_t step_cta_init();
+cudaError_t launch_step_cta(const CtaStepParams &p, size_t smem, cudaStream_t stream);
+
 // Token sampler (sample.cu).
 int sample_max_vocab();
 size_t sample_smem_bytes(int vocab);

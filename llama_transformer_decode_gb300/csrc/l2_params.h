@@ -123,6 +123,24 @@ struct StepKParams {
     float scale;     // 1 / sqrt(head_size)
 };
 
+// Whole batch-1 step of a small model in one CTA (step_cta.cu): the model's
+// base pointers (layer l of a per-layer tensor starts l * its per-layer size
+// further on) and the handle's buffers for slot 0.
+struct CtaStepParams {
+    const float *emb, *rms_att, *rms_ffn, *rms_final;
+    const float *wq, *wk, *wv, *wo, *w1, *w2, *w3, *wcls;
+    float *x;                 // residual stream [dim], left as the step ends it
+    float *logits;            // handle's logits buffer [vocab]
+    float *kcache, *vcache;   // slot 0: [layer][kv_head][seq_len][head_size]
+    const float2 *rope;       // [seq_len][head_size/2] (cos, sin)
+    float *dbg;               // [n_layers][n_heads][seq_len] probabilities (slot 0), or nullptr
+    const StepDev *step;
+    int *err;
+    const Extents *ext;       // buffer sizes (read only by the bounds-checked build)
+    int dim, hidden_dim, n_layers, n_heads, n_kv_heads, head_size, kv_dim, vocab, seq_len;
+    float scale;              // 1 / sqrt(head_size)
+};
+
 // Token sampler (sample.cu): one CTA per sequence.
 struct SampleParams {
     const float *logits;       // [B][vocab]

@@ -74,7 +74,8 @@ def test_injected_graph_instantiate_failure():
     w = pkg.to_device(w_host)
     toks = synth.token_stream(wl, 0, 6)
     want = oracle.Model(wl.config_tuple(), w_host).decode(toks)
-    dec = pkg.Decoder(wl.config_tuple(), w)
+    # batch-1 steps of tiny run as one kernel without a graph unless asked for the graph path
+    dec = pkg.Decoder(wl.config_tuple(), w, flags=pkg.L2_FLAG_NO_ONE_CTA)
     pkg.fail_graph_at(1)
     with pytest.raises(pkg.L2Error) as e:
         dec.forward(int(toks[0]), 0)
@@ -88,7 +89,7 @@ def test_injected_graph_instantiate_failure():
     torch.cuda.synchronize()
     free0, _ = torch.cuda.mem_get_info()
     for _ in range(5):
-        d = pkg.Decoder(wl.config_tuple(), w)
+        d = pkg.Decoder(wl.config_tuple(), w, flags=pkg.L2_FLAG_NO_ONE_CTA)
         pkg.fail_graph_at(1)
         with pytest.raises(pkg.L2Error):
             d.forward(int(toks[0]), 0)

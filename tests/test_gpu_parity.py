@@ -49,9 +49,16 @@ def run_pair(wl, n_steps, att_every=1, flags=pkg.L2_FLAG_DEBUG, weights=None):
     return dec, ref, rel, worst_att
 
 
-def test_tiny_all_steps():
+# tiny and the ragged shape are small enough for the one-block step kernel (the
+# default for them); L2_FLAG_NO_ONE_CTA runs the same steps on the graph of kernels
+PATHS = [pytest.param(0, id="one_cta"), pytest.param(pkg.L2_FLAG_NO_ONE_CTA, id="graph")]
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_tiny_all_steps(path):
     wl = WORKLOADS["tiny"]
-    _, _, rel, att = run_pair(wl, wl.steps)
+    dec, _, rel, att = run_pair(wl, wl.steps, flags=pkg.L2_FLAG_DEBUG | path)
+    assert dec.kernels_per_step() == (1 if path == 0 else 5 * wl.n_layers + 1)
     print(f"tiny: worst relative logit error {rel:.2e}, attention {att:.2e}")
 
 
@@ -113,12 +120,13 @@ def test_sharp_attention_one_layer(name, sharp):
           f"worst relative logit error {rel:.2e}, attention {att:.2e}")
 
 
-def test_ragged_shapes():
+@pytest.mark.parametrize("path", PATHS)
+def test_ragged_shapes(path):
     # head_size 12 (3 of 4 lanes per row), rows not multiples of any tile, 5 heads on 2 KV heads
     wl = WORKLOADS["tiny"].replace(name="ragged", dim=60, hidden_dim=92, n_layers=3, n_heads=5,
                                    n_kv_heads=2, vocab_size=301, seq_len=70, shared_wcls=False,
                                    seed_override=77, std_scale=(("wq", 8.0), ("wk", 8.0)))
-    run_pair(wl, 70, att_every=3)
+    run_pair(wl, 70, att_every=3, flags=pkg.L2_FLAG_DEBUG | path)
 
 
 def test_pos0_attention_is_exactly_one():

@@ -85,7 +85,7 @@ def test_persistent_and_per_kernel_paths_agree(name):
     w = pkg.to_device(synth.make_weights(wl))
     toks = synth.token_stream(wl, 0, 24)
     a = gpu_decode(persistent(wl, w), toks)
-    multi = decoder_for(wl, w)
+    multi = decoder_for(wl, w, flags=pkg.L2_FLAG_NO_ONE_CTA)  # the graph of per-matrix kernels
     assert multi.kernels_per_step() == 5 * wl.n_layers + 1
     b = gpu_decode(multi, toks)
     check_logits(a, b.astype(np.float64), f"{name}: persistent vs one kernel per matmul")
