@@ -607,10 +607,29 @@ def run_ours(args, wl):
         alu = fp32_alu_peak_tflops(props)
         if on_tensor_cores(B, bf16):
             # tensor-core GEMV: 3 tf32 products per multiply-add are far below the tensor
-            # peak, so the weights and the KV cache streamed from HBM bound the step
-            roofline = {"bound": "hbm", "achieved": step_gbs, "peak": hbm, "unit": "GB/s", "frac": step_gbs / hbm,
-                        "traffic": None, "kernel": "whole batched step (tensor-core GEMV kernels + attention)",
-                        "peak_source": peak_src + " (MEASURED_PEAKS.json hbm_gbs)"}
+            # peak, so the weights streamed from HBM bound it.  The dominant kernel (rmsnorm +
+            # W1/W3 + SwiGLU) timed alone at this batch, layers cycled, as at batch 1.
+            reps = max(1, 64 // wl.n_layers)
+            dec.launch_op("w13", 0, 1, batch=B)
+            k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            k0.record(stream)
+            for _ in range(reps):
+                for layer in range(wl.n_layers):
+                    dec.launch_op("w13", layer, 1, batch=B)
+            k1.record(stream)
+            k1.synchronize()
+            w13_ms = k0.elapsed_time(k1) / (reps * wl.n_layers)
+            byts = w13_bytes(wl, wb) + 4 * (B - 1) * (wl.dim + wl.hidden_dim)  # B input and output rows
+            achieved = byts / (w13_ms / 1000.0) / 1e9
+            roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                        "traffic": None,
+                        "kernel": "l2dec_matvec_tc_kernel<GEMV_W13> (rmsnorm + W1/W3 + SwiGLU, tensor cores, "
+                                  f"{B} rows)" + (", bf16 weights" if bf16 else ""),
+                        "bytes_per_launch": byts, "us_per_launch": w13_ms * 1000.0,
+                        "timing": "CUDA events around standalone launches on the decoder's stream, layers cycled",
+                        "peak_source": peak_src + " (MEASURED_PEAKS.json hbm_gbs, copy bandwidth)",
+                        "step": {"achieved": step_gbs, "frac": step_gbs / hbm,
+                                 "what": "whole batched step: weights + KV cache rows over the step time"}}
         elif B / 2.0 < alu * 1e3 / hbm:  # B/2 flop per weight byte, below the fp32 ridge point
             roofline = {"bound": "hbm", "achieved": step_gbs, "peak": hbm, "unit": "GB/s", "frac": step_gbs / hbm,
                         "traffic": None, "kernel": "whole batched step (all kernels)",

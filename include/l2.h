@@ -219,6 +219,17 @@ void l2_destroy(l2_ctx *ctx);
 int l2_launch_op(l2_ctx *ctx, int op, int layer, int count);
 
 /*
+ * l2_launch_op for the kernels of a step of `batch` rows (batched sequences,
+ * or a prompt chunk when the last step was one), as that step launches them
+ * (the tensor-core GEMV for 16-64 rows unless L2_FLAG_NO_TC).  The handle's
+ * last step must have had `batch` rows (else L2_ESTATE); its step block (rows'
+ * tokens, positions, slots, attention chunk plan) is reused.  batch 1 is
+ * l2_launch_op.  Profiling only: it overwrites activations and the cache rows
+ * of that step.  The pages have no counterpart.
+ */
+int l2_launch_op_batch(l2_ctx *ctx, int op, int layer, int batch, int count);
+
+/*
  * Prefill: the T tokens of a prompt, at positions pos0..pos0+T-1 of one
  * sequence (KV-cache slot `slot`), with the pages' causal attention (token
  * i attends to positions 0..pos0+i).  Cache rows pos0.. of the slot are

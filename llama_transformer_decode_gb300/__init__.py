@@ -193,8 +193,13 @@ class Decoder:
         self._check(self._lib.l2_kv_import(self._h, int(slot), int(k.shape[1]), ctypes.c_void_p(k.ctypes.data),
                                            ctypes.c_void_p(v.ctypes.data)))
 
-    def launch_op(self, op, layer: int = 0, count: int = 1):
-        self._check(self._lib.l2_launch_op(self._h, OPS.get(op, op), int(layer), int(count)))
+    def launch_op(self, op, layer: int = 0, count: int = 1, batch: int = 1):
+        """``count`` launches of one kernel of the step (l2_launch_op, or
+        l2_launch_op_batch for a step of ``batch`` rows, the last one run)."""
+        if batch == 1:
+            self._check(self._lib.l2_launch_op(self._h, OPS.get(op, op), int(layer), int(count)))
+        else:
+            self._check(self._lib.l2_launch_op_batch(self._h, OPS.get(op, op), int(layer), int(batch), int(count)))
 
     def step_input_bytes(self) -> int:
         return int(self._lib.l2_step_input_bytes())

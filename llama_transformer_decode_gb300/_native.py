@@ -91,7 +91,7 @@ EXPORTS = ("l2_create", "l2_reset", "l2_forward", "l2_forward_batch", "l2_forwar
            "l2_last_error", "l2_destroy", "l2_launch_op", "l2_kernels_per_step",
            "l2_step_input_bytes", "l2_forward_static", "l2_debug_fail_alloc_at", "l2_sample",
            "l2_forward_dev_tokens", "l2_prefill", "l2_debug_fail_graph_at", "l2_debug_wait_timeout",
-           "l2_debug_bounds_checked", "l2_debug_limit_cache")
+           "l2_debug_bounds_checked", "l2_debug_limit_cache", "l2_launch_op_batch")
 
 _lib = None
 
@@ -117,6 +117,7 @@ def declare(lib):
     lib.l2_destroy.argtypes = [vp]
     lib.l2_destroy.restype = None
     lib.l2_launch_op.argtypes = [vp, i, i, i]
+    lib.l2_launch_op_batch.argtypes = [vp, i, i, i, i]
     lib.l2_kernels_per_step.argtypes = [vp, i]
     lib.l2_forward_static.argtypes = [vp, i, i, fp]
     lib.l2_step_input_bytes.argtypes = []
@@ -139,7 +140,7 @@ def declare(lib):
     lib.l2_debug_limit_cache.restype = i
     for name in ("l2_create", "l2_reset", "l2_forward", "l2_forward_batch", "l2_forward_host",
                  "l2_position", "l2_debug_attention", "l2_kv_export", "l2_kv_import", "l2_sync",
-                 "l2_launch_op", "l2_kernels_per_step", "l2_forward_static"):
+                 "l2_launch_op", "l2_launch_op_batch", "l2_kernels_per_step", "l2_forward_static"):
         getattr(lib, name).restype = i
     return lib
 

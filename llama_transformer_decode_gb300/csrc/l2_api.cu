@@ -130,6 +130,8 @@ struct l2_ctx {
     int attn_per_sm = 1;  // attention CTAs resident per SM
     int attn_cluster = 0;  // steps of one row: chunks per KV head merged in a cluster (0: tickets)
     GemvPlan plan_qkv{}, plan_wo{}, plan_w13{}, plan_w2{}, plan_cls{};
+    int last_rows = 0;         // rows of the last step submitted (l2_launch_op_batch)
+    bool last_prefill = false;  // ... and whether it was a prompt chunk
     bool cta = false;      // batch-1 steps run as the one-block step kernel (small models)
     size_t cta_smem = 0;
     CtaStepParams ctap{};
@@ -824,7 +826,7 @@ int plan_cta(l2_ctx *c) {
     const double d = p.dim, h = p.hidden_dim, kv = c->kv_dim, L = p.n_layers, V = p.vocab_size;
     const double bytes = 4.0 * (L * (2 * d * d + 2 * kv * d + 3 * d * h + 2 * d) + V * d + d);
     if (bytes > kCtaMaxWeightBytes) return L2_OK;
-    const size_t smem = step_cta_smem(p.dim, p.hidden_dim, c->kv_dim, p.n_heads, p.seq_len);
+    const size_t smem = step_cta_smem(p.dim, p.hidden_dim, c->kv_dim, p.n_heads, p.seq_len, p.n_layers);
     if (smem > 227 * 1024) return L2_OK;
     cudaError_t e = step_cta_init();
     if (e != cudaSuccess) return cuda_fail(c, e, "step_cta_init()");
@@ -1027,6 +1029,8 @@ int submit(l2_ctx *c, int B, const int *tokens, const int *pos, float *logits_ou
     sh.logits_out = logits_out;
     sh.B = B;
     sh.sync_count = 0;
+    c->last_rows = B;
+    c->last_prefill = prefill_slot >= 0;
     L2_CUDA(c, cudaMemcpyAsync(c->step_dev, &sh, sizeof(StepDev), cudaMemcpyHostToDevice, c->stream));
     L2_CUDA(c, cudaEventRecord(c->ring_ev[i], c->stream));
     c->ring_used[i] = true;
@@ -1472,18 +1476,24 @@ void l2_destroy(l2_ctx *c) {
     delete c;
 }
 
-int l2_launch_op(l2_ctx *c, int op, int layer, int count) {
+int l2_launch_op(l2_ctx *c, int op, int layer, int count) { return l2_launch_op_batch(c, op, layer, 1, count); }
+
+int l2_launch_op_batch(l2_ctx *c, int op, int layer, int batch, int count) {
     if (!c) return L2_EINVAL;
     if (op < 0 || op > 5 || layer < 0 || layer >= c->cfg.n_layers || count < 0)
         return fail(c, L2_EINVAL, "bad op, layer or count");
+    if (batch < 1 || batch > c->max_rows) return fail(c, L2_EINVAL, "batch %d outside 1..%d", batch, c->max_rows);
     if (c->written[0] == 0) return fail(c, L2_ESTATE, "run a step first");
+    if (batch > 1 && batch != c->last_rows)
+        return fail(c, L2_ESTATE, "the last step had %d rows: run a step of %d rows first", c->last_rows, batch);
     // Standalone launches write the classifier's output only to the handle's buffer.
     L2_CUDA(c, cudaMemsetAsync(reinterpret_cast<char *>(c->step_dev) + offsetof(StepDev, logits_out), 0,
                                sizeof(float *), c->stream));
     // as in the step: consecutive launches linked by programmatic dependent launch
     // unless the handle was created with L2_FLAG_NO_PDL
     const bool pdl = !(c->flags & L2_FLAG_NO_PDL);
-    for (int i = 0; i < count; ++i) L2_CUDA(c, launch_op(c, op, layer, 1, c->stream, pdl));
+    for (int i = 0; i < count; ++i)
+        L2_CUDA(c, launch_op(c, op, layer, batch, c->stream, pdl, batch > 1 && c->last_prefill));
     return L2_OK;
 }
 

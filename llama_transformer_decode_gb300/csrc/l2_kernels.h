@@ -45,7 +45,7 @@ cudaError_t launch_step_kernel(int gq, const StepKParams &p, int grid, size_t sm
 
 // Whole batch-1 step of a small model in one thread block (step_cta.cu): its
 // dynamic shared memory, the one-time attribute set-up, and the launch.
-size_t step_cta_smem(int dim, int hidden, int kv_dim, int n_heads, int seq_len);
+size_t step_cta_smem(int dim, int hidden, int kv_dim, int n_heads, int seq_len, int n_layers);
 cudaError_t step_cta_init();
 cudaError_t launch_step_cta(const CtaStepParams &p, size_t smem, cudaStream_t stream);
 

@@ -13,11 +13,16 @@
 // kernel boundary (about 3.7 us each, 5 per layer), not by bytes.  Here the
 // phases are separated by __syncthreads instead: the activations (x, the
 // normalised x, q, the attention output, the hidden vector) and the attention
-// scores live in shared memory, and 32 warps read the weights straight from
-// L2 with 16-byte loads.  A matrix product gives each output row to a group
-// of G lanes (G the smallest power of two covering the row's 16-byte words,
-// at most 32), so short rows still keep every lane busy; each group reduces
-// its row by shuffles and one lane writes the result.
+// scores live in shared memory with every RMSNorm gain (loaded once), and 32
+// warps read the weights straight from L2 with 16-byte loads.  A matrix
+// product gives each output row to a group of G lanes (G the smallest power
+// of two covering the row's 16-byte words, at most 32), so short rows still
+// keep every lane busy; each group reduces its row by shuffles and one lane
+// writes the result.  With head size <= 16 the attention of a head (scores,
+// softmax, weighted V sum) runs inside one warp, lanes over positions, with no
+// block barrier until all heads are done; larger heads take three block-wide
+// phases.  Each phase costs about one L2 round trip and one barrier (0.3-2 us
+// per phase measured on GB300), which is what bounds the step.
 #include <cuda_runtime.h>
 #include <math_constants.h>
 
@@ -35,9 +40,10 @@ __host__ __device__ constexpr int align4(int n) { return (n + 3) & ~3; }
 
 // Shared-memory layout (floats, every region 16-byte aligned).
 struct CtaLayout {
-    int x, xn, q, att, kn, vn, hb, sc, part, red, total;
-    __host__ __device__ CtaLayout(int dim, int hidden, int kv_dim, int n_heads, int seq_len) {
-        x = 0;
+    int gain, x, xn, q, att, kn, vn, hb, sc, part, red, total;
+    __host__ __device__ CtaLayout(int dim, int hidden, int kv_dim, int n_heads, int seq_len, int n_layers) {
+        gain = 0;                                  // every RMSNorm gain: [layer][att, ffn], final
+        x = gain + align4((2 * n_layers + 1) * dim);
         xn = x + align4(dim);
         q = xn + align4(dim);
         att = q + align4(dim);
@@ -69,12 +75,12 @@ __device__ __forceinline__ float warp_max(float v) {
     return v;
 }
 
-// out = gain * (x / rms(x)), the RMSNorm of "run.c" rmsnorm() (eps 1e-5).
+// out = gain * (x / rms(x)), the RMSNorm of "run.c" rmsnorm() (eps 1e-5); gain in shared memory.
 __device__ void cta_rmsnorm(const float *x, const float *gain, float *out, int n, float *red) {
     float ss = 0.f;
     for (int i = threadIdx.x; i < n; i += kCT) ss = fmaf(x[i], x[i], ss);
     const float inv = 1.0f / sqrtf(cta_sum(ss, red) / (float)n + 1e-5f);
-    for (int i = threadIdx.x; i < n; i += kCT) out[i] = __ldg(gain + i) * (inv * x[i]);
+    for (int i = threadIdx.x; i < n; i += kCT) out[i] = gain[i] * (inv * x[i]);
     __syncthreads();
 }
 
@@ -117,7 +123,8 @@ __global__ void __launch_bounds__(kCT, 1) l2dec_step_cta_kernel(const CtaStepPar
     extern __shared__ __align__(16) float sm[];
     const int dim = p.dim, hidden = p.hidden_dim, kvd = p.kv_dim, hs = p.head_size, H = p.n_heads, KV = p.n_kv_heads;
     const int S = p.seq_len, half = hs >> 1;
-    const CtaLayout ly(dim, hidden, kvd, H, S);
+    const CtaLayout ly(dim, hidden, kvd, H, S, p.n_layers);
+    float *gains = sm + ly.gain;
     float *x = sm + ly.x, *xn = sm + ly.xn, *q = sm + ly.q, *att = sm + ly.att, *kn = sm + ly.kn, *vn = sm + ly.vn;
     float *hb = sm + ly.hb, *sc = sm + ly.sc, *part = sm + ly.part, *red = sm + ly.red;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -125,17 +132,23 @@ __global__ void __launch_bounds__(kCT, 1) l2dec_step_cta_kernel(const CtaStepPar
     const int token = p.step->token[0], pos = p.step->pos[0], P = pos + 1;
     const float2 *rr = p.rope + (size_t)pos * half;
 
-    // step 1: x = the token's embedding row
+    // step 1: x = the token's embedding row; every RMSNorm gain into shared memory
     {
         const size_t e0 = (size_t)token * dim;
         const bool ok = in_bounds(e0, (size_t)dim, p.ext->emb, p.err);
         for (int i = tid; i < dim; i += kCT) x[i] = ok ? p.emb[e0 + i] : 0.f;
+        const int ld = p.n_layers * dim;
+        for (int i = tid; i < 2 * ld + dim; i += kCT) {
+            const int l = i / (2 * dim), r = i - l * 2 * dim;
+            gains[i] = i >= 2 * ld ? __ldg(p.rms_final + (i - 2 * ld))
+                                   : __ldg((r < dim ? p.rms_att : p.rms_ffn) + (size_t)l * dim + (r < dim ? r : r - dim));
+        }
     }
     __syncthreads();
 
     for (int l = 0; l < p.n_layers; ++l) {
         // 2a: attention RMSNorm
-        cta_rmsnorm(x, p.rms_att + (size_t)l * dim, xn, dim, red);
+        cta_rmsnorm(x, gains + (size_t)l * 2 * dim, xn, dim, red);
 
         // 2b-2c: q, k, v = Wq xn, Wk xn, Wv xn (rows of the three matrices stacked)
         const float *wq = p.wq + (size_t)l * dim * dim, *wk = p.wk + (size_t)l * kvd * dim,
@@ -184,65 +197,122 @@ __global__ void __launch_bounds__(kCT, 1) l2dec_step_cta_kernel(const CtaStepPar
         }
         __syncthreads();
 
-        // 2e: attention.  Scores s[h][t] = q_h . K[t, g(h)] / sqrt(head_size) for t <= pos
-        // (the row at pos was just written by this block: read back through L2)
+        // 2e: attention of head h over cache rows t <= pos of KV head g(h): scores
+        // q_h . K[t] / sqrt(head_size), softmax (subtract the maximum, exponentiate, divide
+        // by the sum), out_h = sum_t p_t V[t].  The row at pos was just written by this
+        // block: the cache is read through L2.
         const int hs4 = hs >> 2;
-        for (int e = tid; e < H * P; e += kCT) {
-            const int h = e / P, t = e - h * P;
-            const int g = (int)((long long)h * KV / H);
-            const size_t k0 = ((lbase + (size_t)g * S) + t) * hs;
-            float d = 0.f;
-            if (in_bounds(k0, (size_t)hs, p.ext->cache, p.err)) {
-                const float4 *k4 = reinterpret_cast<const float4 *>(p.kcache + k0);
+        if (hs <= 16) {
+            // one warp per head, no block barrier inside: lanes take positions lane, lane + 32, ..
+            for (int h = warp; h < H; h += kCW) {
+                const int g = (int)((long long)h * KV / H);
+                const size_t r0 = (lbase + (size_t)g * S) * hs;  // the head's cache row 0
+                const bool okc = in_bounds(r0, (size_t)P * hs, p.ext->cache, p.err);
+                const float4 *k4 = reinterpret_cast<const float4 *>(p.kcache + r0);
+                const float4 *v4 = reinterpret_cast<const float4 *>(p.vcache + r0);
                 const float4 *q4 = reinterpret_cast<const float4 *>(q + h * hs);
-                for (int i = 0; i < hs4; ++i) d = dot4(__ldcg(k4 + i), q4[i], d);
+                float *s = sc + h * P;
+                float mx = -CUDART_INF_F;
+                for (int t = lane; t < P; t += 32) {
+                    float d = 0.f;
+                    if (okc)
+                        for (int i = 0; i < hs4; ++i) d = dot4(__ldcg(k4 + (size_t)t * hs4 + i), q4[i], d);
+                    d *= p.scale;
+                    s[t] = d;
+                    mx = fmaxf(mx, d);
+                }
+                mx = warp_max(mx);
+                float sum = 0.f;
+                for (int t = lane; t < P; t += 32) {
+                    const float ex = expf(s[t] - mx);
+                    s[t] = ex;
+                    sum += ex;
+                }
+                sum = warp_sum(sum);
+                float *dbg = p.dbg ? p.dbg + ((size_t)l * H + h) * S : nullptr;
+                if (dbg && !in_bounds(((size_t)l * H + h) * S, (size_t)P, p.ext->dbg, p.err)) dbg = nullptr;
+                float4 acc[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int t = lane; t < P; t += 32) {
+                    const float pr = s[t] / sum;
+                    if (dbg) dbg[t] = pr;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        if (i < hs4 && okc) {
+                            const float4 v = __ldcg(v4 + (size_t)t * hs4 + i);
+                            acc[i] = make_float4(fmaf(pr, v.x, acc[i].x), fmaf(pr, v.y, acc[i].y), fmaf(pr, v.z, acc[i].z),
+                                                 fmaf(pr, v.w, acc[i].w));
+                        }
+                }
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    if (i < hs4) {
+                        const float4 a = make_float4(warp_sum(acc[i].x), warp_sum(acc[i].y), warp_sum(acc[i].z),
+                                                     warp_sum(acc[i].w));
+                        if (lane == 0) reinterpret_cast<float4 *>(att + h * hs)[i] = a;
+                    }
             }
-            sc[h * P + t] = d * p.scale;
-        }
-        __syncthreads();
-        // softmax over t per head: subtract the maximum, exponentiate, divide by the sum
-        for (int h = warp; h < H; h += kCW) {
-            float *s = sc + h * P;
-            float mx = -CUDART_INF_F;
-            for (int t = lane; t < P; t += 32) mx = fmaxf(mx, s[t]);
-            mx = warp_max(mx);
-            float sum = 0.f;
-            for (int t = lane; t < P; t += 32) {
-                const float ex = expf(s[t] - mx);
-                s[t] = ex;
-                sum += ex;
+            __syncthreads();
+        } else {
+            // scores, softmax and the weighted V sum as three block-wide phases
+            for (int e = tid; e < H * P; e += kCT) {
+                const int h = e / P, t = e - h * P;
+                const int g = (int)((long long)h * KV / H);
+                const size_t k0 = ((lbase + (size_t)g * S) + t) * hs;
+                float d = 0.f;
+                if (in_bounds(k0, (size_t)hs, p.ext->cache, p.err)) {
+                    const float4 *k4 = reinterpret_cast<const float4 *>(p.kcache + k0);
+                    const float4 *q4 = reinterpret_cast<const float4 *>(q + h * hs);
+                    for (int i = 0; i < hs4; ++i) d = dot4(__ldcg(k4 + i), q4[i], d);
+                }
+                sc[h * P + t] = d * p.scale;
             }
-            sum = warp_sum(sum);
-            float *dbg = p.dbg ? p.dbg + ((size_t)l * H + h) * S : nullptr;
-            if (dbg && !in_bounds(((size_t)l * H + h) * S, (size_t)P, p.ext->dbg, p.err)) dbg = nullptr;
-            for (int t = lane; t < P; t += 32) {
-                const float pr = s[t] / sum;
-                s[t] = pr;
-                if (dbg) dbg[t] = pr;
+            __syncthreads();
+            // softmax over t per head: subtract the maximum, exponentiate, divide by the sum
+            for (int h = warp; h < H; h += kCW) {
+                float *s = sc + h * P;
+                float mx = -CUDART_INF_F;
+                for (int t = lane; t < P; t += 32) mx = fmaxf(mx, s[t]);
+                mx = warp_max(mx);
+                float sum = 0.f;
+                for (int t = lane; t < P; t += 32) {
+                    const float ex = expf(s[t] - mx);
+                    s[t] = ex;
+                    sum += ex;
+                }
+                sum = warp_sum(sum);
+                float *dbg = p.dbg ? p.dbg + ((size_t)l * H + h) * S : nullptr;
+                if (dbg && !in_bounds(((size_t)l * H + h) * S, (size_t)P, p.ext->dbg, p.err)) dbg = nullptr;
+                for (int t = lane; t < P; t += 32) {
+                    const float pr = s[t] / sum;
+                    s[t] = pr;
+                    if (dbg) dbg[t] = pr;
+                }
             }
-        }
-        __syncthreads();
-        // out[h][d] = sum_t p[h][t] V[t, g(h)][d]: NP threads per output element split t
-        const int NP = dim >= kCT ? 1 : kCT / dim;
-        for (int e = tid; e < dim * NP; e += kCT) {
-            const int i = e % dim, sp = e / dim;
-            const int h = i / hs, d = i - h * hs, g = (int)((long long)h * KV / H);
-            const size_t v0 = (lbase + (size_t)g * S) * hs + d;
-            const float *ph = sc + h * P;
-            float a = 0.f;
-            if (in_bounds(v0 + (size_t)pos * hs, 1, p.ext->cache, p.err)) {
+            __syncthreads();
+            // out[h][d] = sum_t p[h][t] V[t, g(h)][d]: NP threads per output element split t
+            const int NP = dim >= kCT ? 1 : kCT / dim;
+            for (int e = tid; e < dim * NP; e += kCT) {
+                const int i = e % dim, sp = e / dim;
+                const int h = i / hs, d = i - h * hs, g = (int)((long long)h * KV / H);
+                const size_t v0 = (lbase + (size_t)g * S) * hs + d;
+                const float *ph = sc + h * P;
+                float a = 0.f;
+                if (in_bounds(v0 + (size_t)pos * hs, 1, p.ext->cache, p.err)) {
 #pragma unroll 4
-                for (int t = sp; t < P; t += NP) a = fmaf(ph[t], __ldcg(p.vcache + v0 + (size_t)t * hs), a);
+                    for (int t = sp; t < P; t += NP) a = fmaf(ph[t], __ldcg(p.vcache + v0 + (size_t)t * hs), a);
+                }
+                part[sp * dim + i] = a;
             }
-            part[sp * dim + i] = a;
+            __syncthreads();
+            for (int i = tid; i < dim; i += kCT) {
+                float a = 0.f;
+                for (int sp = 0; sp < NP; ++sp) a += part[sp * dim + i];
+                att[i] = a;
+            }
+            __syncthreads();
         }
-        __syncthreads();
-        for (int i = tid; i < dim; i += kCT) {
-            float a = 0.f;
-            for (int sp = 0; sp < NP; ++sp) a += part[sp * dim + i];
-            att[i] = a;
-        }
-        __syncthreads();
 
         // 2f: x += Wo att
         cta_gemv<1>(
@@ -250,7 +320,7 @@ __global__ void __launch_bounds__(kCT, 1) l2dec_step_cta_kernel(const CtaStepPar
         __syncthreads();
 
         // 2g: FFN RMSNorm, hb = silu(W1 xn) * (W3 xn)
-        cta_rmsnorm(x, p.rms_ffn + (size_t)l * dim, xn, dim, red);
+        cta_rmsnorm(x, gains + (size_t)l * 2 * dim + dim, xn, dim, red);
         cta_gemv<2>(
             dim, hidden, xn, [&](int m, int r) { return (m ? w3 : w1) + (size_t)r * dim; },
             [&](int r, const float *y) { hb[r] = y[0] / (1.0f + expf(-y[0])) * y[1]; });
@@ -264,7 +334,7 @@ __global__ void __launch_bounds__(kCT, 1) l2dec_step_cta_kernel(const CtaStepPar
     }
 
     // step 3: final RMSNorm and the classifier
-    cta_rmsnorm(x, p.rms_final, xn, dim, red);
+    cta_rmsnorm(x, gains + (size_t)p.n_layers * 2 * dim, xn, dim, red);
     float *user = p.step->logits_out;
     cta_gemv<1>(
         dim, p.vocab, xn, [&](int, int r) { return p.wcls + (size_t)r * dim; },
@@ -275,8 +345,8 @@ __global__ void __launch_bounds__(kCT, 1) l2dec_step_cta_kernel(const CtaStepPar
     for (int i = tid; i < dim; i += kCT) p.x[i] = x[i];
 }
 
-size_t step_cta_smem(int dim, int hidden, int kv_dim, int n_heads, int seq_len) {
-    return (size_t)CtaLayout(dim, hidden, kv_dim, n_heads, seq_len).total * sizeof(float);
+size_t step_cta_smem(int dim, int hidden, int kv_dim, int n_heads, int seq_len, int n_layers) {
+    return (size_t)CtaLayout(dim, hidden, kv_dim, n_heads, seq_len, n_layers).total * sizeof(float);
 }
 
 cudaError_t step_cta_init() {

@@ -72,7 +72,7 @@ class FakeDecoder:
             if out is not None:
                 out[i].copy_(torch.from_numpy(r))
 
-    def launch_op(self, op, layer=0, count=1):
+    def launch_op(self, op, layer=0, count=1, batch=1):
         pass
 
     def kernels_per_step(self, batch=1):

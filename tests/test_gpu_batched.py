@@ -155,3 +155,30 @@ def test_batch_checks_and_slot_rewind():
     assert [dec.position(b) for b in range(4)] == [2, 0, 2, 0]
     dec.forward_batch([4, 5, 6], [2, 0, 2])  # slot 1 restarts at position 0
     dec.sync()
+
+
+def test_launch_op_of_a_batched_step():
+    # l2_launch_op_batch reruns one kernel of the last step, whose rows it must match
+    wl = WORKLOADS["tiny"]
+    w_host = synth.make_weights(wl)
+    dec = pkg.Decoder(wl.config_tuple(), pkg.to_device(w_host), max_batch=16)
+    B = 16
+    toks = [int(t) for t in synth.token_stream(wl, 9, B)]
+    out = torch.empty((B, wl.vocab_size), device="cuda")
+    dec.forward_batch(toks, [0] * B, out)
+    for op in range(6):
+        dec.launch_op(op, wl.n_layers - 1, 2, batch=B)
+    dec.sync()
+    with pytest.raises(pkg.L2Error) as e:
+        dec.launch_op(3, 0, 1, batch=8)  # the last step had 16 rows
+    assert e.value.code == pkg.L2_ESTATE
+    with pytest.raises(pkg.L2Error) as e:
+        dec.launch_op(3, 0, 1, batch=65)  # more rows than any step of the handle
+    assert e.value.code == pkg.L2_EINVAL
+    # a step after the standalone launches is still the oracle's
+    ref = oracle.Model(wl.config_tuple(), w_host, n_slots=B)
+    want = np.stack([ref.forward(toks[b], 0, slot=b) for b in range(B)])
+    dec.forward_batch(toks, [0] * B, out)
+    dec.sync()
+    check_logits(out.cpu().numpy(), want, "batched step after l2_launch_op_batch")
+    dec.close()

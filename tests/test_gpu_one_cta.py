@@ -1,11 +1,12 @@
 """The one-block step kernel (batch-1 steps of models with at most 4 MiB of
 weights) against the oracle: logits at the parity bounds, probabilities
 within 1e-5, on shapes that exercise its index arithmetic -- grouped heads
-that do not divide evenly (6 query heads on 4 KV heads), a head size of 12,
-a context long enough that the scores of a head span many warps' strides,
-and a hidden size that is not a multiple of 32 words.  Also: which models it
-serves, the device-token and host-output entry points on it, bitwise
-repeatability, and the cache rows it writes."""
+that do not divide evenly (6 query heads on 4 KV heads), head sizes of 8
+and 12 (attention inside one warp per head) and 32 (three block-wide
+phases), contexts long enough that a head's positions take many turns of a
+warp, and hidden sizes that are not a multiple of 32 words.  Also: which
+models it serves, the device-token and host-output entry points on it,
+bitwise repeatability, and the cache rows it writes."""
 import numpy as np
 import pytest
 
@@ -24,6 +25,10 @@ import llama_transformer_decode_gb300 as pkg  # noqa: E402
 
 GQA64 = WORKLOADS["tiny"].replace(name="gqa6on4", dim=48, hidden_dim=132, n_layers=2, n_heads=6, n_kv_heads=4,
                                   vocab_size=203, seq_len=300, shared_wcls=False, seed_override=91)
+# head size 32: the attention runs as three block-wide phases instead of one warp per head
+HS32 = WORKLOADS["tiny"].replace(name="hs32", dim=128, hidden_dim=344, n_layers=2, n_heads=4, n_kv_heads=2,
+                                 vocab_size=700, seq_len=130, shared_wcls=False, seed_override=93,
+                                 std_scale=(("wq", 4.0), ("wk", 4.0)))
 HS12 = WORKLOADS["tiny"].replace(name="hs12", dim=96, hidden_dim=256, n_layers=3, n_heads=8, n_kv_heads=2,
                                  vocab_size=1000, seq_len=160, shared_wcls=False, seed_override=92,
                                  std_scale=(("wq", 6.0), ("wk", 6.0)))
@@ -52,7 +57,8 @@ def _decode_checked(wl, n_steps, att_every):
     return dec, ref
 
 
-@pytest.mark.parametrize("wl,n_steps,att_every", [(GQA64, 300, 23), (HS12, 160, 17)], ids=["gqa6on4", "hs12"])
+@pytest.mark.parametrize("wl,n_steps,att_every", [(GQA64, 300, 23), (HS12, 160, 17), (HS32, 130, 11)],
+                         ids=["gqa6on4", "hs12", "hs32"])
 def test_matches_oracle_to_the_end_of_the_context(wl, n_steps, att_every):
     dec, ref = _decode_checked(wl, n_steps, att_every)
     # the cache rows it wrote, in the pages' layout
