@@ -318,7 +318,7 @@ __device__ __forceinline__ bool warp_stop(TcFixed &fx, bool ok) {
 // Layer-0 inputs of a step on the tensor-core path: x[b] = emb[token[b]],
 // x[b] * gain for the first RMSNorm, and the sum of squares of each row
 // (ss_part row 0, read with ss_parts = 1).
-__global__ void l2dec_tc_embed_kernel(const GemvParams p, float *xg) {
+__global__ void l2dec_tc_embed_kernel(const GemvParams p, float *xg, float *xg_hi, float *xg_lo) {
     const int b = blockIdx.x, tid = threadIdx.x;
     __shared__ float red[32];
     pdl_launch_dependents();
@@ -331,7 +331,14 @@ __global__ void l2dec_tc_embed_kernel(const GemvParams p, float *xg) {
     for (int i = tid; i < p.dim / 4; i += blockDim.x) {
         const float4 v = e4[i], g = __ldg(g4 + i);
         x4[i] = v;
-        xg4[i] = make_float4(v.x * g.x, v.y * g.y, v.z * g.z, v.w * g.w);
+        const float4 xv = make_float4(v.x * g.x, v.y * g.y, v.z * g.z, v.w * g.w);
+        xg4[i] = xv;
+        if (xg_hi) {
+            float4 hi, lo;
+            tf32_split4(xv, hi, lo);
+            reinterpret_cast<float4 *>(xg_hi + (size_t)b * p.dim)[i] = hi;
+            reinterpret_cast<float4 *>(xg_lo + (size_t)b * p.dim)[i] = lo;
+        }
         ss = fmaf(v.x, v.x, ss);
         ss = fmaf(v.y, v.y, ss);
         ss = fmaf(v.z, v.z, ss);
@@ -492,7 +499,13 @@ __global__ void __launch_bounds__(kTT, 1) l2dec_matvec_tc_kernel(const __grid_co
                 const int b = e / nj, j = jlo + (e - b * nj);
                 if (r0 + j >= hidden || !in_bounds((size_t)b * hidden + r0 + j, 1, p.ext->hb, p.err)) continue;
                 const float h1 = src[j * YS + b] * fx.inv[b], h3 = src[(j + kTM / 2) * YS + b] * fx.inv[b];
-                p.hb[(size_t)b * hidden + r0 + j] = silu_t(h1) * h3;
+                const float hv = silu_t(h1) * h3;
+                p.hb[(size_t)b * hidden + r0 + j] = hv;
+                if (tp.hb_hi) {
+                    const float hi = tf32_rna(hv);
+                    tp.hb_hi[(size_t)b * hidden + r0 + j] = hi;
+                    tp.hb_lo[(size_t)b * hidden + r0 + j] = tf32_rna(hv - hi);
+                }
             }
         } else if (MODE == GEMV_RESID) {
             const int dim = tp.mrows[0];
@@ -516,6 +529,11 @@ __global__ void __launch_bounds__(kTT, 1) l2dec_matvec_tc_kernel(const __grid_co
                         const float nv = xv[i] + src[j * YS + b0 + i];
                         p.x[o] = nv;
                         tp.xg[o] = nv * g;
+                        if (tp.xg_hi) {
+                            const float hi = tf32_rna(nv * g);
+                            tp.xg_hi[o] = hi;
+                            tp.xg_lo[o] = tf32_rna(nv * g - hi);
+                        }
                         src[j * YS + b0 + i] = nv;
                     }
             }
@@ -555,7 +573,8 @@ __global__ void __launch_bounds__(kTT, 1) l2dec_matvec_tc_kernel(const __grid_co
         // ---------------- producer: tensor copies into the ring (whole warp, one lane issues) ----------------
         // the copies of a stage: its weights and the two fp32 input boxes (the lo rows or
         // the bf16 parts are written here)
-        const uint32_t stage_tx = wstage_bytes(WT) + 2 * xbox_bytes(BP);
+        const bool xs = !WT && tp.xsplit;  // the inputs' lo rows come by tensor copy too
+        const uint32_t stage_tx = wstage_bytes(WT) + (xs ? 4 : 2) * xbox_bytes(BP);
         long long nl = 0;
         bool stop = false;
         auto issue_weights = [&](int s, int m, int wrow, int kt) {
@@ -612,6 +631,10 @@ __global__ void __launch_bounds__(kTT, 1) l2dec_matvec_tc_kernel(const __grid_co
                     if (nl >= npre) issue_weights(s, m, wrow, kt);
                     tensor2d(xbox(s, 0), &tp.xmap, kt * kSK, 0, &fx.full[s]);
                     tensor2d(xbox(s, 1), &tp.xmap, kt * kSK + kBK, 0, &fx.full[s]);
+                    if (xs) {
+                        tensor2d(xbox(s, 0) + xbox_bytes(BP), &tp.xmap_lo, kt * kSK, 0, &fx.full[s]);
+                        tensor2d(xbox(s, 1) + xbox_bytes(BP), &tp.xmap_lo, kt * kSK + kBK, 0, &fx.full[s]);
+                    }
                 }
                 __syncwarp();
                 ++nl;
@@ -748,7 +771,8 @@ __global__ void __launch_bounds__(kTT, 1) l2dec_matvec_tc_kernel(const __grid_co
                     }
                     tmem_st32(tmem + ((uint32_t)(32 * q) << 16) + wlo_col(s) + (uint32_t)(kBK * h), v);
                 }
-                for (int h = 0; h < 2; ++h) {
+                // (inputs split by the kernel that wrote them arrive split)
+                for (int h = 0; h < (tp.xsplit ? 0 : 2); ++h) {
                     float4 *X4 = reinterpret_cast<float4 *>(xbox(s, h));
                     float4 *Xlo4 = X4 + BP * kBK / 4;  // right after the BP input rows
                     for (int i = ct; i < BP * kBK / 4; i += kRoleThreads) {
@@ -1103,8 +1127,8 @@ static cudaLaunchConfig_t pdl_config(dim3 grid, dim3 block, size_t smem, cudaStr
 cudaError_t launch_tc_embed(const TcParams &tp, int batch, cudaStream_t stream, bool pdl) {
     cudaLaunchAttribute attr[1];
     cudaLaunchConfig_t cfg = pdl_config(dim3(batch), dim3(256), 0, stream, pdl, attr);
-    float *xg = tp.xg;
-    void *args[] = {const_cast<GemvParams *>(&tp.g), &xg};
+    float *xg = tp.xg, *xg_hi = tp.xg_hi, *xg_lo = tp.xg_lo;
+    void *args[] = {const_cast<GemvParams *>(&tp.g), &xg, &xg_hi, &xg_lo};
     return cudaLaunchKernelExC(&cfg, reinterpret_cast<void *>(l2dec_tc_embed_kernel), args);
 }
 

@@ -112,6 +112,9 @@ struct l2_ctx {
     float *ss_part = nullptr;  // batched steps: partial sums of x^2 [kMaxParts][max_rows]
     float *tc_ws = nullptr;       // tensor-core GEMV split-K partial tiles
     float *xg = nullptr;          // tensor-core path: x * gain of the next RMSNorm [max_rows][dim]
+    // tensor-core path with fp32 weights: the inputs' tf32 split (hi, lo) written once by
+    // the kernels that produce them (x * gain, and the SwiGLU output for W2)
+    float *xg_hi = nullptr, *xg_lo = nullptr, *hb_hi = nullptr, *hb_lo = nullptr;
     unsigned *tc_tickets = nullptr;
     size_t tc_tickets_n = 0;      // entries of tc_tickets
     size_t tc_ws_n = 0;           // floats of tc_ws
@@ -541,6 +544,14 @@ int build_tc_set(l2_ctx *c, int batch) {
     auto W = [&](const float *f32, const unsigned short *b16) { return wt ? (const void *)b16 : (const void *)f32; };
     set.tc_ws_floats = 0;
     set.tc_tiles = 0;
+    // the inputs as fp32 (bf16 weights: split into bf16 parts in the kernel), or as their
+    // tf32 hi and lo parts written by the producing kernel (fp32 weights)
+    auto xmaps = [&](TcParams &tp, const float *f32, const float *hi, const float *lo, uint64_t cols) {
+        tp.xsplit = hi && lo ? 1 : 0;
+        if (!tp.xsplit) return encode_matrix_sw128(&tp.xmap, f32, cols, c->max_rows, bpad);
+        return encode_matrix_sw128(&tp.xmap, hi, cols, c->max_rows, bpad) &&
+               encode_matrix_sw128(&tp.xmap_lo, lo, cols, c->max_rows, bpad);
+    };
     for (int k = 0; k < 5; ++k) {
         TcParams &tp = set.tcp[k];
         memset(&tp, 0, sizeof(tp));
@@ -557,7 +568,7 @@ int build_tc_set(l2_ctx *c, int batch) {
                 ok = encode_weights_sw128(&tp.wmap[0], W(c->w.wq, c->b16q), D, L * D, 128, wt) &&
                      encode_weights_sw128(&tp.wmap[1], W(c->w.wk, c->b16k), D, L * KVD, 128, wt) &&
                      encode_weights_sw128(&tp.wmap[2], W(c->w.wv, c->b16v), D, L * KVD, 128, wt) &&
-                     encode_matrix_sw128(&tp.xmap, c->xg, D, c->max_rows, bpad);
+                     xmaps(tp, c->xg, c->xg_hi, c->xg_lo, D);
                 n = p.dim;
                 break;
             case 1:
@@ -572,21 +583,21 @@ int build_tc_set(l2_ctx *c, int batch) {
                 tp.tiles[0] = ceil_div(p.hidden_dim, 64);
                 ok = encode_weights_sw128(&tp.wmap[0], W(c->w.w1, c->b16w1), D, L * H, 64, wt) &&
                      encode_weights_sw128(&tp.wmap[1], W(c->w.w3, c->b16w3), D, L * H, 64, wt) &&
-                     encode_matrix_sw128(&tp.xmap, c->xg, D, c->max_rows, bpad);
+                     xmaps(tp, c->xg, c->xg_hi, c->xg_lo, D);
                 n = p.dim;
                 break;
             case 3:
                 tp.mrows[0] = p.dim;
                 tp.tiles[0] = ceil_div(p.dim, 128);
                 ok = encode_weights_sw128(&tp.wmap[0], W(c->w.w2, c->b16w2), H, L * D, 128, wt) &&
-                     encode_matrix_sw128(&tp.xmap, c->hb, H, c->max_rows, bpad);
+                     xmaps(tp, c->hb, c->hb_hi, c->hb_lo, H);
                 n = p.hidden_dim;
                 break;
             case 4:
                 tp.mrows[0] = p.vocab_size;
                 tp.tiles[0] = ceil_div(p.vocab_size, 128);
                 ok = encode_weights_sw128(&tp.wmap[0], W(c->w.wcls, c->b16cls), D, V, 128, wt) &&
-                     encode_matrix_sw128(&tp.xmap, c->xg, D, c->max_rows, bpad);
+                     xmaps(tp, c->xg, c->xg_hi, c->xg_lo, D);
                 n = p.dim;
                 break;
         }
@@ -699,6 +710,10 @@ cudaError_t launch_batched(l2_ctx *c, int k, const GemvPlan &pl, int layer, int 
         tp.ws = c->tc_ws;
         tp.tickets = c->tc_tickets;
         tp.xg = c->xg;
+        tp.xg_hi = c->xg_hi;
+        tp.xg_lo = c->xg_lo;
+        tp.hb_hi = c->hb_hi;
+        tp.hb_lo = c->hb_lo;
         const L2Config &cf = c->cfg;
         if (k == 1) tp.next_gain = c->w.rms_ffn_weight + (size_t)layer * cf.dim;
         if (k == 3)
@@ -1273,6 +1288,11 @@ int l2_create(const L2Config *config, const L2Weights *weights, int max_batch, u
     if (!(flags & L2_FLAG_NO_TC) && c->max_rows >= tc_min) {
         CREATE_CUDA(gemv_tc_init());
         if ((rc = alloc_n(c, &c->xg, (size_t)c->max_rows * p.dim, "x * gain"))) return bail(rc);
+        if (!c->wt && ((rc = alloc_n(c, &c->xg_hi, (size_t)c->max_rows * p.dim, "x * gain, tf32 hi")) ||
+                       (rc = alloc_n(c, &c->xg_lo, (size_t)c->max_rows * p.dim, "x * gain, tf32 lo")) ||
+                       (rc = alloc_n(c, &c->hb_hi, (size_t)c->max_rows * p.hidden_dim, "hb, tf32 hi")) ||
+                       (rc = alloc_n(c, &c->hb_lo, (size_t)c->max_rows * p.hidden_dim, "hb, tf32 lo"))))
+            return bail(rc);
         size_t ws = 0;
         int tiles = 0;
         for (int b = tc_min; b <= c->max_rows && b <= gemv_tc_max_batch(); ++b) {

@@ -174,6 +174,15 @@ struct alignas(128) TcParams {
     unsigned *tickets;    // [ntiles], zero between launches
     float *xg;            // x * gain of the next RMSNorm [max rows][dim], written by the residual kernels
     const float *next_gain;  // residual kernels: the gain vector of the next RMSNorm
+    // fp32 weights: the inputs' tf32 split made once by the kernel that writes them
+    // (hi = the tf32 value nearest to v, lo = the tf32 value nearest to v - hi) instead of
+    // by every CTA for every tile.  xsplit: this launch's inputs come as xmap (hi) and
+    // xmap_lo (lo); xg_hi/xg_lo (residual and embedding kernels) and hb_hi/hb_lo (W1/W3)
+    // receive the split of what they write, or are null.
+    CUtensorMap xmap_lo;
+    int xsplit;
+    float *xg_hi, *xg_lo;  // [max rows][dim]
+    float *hb_hi, *hb_lo;  // [max rows][hidden_dim]
 };
 
 struct AttnParams {

@@ -35,6 +35,7 @@ namespace {
 
 constexpr int kCT = 1024;      // threads
 constexpr int kCW = kCT / 32;  // warps
+static_assert(kCW == 32, "cta_sum adds one partial per lane of a warp");
 
 __host__ __device__ constexpr int align4(int n) { return (n + 3) & ~3; }
 
@@ -57,16 +58,14 @@ struct CtaLayout {
     }
 };
 
-// Sum over the block, the same value in every thread (warp partials added in warp order).
+// Sum over the block, the same value in every thread: the warps' partials are
+// added by one shuffle tree (the same order in every warp).
 __device__ __forceinline__ float cta_sum(float v, float *red) {
     v = warp_sum(v);
     __syncthreads();  // red is free
     if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
     __syncthreads();
-    float t = 0.f;
-#pragma unroll 8
-    for (int w = 0; w < kCW; ++w) t += red[w];
-    return t;
+    return warp_sum(red[threadIdx.x & 31]);
 }
 
 __device__ __forceinline__ float warp_max(float v) {
