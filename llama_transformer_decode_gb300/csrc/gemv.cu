@@ -285,6 +285,27 @@ __global__ void __launch_bounds__(NW * 32, 1) l2dec_matvec_kernel(const GemvPara
         }
     }
     __syncthreads();
+    if (WT) {
+        // A bf16 weight word (8 weights) meets two input words, 2w and 2w + 1.  Read in
+        // place, lane l's pair sits 32 bytes from lane l+1's, so every load of the input
+        // took two shared-memory wavefronts per 8 lanes (a 2-way bank conflict).  Each
+        // block of 32 weight words (M < 32 in a row's last block) therefore keeps its 2M
+        // input words as [even words | odd words]: the lanes read consecutive words.
+        for (int kb = warp; 32 * kb < nw; kb += NW) {
+            const int M = min(32, nw - 32 * kb);
+            float4 e = make_float4(0.f, 0.f, 0.f, 0.f), o = e;
+            if (lane < M) {
+                e = xs[64 * kb + 2 * lane];
+                o = xs[64 * kb + 2 * lane + 1];
+            }
+            __syncwarp();
+            if (lane < M) {
+                xs[64 * kb + lane] = e;
+                xs[64 * kb + M + lane] = o;
+            }
+        }
+        __syncthreads();
+    }
 
     // ---- stream this warp's weight words ----
     float acc = 0.f;
@@ -330,10 +351,18 @@ __global__ void __launch_bounds__(NW * 32, 1) l2dec_matvec_kernel(const GemvPara
             const float4 *wr = buf + (a - lf);
             const int cnt = b - a;
             if (WT) {
-                const float4 *xr = xs + 2 * (a - rs);
+                // the input words of row word w: block w / 32 at 64 (w / 32), its M words
+                // apart; lane l's word advances by one block per iteration
+                const int w0 = (a - rs) + lane;
+                int wb = w0 & ~31;
+                const float4 *xr = xs + 2 * wb + (w0 & 31);
 #pragma unroll 4
-                for (int i = lane; i < cnt; i += 32)
-                    acc = dot_bf16x8(reinterpret_cast<const uint4 *>(wr)[i], xr[2 * i], xr[2 * i + 1], acc);
+                for (int i = lane; i < cnt; i += 32) {
+                    const int M = min(32, nw - wb);
+                    acc = dot_bf16x8(reinterpret_cast<const uint4 *>(wr)[i], xr[0], xr[M], acc);
+                    xr += 64;
+                    wb += 32;
+                }
             } else {
                 const float4 *xr = xs + (a - rs);
 #pragma unroll 4
