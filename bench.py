@@ -40,10 +40,15 @@ READ_CEILING_GBS = 7250.0  # pure bulk-copy read stream on GB300 (see the roofli
 FALLBACK_HBM_GBS = 6800.0
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of
-# the dominant kernel (rmsnorm + W1/W3 + SwiGLU at the 7B shape), from one ncu
-# capture of that kernel, valid only for the kernel source whose sha256 prefix
-# is recorded beside it.
-W13_NCU_TRAFFIC = (363956480, "4177b02e97bce001")  # (bytes per launch, gemv.cu sha256 prefix)
+# the dominant kernel (rmsnorm + W1/W3 + SwiGLU at the 7B shape), per weight
+# type, from one ncu capture of that kernel: (bytes per launch, the sha256
+# prefixes of gemv.cu it holds for).  The fp32 figure was taken on source
+# 4177b02e...; 5474aa3e... changed only the bf16 branches of the kernel template
+# (`if (WT)`, compiled out of the fp32 kernel), so the fp32 kernel is the same.
+W13_NCU_TRAFFIC = {
+    "f32": (363956480, ("4177b02e97bce001", "5474aa3edc02e859")),
+    "bf16": (183838976, ("5474aa3edc02e859",)),
+}
 
 
 def weight_bytes(wl, wb: int = 4) -> int:
@@ -586,10 +591,11 @@ def run_ours(args, wl):
         w13_ms = k0.elapsed_time(k1) / (reps * wl.n_layers)
         achieved = w13_bytes(wl, wb) / (w13_ms / 1000.0) / 1e9
         traffic = None
-        if W13_NCU_TRAFFIC is not None and (wl.dim, wl.hidden_dim) == (4096, 11008) and not bf16:
+        if (wl.dim, wl.hidden_dim) == (4096, 11008):
             src = open(os.path.join(ROOT, "llama_transformer_decode_gb300", "csrc", "gemv.cu"), "rb").read()
-            if hashlib.sha256(src).hexdigest().startswith(W13_NCU_TRAFFIC[1]):
-                traffic = W13_NCU_TRAFFIC[0]
+            nbytes, sources = W13_NCU_TRAFFIC["bf16" if bf16 else "f32"]
+            if hashlib.sha256(src).hexdigest()[:16] in sources:
+                traffic = nbytes
         roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                     "traffic": traffic,
                     "kernel": "l2dec_matvec_kernel<8,3,512,GEMV_W13> (rmsnorm + W1/W3 + SwiGLU)" + (", bf16 weights" if bf16 else ""),
